@@ -1,0 +1,121 @@
+/*
+ * gdn_oracle.h -- CPU oracle of the Gated DeltaNet (GDN) layer core forward.
+ *
+ * TEST INFRASTRUCTURE. Only the test-suite, the smoke check and the CPU
+ * baseline leg of the benchmark load this library. The CUDA library and its
+ * Python binding never include, link or call it, and it shares no code with
+ * them.
+ *
+ * Every quantity is computed in double precision from float inputs that
+ * already hold the activation-dtype-rounded values. The functions follow the
+ * definitions step by step:
+ *
+ *  - "GDN Elementwise Fusion" (Megatron Core developer guide), option table:
+ *    the pre-GDR steps (causal convolution, SiLU, Q/K L2 normalisation, head
+ *    expansion, beta and decay preparation) and the post-GDR step (output
+ *    RMSNorm then SiLU gating). Section "Execution and numerical behavior":
+ *    the RMSNorm result is materialised in the activation dtype before the
+ *    FP32 gating multiply.
+ *  - "perf(gated_delta_net): fold q/k L2-norm into the gated_delta_rule
+ *    kernel" (Megatron-LM PR #5396), section "Why": L2 norm with eps = 1e-6,
+ *    per head over the last dimension.
+ *  - "fused q/k/v short conv" (flash-linear-attention PR #972), sections
+ *    "Summary" and "Why": depthwise (per-channel) causal short convolution of
+ *    the q/k/v projections; concatenating channels leaves the math unchanged.
+ *  - The gated delta rule of the GDN core:
+ *        S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *        o_t = S_t q_t,  beta = sigmoid(b),  g = -exp(A_log) softplus(a + dt_bias).
+ *
+ * Parity status: every function here is pinned by the CPU tests (closed
+ * forms, brute force on tiny inputs, invariants); see tests/test_oracle_*.py.
+ */
+#ifndef GDN_ORACLE_H
+#define GDN_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* activation dtype codes (rounding of the RMSNorm output) */
+enum { GDN_ORACLE_F32 = 0, GDN_ORACLE_BF16 = 1, GDN_ORACLE_F16 = 2 };
+
+/* Round x to the nearest value of the activation dtype, ties to even. */
+double gdn_oracle_round_act(double x, int act);
+
+/* y[t][c] = silu( sum_{i=0..width-1} w[c][i] * x[t-(width-1)+i][c] ), where x is
+ * zero before the start of the sequence holding t.  seq_start[0..n_seq] are
+ * token offsets; x row t is at x + t*x_stride; y is [ntok][nch] dense. */
+void gdn_oracle_conv_silu(int n_seq, const int64_t *seq_start, int nch, int width,
+                          const float *x, int64_t x_stride, const float *w,
+                          double *y);
+
+/* In place, per row and per head: x <- x / sqrt(sum x^2 + eps). x is
+ * [nrows][nheads*d]. */
+void gdn_oracle_l2norm(int64_t nrows, int nheads, int d, double eps, double *x);
+
+/* beta = sigmoid(b), g = -exp(A_log[h]) * softplus(a + dt_bias[h]);
+ * a, b, beta, g are [ntok][H]. */
+void gdn_oracle_beta_decay(int64_t ntok, int H, const float *a, const float *b,
+                           const float *A_log, const float *dt_bias,
+                           double *beta, double *g);
+
+/* Token-by-token gated delta rule for one (sequence, v head).
+ * q,k: [T][dk] rows at the given strides; v: [T][dv]; beta, g: T values at
+ * stride bg_stride.  h0: initial state stored transposed, h0[i*dv+j] = S[j][i]
+ * (dk x dv), or NULL for zeros.  o: [T][dv] at o_stride (o_t = scale*S_t q_t).
+ * hT: final state, same layout as h0 (may be NULL). */
+void gdn_oracle_delta_rule(int T, int dk, int dv,
+                           const double *q, int64_t q_stride,
+                           const double *k, int64_t k_stride,
+                           const double *v, int64_t v_stride,
+                           const double *beta, const double *g, int64_t bg_stride,
+                           double scale, const double *h0,
+                           double *o, int64_t o_stride, double *hT);
+
+/* The same map computed chunk by chunk (chunk length C) in the WY/UT form;
+ * same arguments and results as gdn_oracle_delta_rule. */
+void gdn_oracle_delta_rule_chunked(int T, int dk, int dv, int C,
+                                   const double *q, int64_t q_stride,
+                                   const double *k, int64_t k_stride,
+                                   const double *v, int64_t v_stride,
+                                   const double *beta, const double *g, int64_t bg_stride,
+                                   double scale, const double *h0,
+                                   double *o, int64_t o_stride, double *hT);
+
+/* y = round_act(norm_w * o / sqrt(mean(o^2) + eps)) * silu(gate), per row of
+ * dv values; o, gate, y rows at the given strides. The product is not
+ * rounded (the caller compares it with a tolerance). */
+void gdn_oracle_gated_rmsnorm(int64_t nrows, int dv,
+                              const double *o, int64_t o_stride,
+                              const float *gate, int64_t gate_stride,
+                              const float *norm_w, double eps, int act,
+                              double *y, int64_t y_stride);
+
+/* Whole core forward for v heads [head_begin, head_end). All inputs are float
+ * arrays over the flattened token axis (ntok = seq_start[n_seq]):
+ *   q_raw, k_raw [ntok][Hk*dk], v_raw [ntok][Hv*dv], a, b [ntok][Hv],
+ *   gate [ntok][Hv*dv], conv_w [2*Hk*dk+Hv*dv][width] (q|k|v order),
+ *   A_log, dt_bias [Hv], norm_w [dv], initial_state [n_seq][Hv][dk][dv] or NULL.
+ * Outputs (double): out [ntok][Hv][dv], final_state [n_seq][Hv][dk][dv] or NULL.
+ * V head h reads q/k head h / (Hv/Hk). Returns 0, or -1 on bad arguments or
+ * allocation failure. */
+typedef struct {
+    int n_seq;
+    const int64_t *seq_start; /* [n_seq+1] */
+    int Hk, Hv, dk, dv, conv_width;
+    int act;
+    double l2_eps, norm_eps, scale;
+    const float *q_raw, *k_raw, *v_raw, *a, *b, *gate, *conv_w;
+    const float *A_log, *dt_bias, *norm_w, *initial_state;
+    double *out, *final_state;
+    int chunked;    /* 0: token loop; >0: chunked variant with this chunk length */
+} gdn_oracle_problem;
+
+int gdn_oracle_forward(const gdn_oracle_problem *p, int head_begin, int head_end);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
