@@ -1,0 +1,172 @@
+/*
+ * gdn.h -- C ABI of the Gated DeltaNet (GDN) layer core forward on GB300 (sm_103a).
+ *
+ * The core forward computes, per token t and v head h (GQA: v head h reads q/k
+ * head h / (Hv/Hk)):
+ *
+ *   1. a width-4 causal depthwise convolution over the channel-concatenated
+ *      [q_raw | k_raw | v_raw] projections followed by SiLU
+ *      ("fused q/k/v short conv", flash-linear-attention PR #972, sections
+ *      "Summary" and "Why"; "GDN Elementwise Fusion", option table, pre-GDR);
+ *   2. per-head L2 normalisation of q and k, x * rsqrt(sum x^2 + 1e-6)
+ *      ("perf(gated_delta_net): fold q/k L2-norm into the gated_delta_rule
+ *      kernel", Megatron-LM PR #5396, section "Why");
+ *   3. beta = sigmoid(b) and the decay g = -exp(A_log) * softplus(a + dt_bias)
+ *      ("GDN Elementwise Fusion", option table: beta and decay preparation);
+ *   4. the gated delta rule S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T)
+ *      + beta_t v_t k_t^T, o_t = scale * S_t q_t, evaluated chunk by chunk
+ *      (64 tokens, WY/UT form) with an fp32 state;
+ *   5. y = RMSNorm(o) * SiLU(gate), the RMSNorm result materialised in the
+ *      activation dtype before the fp32 gating multiply ("GDN Elementwise
+ *      Fusion", post-GDR requirements and "Execution and numerical behavior").
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    never allocates, frees or synchronises (except gdn_device_status, which
+ *    says so). Every call is asynchronous on `stream` (0 = legacy default).
+ *  - Return value: GDN_OK (0) or a negative gdn_status. Argument checks read
+ *    metadata only (no device synchronisation). On an error nothing is
+ *    launched. There is no fallback path for unsupported inputs.
+ *  - Element strides are in elements of the tensor's own dtype; the channel
+ *    (last) dimension is always contiguous.
+ *  - Device-side argument faults (a malformed cu_seqlens) cannot be seen by
+ *    the host without a sync: the kernels then write a status word in the
+ *    workspace and skip their work; read it with gdn_device_status().
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gdn_stream_t; /* == cudaStream_t */
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = -1,  /* null pointer, non-positive size, bad stride or alignment */
+    GDN_ERR_UNSUPPORTED = -2,  /* dk/dv not a power of two in [16, 512], conv_width != 4,
+                                  Hv % Hk != 0, unsupported dtype combination */
+    GDN_ERR_WORKSPACE = -3,    /* workspace missing, misaligned or smaller than
+                                  gdn_workspace_bytes() */
+    GDN_ERR_CUDA = -4,         /* a CUDA launch or query failed */
+    GDN_ERR_DEVICE_SEQLENS = -5 /* (device status) cu_seqlens not 0-based, not
+                                   non-decreasing or not ending at T */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
+
+/* Problem descriptor. Fill it with gdn_desc_init() and then override
+ * strides/dtypes of views as needed. */
+typedef struct {
+    int32_t B, T;        /* batch rows, tokens per row; with cu_seqlens: B = 1 and
+                            T = total packed tokens */
+    int32_t N;           /* sequences: B without cu_seqlens, else cu_seqlens has N+1 entries */
+    int32_t Hk, Hv;      /* q/k heads, v heads (Hv % Hk == 0) */
+    int32_t dk, dv;      /* head dims: powers of two in [16, 512] */
+    int32_t conv_width;  /* short-conv taps; must be 4 */
+    int32_t dtype;       /* gdn_dtype of q_raw, k_raw, v_raw, a, b, conv_w and out */
+    int32_t gate_dtype;  /* dtype, or GDN_F32 */
+    int32_t norm_w_dtype;/* dtype, or GDN_F32 */
+    int32_t reserved0;
+    /* (batch, token) element strides; channel stride is 1 */
+    int64_t q_stride_b, q_stride_t;
+    int64_t k_stride_b, k_stride_t;
+    int64_t v_stride_b, v_stride_t;
+    int64_t a_stride_b, a_stride_t;
+    int64_t b_stride_b, b_stride_t;
+    int64_t gate_stride_b, gate_stride_t;
+    float l2_eps;        /* q/k L2-norm eps, 1e-6 */
+    float norm_eps;      /* output RMSNorm eps, 1e-5 */
+    float scale;         /* q scale in o_t = scale * S_t q_t, 1 */
+    int32_t reserved1;
+} gdn_desc;
+
+/* Fill *d for contiguous tensors: q_raw/k_raw [B,T,Hk*dk], v_raw [B,T,Hv*dv],
+ * a/b [B,T,Hv], gate [B,T,Hv*dv], gate/norm_w in the act dtype,
+ * l2_eps 1e-6, norm_eps 1e-5, scale 1, conv_width 4. N = B when packed == 0;
+ * packed != 0 requires B == 1 and sets N = packed. Returns the validation
+ * status of the filled descriptor. */
+int gdn_desc_init(gdn_desc *d, int B, int T, int packed, int Hk, int Hv, int dk, int dv,
+                  int dtype);
+
+/* Bytes of scratch the forward needs for *d (intermediate q/k/v, beta, the
+ * in-chunk cumulative decay, o, a status word and the chunk table). */
+int gdn_workspace_bytes(const gdn_desc *d, size_t *bytes);
+
+/* Offsets (bytes from the workspace base) of the intermediate tensors, for
+ * inspection by tests and tools:
+ *   q, k [Hk][Ntok][dk] and v [Hv][Ntok][dv] in the act dtype (after conv,
+ *   SiLU and, for q/k, L2 norm); beta and gamma [Hv][Ntok] fp32 (gamma = in-chunk
+ *   inclusive cumulative sum of g); o [Ntok][Hv][dv] act dtype (gated delta rule
+ *   output); status: int32 device status word; chunk_off: int32 [N+1]. */
+typedef struct {
+    size_t status, chunk_off, q, k, v, beta, gamma, o, total;
+} gdn_workspace_layout;
+int gdn_workspace_offsets(const gdn_desc *d, gdn_workspace_layout *layout);
+
+/*
+ * The whole core forward (steps 1-5 above) on `stream`.
+ *   q_raw, k_raw   act dtype, [B,T,Hk*dk] at (q|k)_stride_(b|t); 16-byte aligned
+ *                  base and strides
+ *   v_raw          act dtype, [B,T,Hv*dv] at v_stride_(b|t); 16-byte aligned
+ *   a, b           act dtype, [B,T,Hv] at (a|b)_stride_(b|t); any alignment
+ *   gate           gate_dtype, [B,T,Hv*dv] at gate_stride_(b|t): may be a strided,
+ *                  unaligned view into a wider projection buffer
+ *   conv_w         act dtype, [2*Hk*dk + Hv*dv][4] contiguous, q|k|v channel
+ *                  order, tap 3 multiplies the current token; 16-byte aligned
+ *   A_log, dt_bias fp32 [Hv]
+ *   norm_w         norm_w_dtype [dv] contiguous
+ *   cu_seqlens     NULL, or int32 [N+1] packed-sequence offsets (then B == 1);
+ *                  the conv halo and the state restart at every offset
+ *   initial_state  NULL (zeros) or fp32 [N][Hv][dk][dv], the transposed state
+ *                  S^T of every (sequence, v head); 16-byte aligned
+ *   out            act dtype [B,T,Hv,dv] contiguous; 16-byte aligned
+ *   final_state    NULL (not written) or fp32 [N][Hv][dk][dv]; 16-byte aligned
+ *   workspace      device scratch of >= gdn_workspace_bytes(), 256-byte aligned;
+ *                  calls that share a workspace must not overlap on the GPU
+ * Inputs are only read; initial_state and final_state may alias.
+ */
+int gdn_forward(const gdn_desc *d,
+                const void *q_raw, const void *k_raw, const void *v_raw,
+                const void *a, const void *b, const void *gate,
+                const void *conv_w, const float *A_log, const float *dt_bias,
+                const void *norm_w, const int32_t *cu_seqlens,
+                const float *initial_state, void *out, float *final_state,
+                void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* The three stages of gdn_forward, callable one by one on the same workspace
+ * (gdn_forward is exactly prologue, chunk_rule, epilogue in this order).
+ * gdn_prologue: steps 1-3 plus the in-chunk cumulative decay -> workspace q, k,
+ *   v, beta, gamma (and the chunk table / status word when cu_seqlens is set).
+ * gdn_chunk_rule: step 4 -> workspace o, final_state.
+ * gdn_epilogue: step 5 -> out. */
+int gdn_prologue(const gdn_desc *d, const void *q_raw, const void *k_raw,
+                 const void *v_raw, const void *a, const void *b, const void *conv_w,
+                 const float *A_log, const float *dt_bias, const int32_t *cu_seqlens,
+                 void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+int gdn_chunk_rule(const gdn_desc *d, const int32_t *cu_seqlens,
+                   const float *initial_state, float *final_state,
+                   void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+int gdn_epilogue(const gdn_desc *d, const void *gate, const void *norm_w, void *out,
+                 void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* Wait for `stream`, then read the device status word of the last forward that
+ * used `workspace` into *status (GDN_OK or GDN_ERR_DEVICE_SEQLENS). This call
+ * synchronises the stream. */
+int gdn_device_status(const void *workspace, int *status, gdn_stream_t stream);
+
+/* Static description of a status code. */
+const char *gdn_status_string(int status);
+
+/* Which gated-delta-rule kernel serves *d: 0 = fp32 CUDA-core kernel,
+ * 1 = tcgen05 tensor-core kernel (bf16/fp16). */
+int gdn_chunk_kernel_kind(const gdn_desc *d);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H */

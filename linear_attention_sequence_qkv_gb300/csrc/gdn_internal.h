@@ -1,0 +1,68 @@
+// gdn_internal.h -- internal launch interfaces between the C ABI (gdn_api.cu)
+// and the kernels. Not part of the public boundary (include/gdn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Workspace regions (byte offsets); every region starts on a 256-byte boundary.
+struct Layout {
+    size_t status, chunk_off, q, k, v, beta, gamma, o, total;
+};
+
+inline size_t act_size(int dtype) { return dtype == GDN_F32 ? 4 : 2; }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline Layout make_layout(const gdn_desc &d) {
+    const size_t s = act_size(d.dtype);
+    const size_t ntok = (size_t)d.B * (size_t)d.T;
+    Layout L;
+    size_t off = 0;
+    L.status = off;    off = align_up(off + 256, 256);
+    L.chunk_off = off; off = align_up(off + 4 * ((size_t)d.N + 1), 256);
+    L.q = off;         off = align_up(off + s * ntok * d.Hk * d.dk, 256);
+    L.k = off;         off = align_up(off + s * ntok * d.Hk * d.dk, 256);
+    L.v = off;         off = align_up(off + s * ntok * d.Hv * d.dv, 256);
+    L.beta = off;      off = align_up(off + 4 * ntok * d.Hv, 256);
+    L.gamma = off;     off = align_up(off + 4 * ntok * d.Hv, 256);
+    L.o = off;         off = align_up(off + s * ntok * d.Hv * d.dv, 256);
+    L.total = off;
+    return L;
+}
+
+// Device pointers of one forward, resolved from the descriptor and workspace.
+struct Problem {
+    gdn_desc d;
+    int64_t ntok;
+    const void *q_raw, *k_raw, *v_raw, *a, *b, *gate, *conv_w, *norm_w;
+    const float *A_log, *dt_bias;
+    const int32_t *cu;            // null when not packed
+    const float *h0;              // null: zeros
+    float *hT;                    // null: not written
+    void *out;
+    int32_t *status, *chunk_off;
+    void *q, *k, *v, *o;
+    float *beta, *gamma;
+};
+
+// Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one
+// partial chunk), or the exact count without packing.
+inline int64_t chunk_slots(const Problem &p) {
+    if (p.cu == nullptr) return (int64_t)p.d.N * ((p.d.T + 63) / 64);
+    return (p.ntok + 63) / 64 + p.d.N;
+}
+
+cudaError_t launch_seqlens_scan(const Problem &p, cudaStream_t s);
+cudaError_t launch_prologue(const Problem &p, cudaStream_t s);
+cudaError_t launch_chunk_simt(const Problem &p, cudaStream_t s);
+cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s);
+bool chunk_tc_supports(const gdn_desc &d);
+cudaError_t launch_epilogue(const Problem &p, cudaStream_t s);
+
+}  // namespace gdn

@@ -199,3 +199,39 @@ def make_inputs_device(w: Workload, device, lengths: Optional[list] = None) -> I
         init = normal((n_seq, w.Hv, w.dk, w.dv), std=w.init_state_std)
     return Inputs(w, q_raw, k_raw, v_raw, a, b, gate_buf, conv_w, A_log, dt_bias,
                   norm_w, cu, init)
+
+
+def to_device(inp: Inputs, device) -> Inputs:
+    """Copy every tensor of ``inp`` to ``device`` (views are rebuilt, so the
+    gate stays a strided view into its wider buffer)."""
+    mv = lambda t: None if t is None else t.to(device)
+    return Inputs(inp.w, mv(inp.q_raw), mv(inp.k_raw), mv(inp.v_raw), mv(inp.a), mv(inp.b),
+                  mv(inp.gate_buf), mv(inp.conv_w), mv(inp.A_log), mv(inp.dt_bias),
+                  mv(inp.norm_w), mv(inp.cu_seqlens), mv(inp.initial_state), dict(inp.extras))
+
+
+def head_subproblem(inp: Inputs, heads: list) -> Inputs:
+    """The same problem restricted to v heads ``heads``: each kept v head h
+    brings its own copy of q/k head h // G, so the sub-problem has
+    Hk = Hv = len(heads). Pure slicing; used to check sampled heads of large
+    workloads."""
+    w = inp.w
+    G = w.G
+    m = len(heads)
+    qk_heads = [h // G for h in heads]
+    dk, dv = w.dk, w.dv
+
+    def take(t, width, idx):
+        return torch.cat([t[..., i * width:(i + 1) * width] for i in idx], dim=-1).contiguous()
+
+    ch_qk = w.Hk * dk
+    cw = inp.conv_w
+    conv_w = torch.cat([take(cw[:ch_qk].T, dk, qk_heads).T,
+                        take(cw[ch_qk:2 * ch_qk].T, dk, qk_heads).T,
+                        take(cw[2 * ch_qk:].T, dv, heads).T], dim=0).contiguous()
+    return Inputs(replace(w, Hk=m, Hv=m, gate_extra=0),
+                  take(inp.q_raw, dk, qk_heads), take(inp.k_raw, dk, qk_heads),
+                  take(inp.v_raw, dv, heads), take(inp.a, 1, heads), take(inp.b, 1, heads),
+                  take(inp.gate, dv, heads), conv_w, inp.A_log[heads].contiguous(),
+                  inp.dt_bias[heads].contiguous(), inp.norm_w, inp.cu_seqlens,
+                  None if inp.initial_state is None else inp.initial_state[:, heads].contiguous())

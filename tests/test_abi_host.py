@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point declared in include/gdn.h, and rejects bad arguments with
+status codes on metadata alone, before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_sequence_qkv_gb300 import build, gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gdn.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gdn_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(gdn.EXPORTS)
+
+
+def test_library_is_native_and_sm103a():
+    # the built library exists and was compiled for sm_103a only
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
+    assert os.path.exists(gdn.LIB_PATH)
+
+
+def test_struct_layout_matches_header(lib):
+    # gdn_desc: 12 int32 + 12 int64 + 3 float + 1 int32 = 160 bytes
+    assert ctypes.sizeof(gdn.gdn_desc) == 160
+    assert ctypes.sizeof(gdn.gdn_workspace_layout) == 9 * 8
+
+
+@pytest.mark.parametrize("args,status", [
+    ((2, 2048, 0, 6, 6, 100, 512, gdn.GDN_BF16), gdn.GDN_ERR_UNSUPPORTED),  # dk not pow2
+    ((2, 2048, 0, 6, 6, 256, 1024, gdn.GDN_BF16), gdn.GDN_ERR_UNSUPPORTED),  # dv > 512
+    ((2, 2048, 0, 4, 6, 64, 64, gdn.GDN_BF16), gdn.GDN_ERR_UNSUPPORTED),    # Hv % Hk
+    ((2, 2048, 0, 6, 6, 64, 64, 7), gdn.GDN_ERR_UNSUPPORTED),               # dtype
+    ((0, 2048, 0, 6, 6, 64, 64, gdn.GDN_F32), gdn.GDN_ERR_INVALID_ARG),     # B
+    ((2, -1, 0, 6, 6, 64, 64, gdn.GDN_F32), gdn.GDN_ERR_INVALID_ARG),       # T
+    ((2, 100, 3, 6, 6, 64, 64, gdn.GDN_F32), gdn.GDN_ERR_INVALID_ARG),      # packed needs B == 1
+])
+def test_desc_validation(lib, args, status):
+    d = gdn.gdn_desc()
+    assert lib.gdn_desc_init(ctypes.byref(d), *args) == status
+
+
+def test_valid_descs(lib):
+    for args in ((1, 128, 0, 2, 2, 64, 64, gdn.GDN_F32), (2, 2048, 0, 6, 6, 256, 512, gdn.GDN_BF16),
+                 (2, 100, 0, 6, 6, 64, 128, gdn.GDN_F16), (1, 131072, 0, 16, 32, 128, 128, gdn.GDN_BF16),
+                 (1, 263156, 64, 16, 32, 128, 128, gdn.GDN_BF16), (1, 0, 0, 1, 1, 16, 16, gdn.GDN_F32)):
+        gdn.gdn_desc_init(*args)
+
+
+def test_conv_width_and_strides_checked(lib):
+    d = gdn.gdn_desc_init(2, 100, 0, 6, 6, 64, 128, gdn.GDN_F16)
+    d.conv_width = 3
+    assert lib.gdn_forward(ctypes.byref(d), *([None] * 14), None, 0, None) == gdn.GDN_ERR_UNSUPPORTED
+    d = gdn.gdn_desc_init(2, 100, 0, 6, 6, 64, 128, gdn.GDN_F16)
+    d.q_stride_t = 6 * 64 + 3   # rows not 16-byte aligned
+    assert lib.gdn_forward(ctypes.byref(d), *([None] * 14), None, 0, None) == gdn.GDN_ERR_INVALID_ARG
+    d = gdn.gdn_desc_init(2, 100, 0, 6, 6, 64, 128, gdn.GDN_F16)
+    d.gate_dtype = gdn.GDN_BF16
+    assert lib.gdn_forward(ctypes.byref(d), *([None] * 14), None, 0, None) == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_null_and_workspace_checks(lib):
+    d = gdn.gdn_desc_init(1, 128, 0, 2, 2, 64, 64, gdn.GDN_F32)
+    fake = 1 << 20   # never dereferenced: every call below fails its checks first
+    ptrs = [fake] * 10   # q_raw .. norm_w
+    # null q_raw
+    rc = lib.gdn_forward(ctypes.byref(d), None, *ptrs[1:], None, None, fake, None, fake,
+                         gdn.gdn_workspace_bytes(d), None)
+    assert rc == gdn.GDN_ERR_INVALID_ARG
+    # workspace too small
+    rc = lib.gdn_forward(ctypes.byref(d), *ptrs, None, None, fake, None, fake, 256, None)
+    assert rc == gdn.GDN_ERR_WORKSPACE
+    # workspace misaligned
+    rc = lib.gdn_forward(ctypes.byref(d), *ptrs, None, None, fake, None, fake + 16,
+                         gdn.gdn_workspace_bytes(d), None)
+    assert rc == gdn.GDN_ERR_WORKSPACE
+    # misaligned out
+    rc = lib.gdn_forward(ctypes.byref(d), *ptrs, None, None, fake + 4, None, fake,
+                         gdn.gdn_workspace_bytes(d), None)
+    assert rc == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_device_status(None, None, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_workspace_layout(lib):
+    d = gdn.gdn_desc_init(2, 2048, 0, 6, 6, 256, 512, gdn.GDN_BF16)
+    lay = gdn.gdn_workspace_offsets(d)
+    ntok = 4096
+    assert lay.status == 0
+    for name in ("chunk_off", "q", "k", "v", "beta", "gamma", "o", "total"):
+        assert getattr(lay, name) % 256 == 0
+    assert lay.k - lay.q >= ntok * 6 * 256 * 2
+    assert lay.beta - lay.v >= ntok * 6 * 512 * 2
+    assert lay.total - lay.o >= ntok * 6 * 512 * 2
+    assert gdn.gdn_workspace_bytes(d) == lay.total
+
+
+def test_status_strings(lib):
+    for s in (0, -1, -2, -3, -4, -5):
+        assert gdn.status_string(s) not in ("", "unknown status")
+    assert gdn.status_string(42) == "unknown status"
+
+
+def test_chunk_kernel_kind(lib):
+    assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(1, 128, 0, 2, 2, 64, 64, gdn.GDN_F32)) == 0
