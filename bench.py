@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Throughput of the Gated DeltaNet (GDN) layer core forward on GB300.
+
+One step = one pass of the whole core forward (prologue, chunked gated delta
+rule, gated RMSNorm epilogue) over one batch of synthetic input already
+resident in HBM. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and a device synchronisation; L2 is flushed (a 512 MiB write) before every
+timed step, outside the events; per-kernel durations come from CUDA events
+recorded on the launching stream between the three stages. For N > 1 every
+rank runs its own replica (the path has no data exchange): value = tokens of
+all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN core fwd tokens/s at 1 GB300 and % of roofline (HBM / BF16 MMA)"
+CHUNK = 64
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one
+# ncu capture, keyed by kernel; each entry is only used while the kernel's
+# source file still hashes to the recorded value.
+# kernel -> (source file, sha256 of it, workload, bytes per launch)
+NCU_TRAFFIC: dict = {}
+
+
+def sha256(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="layer_bf16")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def algorithmic(w, ntok, n_seq, has_h0):
+    """Bytes (and MMA flops) that each kernel must move (do), per launch."""
+    s = 4 if w.dtype == "fp32" else 2
+    ch = 2 * w.Hk * w.dk + w.Hv * w.dv
+    state = n_seq * w.Hv * w.dk * w.dv * 4
+    k1 = ntok * (2 * ch * s + 2 * w.Hv * s + 8 * w.Hv)
+    k2 = ntok * (ch * s + 8 * w.Hv + w.Hv * w.dv * s) + state * (2 if has_h0 else 1)
+    k3 = ntok * 3 * w.Hv * w.dv * s
+    C = CHUNK
+    k2_flops = ntok * w.Hv * (6 * C * w.dk + 4 * C * w.dv + 6 * w.dk * w.dv + (2.0 / 3.0) * C * C)
+    return {"prologue": (k1, 0.0), "chunk_rule": (k2, k2_flops), "epilogue": (k3, 0.0)}
+
+
+def roofline_entry(name, bytes_, flops, ms, pk, dtype):
+    t = ms / 1e3
+    t_hbm = bytes_ / (pk["hbm_gbs"] * 1e9)
+    t_mma = flops / (pk["bf16_tflops"] * 1e12) if flops else 0.0
+    if flops and t_mma >= t_hbm and dtype != "fp32":
+        ach = flops / t / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"], "algorithmic_flops": flops,
+                "algorithmic_bytes": bytes_, "ms": ms}
+    ach = bytes_ / t / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / pk["hbm_gbs"], "algorithmic_bytes": bytes_, "ms": ms}
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_id is not None:
+            cmd.insert(1, f"--id={gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxs.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ reference arm
+def oracle_sample(w):
+    """Bounded sample of the workload for the CPU oracle: the first sequence,
+    every v head (all of them for the small workloads)."""
+    from linear_attention_sequence_qkv_gb300.workloads import head_subproblem, make_inputs, replace
+    if w.n_packed:
+        w1 = replace(w, n_packed=0, B=1, T=min(w.max_len, 2048))
+    else:
+        w1 = replace(w, B=1, T=min(w.T, 2048))
+    inp = make_inputs(w1)
+    heads = list(range(w1.Hv))
+    if w1.Hv * w1.dk * w1.dv * w1.T > 6 * 256 * 512 * 2048:
+        heads = heads[:2]
+        inp = head_subproblem(inp, heads)
+    return inp, w1, len(heads)
+
+
+def run_oracle_once(inp, threads):
+    from oracle import oracle as O
+    w = inp.w
+    flat = lambda x: x.float().reshape(-1, x.shape[-1]).numpy()
+    args = dict(q_raw=flat(inp.q_raw), k_raw=flat(inp.k_raw), v_raw=flat(inp.v_raw), a=flat(inp.a),
+                b=flat(inp.b), gate=flat(inp.gate.contiguous()), conv_w=inp.conv_w.float().numpy(),
+                A_log=inp.A_log.numpy(), dt_bias=inp.dt_bias.numpy(), norm_w=inp.norm_w.float().numpy(),
+                seq_start=inp.seq_starts(), Hk=w.Hk, Hv=w.Hv, dk=w.dk, dv=w.dv, dtype=w.dtype,
+                initial_state=None if inp.initial_state is None else inp.initial_state.numpy(),
+                threads=threads)
+    t0 = time.perf_counter()
+    O.forward(**args)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w):
+    from oracle import oracle as O
+    O.build()
+    inp, w1, nheads = oracle_sample(w)
+    threads = max(1, min(os.cpu_count() or 1, nheads))
+    dt = run_oracle_once(inp, threads)
+    # tokens of the full workload per second: the sample covers nheads of w.Hv heads
+    tps = w1.B * w1.T / dt * (nheads / w.Hv)
+    return {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{w1.B * w1.T} tokens x {nheads}/{w.Hv} v heads of {w.name}, "
+                      f"{dt:.2f} s wall, scaled to all heads"}
+
+
+def reference_arm(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    O.build()
+    inp, w1, nheads = oracle_sample(w)
+    threads = max(1, min(os.cpu_count() or 1, nheads))
+    for _ in range(args.warmup):
+        run_oracle_once(inp, threads)
+    times = [run_oracle_once(inp, threads) for _ in range(args.steps)]
+    tot = sum(times)
+    tps = w1.B * w1.T * args.steps / tot * (nheads / w.Hv)
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample_tokens": w1.B * w1.T, "sample_heads": nheads,
+                       "Hv": w.Hv, "dk": w.dk, "dv": w.dv},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{w1.B * w1.T} tokens x {nheads}/{w.Hv} v heads per step"},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- our arm
+def main():
+    args = parse()
+    from linear_attention_sequence_qkv_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    # CPU baseline first (host threads only; before any GPU work)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    from linear_attention_sequence_qkv_gb300 import build, gdn
+    from linear_attention_sequence_qkv_gb300.workloads import make_inputs_device
+
+    build.build()
+    gdn.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    inp = make_inputs_device(w, dev)
+    d = gdn.make_desc(inp)
+    bufs = gdn.alloc(d, dev)
+    ntok = d.B * d.T
+    n_seq = d.N
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        gdn.gdn_prologue(d, inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.conv_w, inp.A_log,
+                         inp.dt_bias, inp.cu_seqlens, bufs.workspace, bufs.ws_bytes, stream)
+        if ev:
+            ev[1].record()
+        gdn.gdn_chunk_rule(d, inp.cu_seqlens, inp.initial_state, bufs.final_state, bufs.workspace,
+                           bufs.ws_bytes, stream)
+        if ev:
+            ev[2].record()
+        gdn.gdn_epilogue(d, inp.gate, inp.norm_w, bufs.out, bufs.workspace, bufs.ws_bytes, stream)
+        if ev:
+            ev[3].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status(bufs.workspace) == gdn.GDN_OK
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = None if args.no_clocks else ClockSampler(gpu_id)
+    torch.cuda.synchronize()
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+
+    per = {"prologue": [], "chunk_rule": [], "epilogue": [], "step": []}
+    for e in evs:
+        per["prologue"].append(e[0].elapsed_time(e[1]))
+        per["chunk_rule"].append(e[1].elapsed_time(e[2]))
+        per["epilogue"].append(e[2].elapsed_time(e[3]))
+        per["step"].append(e[0].elapsed_time(e[3]))
+    ms_step = sum(per["step"]) / len(per["step"])
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = ntok * world / (ms_step / 1e3)
+
+    pk = peaks()
+    alg = algorithmic(w, ntok, n_seq, inp.initial_state is not None)
+    kernels = {}
+    for name in ("prologue", "chunk_rule", "epilogue"):
+        ms = sum(per[name]) / len(per[name])
+        kernels[name] = roofline_entry(name, alg[name][0], alg[name][1], ms, pk, w.dtype)
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    roof = dict(kernels[dom])
+    roof["kernel"] = dom
+    tr = NCU_TRAFFIC.get(dom)
+    roof["traffic"] = None
+    if tr is not None:
+        src, digest, wl, nbytes = tr
+        if wl == w.name and os.path.exists(os.path.join(ROOT, src)) and sha256(os.path.join(ROOT, src)) == digest:
+            roof["traffic"] = nbytes
+    roof["peak_source"] = pk["source"]
+
+    # end to end through the C ABI with host buffers: pinned H2D of every input,
+    # the forward, D2H of the output, all inside the events
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        names = ["q_raw", "k_raw", "v_raw", "a", "b", "gate_buf", "conv_w", "A_log", "dt_bias", "norm_w"]
+        if inp.cu_seqlens is not None:
+            names.append("cu_seqlens")
+        if inp.initial_state is not None:
+            names.append("initial_state")
+        for nm in names:
+            host[nm] = getattr(inp, nm).cpu().pin_memory()
+        out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        dv_ = {nm: torch.empty_like(getattr(inp, nm)) for nm in names}
+        ksteps = min(args.steps, 100)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(ksteps)]
+
+        def e2e_step(e):
+            e[0].record()
+            for nm in names:
+                dv_[nm].copy_(host[nm], non_blocking=True)
+            gate = dv_["gate_buf"][..., : w.Hv * w.dv]
+            gdn.gdn_forward(d, dv_["q_raw"], dv_["k_raw"], dv_["v_raw"], dv_["a"], dv_["b"], gate,
+                            dv_["conv_w"], dv_["A_log"], dv_["dt_bias"], dv_["norm_w"],
+                            dv_.get("cu_seqlens"), dv_.get("initial_state"), bufs.out,
+                            bufs.final_state, bufs.workspace, bufs.ws_bytes, stream)
+            out_host.copy_(bufs.out, non_blocking=True)
+            e[1].record()
+
+        for _ in range(3):
+            e2e_step(ev2[0])
+        torch.cuda.synchronize()
+        barrier()
+        for i in range(ksteps):
+            flush.zero_()
+            e2e_step(ev2[i])
+        torch.cuda.synchronize()
+        barrier()
+        ms_e2e = sum(a.elapsed_time(b) for a, b in ev2) / ksteps
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": ntok * world / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+               "steps": ksteps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    launches_per_step = 3 + (1 if inp.cu_seqlens is not None else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp32": "f32", "bf16": "bf16", "fp16": "f16"}[w.dtype], "data": "synthetic",
+        "config": {"workload": w.name, "B": d.B, "T": d.T, "N": d.N, "Hk": w.Hk, "Hv": w.Hv,
+                   "dk": w.dk, "dv": w.dv, "tokens_per_step": ntok, "chunk": CHUNK,
+                   "l2": "flushed before every timed step (512 MiB write)",
+                   "parallelism": f"replicas x{world}",
+                   "chunk_kernel": "tcgen05" if gdn.gdn_chunk_kernel_kind(d) == 1 else "cuda-core fp32"},
+        "roofline": roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_per_step": launches_per_step,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -125,6 +125,7 @@ int gdn_workspace_offsets(const gdn_desc *d, gdn_workspace_layout *layout);
  *   initial_state  NULL (zeros) or fp32 [N][Hv][dk][dv], the transposed state
  *                  S^T of every (sequence, v head); 16-byte aligned
  *   out            act dtype [B,T,Hv,dv] contiguous; 16-byte aligned
+ *                  (token tensors and out may be NULL when B*T == 0)
  *   final_state    NULL (not written) or fp32 [N][Hv][dk][dv]; 16-byte aligned
  *   workspace      device scratch of >= gdn_workspace_bytes(), 256-byte aligned;
  *                  calls that share a workspace must not overlap on the GPU

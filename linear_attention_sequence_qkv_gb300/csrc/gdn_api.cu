@@ -155,7 +155,8 @@ int gdn_prologue(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
                  size_t workspace_bytes, gdn_stream_t stream) {
     int rc = check_desc(d, cu_seqlens != nullptr);
     if (rc != GDN_OK) return rc;
-    if (!q_raw || !k_raw || !v_raw || !a || !b || !conv_w || !A_log || !dt_bias)
+    const bool tok = (int64_t)d->B * d->T > 0;   // token tensors may be empty (null)
+    if ((tok && (!q_raw || !k_raw || !v_raw || !a || !b)) || !conv_w || !A_log || !dt_bias)
         return GDN_ERR_INVALID_ARG;
     if (!aligned(q_raw, 16) || !aligned(k_raw, 16) || !aligned(v_raw, 16) || !aligned(conv_w, 16))
         return GDN_ERR_INVALID_ARG;
@@ -191,7 +192,8 @@ int gdn_epilogue(const gdn_desc *d, const void *gate, const void *norm_w, void *
     // the epilogue works per token, so packing does not change it (B == 1 when packed)
     int rc = check_desc(d, d && d->N != d->B);
     if (rc != GDN_OK) return rc;
-    if (!gate || !norm_w || !out) return GDN_ERR_INVALID_ARG;
+    const bool tok = (int64_t)d->B * d->T > 0;   // token tensors may be empty (null)
+    if ((tok && (!gate || !out)) || !norm_w) return GDN_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(norm_w, 4)) return GDN_ERR_INVALID_ARG;
     if ((rc = check_ws(d, workspace, workspace_bytes)) != GDN_OK) return rc;
     Problem p = base_problem(d, nullptr, workspace);
@@ -209,8 +211,9 @@ int gdn_forward(const gdn_desc *d, const void *q_raw, const void *k_raw, const v
                 gdn_stream_t stream) {
     int rc = check_desc(d, cu_seqlens != nullptr);
     if (rc != GDN_OK) return rc;
-    if (!q_raw || !k_raw || !v_raw || !a || !b || !gate || !conv_w || !A_log || !dt_bias ||
-        !norm_w || !out)
+    const bool tok = (int64_t)d->B * d->T > 0;   // token tensors may be empty (null)
+    if ((tok && (!q_raw || !k_raw || !v_raw || !a || !b || !gate || !out)) || !conv_w || !A_log ||
+        !dt_bias || !norm_w)
         return GDN_ERR_INVALID_ARG;
     if (!aligned(q_raw, 16) || !aligned(k_raw, 16) || !aligned(v_raw, 16) ||
         !aligned(conv_w, 16) || !aligned(out, 16) || !aligned(norm_w, 4))
