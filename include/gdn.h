@@ -53,8 +53,11 @@ typedef enum {
     GDN_ERR_WORKSPACE = -3,    /* workspace missing, misaligned or smaller than
                                   gdn_workspace_bytes() */
     GDN_ERR_CUDA = -4,         /* a CUDA launch or query failed */
-    GDN_ERR_DEVICE_SEQLENS = -5 /* (device status) cu_seqlens not 0-based, not
-                                   non-decreasing or not ending at T */
+    GDN_ERR_DEVICE_SEQLENS = -5, /* (device status) cu_seqlens not 0-based, not
+                                    non-decreasing or not ending at T */
+    GDN_ERR_DEVICE_RANGE = -6   /* (device status) a non-finite gated-delta-rule output
+                                   reached the epilogue: a non-finite input, or a value
+                                   beyond the fp16 range of the intermediates */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
@@ -99,10 +102,12 @@ int gdn_workspace_bytes(const gdn_desc *d, size_t *bytes);
 
 /* Offsets (bytes from the workspace base) of the intermediate tensors, for
  * inspection by tests and tools:
- *   q, k [Hk][Ntok][dk] and v [Hv][Ntok][dv] in the act dtype (after conv,
- *   SiLU and, for q/k, L2 norm); beta and gamma [Hv][Ntok] fp32 (gamma = in-chunk
- *   inclusive cumulative sum of g); o [Ntok][Hv][dv] act dtype (gated delta rule
- *   output); status: int32 device status word; chunk_off: int32 [N+1]. */
+ *   q, k [Hk][Ntok][dk] and v [Hv][Ntok][dv] (after conv, SiLU and, for q/k,
+ *   L2 norm) and o [Ntok][Hv][dv] (gated delta rule output), stored in fp16 for
+ *   bf16/fp16 activations and in fp32 for fp32 activations; beta [Hv][Ntok] fp32;
+ *   gamma [Hv][Ntok] = in-chunk inclusive cumulative sum of g, fp64 for fp32
+ *   activations and fp32 otherwise; status: int32 device status word;
+ *   chunk_off: int32 [N+1]. */
 typedef struct {
     size_t status, chunk_off, q, k, v, beta, gamma, o, total;
 } gdn_workspace_layout;
@@ -156,8 +161,8 @@ int gdn_epilogue(const gdn_desc *d, const void *gate, const void *norm_w, void *
                  void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /* Wait for `stream`, then read the device status word of the last forward that
- * used `workspace` into *status (GDN_OK or GDN_ERR_DEVICE_SEQLENS). This call
- * synchronises the stream. */
+ * used `workspace` into *status (GDN_OK, GDN_ERR_DEVICE_SEQLENS or
+ * GDN_ERR_DEVICE_RANGE). This call synchronises the stream. */
 int gdn_device_status(const void *workspace, int *status, gdn_stream_t stream);
 
 /* Static description of a status code. */

@@ -65,7 +65,7 @@ Problem base_problem(const gdn_desc *d, const int32_t *cu, void *ws) {
     p.k = w + L.k;
     p.v = w + L.v;
     p.beta = (float *)(w + L.beta);
-    p.gamma = (float *)(w + L.gamma);
+    p.gamma = w + L.gamma;
     p.o = w + L.o;
     return p;
 }
@@ -260,6 +260,7 @@ const char *gdn_status_string(int status) {
     case GDN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case GDN_ERR_CUDA: return "CUDA launch or query failed";
     case GDN_ERR_DEVICE_SEQLENS: return "cu_seqlens malformed (device check)";
+    case GDN_ERR_DEVICE_RANGE: return "non-finite intermediate (device check)";
     default: return "unknown status";
     }
 }

@@ -29,11 +29,13 @@ constexpr int LDS = DS + 1;
 
 template <int NV>
 size_t simt_smem_floats(int dk) {
-    return (size_t)dk * NV + 3 * kChunk * LDA + 2 * kChunk * LDS + 3 * kChunk * NV + 2 * kChunk;
+    return (size_t)dk * NV + 3 * kChunk * LDA + 2 * kChunk * LDS + 3 * kChunk * NV + 4 * kChunk;
 }
 
 template <typename T, int NV>
 __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, int ntiles) {
+    using S = typename Inter<T>::S;   // storage of q, k, v, o
+    using GT = typename Inter<T>::G;  // in-chunk cumulative decay
     constexpr int NB = NV / 16;     // output columns per thread
     extern __shared__ float sm[];
     const gdn_desc &d = p.d;
@@ -59,16 +61,16 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
     float *Vs = Qs + kChunk * LDS;           // [64][NV]   V tile, then R
     float *Vn = Vs + kChunk * NV;            // [64][NV]
     float *Xs = Vn + kChunk * NV;            // [64][NV]   scratch of the solve
-    float *gam = Xs + kChunk * NV;           // [64]
-    float *bet = gam + kChunk;               // [64]
+    float *bet = Xs + kChunk * NV;           // [64]
+    GT *gam = (GT *)(bet + 2 * kChunk);      // [64] (8-byte aligned)
 
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const T *kq = (const T *)p.k + (int64_t)hk * p.ntok * dk;
-    const T *qq = (const T *)p.q + (int64_t)hk * p.ntok * dk;
-    const T *vv = (const T *)p.v + (int64_t)j * p.ntok * dv;
-    const float *gw = p.gamma + (int64_t)j * p.ntok;
+    const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
+    const S *qq = (const S *)p.q + (int64_t)hk * p.ntok * dk;
+    const S *vv = (const S *)p.v + (int64_t)j * p.ntok * dv;
+    const GT *gw = (const GT *)p.gamma + (int64_t)j * p.ntok;
     const float *bw = p.beta + (int64_t)j * p.ntok;
-    T *o = (T *)p.o;
+    S *o = (S *)p.o;
 
     // state slice
     const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
         }
         for (int idx = tid; idx < kChunk * NV; idx += kThreads) {
             const int i = idx / NV, c = idx - i * NV;
-            Vs[idx] = i < L ? to_f<T>(vv[(tok0 + i) * dv + v0 + c]) : 0.f;
+            Vs[idx] = i < L ? to_f<S>(vv[(tok0 + i) * dv + v0 + c]) : 0.f;
         }
         // ---- K K^T, Q K^T, K H, Q H over dk slices
         float kk[4][4], qk[4][4], kh[4][NB], qh[4][NB];
@@ -104,8 +106,8 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
             for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
                 const int i = idx / DS, c = idx - i * DS;
                 const bool ok = i < L && d0 + c < dk;
-                Ks[i * LDS + c] = ok ? to_f<T>(kq[(tok0 + i) * dk + d0 + c]) : 0.f;
-                Qs[i * LDS + c] = ok ? to_f<T>(qq[(tok0 + i) * dk + d0 + c]) : 0.f;
+                Ks[i * LDS + c] = ok ? to_f<S>(kq[(tok0 + i) * dk + d0 + c]) : 0.f;
+                Qs[i * LDS + c] = ok ? to_f<S>(qq[(tok0 + i) * dk + d0 + c]) : 0.f;
             }
             __syncthreads();
             const int dn = min(DS, dk - d0);
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int jj = tx + 16 * b;
-                const float dec = jj <= i ? expf(gam[i] - gam[jj]) : 0.f;
+                const float dec = jj <= i ? expf((float)(gam[i] - gam[jj])) : 0.f;
                 As[i * LDA + jj] = jj < i ? bet[i] * dec * kk[a][b] : 0.f;
                 Ps[i * LDA + jj] = dec * qk[a][b];
                 Ts[i * LDA + jj] = 0.f;
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const int i = ty + 16 * a;
-            const float eg = expf(gam[i]);
+            const float eg = expf((float)gam[i]);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 const int c = tx + 16 * b;
@@ -220,20 +222,20 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
                 for (int b = 0; b < NB; ++b) qh[a][b] = fmaf(pv, Vn[m * NV + tx + 16 * b], qh[a][b]);
             }
             if (i < L) {
-                T *orow = o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0;
+                S *orow = o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0;
 #pragma unroll
-                for (int b = 0; b < NB; ++b) orow[tx + 16 * b] = from_f<T>(qh[a][b] * d.scale);
+                for (int b = 0; b < NB; ++b) orow[tx + 16 * b] = from_f<S>(qh[a][b] * d.scale);
             }
         }
         // ---- H <- e^{gam_L} H + (e^{gam_L - gam} K)^T Vn, over dk slices
-        const float eL = expf(gam[kChunk - 1]);
+        const float eL = expf((float)gam[kChunk - 1]);
         for (int d0 = 0; d0 < dk; d0 += DS) {
             __syncthreads();
             for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
                 const int i = idx / DS, c = idx - i * DS;
                 const bool ok = i < L && d0 + c < dk;
-                Ks[i * LDS + c] = ok ? to_f<T>(kq[(tok0 + i) * dk + d0 + c]) *
-                                           expf(gam[kChunk - 1] - gam[i]) : 0.f;
+                Ks[i * LDS + c] = ok ? to_f<S>(kq[(tok0 + i) * dk + d0 + c]) *
+                                           expf((float)(gam[kChunk - 1] - gam[i])) : 0.f;
             }
             __syncthreads();
             const int dn = min(DS, dk - d0);

@@ -31,6 +31,11 @@ template <> struct Dt<__half> {
 template <typename T> __device__ __forceinline__ float to_f(T x) { return Dt<T>::to_f(x); }
 template <typename T> __device__ __forceinline__ T from_f(float x) { return Dt<T>::from_f(x); }
 
+// Storage type of the intermediates (q, k, v, o) for activation type T, and the
+// type of the in-chunk cumulative decay (see gdn_internal.h).
+template <typename T> struct Inter { using S = __half; using G = float; };
+template <> struct Inter<float> { using S = float; using G = double; };
+
 // round a float through the storage type T and back
 template <typename T> __device__ __forceinline__ float round_through(float x) {
     return to_f<T>(from_f<T>(x));

@@ -33,7 +33,9 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     const int cc = (threadIdx.x - sub * lpr) * CPT;
     const float inv_dv = 1.0f / (float)dv;
     const int64_t nrows = p.ntok * d.Hv;
-    const T *o = (const T *)p.o;
+    using S = typename Inter<T>::S;    // storage of o
+    const S *o = (const S *)p.o;
+    bool finite = true;
     const G *gate = (const G *)p.gate;
     T *out = (T *)p.out;
 
@@ -46,7 +48,9 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
             const int64_t tok = r / d.Hv;
             const int h = (int)(r - tok * d.Hv);
 #pragma unroll
-            for (int v = 0; v < NVEC; ++v) load16_f<T>(o + r * dv + cc + v * VEC, x + v * VEC);
+            for (int v = 0; v < NVEC; ++v) load16_f<S>(o + r * dv + cc + v * VEC, x + v * VEC);
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) finite = finite && isfinite(x[i]);
             const G *gp = gate + tok_offset(tok, d.T, d.gate_stride_b, d.gate_stride_t) + h * dv + cc;
             if (GVEC) {
                 constexpr int GV = Vec16<G>::N;
@@ -76,6 +80,10 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
             for (int v = 0; v < NVEC; ++v) store16_f_cs<T>(out + r * dv + cc + v * VEC, y + v * VEC);
         }
     }
+    // a non-finite gated-delta-rule output (unless an earlier stage already
+    // reported a malformed cu_seqlens, after which o holds nothing meaningful)
+    if (__syncthreads_or(!finite) && threadIdx.x == 0 && *p.status == GDN_OK)
+        *p.status = GDN_ERR_DEVICE_RANGE;
 }
 
 template <typename T, typename G, typename W, int NVEC>

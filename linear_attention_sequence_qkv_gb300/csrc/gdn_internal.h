@@ -17,6 +17,13 @@ struct Layout {
 
 inline size_t act_size(int dtype) { return dtype == GDN_F32 ? 4 : 2; }
 
+// Intermediates (q, k, v after the prologue, o after the chunk rule) are stored
+// in fp16 for bf16 and fp16 activations (3 more mantissa bits than bf16 at the
+// same size) and in fp32 for fp32 activations. The in-chunk cumulative decay is
+// fp64 for fp32 activations (so that differences of large sums stay exact to
+// fp32 precision) and fp32 otherwise.
+inline size_t gamma_size(int dtype) { return dtype == GDN_F32 ? 8 : 4; }
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline Layout make_layout(const gdn_desc &d) {
@@ -30,7 +37,7 @@ inline Layout make_layout(const gdn_desc &d) {
     L.k = off;         off = align_up(off + s * ntok * d.Hk * d.dk, 256);
     L.v = off;         off = align_up(off + s * ntok * d.Hv * d.dv, 256);
     L.beta = off;      off = align_up(off + 4 * ntok * d.Hv, 256);
-    L.gamma = off;     off = align_up(off + 4 * ntok * d.Hv, 256);
+    L.gamma = off;     off = align_up(off + gamma_size(d.dtype) * ntok * d.Hv, 256);
     L.o = off;         off = align_up(off + s * ntok * d.Hv * d.dv, 256);
     L.total = off;
     return L;
@@ -48,7 +55,8 @@ struct Problem {
     void *out;
     int32_t *status, *chunk_off;
     void *q, *k, *v, *o;
-    float *beta, *gamma;
+    float *beta;
+    void *gamma;                  // float, or double for fp32 activations
 };
 
 // Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one

@@ -96,23 +96,24 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
 
     // which tensor / channel range
     const T *src;
-    T *dst;
+    typename Inter<T>::S *dst;
     int64_t sb, st;
     int nch, hd, w_base;
     bool norm;
     int g = gy;
     const int ch_qk = d.Hk * d.dk;
     if (g < A.groups_qk) {
-        src = (const T *)p.q_raw; dst = (T *)p.q; sb = d.q_stride_b; st = d.q_stride_t;
+        src = (const T *)p.q_raw; dst = (typename Inter<T>::S *)p.q; sb = d.q_stride_b; st = d.q_stride_t;
         nch = ch_qk; hd = d.dk; w_base = 0; norm = true;
     } else if ((g -= A.groups_qk) < A.groups_qk) {
-        src = (const T *)p.k_raw; dst = (T *)p.k; sb = d.k_stride_b; st = d.k_stride_t;
+        src = (const T *)p.k_raw; dst = (typename Inter<T>::S *)p.k; sb = d.k_stride_b; st = d.k_stride_t;
         nch = ch_qk; hd = d.dk; w_base = ch_qk; norm = true;
     } else {
         g -= A.groups_qk;
-        src = (const T *)p.v_raw; dst = (T *)p.v; sb = d.v_stride_b; st = d.v_stride_t;
+        src = (const T *)p.v_raw; dst = (typename Inter<T>::S *)p.v; sb = d.v_stride_b; st = d.v_stride_t;
         nch = d.Hv * d.dv; hd = d.dv; w_base = 2 * ch_qk; norm = false;
     }
+    using S = typename Inter<T>::S;
     const int c0 = g * (kThreads * CPT) + tid * CPT;
     const bool active = c0 < nch;
     const int lanes_per_head = hd / CPT;      // <= 32 for q/k by construction
@@ -161,7 +162,7 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
 
     const int head = c0 / hd;
     const int dd = c0 - head * hd;
-    T *dbase = dst + ((int64_t)head * p.ntok) * hd + dd;
+    S *dbase = dst + ((int64_t)head * p.ntok) * hd + dd;
 
     for (int base = 0; base < c.len; base += BATCH) {
         uint4 xr[BATCH][NVEC];
@@ -199,9 +200,9 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
                 for (int i = 0; i < CPT; ++i) y[i] *= inv;
             }
             if (active) {
-                T *op = dbase + (c.tok0 + base + u) * (int64_t)hd;
+                S *op = dbase + (c.tok0 + base + u) * (int64_t)hd;
 #pragma unroll
-                for (int v = 0; v < NVEC; ++v) store16_f<T>(op + v * VEC, y + v * VEC);
+                for (int v = 0; v < NVEC; ++v) store16_f<S>(op + v * VEC, y + v * VEC);
             }
         }
     }
@@ -231,22 +232,24 @@ __device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c) 
             bs[i][hh] = bv;
         }
         __syncthreads();
+        using GT = typename Inter<T>::G;
+        GT *gamma = (GT *)p.gamma;
         for (int hh = warp; hh < nh; hh += kThreads / 32) {
-            const float g0 = gs[2 * lane][hh], g1 = gs[2 * lane + 1][hh];
-            float x = g0 + g1;
+            const GT g0 = gs[2 * lane][hh], g1 = gs[2 * lane + 1][hh];
+            GT x = g0 + g1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                const GT y = __shfl_up_sync(0xffffffffu, x, off);
                 if (lane >= off) x += y;
             }
-            const float excl = x - (g0 + g1);
+            const GT excl = x - (g0 + g1);
             const int64_t row = (int64_t)(h0 + hh) * p.ntok + c.tok0;
             if (2 * lane < c.len) {
-                p.gamma[row + 2 * lane] = excl + g0;
+                gamma[row + 2 * lane] = excl + g0;
                 p.beta[row + 2 * lane] = bs[2 * lane][hh];
             }
             if (2 * lane + 1 < c.len) {
-                p.gamma[row + 2 * lane + 1] = excl + g0 + g1;
+                gamma[row + 2 * lane + 1] = excl + g0 + g1;
                 p.beta[row + 2 * lane + 1] = bs[2 * lane + 1][hh];
             }
         }

@@ -24,6 +24,7 @@ GDN_ERR_UNSUPPORTED = -2
 GDN_ERR_WORKSPACE = -3
 GDN_ERR_CUDA = -4
 GDN_ERR_DEVICE_SEQLENS = -5
+GDN_ERR_DEVICE_RANGE = -6
 
 GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 DTYPE_CODES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
@@ -227,10 +228,13 @@ class Buffers:
         d = self.desc
         lay = gdn_workspace_offsets(d)
         ntok = d.B * d.T
-        act = ACT_TORCH[d.dtype]
-        shapes = {"q": ((d.Hk, ntok, d.dk), act), "k": ((d.Hk, ntok, d.dk), act),
-                  "v": ((d.Hv, ntok, d.dv), act), "beta": ((d.Hv, ntok), torch.float32),
-                  "gamma": ((d.Hv, ntok), torch.float32), "o": ((ntok, d.Hv, d.dv), act),
+        # intermediates: fp16 for bf16/fp16 activations, fp32 for fp32; the
+        # cumulative decay is fp64 for fp32 activations
+        st = torch.float32 if d.dtype == GDN_F32 else torch.float16
+        gt = torch.float64 if d.dtype == GDN_F32 else torch.float32
+        shapes = {"q": ((d.Hk, ntok, d.dk), st), "k": ((d.Hk, ntok, d.dk), st),
+                  "v": ((d.Hv, ntok, d.dv), st), "beta": ((d.Hv, ntok), torch.float32),
+                  "gamma": ((d.Hv, ntok), gt), "o": ((ntok, d.Hv, d.dv), st),
                   "status": ((1,), torch.int32), "chunk_off": ((d.N + 1,), torch.int32)}
         shape, dt = shapes[name]
         off = getattr(lay, name)

@@ -113,7 +113,7 @@ def test_workspace_layout(lib):
 
 
 def test_status_strings(lib):
-    for s in (0, -1, -2, -3, -4, -5):
+    for s in (0, -1, -2, -3, -4, -5, -6):
         assert gdn.status_string(s) not in ("", "unknown status")
     assert gdn.status_string(42) == "unknown status"
 
