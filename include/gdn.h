@@ -102,9 +102,11 @@ int gdn_workspace_bytes(const gdn_desc *d, size_t *bytes);
 
 /* Offsets (bytes from the workspace base) of the intermediate tensors, for
  * inspection by tests and tools:
- *   q, k [Hk][Ntok][dk] and v [Hv][Ntok][dv] (after conv, SiLU and, for q/k,
- *   L2 norm) and o [Ntok][Hv][dv] (gated delta rule output), stored in fp16 for
- *   bf16/fp16 activations and in fp32 for fp32 activations; beta [Hv][Ntok] fp32;
+ *   q, k [Hk][Ntok][dk] after conv, SiLU and L2 norm: fp32 for fp32
+ *   activations, else two fp16 planes (hi = fp16(x) at the offset, then
+ *   lo = fp16(x - hi) right after the Hk*Ntok*dk hi elements); v [Hv][Ntok][dv]
+ *   after conv and SiLU and o [Ntok][Hv][dv] (gated delta rule output): fp16 for
+ *   bf16/fp16 activations, fp32 for fp32 activations; beta [Hv][Ntok] fp32;
  *   gamma [Hv][Ntok] = in-chunk inclusive cumulative sum of g, fp64 for fp32
  *   activations and fp32 otherwise; status: int32 device status word;
  *   chunk_off: int32 [N+1]. */

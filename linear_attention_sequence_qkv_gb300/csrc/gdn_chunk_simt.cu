@@ -71,6 +71,12 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
     const GT *gw = (const GT *)p.gamma + (int64_t)j * p.ntok;
     const float *bw = p.beta + (int64_t)j * p.ntok;
     S *o = (S *)p.o;
+    // q/k: fp32, or fp16 hi + lo planes for 2-byte activations
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    auto load_qk = [&](const S *base, int64_t idx) -> float {
+        if (sizeof(S) == 4) return to_f<S>(base[idx]);
+        return to_f<S>(base[idx]) + to_f<S>(base[idx + plane]);
+    };
 
     // state slice
     const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
@@ -106,8 +112,8 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
             for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
                 const int i = idx / DS, c = idx - i * DS;
                 const bool ok = i < L && d0 + c < dk;
-                Ks[i * LDS + c] = ok ? to_f<S>(kq[(tok0 + i) * dk + d0 + c]) : 0.f;
-                Qs[i * LDS + c] = ok ? to_f<S>(qq[(tok0 + i) * dk + d0 + c]) : 0.f;
+                Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c) : 0.f;
+                Qs[i * LDS + c] = ok ? load_qk(qq, (tok0 + i) * dk + d0 + c) : 0.f;
             }
             __syncthreads();
             const int dn = min(DS, dk - d0);
@@ -234,7 +240,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
             for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
                 const int i = idx / DS, c = idx - i * DS;
                 const bool ok = i < L && d0 + c < dk;
-                Ks[i * LDS + c] = ok ? to_f<S>(kq[(tok0 + i) * dk + d0 + c]) *
+                Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c) *
                                            expf((float)(gam[kChunk - 1] - gam[i])) : 0.f;
             }
             __syncthreads();

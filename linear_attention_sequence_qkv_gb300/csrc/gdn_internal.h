@@ -17,12 +17,17 @@ struct Layout {
 
 inline size_t act_size(int dtype) { return dtype == GDN_F32 ? 4 : 2; }
 
-// Intermediates (q, k, v after the prologue, o after the chunk rule) are stored
+// Intermediates. v (after the prologue) and o (after the chunk rule) are stored
 // in fp16 for bf16 and fp16 activations (3 more mantissa bits than bf16 at the
-// same size) and in fp32 for fp32 activations. The in-chunk cumulative decay is
-// fp64 for fp32 activations (so that differences of large sums stay exact to
-// fp32 precision) and fp32 otherwise.
+// same size) and in fp32 for fp32 activations. The normalised q and k carry
+// about fp32 precision (the q.k products of nearly orthogonal pairs cancel, and
+// the output RMSNorm would amplify their rounding): fp32 for fp32 activations,
+// otherwise two fp16 planes hi = fp16(x), lo = fp16(x - hi), so that the tensor
+// cores can take both parts directly. The in-chunk cumulative decay is fp64 for
+// fp32 activations (differences of large sums stay exact to fp32 precision) and
+// fp32 otherwise.
 inline size_t gamma_size(int dtype) { return dtype == GDN_F32 ? 8 : 4; }
+inline size_t qk_size(int) { return 4; }   // fp32, or fp16 hi + fp16 lo
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -33,8 +38,8 @@ inline Layout make_layout(const gdn_desc &d) {
     size_t off = 0;
     L.status = off;    off = align_up(off + 256, 256);
     L.chunk_off = off; off = align_up(off + 4 * ((size_t)d.N + 1), 256);
-    L.q = off;         off = align_up(off + s * ntok * d.Hk * d.dk, 256);
-    L.k = off;         off = align_up(off + s * ntok * d.Hk * d.dk, 256);
+    L.q = off;         off = align_up(off + qk_size(d.dtype) * ntok * d.Hk * d.dk, 256);
+    L.k = off;         off = align_up(off + qk_size(d.dtype) * ntok * d.Hk * d.dk, 256);
     L.v = off;         off = align_up(off + s * ntok * d.Hv * d.dv, 256);
     L.beta = off;      off = align_up(off + 4 * ntok * d.Hv, 256);
     L.gamma = off;     off = align_up(off + gamma_size(d.dtype) * ntok * d.Hv, 256);

@@ -8,7 +8,8 @@
 //     "Summary": one depthwise conv over concatenated channels equals three);
 //   * per-head L2 norm of q and k, x * rsqrt(sum x^2 + eps), eps = 1e-6
 //     ("fold q/k L2-norm into the gated_delta_rule kernel", Megatron-LM PR #5396,
-//     "Why");
+//     "Why"); q and k leave as fp32, or for 2-byte activations as two fp16
+//     planes hi + lo carrying about fp32 precision;
 //   * beta = sigmoid(b), g = -exp(A_log) * softplus(a + dt_bias) and the
 //     inclusive cumulative sum of g inside each 64-token chunk.
 // Grid: x = chunk slot (one 64-token chunk of one sequence), y = channel group
@@ -163,6 +164,9 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
     const int head = c0 / hd;
     const int dd = c0 - head * hd;
     S *dbase = dst + ((int64_t)head * p.ntok) * hd + dd;
+    // q/k of 2-byte activations: hi plane here, lo plane `plane` elements further
+    const bool split = norm && sizeof(S) == 2;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * d.dk;
 
     for (int base = 0; base < c.len; base += BATCH) {
         uint4 xr[BATCH][NVEC];
@@ -203,6 +207,13 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
                 S *op = dbase + (c.tok0 + base + u) * (int64_t)hd;
 #pragma unroll
                 for (int v = 0; v < NVEC; ++v) store16_f<S>(op + v * VEC, y + v * VEC);
+                if (split) {   // lo plane: what fp16 rounding of y left out
+                    float lo[CPT];
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) lo[i] = y[i] - round_through<S>(y[i]);
+#pragma unroll
+                    for (int v = 0; v < NVEC; ++v) store16_f<S>(op + plane + v * VEC, lo + v * VEC);
+                }
             }
         }
     }

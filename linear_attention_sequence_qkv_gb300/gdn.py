@@ -232,7 +232,8 @@ class Buffers:
         # cumulative decay is fp64 for fp32 activations
         st = torch.float32 if d.dtype == GDN_F32 else torch.float16
         gt = torch.float64 if d.dtype == GDN_F32 else torch.float32
-        shapes = {"q": ((d.Hk, ntok, d.dk), st), "k": ((d.Hk, ntok, d.dk), st),
+        qk = (d.Hk, ntok, d.dk) if d.dtype == GDN_F32 else (2, d.Hk, ntok, d.dk)  # hi, lo planes
+        shapes = {"q": (qk, st), "k": (qk, st),
                   "v": ((d.Hv, ntok, d.dv), st), "beta": ((d.Hv, ntok), torch.float32),
                   "gamma": ((d.Hv, ntok), gt), "o": ((ntok, d.Hv, d.dv), st),
                   "status": ((1,), torch.int32), "chunk_off": ((d.N + 1,), torch.int32)}

@@ -198,16 +198,21 @@ def test_prologue_intermediates(dev, name):
     # intermediates are stored in fp16 for bf16/fp16 activations, fp32 for fp32
     rnd = torch.float32 if w.dtype == "fp32" else torch.float16
     as_act = lambda x: torch.from_numpy(x).to(rnd).double().numpy()
-    q = as_act(O.l2norm(O.conv_silu(flat(inp.q_raw), cw[:ch], s), w.dk))
-    k = as_act(O.l2norm(O.conv_silu(flat(inp.k_raw), cw[ch:2 * ch], s), w.dk))
-    v = as_act(O.conv_silu(flat(inp.v_raw), cw[2 * ch:], s))
+    q = O.l2norm(O.conv_silu(flat(inp.q_raw), cw[:ch], s), w.dk)
+    k = O.l2norm(O.conv_silu(flat(inp.k_raw), cw[ch:2 * ch], s), w.dk)
+    v = O.conv_silu(flat(inp.v_raw), cw[2 * ch:], s)
     tol = 1e-5 if w.dtype == "fp32" else 2.0 ** -9
     for name_, ref, hd, H in (("q", q, w.dk, w.Hk), ("k", k, w.dk, w.Hk), ("v", v, w.dv, w.Hv)):
-        got = bufs.ws_view(name_).double().cpu().numpy()          # [H][ntok][d]
-        ref = ref.reshape(-1, H, hd).transpose(1, 0, 2)
-        err = np.abs(got - ref).max()
+        got = bufs.ws_view(name_).double().cpu().numpy()
+        ref = ref.reshape(-1, H, hd).transpose(1, 0, 2)           # [H][ntok][d]
+        if name_ == "v":                    # stored in the intermediate dtype
+            err, bound = np.abs(got - as_act(ref)).max(), tol
+        elif w.dtype == "fp32":
+            err, bound = np.abs(got - ref).max(), 1e-5
+        else:                               # fp16 hi + lo planes: about fp32 precision
+            err, bound = np.abs(got[0] + got[1] - ref).max(), 2e-6
         print(f"[prologue] {name}: {name_} max abs {err:.3e}")
-        assert err <= tol * max(1.0, np.abs(ref).max())
+        assert err <= bound * max(1.0, np.abs(ref).max())
     beta, g = O.beta_decay(flat(inp.a), flat(inp.b), inp.A_log.numpy(), inp.dt_bias.numpy())
     gam = np.zeros_like(g)
     for s0, s1 in zip(s[:-1], s[1:]):
