@@ -170,6 +170,37 @@ int gdn_device_status(const void *workspace, int *status, gdn_stream_t stream);
 /* Static description of a status code. */
 const char *gdn_status_string(int status);
 
+/*
+ * gdn_forward without a caller-provided workspace, for callers that cannot
+ * allocate device memory (code running inside another framework's memory
+ * arena, plugins without an allocator, hosts that forbid allocation while
+ * serving). The pages describe no such entry point; it has no counterpart there.
+ *
+ * The scratch is a fixed device array of GDN_STATIC_WORKSPACE_BYTES inside the
+ * library; every GPU that loads the library holds it until the process exits.
+ * Arguments and results are those of gdn_forward (same pointers, layouts and
+ * status codes, without workspace and workspace_bytes).
+ *  - Problems whose gdn_workspace_bytes() exceeds GDN_STATIC_WORKSPACE_BYTES are
+ *    rejected with GDN_ERR_WORKSPACE before anything is launched.
+ *  - The device is the current CUDA device; `stream` must belong to it. The
+ *    first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ *    routine).
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents: calls that overlap on the GPU (different streams, or host
+ *    threads racing on one device) race on it and must be serialised by the
+ *    caller.
+ */
+#define GDN_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+int gdn_forward_static_ws(const gdn_desc *d,
+                          const void *q_raw, const void *k_raw, const void *v_raw,
+                          const void *a, const void *b, const void *gate,
+                          const void *conv_w, const float *A_log, const float *dt_bias,
+                          const void *norm_w, const int32_t *cu_seqlens,
+                          const float *initial_state, void *out, float *final_state,
+                          gdn_stream_t stream);
+
 /* Which gated-delta-rule kernel serves *d: 0 = fp32 CUDA-core kernel,
  * 1 = tcgen05 tensor-core kernel (bf16/fp16). */
 int gdn_chunk_kernel_kind(const gdn_desc *d);

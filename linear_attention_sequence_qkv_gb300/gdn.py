@@ -33,7 +33,10 @@ ACT_TORCH = {GDN_F32: torch.float32, GDN_BF16: torch.bfloat16, GDN_F16: torch.fl
 # every entry point declared in include/gdn.h
 EXPORTS = ("gdn_desc_init", "gdn_workspace_bytes", "gdn_workspace_offsets", "gdn_forward",
            "gdn_prologue", "gdn_chunk_rule", "gdn_epilogue", "gdn_device_status",
-           "gdn_status_string", "gdn_chunk_kernel_kind")
+           "gdn_status_string", "gdn_chunk_kernel_kind", "gdn_forward_static_ws")
+
+# bytes of the library's fixed device scratch used by gdn_forward_static_ws
+GDN_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
 class GdnError(RuntimeError):
@@ -89,6 +92,7 @@ def load(path: str = LIB_PATH):
     L.gdn_status_string.argtypes = [i32]
     L.gdn_status_string.restype = ctypes.c_char_p
     L.gdn_chunk_kernel_kind.argtypes = [dp]
+    L.gdn_forward_static_ws.argtypes = [dp] + [vp] * 14 + [vp]
     for name in EXPORTS:
         if name != "gdn_status_string":
             getattr(L, name).restype = i32
@@ -151,6 +155,21 @@ def gdn_forward(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm
                             _stream(stream))
     if check:
         _check(rc, "gdn_forward")
+    return rc
+
+
+def gdn_forward_static_ws(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
+                          cu_seqlens, initial_state, out, final_state, stream=None,
+                          check=True) -> int:
+    """gdn_forward on the library's fixed device scratch (no workspace argument):
+    for callers that cannot allocate device memory."""
+    rc = load().gdn_forward_static_ws(ctypes.byref(d), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw),
+                                      _ptr(a), _ptr(b), _ptr(gate), _ptr(conv_w), _ptr(A_log),
+                                      _ptr(dt_bias), _ptr(norm_w), _ptr(cu_seqlens),
+                                      _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                      _stream(stream))
+    if check:
+        _check(rc, "gdn_forward_static_ws")
     return rc
 
 
