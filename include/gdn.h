@@ -55,9 +55,11 @@ typedef enum {
     GDN_ERR_CUDA = -4,         /* a CUDA launch or query failed */
     GDN_ERR_DEVICE_SEQLENS = -5, /* (device status) cu_seqlens not 0-based, not
                                     non-decreasing or not ending at T */
-    GDN_ERR_DEVICE_RANGE = -6   /* (device status) a non-finite gated-delta-rule output
+    GDN_ERR_DEVICE_RANGE = -6,  /* (device status) a non-finite gated-delta-rule output
                                    reached the epilogue: a non-finite input, or a value
                                    beyond the fp16 range of the intermediates */
+    GDN_ERR_DEVICE_TIMEOUT = -7 /* (device status) a tensor-core kernel gave up waiting
+                                   (about 1 s) for a copy or an MMA; results are invalid */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
@@ -109,9 +111,10 @@ int gdn_workspace_bytes(const gdn_desc *d, size_t *bytes);
  *   bf16/fp16 activations, fp32 for fp32 activations; beta [Hv][Ntok] fp32;
  *   gamma [Hv][Ntok] = in-chunk inclusive cumulative sum of g, fp64 for fp32
  *   activations and fp32 otherwise; status: int32 device status word;
- *   chunk_off: int32 [N+1]. */
+ *   chunk_off: int32 [N+1]; tpt: per (v head, chunk) the 128x64 fp16 tile
+ *   [T; P T] of the tensor-core kernels (empty where they do not run). */
 typedef struct {
-    size_t status, chunk_off, q, k, v, beta, gamma, o, total;
+    size_t status, chunk_off, q, k, v, beta, gamma, o, tpt, total;
 } gdn_workspace_layout;
 int gdn_workspace_offsets(const gdn_desc *d, gdn_workspace_layout *layout);
 
@@ -163,8 +166,8 @@ int gdn_epilogue(const gdn_desc *d, const void *gate, const void *norm_w, void *
                  void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /* Wait for `stream`, then read the device status word of the last forward that
- * used `workspace` into *status (GDN_OK, GDN_ERR_DEVICE_SEQLENS or
- * GDN_ERR_DEVICE_RANGE). This call synchronises the stream. */
+ * used `workspace` into *status (GDN_OK or a GDN_ERR_DEVICE_* code). This call
+ * synchronises the stream. */
 int gdn_device_status(const void *workspace, int *status, gdn_stream_t stream);
 
 /* Static description of a status code. */

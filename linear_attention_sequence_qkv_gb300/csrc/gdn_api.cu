@@ -67,6 +67,7 @@ Problem base_problem(const gdn_desc *d, const int32_t *cu, void *ws) {
     p.beta = (float *)(w + L.beta);
     p.gamma = w + L.gamma;
     p.o = w + L.o;
+    p.tpt = w + L.tpt;
     return p;
 }
 
@@ -145,6 +146,7 @@ int gdn_workspace_offsets(const gdn_desc *d, gdn_workspace_layout *out) {
     out->beta = L.beta;
     out->gamma = L.gamma;
     out->o = L.o;
+    out->tpt = L.tpt;
     out->total = L.total;
     return GDN_OK;
 }
@@ -261,6 +263,7 @@ const char *gdn_status_string(int status) {
     case GDN_ERR_CUDA: return "CUDA launch or query failed";
     case GDN_ERR_DEVICE_SEQLENS: return "cu_seqlens malformed (device check)";
     case GDN_ERR_DEVICE_RANGE: return "non-finite intermediate (device check)";
+    case GDN_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
     default: return "unknown status";
     }
 }

@@ -1,11 +1,681 @@
 // gdn_chunk_tc.cu -- chunked gated delta rule on the tcgen05 tensor cores
-// (bf16/fp16 activations). Not yet routed: every dtype uses the CUDA-core kernel.
+// (bf16/fp16 activations; fp16 operands, fp32 accumulators in tensor memory).
+//
+// Per chunk of 64 tokens (gam = in-chunk cumulative decay, H = S^T [dk][dv]):
+//   A   = strict_lower( beta_i exp(gam_i - gam_j) k_i.k_j ),  P = lower( exp(gam_i - gam_j) q_i.k_j )
+//   T   = (I + A)^{-1}
+//   R   = diag(beta) (V - diag(exp(gam)) K H)
+//   [Vn; P Vn] = [T; P T] R
+//   O   = diag(exp(gam)) Q H + P Vn
+//   H  <- exp(gam_L) H + K^T diag(exp(gam_L - gam)) Vn
+// Two kernels:
+//  * prep (one CTA per chunk and v head, fully parallel): [K;Q] K^T on the
+//    tensor cores in split precision (q and k arrive as fp16 hi + lo planes;
+//    hi*hi + hi*lo + lo*hi recovers ~fp32 dot products, which the output RMSNorm
+//    needs for nearly orthogonal q, k), decay masks, the 64x64 unit-triangular
+//    solve on CUDA cores in fp32, then P T on the tensor cores. Writes the
+//    [T; P T] tile (128 x 64 fp16, 16 KB) already in the 128-byte-swizzled
+//    layout, so the chain kernel fetches it with one bulk copy.
+//  * chain (one CTA per sequence, v head and 64-column dv tile): the state slice
+//    H [dk][64] stays in tensor memory in fp32 across chunks (an fp16 copy in
+//    shared memory feeds the next MMA); per chunk three dependent MMAs
+//    [K; Q e^gam] H, [T; P T] R and K^T Vn'. Inputs of chunk c+1 (and c+2) are
+//    fetched by TMA while chunk c computes.
+// Every wait on an mbarrier gives up after about a second; the kernel then
+// records GDN_ERR_DEVICE_TIMEOUT in the status word, waits (bounded) for its own
+// copies and MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "gdn_common.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
+namespace {
 
-bool chunk_tc_supports(const gdn_desc &) { return false; }
+using namespace tc;
 
-cudaError_t launch_chunk_tc(const Problem &, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kThreads = 128;
+constexpr int LDA = kChunk + 1;
+constexpr uint32_t kTileBytes = 64 * 128;      // one 64x64 fp16 tile (8 KB)
+constexpr uint32_t kTPTBytes = 2 * kTileBytes; // [T; P T] 128x64 fp16
+
+struct PrepMaps {
+    CUtensorMap q_hi, q_lo, k_hi, k_lo;
+};
+struct ChainMaps {
+    CUtensorMap q_hi, k_hi, v;
+};
+
+__device__ __forceinline__ void set_timeout(const Problem &p) {
+    atomicCAS(p.status, GDN_OK, GDN_ERR_DEVICE_TIMEOUT);
+}
+
+// row of 64 fp32 -> fp16, written into a 128-byte-swizzled tile row
+__device__ __forceinline__ void store_row_f16(unsigned char *tile, int row, const float *v64) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 u;
+        __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v64[8 * c + 2 * e], v64[8 * c + 2 * e + 1]);
+        *reinterpret_cast<uint4 *>(tile + sw128_off(row, 8 * c)) = u;
+    }
+}
+
+__device__ __forceinline__ void load_row_f16(const unsigned char *tile, int row, float *v64) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_off(row, 8 * c));
+        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(h[e]);
+            v64[8 * c + 2 * e] = f.x;
+            v64[8 * c + 2 * e + 1] = f.y;
+        }
+    }
+}
+
+// 64 fp32 columns of this thread's lane
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
+#pragma unroll
+    for (int c = 0; c < 64; c += 16) tmem_ld16(taddr + c, v + c);
+}
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const float *v) {
+#pragma unroll
+    for (int c = 0; c < 64; c += 16) tmem_st16(taddr + c, v + c);
+}
+
+// ================================================================ prep kernel
+struct PrepSmem {
+    int blocks;            // dk / 64
+    size_t hi, lo, As, Ts, Xs, tp, gam, bet, bars, total;
+    __host__ __device__ PrepSmem(int dk) {
+        blocks = dk / 64;
+        size_t o = 0;
+        hi = o; o += (size_t)blocks * 2 * kTileBytes;
+        lo = o;                                      // lo stack; reused by the solve after S1
+        As = lo;
+        Ts = As + kChunk * LDA * 4;
+        Xs = Ts + kChunk * LDA * 4;
+        size_t solve_end = Xs + 768 * 4;
+        size_t lo_end = lo + (size_t)blocks * 2 * kTileBytes;
+        o = (solve_end > lo_end ? solve_end : lo_end);
+        o = (o + 1023) & ~(size_t)1023;
+        tp = o; o += kTPTBytes;
+        gam = o; o += kChunk * 4;
+        bet = o; o += kChunk * 4;
+        bars = o; o += 64;
+        total = o + 1024;    // slack for aligning the base to 1024 B
+    }
+};
+
+__global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
+                                                              const Problem p, int64_t nslots,
+                                                              unsigned char *tpt) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    const gdn_desc &d = p.d;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int j = blockIdx.y;
+    const int64_t slot = blockIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    ChunkLoc c;
+    if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, c)) return;
+    const int hk = j / (d.Hv / d.Hk);
+    const PrepSmem L(d.dk);
+    unsigned char *hi = sm + L.hi, *lo = sm + L.lo, *tp = sm + L.tp;
+    float *As = (float *)(sm + L.As), *Ts = (float *)(sm + L.Ts), *Xs = (float *)(sm + L.Xs);
+    float *gam = (float *)(sm + L.gam), *bet = (float *)(sm + L.bet);
+    uint64_t *bar_load = (uint64_t *)(sm + L.bars), *bar_mma = bar_load + 1;
+    uint32_t *tslot = (uint32_t *)(bar_load + 2);
+    __shared__ int s_err;
+
+    if (tid == 0) {
+        s_err = 0;
+        mbar_init(bar_load, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) tmem_alloc(tslot, 128);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *tslot;
+    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    bool load_out = false, mma_out = false;
+
+    if (tid == 0) {
+        mbar_expect_tx(bar_load, (uint32_t)L.blocks * 4 * kTileBytes);
+        const int y = (int)((int64_t)hk * p.ntok + c.tok0);
+        for (int b = 0; b < L.blocks; ++b) {
+            tma_load_2d(hi + b * 2 * kTileBytes, &maps.k_hi, 64 * b, y, bar_load);
+            tma_load_2d(hi + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, y, bar_load);
+            tma_load_2d(lo + b * 2 * kTileBytes, &maps.k_lo, 64 * b, y, bar_load);
+            tma_load_2d(lo + b * 2 * kTileBytes + kTileBytes, &maps.q_lo, 64 * b, y, bar_load);
+        }
+    }
+    load_out = true;
+    if (tid < kChunk) {
+        const float *gw = (const float *)p.gamma + (int64_t)j * p.ntok;
+        const int i = tid < c.len ? tid : c.len - 1;
+        gam[tid] = gw[c.tok0 + i];
+        bet[tid] = tid < c.len ? p.beta[(int64_t)j * p.ntok + c.tok0 + tid] : 0.f;
+    }
+    if (!mbar_wait(bar_load, 0)) s_err = 1;
+    __syncthreads();
+    if (s_err) goto cleanup;
+    load_out = false;
+
+    // S1 = [Kh;Qh] Kh^T + [Kh;Qh] Kl^T + [Kl;Ql] Kh^T  -> TMEM cols [0, 64)
+    if (tid == 0) {
+        const uint32_t id = idesc_f16(128, 64, false, false);
+        for (int b = 0; b < L.blocks; ++b)
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t oh = smem_u32(hi + b * 2 * kTileBytes) + 32 * ks;
+                const uint32_t ol = smem_u32(lo + b * 2 * kTileBytes) + 32 * ks;
+                const uint64_t ah = sw128_desc(oh, 16, 1024), al = sw128_desc(ol, 16, 1024);
+                mma_f16(tbase, ah, ah, id, (b | ks) != 0);
+                mma_f16(tbase, ah, al, id, 1);
+                mma_f16(tbase, al, ah, id, 1);
+            }
+        mma_commit(bar_mma);
+    }
+    mma_out = true;
+    if (!mbar_wait(bar_mma, 0)) s_err = 1;
+    __syncthreads();
+    if (s_err) goto cleanup;
+    mma_out = false;
+    fence_after_sync();
+
+    {   // decay masks: rows 0..63 -> A (fp32, solve input); rows 64..127 -> P (fp16 tile)
+        float v[64];
+        tmem_ld64(lane_addr, v);
+        if (tid < kChunk) {
+            const int i = tid;
+            for (int jj = 0; jj < kChunk; ++jj)
+                As[i * LDA + jj] = jj < i ? bet[i] * expf(gam[i] - gam[jj]) * v[jj] : 0.f;
+        } else {
+            const int i = tid - kChunk;
+            for (int jj = 0; jj < kChunk; ++jj) v[jj] = jj <= i ? expf(gam[i] - gam[jj]) * v[jj] : 0.f;
+            store_row_f16(tp, tid, v);
+        }
+    }
+    for (int e = tid; e < kChunk * LDA; e += kThreads) Ts[e] = 0.f;
+    fence_before_sync();
+    __syncthreads();
+    // T = (I + A)^{-1}: 16x16 diagonal blocks by forward substitution ...
+    if (tid < kChunk) {
+        const int blk = tid >> 4, cc = tid & 15, o0 = blk * 16;
+        for (int r = cc; r < 16; ++r) {
+            float val = (r == cc) ? 1.f : 0.f;
+            for (int m = cc; m < r; ++m) val -= As[(o0 + r) * LDA + o0 + m] * Ts[(o0 + m) * LDA + o0 + cc];
+            Ts[(o0 + r) * LDA + o0 + cc] = val;
+        }
+    }
+    __syncthreads();
+    // ... then one block diagonal at a time: T[bi][bj] = -T[bi][bi] sum_m A[bi][m] T[m][bj]
+    for (int dd = 1; dd < 4; ++dd) {
+        const int npairs = 4 - dd;
+        for (int e = tid; e < npairs * 256; e += kThreads) {
+            const int pr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int bj = pr, bi = pr + dd;
+            float x = 0.f;
+            for (int m = bj * 16; m < bi * 16; ++m) x += As[(bi * 16 + r) * LDA + m] * Ts[m * LDA + bj * 16 + cc];
+            Xs[pr * 256 + r * 16 + cc] = x;
+        }
+        __syncthreads();
+        for (int e = tid; e < npairs * 256; e += kThreads) {
+            const int pr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int bj = pr, bi = pr + dd;
+            float t = 0.f;
+            for (int m = 0; m < 16; ++m) t += Ts[(bi * 16 + r) * LDA + bi * 16 + m] * Xs[pr * 256 + m * 16 + cc];
+            Ts[(bi * 16 + r) * LDA + bj * 16 + cc] = -t;
+        }
+        __syncthreads();
+    }
+    if (tid < kChunk) {   // T rows into the fp16 tile (rows 0..63)
+        float v[64];
+        for (int jj = 0; jj < kChunk; ++jj) v[jj] = Ts[tid * LDA + jj];
+        store_row_f16(tp, tid, v);
+    }
+    fence_async_smem();
+    __syncthreads();
+    // P T: A = [T; P] (K-major), B = T (MN-major, rows 0..63 of the same tile) -> cols [64, 128)
+    if (tid == 0) {
+        const uint32_t id = idesc_f16(128, 64, false, true);
+        for (int ks = 0; ks < 4; ++ks)
+            mma_f16(tbase + 64, sw128_desc(smem_u32(tp) + 32 * ks, 16, 1024),
+                    sw128_desc(smem_u32(tp) + 2048 * ks, 8192, 1024), id, ks != 0);
+        mma_commit(bar_mma);
+    }
+    mma_out = true;
+    if (!mbar_wait(bar_mma, 1)) s_err = 1;
+    __syncthreads();
+    if (s_err) goto cleanup;
+    mma_out = false;
+    fence_after_sync();
+    if (tid >= kChunk) {   // P T replaces P in rows 64..127
+        float v[64];
+        tmem_ld64(lane_addr + 64, v);
+        store_row_f16(tp, tid, v);
+    }
+    __syncthreads();
+    {
+        uint4 *dst = reinterpret_cast<uint4 *>(tpt + ((int64_t)j * nslots + slot) * kTPTBytes);
+        const uint4 *src = reinterpret_cast<const uint4 *>(tp);
+        for (int e = tid; e < (int)(kTPTBytes / 16); e += kThreads) dst[e] = src[e];
+    }
+
+cleanup:
+    if (s_err) {
+        if (tid == 0) {
+            set_timeout(p);
+            if (load_out) mbar_wait(bar_load, 0);
+            if (mma_out) { mbar_wait(bar_mma, 0); mbar_wait(bar_mma, 1); }
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 128);
+}
+
+// =============================================================== chain kernel
+struct ChainSmem {
+    int blocks, stages;
+    size_t stage_bytes, stack, v, tpt, h16, r16, vn16, gam, bet, bars, total;
+    __host__ __device__ ChainSmem(int dk, int nstages) {
+        blocks = dk / 64;
+        stages = nstages;
+        stack = 0;
+        v = (size_t)blocks * 2 * kTileBytes;
+        tpt = v + kTileBytes;
+        stage_bytes = tpt + kTPTBytes;
+        size_t o = stage_bytes * stages;
+        h16 = o; o += (size_t)(dk < 128 ? 128 : dk) * 128;
+        r16 = o; o += kTileBytes;
+        vn16 = o; o += kTileBytes;
+        gam = o; o += 2 * kChunk * 4;
+        bet = o; o += 2 * kChunk * 4;
+        bars = o; o += 64;
+        total = o + 1024;
+    }
+};
+
+__global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_constant__ ChainMaps maps,
+                                                               const Problem p, int ntiles, int nstages,
+                                                               int64_t nslots, const unsigned char *tpt) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    const gdn_desc &d = p.d;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    int bid = blockIdx.x;
+    const int tile = bid % ntiles;
+    bid /= ntiles;
+    const int j = bid % d.Hv;
+    const int n = bid / d.Hv;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    const int hk = j / (Hv / d.Hk);
+    const int v0 = tile * 64;
+    const int64_t seq0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
+    const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : seq0 + d.T;
+    const int nchunks = (int)((seq1 - seq0 + kChunk - 1) / kChunk);
+    const int64_t slot0 = p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk);
+    const ChainSmem L(dk, nstages);
+    const int halves = dk >= 128 ? dk / 128 : 1;  // M=128 row groups of the state
+    unsigned char *h16 = sm + L.h16, *r16 = sm + L.r16, *vn16 = sm + L.vn16;
+    float *gam_s = (float *)(sm + L.gam), *bet_s = (float *)(sm + L.bet);
+    uint64_t *bar_load = (uint64_t *)(sm + L.bars);   // [2]
+    uint64_t *bar_mma = bar_load + 2;
+    uint32_t *tslot = (uint32_t *)(bar_load + 3);
+    __shared__ int s_err;
+    const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
+    const float *gw = (const float *)p.gamma + (int64_t)j * p.ntok;
+    const float *bw = p.beta + (int64_t)j * p.ntok;
+    __half *o = (__half *)p.o;
+
+    if (tid == 0) {
+        s_err = 0;
+        mbar_init(&bar_load[0], 1);
+        mbar_init(&bar_load[1], 1);
+        mbar_init(bar_mma, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *tslot;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tD1 = tbase, tD2 = tbase + 64, tDH = tbase + 128;   // D_H half h at +64h
+    uint32_t mma_phase = 0;
+    int loads_in_flight = 0;      // bitmask of stages with outstanding TMA
+    uint32_t load_uses[2] = {0, 0};
+
+    auto issue_loads = [&](int cidx) {   // thread 0 only
+        const int s = cidx % nstages;
+        unsigned char *st = sm + s * L.stage_bytes;
+        const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
+        const int yk = (int)((int64_t)hk * p.ntok + tok0);
+        const int yv = (int)((int64_t)j * p.ntok + tok0);
+        mbar_expect_tx(&bar_load[s], (uint32_t)L.blocks * 2 * kTileBytes + kTileBytes + kTPTBytes);
+        for (int b = 0; b < L.blocks; ++b) {
+            tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar_load[s]);
+            tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar_load[s]);
+        }
+        tma_load_2d(st + L.v, &maps.v, v0, yv, &bar_load[s]);
+        bulk_load(st + L.tpt, tpt + ((int64_t)j * nslots + slot0 + cidx) * kTPTBytes, kTPTBytes,
+                  &bar_load[s]);
+    };
+    auto load_gb = [&](int cidx, float &g, float &b) {   // threads < 64
+        const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
+        const int len = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
+        const int i = tid < len ? tid : len - 1;
+        g = gw[tok0 + i];
+        b = tid < len ? bw[tok0 + i] : 0.f;
+    };
+
+    // initial state: fp32 into TMEM (D_H), fp16 copy into h16 (MN-major B operand)
+    for (int h = 0; h < halves; ++h) {
+        const int row = 128 * h + tid;
+        float v[64];
+        if (row < dk && p.h0) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)row * dv + v0);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float4 f = src[q];
+                v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 64; ++q) v[q] = 0.f;
+        }
+        tmem_st64(tDH + 64 * h + lane_off, v);
+        if (row < dk) store_row_f16(h16, row, v);
+    }
+    if (nchunks > 0) {
+        if (tid == 0) {
+            for (int cidx = 0; cidx < nstages && cidx < nchunks; ++cidx) {
+                issue_loads(cidx);
+                loads_in_flight |= 1 << cidx;
+            }
+        }
+        if (tid < kChunk) load_gb(0, gam_s[tid], bet_s[tid]);
+    }
+    float g_next = 0.f, b_next = 0.f;
+    if (tid < kChunk && nchunks > 1) load_gb(1, g_next, b_next);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+
+    for (int cidx = 0; cidx < nchunks; ++cidx) {
+        const int s = cidx % nstages;
+        const int gs = cidx & 1;                 // gamma/beta double buffer
+        unsigned char *st = sm + s * L.stage_bytes;
+        const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
+        const int len = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
+        const float *gam = gam_s + gs * kChunk, *bet = bet_s + gs * kChunk;
+
+        if (!mbar_wait(&bar_load[s], load_uses[s] & 1)) s_err = 1;
+        __syncthreads();
+        if (s_err) break;
+        load_uses[s]++;
+        if (tid == 0) loads_in_flight &= ~(1 << s);
+        // Q rows of the stack -> Q e^gam, in place (row scaling ignores the swizzle)
+        for (int e = tid; e < L.blocks * kChunk * 8; e += kThreads) {
+            const int b = e / (kChunk * 8), r = (e >> 3) & 63, ch = e & 7;
+            uint4 *pp = reinterpret_cast<uint4 *>(st + b * 2 * kTileBytes + kTileBytes + r * 128 + ch * 16);
+            uint4 u = *pp;
+            __half2 *hh = reinterpret_cast<__half2 *>(&u);
+            const __half2 sc = __float2half2_rn(expf(gam[r]));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) hh[q] = __hmul2(hh[q], sc);
+            *pp = u;
+        }
+        fence_async_smem();
+        __syncthreads();
+        // C1: D1 = [K; Q e^gam] H   (A K-major from the stack, B = h16 MN-major)
+        if (tid == 0) {
+            const uint32_t id = idesc_f16(128, 64, false, true);
+            for (int b = 0; b < L.blocks; ++b)
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tD1, sw128_desc(smem_u32(st + b * 2 * kTileBytes) + 32 * ks, 16, 1024),
+                            sw128_desc(smem_u32(h16) + (b * 4 + ks) * 2048, 8192, 1024), id,
+                            (b | ks) != 0);
+            mma_commit(bar_mma);
+        }
+        if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
+        mma_phase++;
+        __syncthreads();
+        if (s_err) break;
+        fence_after_sync();
+        // E1: R = beta (V - e^gam K H) -> r16 (rows = tokens, MN-major B of C2)
+        if (tid < kChunk) {
+            float kh[64], vv[64];
+            tmem_ld64(tD1 + lane_off, kh);
+            load_row_f16(st + L.v, tid, vv);
+            const float eg = expf(gam[tid]), bb = bet[tid];
+#pragma unroll
+            for (int q = 0; q < 64; ++q) kh[q] = bb * (vv[q] - eg * kh[q]);
+            store_row_f16(r16, tid, kh);
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        // C2: D2 = [T; P T] R
+        if (tid == 0) {
+            const uint32_t id = idesc_f16(128, 64, false, true);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16(tD2, sw128_desc(smem_u32(st + L.tpt) + 32 * ks, 16, 1024),
+                        sw128_desc(smem_u32(r16) + 2048 * ks, 8192, 1024), id, ks != 0);
+            mma_commit(bar_mma);
+        }
+        if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
+        mma_phase++;
+        __syncthreads();
+        if (s_err) break;
+        fence_after_sync();
+        // E2: Vn' = e^{gam_L - gam} Vn -> vn16; O = e^gam Q H + P Vn -> o; H *= e^{gam_L}
+        {
+            const float gL = gam[kChunk - 1];
+            float a[64];
+            if (tid < kChunk) {
+                tmem_ld64(tD2 + lane_off, a);
+                const float sc = expf(gL - gam[tid]);
+#pragma unroll
+                for (int q = 0; q < 64; ++q) a[q] *= sc;
+                store_row_f16(vn16, tid, a);
+            } else {
+                const int i = tid - kChunk;
+                float b2[64];
+                tmem_ld64(tD1 + lane_off, a);
+                tmem_ld64(tD2 + lane_off, b2);
+                if (i < len) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0);
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint4 u;
+                        __half2 *hh = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            hh[e] = __floats2half2_rn((a[8 * ch + 2 * e] + b2[8 * ch + 2 * e]) * d.scale,
+                                                      (a[8 * ch + 2 * e + 1] + b2[8 * ch + 2 * e + 1]) * d.scale);
+                        dst[ch] = u;
+                    }
+                }
+            }
+            const float eL = expf(gL);
+            for (int h = 0; h < halves; ++h) {
+                tmem_ld64(tDH + 64 * h + lane_off, a);
+#pragma unroll
+                for (int q = 0; q < 64; ++q) a[q] *= eL;
+                tmem_st64(tDH + 64 * h + lane_off, a);
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        // C4: D_H[h] += K^T Vn'   (A = K rows of the stack read MN-major, B = vn16 MN-major)
+        if (tid == 0) {
+            const uint32_t id = idesc_f16(128, 64, true, true);
+            // dk = 64 has a single 64-row block: LBO 0 repeats it as rows 64..127 (ignored)
+            const uint32_t lbo = dk >= 128 ? 2 * kTileBytes : 0;
+            for (int h = 0; h < halves; ++h)
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tDH + 64 * h,
+                            sw128_desc(smem_u32(st + (2 * h) * 2 * kTileBytes) + 2048 * ks, lbo, 1024),
+                            sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id, 1);
+            mma_commit(bar_mma);
+        }
+        if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
+        mma_phase++;
+        __syncthreads();
+        if (s_err) break;
+        fence_after_sync();
+        // E4: H (fp32, TMEM) -> h16 for the next chunk; final state after the last chunk
+        for (int h = 0; h < halves; ++h) {
+            const int row = 128 * h + tid;
+            float a[64];
+            tmem_ld64(tDH + 64 * h + lane_off, a);
+            if (row < dk) {
+                store_row_f16(h16, row, a);
+                if (cidx == nchunks - 1 && p.hT) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)row * dv + v0);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) dst[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+                }
+            }
+        }
+        if (tid < kChunk && cidx + 1 < nchunks) {
+            gam_s[(gs ^ 1) * kChunk + tid] = g_next;
+            bet_s[(gs ^ 1) * kChunk + tid] = b_next;
+            if (cidx + 2 < nchunks) load_gb(cidx + 2, g_next, b_next);
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        // refill this stage with chunk cidx + nstages (its last reader, C4, is done)
+        if (tid == 0 && cidx + nstages < nchunks) {
+            issue_loads(cidx + nstages);
+            loads_in_flight |= 1 << s;
+        }
+    }
+    if (nchunks == 0 && p.hT) {      // empty sequence: final state = initial state
+        for (int h = 0; h < halves; ++h) {
+            const int row = 128 * h + tid;
+            if (row >= dk) continue;
+            float a[64];
+            tmem_ld64(tDH + 64 * h + lane_off, a);
+            float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)row * dv + v0);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) dst[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+        }
+    }
+    if (s_err && tid == 0) {
+        set_timeout(p);
+        for (int s = 0; s < 2; ++s)
+            if (loads_in_flight & (1 << s)) mbar_wait(&bar_load[s], load_uses[s] & 1);
+        mbar_wait(bar_mma, mma_phase & 1);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+// ===================================================================== host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+        return (PFN_cuTensorMapEncodeTiled_v12000)f;
+    }();
+    return fn;
+}
+
+// 2-D fp16 map over [rows][cols] with 64x64 boxes and 128-byte swizzle
+bool encode_tile_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int max_dyn_smem() {
+    int dev = 0, v = 232448;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return v;
+}
+
+}  // namespace
+
+bool chunk_tc_supports(const gdn_desc &d) {
+    return (d.dtype == GDN_BF16 || d.dtype == GDN_F16) && (d.dk == 64 || d.dk == 128 || d.dk == 256) &&
+           d.dv >= 64 && d.dv % 64 == 0;
+}
+
+size_t chunk_tc_workspace(const gdn_desc &d) {
+    if (!chunk_tc_supports(d)) return 0;
+    return (size_t)d.Hv * (size_t)chunk_slot_bound(d) * kTPTBytes;
+}
+
+cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
+    const gdn_desc &d = p.d;
+    const int64_t nslots_alloc = chunk_slot_bound(d);
+    const int64_t nslots = chunk_slots(p);
+    if (nslots > nslots_alloc || p.tpt == nullptr) return cudaErrorInvalidValue;
+    unsigned char *tpt = (unsigned char *)p.tpt;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * d.dk;
+    if (p.ntok > 0) {
+        PrepMaps pm;
+        const __half *q = (const __half *)p.q, *k = (const __half *)p.k;
+        if (!encode_tile_map(&pm.q_hi, q, (uint64_t)d.Hk * p.ntok, d.dk) ||
+            !encode_tile_map(&pm.q_lo, q + plane, (uint64_t)d.Hk * p.ntok, d.dk) ||
+            !encode_tile_map(&pm.k_hi, k, (uint64_t)d.Hk * p.ntok, d.dk) ||
+            !encode_tile_map(&pm.k_lo, k + plane, (uint64_t)d.Hk * p.ntok, d.dk))
+            return cudaErrorInvalidValue;
+        const PrepSmem ps(d.dk);
+        cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)ps.total);
+        if (e != cudaSuccess) return e;
+        if (nslots > 0) {
+            chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hv), kThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+    }
+    ChainMaps cm;
+    if (p.ntok > 0) {
+        if (!encode_tile_map(&cm.q_hi, p.q, (uint64_t)d.Hk * p.ntok, d.dk) ||
+            !encode_tile_map(&cm.k_hi, p.k, (uint64_t)d.Hk * p.ntok, d.dk) ||
+            !encode_tile_map(&cm.v, p.v, (uint64_t)d.Hv * p.ntok, d.dv))
+            return cudaErrorInvalidValue;
+    } else {
+        memset(&cm, 0, sizeof(cm));
+    }
+    const int maxs = max_dyn_smem();
+    int nstages = 2;
+    if ((int)ChainSmem(d.dk, 2).total > maxs) nstages = 1;
+    const ChainSmem cs(d.dk, nstages);
+    if ((int)cs.total > maxs) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)cs.total);
+    if (e != cudaSuccess) return e;
+    const int ntiles = d.dv / 64;
+    const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
+    if (blocks == 0) return cudaSuccess;
+    chunk_chain_kernel<<<(unsigned)blocks, kThreads, cs.total, s>>>(cm, p, ntiles, nstages, nslots_alloc, tpt);
+    return cudaGetLastError();
+}
 
 }  // namespace gdn

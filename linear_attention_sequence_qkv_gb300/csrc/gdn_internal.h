@@ -12,8 +12,17 @@ namespace gdn {
 
 // Workspace regions (byte offsets); every region starts on a 256-byte boundary.
 struct Layout {
-    size_t status, chunk_off, q, k, v, beta, gamma, o, total;
+    size_t status, chunk_off, q, k, v, beta, gamma, o, tpt, total;
 };
+
+// Chunk slots: an upper bound of the number of 64-token chunks over all
+// sequences, ceil(ntok / 64) + N (each sequence adds at most one partial chunk).
+inline int64_t chunk_slot_bound(const gdn_desc &d) {
+    return ((int64_t)d.B * d.T + 63) / 64 + d.N;
+}
+
+// Bytes of the tensor-core kernels' [T; P T] tiles (0 where they do not run).
+size_t chunk_tc_workspace(const gdn_desc &d);
 
 inline size_t act_size(int dtype) { return dtype == GDN_F32 ? 4 : 2; }
 
@@ -31,6 +40,8 @@ inline size_t qk_size(int) { return 4; }   // fp32, or fp16 hi + fp16 lo
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+size_t chunk_tc_workspace(const gdn_desc &d);
+
 inline Layout make_layout(const gdn_desc &d) {
     const size_t s = act_size(d.dtype);
     const size_t ntok = (size_t)d.B * (size_t)d.T;
@@ -44,6 +55,7 @@ inline Layout make_layout(const gdn_desc &d) {
     L.beta = off;      off = align_up(off + 4 * ntok * d.Hv, 256);
     L.gamma = off;     off = align_up(off + gamma_size(d.dtype) * ntok * d.Hv, 256);
     L.o = off;         off = align_up(off + s * ntok * d.Hv * d.dv, 256);
+    L.tpt = off;       off = align_up(off + chunk_tc_workspace(d), 256);
     L.total = off;
     return L;
 }
@@ -62,6 +74,7 @@ struct Problem {
     void *q, *k, *v, *o;
     float *beta;
     void *gamma;                  // float, or double for fp32 activations
+    void *tpt;                    // [T; P T] tiles of the tensor-core kernels
 };
 
 // Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one

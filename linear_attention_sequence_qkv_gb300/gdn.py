@@ -25,6 +25,7 @@ GDN_ERR_WORKSPACE = -3
 GDN_ERR_CUDA = -4
 GDN_ERR_DEVICE_SEQLENS = -5
 GDN_ERR_DEVICE_RANGE = -6
+GDN_ERR_DEVICE_TIMEOUT = -7
 
 GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 DTYPE_CODES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
@@ -65,7 +66,7 @@ class gdn_desc(ctypes.Structure):
 
 class gdn_workspace_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("status", "chunk_off", "q", "k", "v", "beta", "gamma", "o", "total")]
+                ("status", "chunk_off", "q", "k", "v", "beta", "gamma", "o", "tpt", "total")]
 
 
 _lib = None

@@ -41,7 +41,7 @@ def test_library_is_native_and_sm103a():
 def test_struct_layout_matches_header(lib):
     # gdn_desc: 12 int32 + 12 int64 + 3 float + 1 int32 = 160 bytes
     assert ctypes.sizeof(gdn.gdn_desc) == 160
-    assert ctypes.sizeof(gdn.gdn_workspace_layout) == 9 * 8
+    assert ctypes.sizeof(gdn.gdn_workspace_layout) == 10 * 8
 
 
 @pytest.mark.parametrize("args,status", [
@@ -104,19 +104,24 @@ def test_workspace_layout(lib):
     lay = gdn.gdn_workspace_offsets(d)
     ntok = 4096
     assert lay.status == 0
-    for name in ("chunk_off", "q", "k", "v", "beta", "gamma", "o", "total"):
+    for name in ("chunk_off", "q", "k", "v", "beta", "gamma", "o", "tpt", "total"):
         assert getattr(lay, name) % 256 == 0
     assert lay.k - lay.q >= ntok * 6 * 256 * 2
     assert lay.beta - lay.v >= ntok * 6 * 512 * 2
-    assert lay.total - lay.o >= ntok * 6 * 512 * 2
+    assert lay.tpt - lay.o >= ntok * 6 * 512 * 2
+    assert lay.total - lay.tpt >= 6 * (ntok // 64) * 128 * 64 * 2
     assert gdn.gdn_workspace_bytes(d) == lay.total
 
 
 def test_status_strings(lib):
-    for s in (0, -1, -2, -3, -4, -5, -6):
+    for s in (0, -1, -2, -3, -4, -5, -6, -7):
         assert gdn.status_string(s) not in ("", "unknown status")
     assert gdn.status_string(42) == "unknown status"
 
 
 def test_chunk_kernel_kind(lib):
     assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(1, 128, 0, 2, 2, 64, 64, gdn.GDN_F32)) == 0
+    assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(2, 2048, 0, 6, 6, 256, 512, gdn.GDN_BF16)) == 1
+    assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(2, 100, 0, 6, 6, 64, 128, gdn.GDN_F16)) == 1
+    assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(1, 70, 0, 1, 1, 512, 512, gdn.GDN_BF16)) == 0
+    assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(1, 70, 0, 1, 1, 64, 32, gdn.GDN_BF16)) == 0
