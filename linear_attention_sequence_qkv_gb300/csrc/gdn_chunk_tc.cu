@@ -19,7 +19,7 @@
 //  * chain (one CTA per sequence, v head and 64-column dv tile): the state slice
 //    H [dk][64] stays in tensor memory in fp32 across chunks (an fp16 copy in
 //    shared memory feeds the next MMA); per chunk three dependent MMAs
-//    [K; Q e^gam] H, [T; P T] R and K^T Vn'. Inputs of chunk c+1 (and c+2) are
+//    [K; Q] H, [T; P T] R and K^T Vn'. Inputs of chunk c+1 (and c+2) are
 //    fetched by TMA while chunk c computes.
 // Every wait on an mbarrier gives up after about a second; the kernel then
 // records GDN_ERR_DEVICE_TIMEOUT in the status word, waits (bounded) for its own
@@ -75,16 +75,6 @@ __device__ __forceinline__ void load_row_f16(const unsigned char *tile, int row,
             v64[8 * c + 2 * e + 1] = f.y;
         }
     }
-}
-
-// 64 fp32 columns of this thread's lane
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
-#pragma unroll
-    for (int c = 0; c < 64; c += 16) tmem_ld16(taddr + c, v + c);
-}
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const float *v) {
-#pragma unroll
-    for (int c = 0; c < 64; c += 16) tmem_st16(taddr + c, v + c);
 }
 
 // ================================================================ prep kernel
@@ -194,11 +184,15 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
         tmem_ld64(lane_addr, v);
         if (tid < kChunk) {
             const int i = tid;
+            const float gi = gam[i], bi = bet[i];
+#pragma unroll
             for (int jj = 0; jj < kChunk; ++jj)
-                As[i * LDA + jj] = jj < i ? bet[i] * expf(gam[i] - gam[jj]) * v[jj] : 0.f;
+                As[i * LDA + jj] = jj < i ? bi * expf(gi - gam[jj]) * v[jj] : 0.f;
         } else {
             const int i = tid - kChunk;
-            for (int jj = 0; jj < kChunk; ++jj) v[jj] = jj <= i ? expf(gam[i] - gam[jj]) * v[jj] : 0.f;
+            const float gi = gam[i];
+#pragma unroll
+            for (int jj = 0; jj < kChunk; ++jj) v[jj] = jj <= i ? expf(gi - gam[jj]) * v[jj] : 0.f;
             store_row_f16(tp, tid, v);
         }
     }
@@ -237,6 +231,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
     }
     if (tid < kChunk) {   // T rows into the fp16 tile (rows 0..63)
         float v[64];
+#pragma unroll
         for (int jj = 0; jj < kChunk; ++jj) v[jj] = Ts[tid * LDA + jj];
         store_row_f16(tp, tid, v);
     }
@@ -423,20 +418,7 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
         if (s_err) break;
         load_uses[s]++;
         if (tid == 0) loads_in_flight &= ~(1 << s);
-        // Q rows of the stack -> Q e^gam, in place (row scaling ignores the swizzle)
-        for (int e = tid; e < L.blocks * kChunk * 8; e += kThreads) {
-            const int b = e / (kChunk * 8), r = (e >> 3) & 63, ch = e & 7;
-            uint4 *pp = reinterpret_cast<uint4 *>(st + b * 2 * kTileBytes + kTileBytes + r * 128 + ch * 16);
-            uint4 u = *pp;
-            __half2 *hh = reinterpret_cast<__half2 *>(&u);
-            const __half2 sc = __float2half2_rn(expf(gam[r]));
-#pragma unroll
-            for (int q = 0; q < 4; ++q) hh[q] = __hmul2(hh[q], sc);
-            *pp = u;
-        }
-        fence_async_smem();
-        __syncthreads();
-        // C1: D1 = [K; Q e^gam] H   (A K-major from the stack, B = h16 MN-major)
+        // C1: D1 = [K; Q] H   (A K-major from the stack, B = h16 MN-major)
         if (tid == 0) {
             const uint32_t id = idesc_f16(128, 64, false, true);
             for (int b = 0; b < L.blocks; ++b)
@@ -477,7 +459,7 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
         __syncthreads();
         if (s_err) break;
         fence_after_sync();
-        // E2: Vn' = e^{gam_L - gam} Vn -> vn16; O = e^gam Q H + P Vn -> o; H *= e^{gam_L}
+        // E2: Vn' = e^{gam_L - gam} Vn -> vn16; O = e^gam (Q H) + P Vn -> o; H *= e^{gam_L}
         {
             const float gL = gam[kChunk - 1];
             float a[64];
@@ -493,6 +475,7 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
                 tmem_ld64(tD1 + lane_off, a);
                 tmem_ld64(tD2 + lane_off, b2);
                 if (i < len) {
+                    const float eg = expf(gam[i]);
                     uint4 *dst = reinterpret_cast<uint4 *>(o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0);
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
@@ -500,8 +483,8 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
                         __half2 *hh = reinterpret_cast<__half2 *>(&u);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            hh[e] = __floats2half2_rn((a[8 * ch + 2 * e] + b2[8 * ch + 2 * e]) * d.scale,
-                                                      (a[8 * ch + 2 * e + 1] + b2[8 * ch + 2 * e + 1]) * d.scale);
+                            hh[e] = __floats2half2_rn(fmaf(eg, a[8 * ch + 2 * e], b2[8 * ch + 2 * e]) * d.scale,
+                                                      fmaf(eg, a[8 * ch + 2 * e + 1], b2[8 * ch + 2 * e + 1]) * d.scale);
                         dst[ch] = u;
                     }
                 }

@@ -82,7 +82,7 @@ __device__ __forceinline__ void store16_f_cs(T *p, const float *in) {
     __stcs(reinterpret_cast<uint4 *>(p), pack16<T>(in));
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 

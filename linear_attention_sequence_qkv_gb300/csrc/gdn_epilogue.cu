@@ -6,10 +6,10 @@
 // input projection with separate batch and token strides, consumed in place;
 // "Execution and numerical behavior": the RMSNorm result is materialised in the
 // activation dtype before the fp32 SiLU-gating multiply).
-// HBM-bound streaming kernel: each row is read once (o, gate) and written once
-// with 16-byte accesses where the gate view's alignment allows, scalar gate
-// loads where it does not. A row spans at most one warp, so the mean of
-// squares is a shuffle reduction.
+// HBM-bound streaming kernel: one row slice per thread, all of its loads issued
+// first; each row is read once (o, gate) and written once with 16-byte accesses
+// (scalar gate loads where the view's alignment does not allow 16 bytes). A row
+// spans at most one warp, so the mean of squares is a shuffle reduction.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -20,65 +20,84 @@ constexpr int kThreads = 256;
 template <typename T, typename G, typename W, int NVEC, bool GVEC>
 __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     constexpr int VEC = Vec16<T>::N;
-    constexpr int CPT = NVEC * VEC;
-    __shared__ float nw[512];
+    constexpr int CPT = NVEC * VEC;            // columns per thread
+    constexpr int GN = GVEC ? CPT * (int)sizeof(G) / 16 : 1;   // 16-byte gate vectors
+    using S = typename Inter<T>::S;            // storage of o
+    // norm weights, one padding slot after every CPT of them: lane l reads
+    // [l*(CPT+1), +CPT) without bank conflicts
+    __shared__ float nwp[512 + 512 / 4];
     const gdn_desc &d = p.d;
     const int dv = d.dv;
-    for (int i = threadIdx.x; i < dv; i += kThreads) nw[i] = to_f<W>(((const W *)p.norm_w)[i]);
+    for (int i = threadIdx.x; i < dv; i += kThreads) nwp[(i / CPT) * (CPT + 1) + i % CPT] = to_f<W>(((const W *)p.norm_w)[i]);
     __syncthreads();
 
     const int lpr = dv / CPT;                  // lanes per row (power of two, <= 32)
     const int rows_per_block = kThreads / lpr;
-    const int sub = threadIdx.x / lpr;         // row slot in the block
-    const int cc = (threadIdx.x - sub * lpr) * CPT;
-    const float inv_dv = 1.0f / (float)dv;
+    const int sub = threadIdx.x / lpr;
+    const int lane_in_row = threadIdx.x - sub * lpr;
+    const int cc = lane_in_row * CPT;
     const int64_t nrows = p.ntok * d.Hv;
-    using S = typename Inter<T>::S;    // storage of o
-    const S *o = (const S *)p.o;
-    bool finite = true;
-    const G *gate = (const G *)p.gate;
-    T *out = (T *)p.out;
+    const int64_t r = (int64_t)blockIdx.x * rows_per_block + sub;
+    const bool valid = r < nrows;
 
-    for (int64_t r0 = (int64_t)blockIdx.x * rows_per_block; r0 < nrows;
-         r0 += (int64_t)gridDim.x * rows_per_block) {
-        const int64_t r = r0 + sub;
-        const bool valid = r < nrows;
-        float x[CPT], gv[CPT];
-        if (valid) {
-            const int64_t tok = r / d.Hv;
-            const int h = (int)(r - tok * d.Hv);
+    // every load of this thread first
+    uint4 ox[NVEC];
+    uint4 gx[GN];
+    float gs[GVEC ? 1 : CPT];
+    if (valid) {
+        const int64_t tok = r / d.Hv;
+        const int h = (int)(r - tok * d.Hv);
+        const uint4 *op = reinterpret_cast<const uint4 *>((const S *)p.o + r * dv + cc);
 #pragma unroll
-            for (int v = 0; v < NVEC; ++v) load16_f<S>(o + r * dv + cc + v * VEC, x + v * VEC);
+        for (int v = 0; v < NVEC; ++v) ox[v] = __ldcs(op + v);
+        const G *gp = (const G *)p.gate + tok_offset(tok, d.T, d.gate_stride_b, d.gate_stride_t) + h * dv + cc;
+        if (GVEC) {
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) finite = finite && isfinite(x[i]);
-            const G *gp = gate + tok_offset(tok, d.T, d.gate_stride_b, d.gate_stride_t) + h * dv + cc;
-            if (GVEC) {
-                constexpr int GV = Vec16<G>::N;
-#pragma unroll
-                for (int v = 0; v < CPT; v += GV) load16_f<G>(gp + v, gv + v);
-            } else {
-#pragma unroll
-                for (int i = 0; i < CPT; ++i) gv[i] = to_f<G>(gp[i]);
-            }
+            for (int v = 0; v < GN; ++v) gx[v] = __ldcs(reinterpret_cast<const uint4 *>(gp) + v);
         } else {
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) x[i] = gv[i] = 0.f;
+            for (int i = 0; i < (GVEC ? 1 : CPT); ++i) gs[i] = to_f<G>(gp[i]);
         }
-        float ss = 0.f;
+    } else {
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) ss = fmaf(x[i], x[i], ss);
-        for (int off = lpr >> 1; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float inv = rsqrtf(ss * inv_dv + d.norm_eps);
-        if (valid) {
-            float y[CPT];
+        for (int v = 0; v < NVEC; ++v) ox[v] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) {
-                const float rn = round_through<T>(nw[cc + i] * (x[i] * inv));
-                y[i] = rn * silu_f(gv[i]);
-            }
+        for (int v = 0; v < GN; ++v) gx[v] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int v = 0; v < NVEC; ++v) store16_f_cs<T>(out + r * dv + cc + v * VEC, y + v * VEC);
+        for (int i = 0; i < (GVEC ? 1 : CPT); ++i) gs[i] = 0.f;
+    }
+    float x[CPT];
+#pragma unroll
+    for (int v = 0; v < NVEC; ++v) unpack16<S>(ox[v], x + v * VEC);
+    float ss = 0.f;
+    bool finite = true;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        ss = fmaf(x[i], x[i], ss);
+        finite = finite && isfinite(x[i]);
+    }
+    for (int off = lpr >> 1; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float inv = rsqrtf(ss * (1.0f / (float)dv) + d.norm_eps);
+    if (valid) {
+        float gv[CPT];
+        if (GVEC) {
+            constexpr int GE = 16 / sizeof(G);
+#pragma unroll
+            for (int v = 0; v < GN; ++v) unpack16<G>(gx[v], gv + v * GE);
+        } else {
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) gv[i] = gs[GVEC ? 0 : i];
         }
+        const float *wv = nwp + lane_in_row * (CPT + 1);
+        float y[CPT];
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const float rn = round_through<T>(wv[i] * (x[i] * inv));
+            y[i] = rn * silu_f(gv[i]);
+        }
+        T *out = (T *)p.out + r * dv + cc;
+#pragma unroll
+        for (int v = 0; v < NVEC; ++v) store16_f_cs<T>(out + v * VEC, y + v * VEC);
     }
     // a non-finite gated-delta-rule output (unless an earlier stage already
     // reported a malformed cu_seqlens, after which o holds nothing meaningful)
@@ -92,14 +111,7 @@ cudaError_t launch_g(const Problem &p, cudaStream_t s) {
     const int lpr = p.d.dv / CPT;
     const int rows_per_block = kThreads / lpr;
     const int64_t nrows = p.ntok * p.d.Hv;
-    int64_t blocks = (nrows + rows_per_block - 1) / rows_per_block;
-    int sms = 152;
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t cap = (int64_t)sms * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    const int64_t blocks = (nrows + rows_per_block - 1) / rows_per_block;
     const size_t gs = sizeof(G);
     const bool gvec = ((uintptr_t)p.gate % 16 == 0) && ((p.d.gate_stride_b * gs) % 16 == 0) &&
                       ((p.d.gate_stride_t * gs) % 16 == 0) && ((CPT * gs) % 16 == 0);

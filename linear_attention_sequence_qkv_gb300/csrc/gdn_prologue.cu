@@ -12,10 +12,11 @@
 //     planes hi + lo carrying about fp32 precision;
 //   * beta = sigmoid(b), g = -exp(A_log) * softplus(a + dt_bias) and the
 //     inclusive cumulative sum of g inside each 64-token chunk.
-// Grid: x = chunk slot (one 64-token chunk of one sequence), y = channel group
-// of q, k or v (128 threads x 16-byte vectors), the last y = beta/decay group.
-// Every input row is read once (plus a 3-token halo per chunk) with coalesced
-// 16-byte loads; q/k/v are written head-major [H][Ntok][d] for the chunk kernel.
+// Grid: x = chunk slot (one 64-token chunk of one sequence), y = (channel group
+// of q, k or v: 128 threads x 16-byte vectors) x (token slice of the chunk), the
+// last y = beta/decay group. Every input row is read once plus a 3-token halo per
+// slice (L2 hits), with coalesced 16-byte loads all issued up front; q/k/v are
+// written head-major [H][Ntok][d] for the chunk kernels.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -86,40 +87,78 @@ struct PrologueArgs {
 };
 
 // ------------------------------------------------------------ conv group
+// One CTA covers one channel group (128 threads x CPT channels) of one token
+// slice (TOKS tokens) of one chunk. Each thread copies the TOKS + 3 rows of its
+// channels (16-byte vectors, zero-filled before the sequence start) into shared
+// memory with cp.async, all in flight at once without holding registers, then
+// runs the 4-tap window over them.
+template <int NVEC> struct ConvShape {
+    static constexpr int TOKS = 16 / NVEC;
+    static constexpr int ROWS = TOKS + kConvW - 1;
+    static constexpr int SLICES = kChunk / TOKS;
+    static constexpr size_t SMEM = (size_t)ROWS * NVEC * kThreads * 16;
+};
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool ok) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem), "r"(ok ? 16 : 0)
+                 : "memory");
+}
+
 template <typename T, int NVEC>
-__device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc &c, int gy) {
+__device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc &c, int gy,
+                                           uint4 *stage) {
     constexpr int VEC = Vec16<T>::N;
     constexpr int CPT = NVEC * VEC;           // channels per thread
-    constexpr int BATCH = 8 / NVEC;           // rows loaded ahead
+    using Shape = ConvShape<NVEC>;
+    constexpr int TOKS = Shape::TOKS;
+    constexpr int ROWS = Shape::ROWS;
+    using S = typename Inter<T>::S;
     const Problem &p = A.p;
     const gdn_desc &d = p.d;
     const int tid = threadIdx.x;
+    const int slice = gy % Shape::SLICES;
+    int g = gy / Shape::SLICES;
+    const int t_begin = slice * TOKS;
+    if (t_begin >= c.len) return;
+    const int ntok = min(TOKS, c.len - t_begin);
 
     // which tensor / channel range
     const T *src;
-    typename Inter<T>::S *dst;
+    S *dst;
     int64_t sb, st;
     int nch, hd, w_base;
     bool norm;
-    int g = gy;
     const int ch_qk = d.Hk * d.dk;
     if (g < A.groups_qk) {
-        src = (const T *)p.q_raw; dst = (typename Inter<T>::S *)p.q; sb = d.q_stride_b; st = d.q_stride_t;
+        src = (const T *)p.q_raw; dst = (S *)p.q; sb = d.q_stride_b; st = d.q_stride_t;
         nch = ch_qk; hd = d.dk; w_base = 0; norm = true;
     } else if ((g -= A.groups_qk) < A.groups_qk) {
-        src = (const T *)p.k_raw; dst = (typename Inter<T>::S *)p.k; sb = d.k_stride_b; st = d.k_stride_t;
+        src = (const T *)p.k_raw; dst = (S *)p.k; sb = d.k_stride_b; st = d.k_stride_t;
         nch = ch_qk; hd = d.dk; w_base = ch_qk; norm = true;
     } else {
         g -= A.groups_qk;
-        src = (const T *)p.v_raw; dst = (typename Inter<T>::S *)p.v; sb = d.v_stride_b; st = d.v_stride_t;
+        src = (const T *)p.v_raw; dst = (S *)p.v; sb = d.v_stride_b; st = d.v_stride_t;
         nch = d.Hv * d.dv; hd = d.dv; w_base = 2 * ch_qk; norm = false;
     }
-    using S = typename Inter<T>::S;
     const int c0 = g * (kThreads * CPT) + tid * CPT;
     const bool active = c0 < nch;
     const int lanes_per_head = hd / CPT;      // <= 32 for q/k by construction
 
-    // conv taps of my channels
+    // rows into shared memory: stage[(r * NVEC + v) * kThreads + tid]
+    const int64_t first = c.tok0 + t_begin - (kConvW - 1);
+    const int64_t brow = p.cu ? 0 : c.n;     // batch row of this sequence
+    const T *rp = src + brow * sb + (first - brow * (int64_t)d.T) * st + (active ? c0 : 0);
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const bool ok = active && r < ntok + kConvW - 1 && first + r >= c.seq0;
+#pragma unroll
+        for (int v = 0; v < NVEC; ++v)
+            cp_async16(&stage[(r * NVEC + v) * kThreads + tid], ok ? (const void *)(rp + r * st + v * VEC)
+                                                                   : (const void *)src, ok);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    // conv taps of my channels (overlaps the copies)
     float w[CPT][kConvW];
     if (active) {
         const T *wp = (const T *)p.conv_w + (int64_t)(w_base + c0) * kConvW;
@@ -136,84 +175,57 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
 #pragma unroll
             for (int j = 0; j < kConvW; ++j) w[i][j] = 0.f;
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");   // each thread reads only its own rows
 
-    auto load_raw = [&](int64_t tok, uint4 *out) {
-        if (active && tok >= c.seq0) {
-            const uint4 *rp = reinterpret_cast<const uint4 *>(src + tok_offset(tok, d.T, sb, st) + c0);
+    auto row = [&](int r, float *out) {
 #pragma unroll
-            for (int v = 0; v < NVEC; ++v) out[v] = __ldg(rp + v);
-        } else {
-#pragma unroll
-            for (int v = 0; v < NVEC; ++v) out[v] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        for (int v = 0; v < NVEC; ++v) unpack16<T>(stage[(r * NVEC + v) * kThreads + tid], out + v * VEC);
     };
-    auto to_floats = [&](const uint4 *raw, float *out) {
-#pragma unroll
-        for (int v = 0; v < NVEC; ++v) unpack16<T>(raw[v], out + v * VEC);
-    };
-
-    // sliding window: x[t-3], x[t-2], x[t-1]
     float x3[CPT], x2[CPT], x1[CPT];
-    {
-        uint4 r[NVEC];
-        load_raw(c.tok0 - 3, r); to_floats(r, x3);
-        load_raw(c.tok0 - 2, r); to_floats(r, x2);
-        load_raw(c.tok0 - 1, r); to_floats(r, x1);
-    }
+    row(0, x3);
+    row(1, x2);
+    row(2, x1);
 
     const int head = c0 / hd;
     const int dd = c0 - head * hd;
-    S *dbase = dst + ((int64_t)head * p.ntok) * hd + dd;
+    S *dbase = dst + ((int64_t)head * p.ntok + c.tok0 + t_begin) * hd + dd;
     // q/k of 2-byte activations: hi plane here, lo plane `plane` elements further
     const bool split = norm && sizeof(S) == 2;
     const int64_t plane = (int64_t)d.Hk * p.ntok * d.dk;
 
-    for (int base = 0; base < c.len; base += BATCH) {
-        uint4 xr[BATCH][NVEC];
+    for (int u = 0; u < ntok; ++u) {          // uniform across the block
+        float x0[CPT], y[CPT];
+        row(u + kConvW - 1, x0);
+        float ss = 0.f;
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            if (base + u < c.len) load_raw(c.tok0 + base + u, xr[u]);
-            else {
-#pragma unroll
-                for (int v = 0; v < NVEC; ++v) xr[u][v] = make_uint4(0u, 0u, 0u, 0u);
-            }
+        for (int i = 0; i < CPT; ++i) {
+            float acc = w[i][0] * x3[i];
+            acc = fmaf(w[i][1], x2[i], acc);
+            acc = fmaf(w[i][2], x1[i], acc);
+            acc = fmaf(w[i][3], x0[i], acc);
+            y[i] = silu_f(acc);
+            ss = fmaf(y[i], y[i], ss);
+            x3[i] = x2[i];
+            x2[i] = x1[i];
+            x1[i] = x0[i];
         }
+        if (norm) {
+            for (int off = lanes_per_head >> 1; off >= 1; off >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = rsqrtf(ss + d.l2_eps);
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            if (base + u >= c.len) break;          // uniform across the block
-            float x0[CPT], y[CPT];
-            to_floats(xr[u], x0);
-            float ss = 0.f;
+            for (int i = 0; i < CPT; ++i) y[i] *= inv;
+        }
+        if (active) {
+            S *op = dbase + (int64_t)u * hd;
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) {
-                float acc = w[i][0] * x3[i];
-                acc = fmaf(w[i][1], x2[i], acc);
-                acc = fmaf(w[i][2], x1[i], acc);
-                acc = fmaf(w[i][3], x0[i], acc);
-                y[i] = silu_f(acc);
-                ss = fmaf(y[i], y[i], ss);
-                x3[i] = x2[i];
-                x2[i] = x1[i];
-                x1[i] = x0[i];
-            }
-            if (norm) {
-                for (int off = lanes_per_head >> 1; off >= 1; off >>= 1)
-                    ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                const float inv = rsqrtf(ss + d.l2_eps);
+            for (int v = 0; v < NVEC; ++v) store16_f<S>(op + v * VEC, y + v * VEC);
+            if (split) {   // lo plane: what fp16 rounding of y left out
+                float lo[CPT];
 #pragma unroll
-                for (int i = 0; i < CPT; ++i) y[i] *= inv;
-            }
-            if (active) {
-                S *op = dbase + (c.tok0 + base + u) * (int64_t)hd;
+                for (int i = 0; i < CPT; ++i) lo[i] = y[i] - round_through<S>(y[i]);
 #pragma unroll
-                for (int v = 0; v < NVEC; ++v) store16_f<S>(op + v * VEC, y + v * VEC);
-                if (split) {   // lo plane: what fp16 rounding of y left out
-                    float lo[CPT];
-#pragma unroll
-                    for (int i = 0; i < CPT; ++i) lo[i] = y[i] - round_through<S>(y[i]);
-#pragma unroll
-                    for (int v = 0; v < NVEC; ++v) store16_f<S>(op + plane + v * VEC, lo + v * VEC);
-                }
+                for (int v = 0; v < NVEC; ++v) store16_f<S>(op + plane + v * VEC, lo + v * VEC);
             }
         }
     }
@@ -221,9 +233,9 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
 
 // ------------------------------------------------------- beta/decay group
 template <typename T>
-__device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c) {
-    __shared__ float gs[kChunk][33];
-    __shared__ float bs[kChunk][33];
+__device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c, float *smem) {
+    float (*gs)[33] = reinterpret_cast<float (*)[33]>(smem);
+    float (*bs)[33] = reinterpret_cast<float (*)[33]>(smem + kChunk * 33);
     const gdn_desc &d = p.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int h0 = 0; h0 < d.Hv; h0 += 32) {
@@ -270,6 +282,7 @@ __device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c) 
 
 template <typename T, int NVEC>
 __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueArgs A) {
+    extern __shared__ uint4 stage[];
     const Problem &p = A.p;
     if (p.cu == nullptr) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = GDN_OK;
@@ -279,8 +292,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueArgs A
     ChunkLoc c;
     if (!locate_chunk(blockIdx.x, p.cu, p.chunk_off, p.d.N, p.d.T, c)) return;
     const int gy = blockIdx.y;
-    if (gy == 2 * A.groups_qk + A.groups_v) gate_group<T>(p, c);
-    else conv_group<T, NVEC>(A, c, gy);
+    if (gy == (2 * A.groups_qk + A.groups_v) * ConvShape<NVEC>::SLICES) gate_group<T>(p, c, (float *)stage);
+    else conv_group<T, NVEC>(A, c, gy, stage);
 }
 
 template <typename T, int NVEC>
@@ -291,8 +304,15 @@ cudaError_t launch_t(const Problem &p, cudaStream_t s) {
     const int gc = kThreads * CPT;
     A.groups_qk = (p.d.Hk * p.d.dk + gc - 1) / gc;
     A.groups_v = (p.d.Hv * p.d.dv + gc - 1) / gc;
-    dim3 grid((unsigned)chunk_slots(p), 2 * A.groups_qk + A.groups_v + 1);
-    prologue_kernel<T, NVEC><<<grid, kThreads, 0, s>>>(A);
+    using Shape = ConvShape<NVEC>;
+    static_assert(Shape::SMEM >= 2 * kChunk * 33 * 4, "gate group scratch");
+    dim3 grid((unsigned)chunk_slots(p), (2 * A.groups_qk + A.groups_v) * Shape::SLICES + 1);
+    if (Shape::SMEM > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(prologue_kernel<T, NVEC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Shape::SMEM);
+        if (e != cudaSuccess) return e;
+    }
+    prologue_kernel<T, NVEC><<<grid, kThreads, Shape::SMEM, s>>>(A);
     return cudaGetLastError();
 }
 
