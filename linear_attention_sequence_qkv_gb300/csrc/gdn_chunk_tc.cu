@@ -16,11 +16,12 @@
 //    solve on CUDA cores in fp32, then P T on the tensor cores. Writes the
 //    [T; P T] tile (128 x 64 fp16, 16 KB) already in the 128-byte-swizzled
 //    layout, so the chain kernel fetches it with one bulk copy.
-//  * chain (one CTA per sequence, v head and 64-column dv tile): the state slice
-//    H [dk][64] stays in tensor memory in fp32 across chunks (an fp16 copy in
-//    shared memory feeds the next MMA); per chunk three dependent MMAs
-//    [K; Q] H, [T; P T] R and K^T Vn'. Inputs of chunk c+1 (and c+2) are
-//    fetched by TMA while chunk c computes.
+//  * chain (one CTA of 8 warps per sequence, v head and 64-column dv tile): the
+//    state slice H [dk][64] stays in registers in fp32 across chunks (warps w
+//    and w+4 read the same tensor-memory lanes and split the columns; an fp16
+//    copy in shared memory feeds the next MMA); per chunk three dependent MMAs
+//    [K; Q] H, [T; P T] R and dH = K^T Vn', then H = e^{gam_L} H + dH. Inputs of
+//    chunk c+1 (and c+2) are fetched by TMA while chunk c computes.
 // Every wait on an mbarrier gives up after about a second; the kernel then
 // records GDN_ERR_DEVICE_TIMEOUT in the status word, waits (bounded) for its own
 // copies and MMAs, frees its tensor memory and returns.
@@ -73,6 +74,31 @@ __device__ __forceinline__ void load_row_f16(const unsigned char *tile, int row,
             const float2 f = __half22float2(h[e]);
             v64[8 * c + 2 * e] = f.x;
             v64[8 * c + 2 * e + 1] = f.y;
+        }
+    }
+}
+
+// 32 columns [c0, c0 + 32) of a swizzled tile row, fp32 <-> fp16
+__device__ __forceinline__ void store_half_row_f16(unsigned char *tile, int row, int c0, const float *v32) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint4 u;
+        __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v32[8 * c + 2 * e], v32[8 * c + 2 * e + 1]);
+        *reinterpret_cast<uint4 *>(tile + sw128_off(row, c0 + 8 * c)) = u;
+    }
+}
+__device__ __forceinline__ void load_half_row_f16(const unsigned char *tile, int row, int c0, float *v32) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_off(row, c0 + 8 * c));
+        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(h[e]);
+            v32[8 * c + 2 * e] = f.x;
+            v32[8 * c + 2 * e + 1] = f.y;
         }
     }
 }
@@ -298,13 +324,17 @@ struct ChainSmem {
     }
 };
 
-__global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_constant__ ChainMaps maps,
-                                                               const Problem p, int ntiles, int nstages,
-                                                               int64_t nslots, const unsigned char *tpt) {
+constexpr int kChainThreads = 256;   // 8 warps: warps w and w+4 share TMEM lanes, split columns
+
+__global__ void __launch_bounds__(kChainThreads, 1)
+chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles, int nstages,
+                   int64_t nslots, const unsigned char *tpt) {
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const gdn_desc &d = p.d;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int row = tid & 127;                 // TMEM lane = tile row of this thread
+    const int c0 = (warp >> 2) * 32;           // its 32 of the 64 columns
     int bid = blockIdx.x;
     const int tile = bid % ntiles;
     bid /= ntiles;
@@ -343,10 +373,11 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tD1 = tbase, tD2 = tbase + 64, tDH = tbase + 128;   // D_H half h at +64h
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tD1 = tbase + lane_off + c0, tD2 = tbase + 64 + lane_off + c0;
+    const uint32_t tDH = tbase + 128 + lane_off + c0;   // + 64 h for row group h
     uint32_t mma_phase = 0;
-    int loads_in_flight = 0;      // bitmask of stages with outstanding TMA
+    int loads_in_flight = 0;      // bitmask of stages with outstanding TMA (thread 0)
     uint32_t load_uses[2] = {0, 0};
 
     auto issue_loads = [&](int cidx) {   // thread 0 only
@@ -372,23 +403,24 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
         b = tid < len ? bw[tok0 + i] : 0.f;
     };
 
-    // initial state: fp32 into TMEM (D_H), fp16 copy into h16 (MN-major B operand)
-    for (int h = 0; h < halves; ++h) {
-        const int row = 128 * h + tid;
-        float v[64];
-        if (row < dk && p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)row * dv + v0);
+    // fp32 state slice in registers: rows 128h + row, columns c0..c0+31;
+    // an fp16 copy in h16 is the B operand of the next chunk's first MMA
+    float Hreg[2][32];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
+    for (int h = 0; h < 2; ++h) {
+        const int hrow = 128 * h + row;
+        if (h < halves && hrow < dk && p.h0) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)hrow * dv + v0 + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
                 const float4 f = src[q];
-                v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+                Hreg[h][4 * q] = f.x; Hreg[h][4 * q + 1] = f.y; Hreg[h][4 * q + 2] = f.z; Hreg[h][4 * q + 3] = f.w;
             }
         } else {
 #pragma unroll
-            for (int q = 0; q < 64; ++q) v[q] = 0.f;
+            for (int q = 0; q < 32; ++q) Hreg[h][q] = 0.f;
         }
-        tmem_st64(tDH + 64 * h + lane_off, v);
-        if (row < dk) store_row_f16(h16, row, v);
+        if (h < halves && hrow < dk) store_half_row_f16(h16, hrow, c0, Hreg[h]);
     }
     if (nchunks > 0) {
         if (tid == 0) {
@@ -423,7 +455,7 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
             const uint32_t id = idesc_f16(128, 64, false, true);
             for (int b = 0; b < L.blocks; ++b)
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tD1, sw128_desc(smem_u32(st + b * 2 * kTileBytes) + 32 * ks, 16, 1024),
+                    mma_f16(tbase, sw128_desc(smem_u32(st + b * 2 * kTileBytes) + 32 * ks, 16, 1024),
                             sw128_desc(smem_u32(h16) + (b * 4 + ks) * 2048, 8192, 1024), id,
                             (b | ks) != 0);
             mma_commit(bar_mma);
@@ -434,14 +466,14 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
         if (s_err) break;
         fence_after_sync();
         // E1: R = beta (V - e^gam K H) -> r16 (rows = tokens, MN-major B of C2)
-        if (tid < kChunk) {
-            float kh[64], vv[64];
-            tmem_ld64(tD1 + lane_off, kh);
-            load_row_f16(st + L.v, tid, vv);
-            const float eg = expf(gam[tid]), bb = bet[tid];
+        if (row < kChunk) {
+            float kh[32], vv[32];
+            tmem_ld32(tD1, kh);
+            load_half_row_f16(st + L.v, row, c0, vv);
+            const float eg = expf(gam[row]), bb = bet[row];
 #pragma unroll
-            for (int q = 0; q < 64; ++q) kh[q] = bb * (vv[q] - eg * kh[q]);
-            store_row_f16(r16, tid, kh);
+            for (int q = 0; q < 32; ++q) kh[q] = bb * (vv[q] - eg * kh[q]);
+            store_half_row_f16(r16, row, c0, kh);
         }
         fence_async_smem();
         fence_before_sync();
@@ -450,7 +482,7 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
         if (tid == 0) {
             const uint32_t id = idesc_f16(128, 64, false, true);
             for (int ks = 0; ks < 4; ++ks)
-                mma_f16(tD2, sw128_desc(smem_u32(st + L.tpt) + 32 * ks, 16, 1024),
+                mma_f16(tbase + 64, sw128_desc(smem_u32(st + L.tpt) + 32 * ks, 16, 1024),
                         sw128_desc(smem_u32(r16) + 2048 * ks, 8192, 1024), id, ks != 0);
             mma_commit(bar_mma);
         }
@@ -459,57 +491,48 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
         __syncthreads();
         if (s_err) break;
         fence_after_sync();
-        // E2: Vn' = e^{gam_L - gam} Vn -> vn16; O = e^gam (Q H) + P Vn -> o; H *= e^{gam_L}
-        {
-            const float gL = gam[kChunk - 1];
-            float a[64];
-            if (tid < kChunk) {
-                tmem_ld64(tD2 + lane_off, a);
-                const float sc = expf(gL - gam[tid]);
+        const float gL = gam[kChunk - 1];
+        // E2: rows 0..63: Vn' = e^{gam_L - gam} Vn -> vn16; rows 64..127: O = e^gam (Q H) + P Vn -> o
+        if (row < kChunk) {
+            float a[32];
+            tmem_ld32(tD2, a);
+            const float sc = expf(gL - gam[row]);
 #pragma unroll
-                for (int q = 0; q < 64; ++q) a[q] *= sc;
-                store_row_f16(vn16, tid, a);
-            } else {
-                const int i = tid - kChunk;
-                float b2[64];
-                tmem_ld64(tD1 + lane_off, a);
-                tmem_ld64(tD2 + lane_off, b2);
-                if (i < len) {
-                    const float eg = expf(gam[i]);
-                    uint4 *dst = reinterpret_cast<uint4 *>(o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0);
+            for (int q = 0; q < 32; ++q) a[q] *= sc;
+            store_half_row_f16(vn16, row, c0, a);
+        } else {
+            const int i = row - kChunk;
+            float a[32], b2[32];
+            tmem_ld32(tD1, a);
+            tmem_ld32(tD2, b2);
+            if (i < len) {
+                const float eg = expf(gam[i]);
+                uint4 *dst = reinterpret_cast<uint4 *>(o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0 + c0);
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4 u;
-                        __half2 *hh = reinterpret_cast<__half2 *>(&u);
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint4 u;
+                    __half2 *hh = reinterpret_cast<__half2 *>(&u);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            hh[e] = __floats2half2_rn(fmaf(eg, a[8 * ch + 2 * e], b2[8 * ch + 2 * e]) * d.scale,
-                                                      fmaf(eg, a[8 * ch + 2 * e + 1], b2[8 * ch + 2 * e + 1]) * d.scale);
-                        dst[ch] = u;
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        hh[e] = __floats2half2_rn(fmaf(eg, a[8 * ch + 2 * e], b2[8 * ch + 2 * e]) * d.scale,
+                                                  fmaf(eg, a[8 * ch + 2 * e + 1], b2[8 * ch + 2 * e + 1]) * d.scale);
+                    dst[ch] = u;
                 }
-            }
-            const float eL = expf(gL);
-            for (int h = 0; h < halves; ++h) {
-                tmem_ld64(tDH + 64 * h + lane_off, a);
-#pragma unroll
-                for (int q = 0; q < 64; ++q) a[q] *= eL;
-                tmem_st64(tDH + 64 * h + lane_off, a);
             }
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        // C4: D_H[h] += K^T Vn'   (A = K rows of the stack read MN-major, B = vn16 MN-major)
+        // C4: dH[h] = K^T Vn'   (A = K rows of the stack read MN-major, B = vn16 MN-major)
         if (tid == 0) {
             const uint32_t id = idesc_f16(128, 64, true, true);
             // dk = 64 has a single 64-row block: LBO 0 repeats it as rows 64..127 (ignored)
             const uint32_t lbo = dk >= 128 ? 2 * kTileBytes : 0;
             for (int h = 0; h < halves; ++h)
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tDH + 64 * h,
+                    mma_f16(tbase + 128 + 64 * h,
                             sw128_desc(smem_u32(st + (2 * h) * 2 * kTileBytes) + 2048 * ks, lbo, 1024),
-                            sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id, 1);
+                            sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id, ks != 0);
             mma_commit(bar_mma);
         }
         if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
@@ -517,17 +540,25 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
         __syncthreads();
         if (s_err) break;
         fence_after_sync();
-        // E4: H (fp32, TMEM) -> h16 for the next chunk; final state after the last chunk
-        for (int h = 0; h < halves; ++h) {
-            const int row = 128 * h + tid;
-            float a[64];
-            tmem_ld64(tDH + 64 * h + lane_off, a);
-            if (row < dk) {
-                store_row_f16(h16, row, a);
-                if (cidx == nchunks - 1 && p.hT) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)row * dv + v0);
+        // E4: H = e^{gam_L} H + dH (fp32 in registers) -> h16; final state after the last chunk
+        {
+            const float eL = expf(gL);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) dst[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+            for (int h = 0; h < 2; ++h) {
+                const int hrow = 128 * h + row;
+                if (h >= halves) break;
+                float a[32];
+                tmem_ld32(tDH + 64 * h, a);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) Hreg[h][q] = fmaf(eL, Hreg[h][q], a[q]);
+                if (hrow < dk) {
+                    store_half_row_f16(h16, hrow, c0, Hreg[h]);
+                    if (cidx == nchunks - 1 && p.hT) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
+                    }
                 }
             }
         }
@@ -546,14 +577,14 @@ __global__ void __launch_bounds__(kThreads) chunk_chain_kernel(const __grid_cons
         }
     }
     if (nchunks == 0 && p.hT) {      // empty sequence: final state = initial state
-        for (int h = 0; h < halves; ++h) {
-            const int row = 128 * h + tid;
-            if (row >= dk) continue;
-            float a[64];
-            tmem_ld64(tDH + 64 * h + lane_off, a);
-            float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)row * dv + v0);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) dst[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+        for (int h = 0; h < 2; ++h) {
+            const int hrow = 128 * h + row;
+            if (h >= halves || hrow >= dk) continue;
+            float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
         }
     }
     if (s_err && tid == 0) {
@@ -657,7 +688,7 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
     const int ntiles = d.dv / 64;
     const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
     if (blocks == 0) return cudaSuccess;
-    chunk_chain_kernel<<<(unsigned)blocks, kThreads, cs.total, s>>>(cm, p, ntiles, nstages, nslots_alloc, tpt);
+    chunk_chain_kernel<<<(unsigned)blocks, kChainThreads, cs.total, s>>>(cm, p, ntiles, nstages, nslots_alloc, tpt);
     return cudaGetLastError();
 }
 
