@@ -319,12 +319,19 @@ struct ChainSmem {
         vn16 = o; o += kTileBytes;
         gam = o; o += 2 * kChunk * 4;
         bet = o; o += 2 * kChunk * 4;
-        bars = o; o += 64;
+        bars = o; o += 128;
         total = o + 1024;
     }
 };
 
-constexpr int kChainThreads = 256;   // 8 warps: warps w and w+4 share TMEM lanes, split columns
+// 8 epilogue warps (warps w and w+4 share tensor-memory lanes and split the 64
+// columns) plus one control warp that issues every TMA copy and MMA. The roles
+// meet on mbarriers, one arrival per warp, so the control thread issues the next
+// MMA as soon as its operands are written; the output store of rows 64..127 is
+// off the critical path.
+constexpr int kEpiWarps = 8;
+constexpr int kChainThreads = (kEpiWarps + 1) * 32;
+enum ChainBar { B_LOAD0 = 0, B_LOAD1, B_C1, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_COUNT };
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles, int nstages,
@@ -332,9 +339,10 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const gdn_desc &d = p.d;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = tid & 127;                 // TMEM lane = tile row of this thread
-    const int c0 = (warp >> 2) * 32;           // its 32 of the 64 columns
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool ctrl = warp == kEpiWarps;
+    const int row = tid & 127;                 // TMEM lane = tile row (epilogue warps)
+    const int c0 = ((warp >> 2) & 1) * 32;     // its 32 of the 64 columns
     int bid = blockIdx.x;
     const int tile = bid % ntiles;
     bid /= ntiles;
@@ -352,10 +360,9 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     const int halves = dk >= 128 ? dk / 128 : 1;  // M=128 row groups of the state
     unsigned char *h16 = sm + L.h16, *r16 = sm + L.r16, *vn16 = sm + L.vn16;
     float *gam_s = (float *)(sm + L.gam), *bet_s = (float *)(sm + L.bet);
-    uint64_t *bar_load = (uint64_t *)(sm + L.bars);   // [2]
-    uint64_t *bar_mma = bar_load + 2;
-    uint32_t *tslot = (uint32_t *)(bar_load + 3);
-    __shared__ int s_err;
+    uint64_t *bar = (uint64_t *)(sm + L.bars);
+    uint32_t *tslot = (uint32_t *)(bar + B_COUNT);
+    __shared__ volatile int s_err;
     const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
     const float *gw = (const float *)p.gamma + (int64_t)j * p.ntok;
     const float *bw = p.beta + (int64_t)j * p.ntok;
@@ -363,9 +370,15 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
 
     if (tid == 0) {
         s_err = 0;
-        mbar_init(&bar_load[0], 1);
-        mbar_init(&bar_load[1], 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(&bar[B_LOAD0], 1);
+        mbar_init(&bar[B_LOAD1], 1);
+        mbar_init(&bar[B_C1], 1);
+        mbar_init(&bar[B_C2], 1);
+        mbar_init(&bar[B_C4], 1);
+        mbar_init(&bar[B_R], 4);     // rows 0..63: warps 0, 1, 4, 5
+        mbar_init(&bar[B_VN], 4);
+        mbar_init(&bar[B_O], 4);     // rows 64..127: warps 2, 3, 6, 7
+        mbar_init(&bar[B_H], kEpiWarps);
         mbar_init_fence();
     }
     if (warp == 0) tmem_alloc(tslot, 256);
@@ -376,24 +389,21 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tD1 = tbase + lane_off + c0, tD2 = tbase + 64 + lane_off + c0;
     const uint32_t tDH = tbase + 128 + lane_off + c0;   // + 64 h for row group h
-    uint32_t mma_phase = 0;
-    int loads_in_flight = 0;      // bitmask of stages with outstanding TMA (thread 0)
-    uint32_t load_uses[2] = {0, 0};
 
-    auto issue_loads = [&](int cidx) {   // thread 0 only
+    auto issue_loads = [&](int cidx) {   // control thread
         const int s = cidx % nstages;
         unsigned char *st = sm + s * L.stage_bytes;
         const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
         const int yk = (int)((int64_t)hk * p.ntok + tok0);
         const int yv = (int)((int64_t)j * p.ntok + tok0);
-        mbar_expect_tx(&bar_load[s], (uint32_t)L.blocks * 2 * kTileBytes + kTileBytes + kTPTBytes);
+        mbar_expect_tx(&bar[B_LOAD0 + s], (uint32_t)L.blocks * 2 * kTileBytes + kTileBytes + kTPTBytes);
         for (int b = 0; b < L.blocks; ++b) {
-            tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar_load[s]);
-            tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar_load[s]);
+            tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
+            tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
         }
-        tma_load_2d(st + L.v, &maps.v, v0, yv, &bar_load[s]);
+        tma_load_2d(st + L.v, &maps.v, v0, yv, &bar[B_LOAD0 + s]);
         bulk_load(st + L.tpt, tpt + ((int64_t)j * nslots + slot0 + cidx) * kTPTBytes, kTPTBytes,
-                  &bar_load[s]);
+                  &bar[B_LOAD0 + s]);
     };
     auto load_gb = [&](int cidx, float &g, float &b) {   // threads < 64
         const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
@@ -402,196 +412,206 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         g = gw[tok0 + i];
         b = tid < len ? bw[tok0 + i] : 0.f;
     };
+    // wait on an mbarrier phase; a timeout flags the CTA (every role then drains)
+    auto wait = [&](int b, uint32_t parity) -> bool {
+        if (s_err) return false;
+        if (!mbar_wait(&bar[b], parity)) { s_err = 1; return false; }
+        return true;
+    };
+    // one arrival per warp, after every lane's shared/tensor-memory accesses
+    auto warp_arrive = [&](int b) {
+        fence_async_smem();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[b]);
+    };
 
-    // fp32 state slice in registers: rows 128h + row, columns c0..c0+31;
-    // an fp16 copy in h16 is the B operand of the next chunk's first MMA
+    // fp32 state slice in registers (epilogue warps): rows 128h + row, columns
+    // c0..c0+31; an fp16 copy in h16 is the B operand of the next chunk's C1
     float Hreg[2][32];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int hrow = 128 * h + row;
-        if (h < halves && hrow < dk && p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)hrow * dv + v0 + c0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 f = src[q];
-                Hreg[h][4 * q] = f.x; Hreg[h][4 * q + 1] = f.y; Hreg[h][4 * q + 2] = f.z; Hreg[h][4 * q + 3] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) Hreg[h][q] = 0.f;
-        }
-        if (h < halves && hrow < dk) store_half_row_f16(h16, hrow, c0, Hreg[h]);
-    }
-    if (nchunks > 0) {
-        if (tid == 0) {
-            for (int cidx = 0; cidx < nstages && cidx < nchunks; ++cidx) {
-                issue_loads(cidx);
-                loads_in_flight |= 1 << cidx;
-            }
-        }
-        if (tid < kChunk) load_gb(0, gam_s[tid], bet_s[tid]);
-    }
-    float g_next = 0.f, b_next = 0.f;
-    if (tid < kChunk && nchunks > 1) load_gb(1, g_next, b_next);
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-
-    for (int cidx = 0; cidx < nchunks; ++cidx) {
-        const int s = cidx % nstages;
-        const int gs = cidx & 1;                 // gamma/beta double buffer
-        unsigned char *st = sm + s * L.stage_bytes;
-        const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
-        const int len = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
-        const float *gam = gam_s + gs * kChunk, *bet = bet_s + gs * kChunk;
-
-        if (!mbar_wait(&bar_load[s], load_uses[s] & 1)) s_err = 1;
-        __syncthreads();
-        if (s_err) break;
-        load_uses[s]++;
-        if (tid == 0) loads_in_flight &= ~(1 << s);
-        // C1: D1 = [K; Q] H   (A K-major from the stack, B = h16 MN-major)
-        if (tid == 0) {
-            const uint32_t id = idesc_f16(128, 64, false, true);
-            for (int b = 0; b < L.blocks; ++b)
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tbase, sw128_desc(smem_u32(st + b * 2 * kTileBytes) + 32 * ks, 16, 1024),
-                            sw128_desc(smem_u32(h16) + (b * 4 + ks) * 2048, 8192, 1024), id,
-                            (b | ks) != 0);
-            mma_commit(bar_mma);
-        }
-        if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
-        mma_phase++;
-        __syncthreads();
-        if (s_err) break;
-        fence_after_sync();
-        // E1: R = beta (V - e^gam K H) -> r16 (rows = tokens, MN-major B of C2)
-        if (row < kChunk) {
-            float kh[32], vv[32];
-            tmem_ld32(tD1, kh);
-            load_half_row_f16(st + L.v, row, c0, vv);
-            const float eg = expf(gam[row]), bb = bet[row];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) kh[q] = bb * (vv[q] - eg * kh[q]);
-            store_half_row_f16(r16, row, c0, kh);
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        // C2: D2 = [T; P T] R
-        if (tid == 0) {
-            const uint32_t id = idesc_f16(128, 64, false, true);
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16(tbase + 64, sw128_desc(smem_u32(st + L.tpt) + 32 * ks, 16, 1024),
-                        sw128_desc(smem_u32(r16) + 2048 * ks, 8192, 1024), id, ks != 0);
-            mma_commit(bar_mma);
-        }
-        if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
-        mma_phase++;
-        __syncthreads();
-        if (s_err) break;
-        fence_after_sync();
-        const float gL = gam[kChunk - 1];
-        // E2: rows 0..63: Vn' = e^{gam_L - gam} Vn -> vn16; rows 64..127: O = e^gam (Q H) + P Vn -> o
-        if (row < kChunk) {
-            float a[32];
-            tmem_ld32(tD2, a);
-            const float sc = expf(gL - gam[row]);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) a[q] *= sc;
-            store_half_row_f16(vn16, row, c0, a);
-        } else {
-            const int i = row - kChunk;
-            float a[32], b2[32];
-            tmem_ld32(tD1, a);
-            tmem_ld32(tD2, b2);
-            if (i < len) {
-                const float eg = expf(gam[i]);
-                uint4 *dst = reinterpret_cast<uint4 *>(o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0 + c0);
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint4 u;
-                    __half2 *hh = reinterpret_cast<__half2 *>(&u);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        hh[e] = __floats2half2_rn(fmaf(eg, a[8 * ch + 2 * e], b2[8 * ch + 2 * e]) * d.scale,
-                                                  fmaf(eg, a[8 * ch + 2 * e + 1], b2[8 * ch + 2 * e + 1]) * d.scale);
-                    dst[ch] = u;
-                }
-            }
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        // C4: dH[h] = K^T Vn'   (A = K rows of the stack read MN-major, B = vn16 MN-major)
-        if (tid == 0) {
-            const uint32_t id = idesc_f16(128, 64, true, true);
-            // dk = 64 has a single 64-row block: LBO 0 repeats it as rows 64..127 (ignored)
-            const uint32_t lbo = dk >= 128 ? 2 * kTileBytes : 0;
-            for (int h = 0; h < halves; ++h)
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tbase + 128 + 64 * h,
-                            sw128_desc(smem_u32(st + (2 * h) * 2 * kTileBytes) + 2048 * ks, lbo, 1024),
-                            sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id, ks != 0);
-            mma_commit(bar_mma);
-        }
-        if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
-        mma_phase++;
-        __syncthreads();
-        if (s_err) break;
-        fence_after_sync();
-        // E4: H = e^{gam_L} H + dH (fp32 in registers) -> h16; final state after the last chunk
-        {
-            const float eL = expf(gL);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int hrow = 128 * h + row;
-                if (h >= halves) break;
-                float a[32];
-                tmem_ld32(tDH + 64 * h, a);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) Hreg[h][q] = fmaf(eL, Hreg[h][q], a[q]);
-                if (hrow < dk) {
-                    store_half_row_f16(h16, hrow, c0, Hreg[h]);
-                    if (cidx == nchunks - 1 && p.hT) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
-                    }
-                }
-            }
-        }
-        if (tid < kChunk && cidx + 1 < nchunks) {
-            gam_s[(gs ^ 1) * kChunk + tid] = g_next;
-            bet_s[(gs ^ 1) * kChunk + tid] = b_next;
-            if (cidx + 2 < nchunks) load_gb(cidx + 2, g_next, b_next);
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        // refill this stage with chunk cidx + nstages (its last reader, C4, is done)
-        if (tid == 0 && cidx + nstages < nchunks) {
-            issue_loads(cidx + nstages);
-            loads_in_flight |= 1 << s;
-        }
-    }
-    if (nchunks == 0 && p.hT) {      // empty sequence: final state = initial state
+    if (!ctrl) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int hrow = 128 * h + row;
-            if (h >= halves || hrow >= dk) continue;
-            float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
+            if (h < halves && hrow < dk && p.h0) {
+                const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)hrow * dv + v0 + c0);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
+                for (int q = 0; q < 8; ++q) {
+                    const float4 f = src[q];
+                    Hreg[h][4 * q] = f.x; Hreg[h][4 * q + 1] = f.y; Hreg[h][4 * q + 2] = f.z; Hreg[h][4 * q + 3] = f.w;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) Hreg[h][q] = 0.f;
+            }
+            if (h < halves && hrow < dk) store_half_row_f16(h16, hrow, c0, Hreg[h]);
         }
     }
-    if (s_err && tid == 0) {
+    if (nchunks > 0 && tid < kChunk) load_gb(0, gam_s[tid], bet_s[tid]);
+    float g_next = 0.f, b_next = 0.f;
+    if (tid < kChunk && nchunks > 1) load_gb(1, g_next, b_next);
+    fence_async_smem();
+    __syncthreads();
+
+    if (ctrl) {
+        // ------------------------------------------------------ control warp
+        if (lane == 0) {
+            for (int cidx = 0; cidx < nstages && cidx < nchunks; ++cidx) issue_loads(cidx);
+            const uint32_t id_c1 = idesc_f16(128, 64, false, true);
+            const uint32_t id_c4 = idesc_f16(128, 64, true, true);
+            // dk = 64 has a single 64-row block: LBO 0 repeats it as rows 64..127 (ignored)
+            const uint32_t lbo4 = dk >= 128 ? 2 * kTileBytes : 0;
+            for (int cidx = 0; cidx < nchunks; ++cidx) {
+                const int s = cidx % nstages;
+                const uint32_t ph = cidx & 1;
+                unsigned char *st = sm + s * L.stage_bytes;
+                if (!wait(B_LOAD0 + s, (cidx / nstages) & 1)) break;
+                if (cidx > 0 && (!wait(B_H, ph ^ 1) || !wait(B_O, ph ^ 1))) break;
+                fence_after_sync();
+                // C1: D1 = [K; Q] H
+                for (int b = 0; b < L.blocks; ++b)
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tbase, sw128_desc(smem_u32(st + b * 2 * kTileBytes) + 32 * ks, 16, 1024),
+                                sw128_desc(smem_u32(h16) + (b * 4 + ks) * 2048, 8192, 1024), id_c1,
+                                (b | ks) != 0);
+                mma_commit(&bar[B_C1]);
+                // C2: D2 = [T; P T] R, once R is written
+                if (!wait(B_R, ph)) break;
+                fence_after_sync();
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tbase + 64, sw128_desc(smem_u32(st + L.tpt) + 32 * ks, 16, 1024),
+                            sw128_desc(smem_u32(r16) + 2048 * ks, 8192, 1024), id_c1, ks != 0);
+                mma_commit(&bar[B_C2]);
+                // C4: dH[h] = K^T Vn', once Vn' is written
+                if (!wait(B_VN, ph)) break;
+                fence_after_sync();
+                for (int h = 0; h < halves; ++h)
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tbase + 128 + 64 * h,
+                                sw128_desc(smem_u32(st + (2 * h) * 2 * kTileBytes) + 2048 * ks, lbo4, 1024),
+                                sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id_c4, ks != 0);
+                mma_commit(&bar[B_C4]);
+                // refill this stage once C4 (its last reader) is done
+                if (cidx + nstages < nchunks) {
+                    if (!wait(B_C4, ph)) break;
+                    issue_loads(cidx + nstages);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue warps
+        const bool top = row < kChunk;         // rows 0..63 (R, Vn) vs 64..127 (O)
+        for (int cidx = 0; cidx < nchunks; ++cidx) {
+            const int s = cidx % nstages;
+            const uint32_t ph = cidx & 1;
+            const int gs = cidx & 1;
+            unsigned char *st = sm + s * L.stage_bytes;
+            const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
+            const int len = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
+            const float *gam = gam_s + gs * kChunk, *bet = bet_s + gs * kChunk;
+            // gam/bet of this chunk are read only after C1 (top rows) or C2 (the
+            // others) completed: both follow every warp's arrival for the last chunk
+            if (top) {
+                // E1: R = beta (V - e^gam K H) -> r16
+                if (!wait(B_LOAD0 + s, (cidx / nstages) & 1) || !wait(B_C1, ph)) break;
+                fence_after_sync();
+                {
+                    float kh[32], vv[32];
+                    tmem_ld32(tD1, kh);
+                    load_half_row_f16(st + L.v, row, c0, vv);
+                    const float eg = expf(gam[row]), bb = bet[row];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) kh[q] = bb * (vv[q] - eg * kh[q]);
+                    store_half_row_f16(r16, row, c0, kh);
+                }
+                warp_arrive(B_R);
+                // E2a: Vn' = e^{gam_L - gam} Vn -> vn16
+                if (!wait(B_C2, ph)) break;
+                fence_after_sync();
+                {
+                    float a[32];
+                    tmem_ld32(tD2, a);
+                    const float sc = expf(gam[kChunk - 1] - gam[row]);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) a[q] *= sc;
+                    store_half_row_f16(vn16, row, c0, a);
+                }
+                warp_arrive(B_VN);
+            } else {
+                // E2b: O = e^gam (Q H) + P Vn -> o   (off the critical path)
+                if (!wait(B_C2, ph)) break;
+                fence_after_sync();
+                const int i = row - kChunk;
+                float a[32], b2[32];
+                tmem_ld32(tD1, a);
+                tmem_ld32(tD2, b2);
+                warp_arrive(B_O);
+                if (i < len) {
+                    const float eg = expf(gam[i]);
+                    uint4 *dst = reinterpret_cast<uint4 *>(o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0 + c0);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint4 u;
+                        __half2 *hh = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            hh[e] = __floats2half2_rn(fmaf(eg, a[8 * ch + 2 * e], b2[8 * ch + 2 * e]) * d.scale,
+                                                      fmaf(eg, a[8 * ch + 2 * e + 1], b2[8 * ch + 2 * e + 1]) * d.scale);
+                        dst[ch] = u;
+                    }
+                }
+            }
+            // E4: H = e^{gam_L} H + dH (fp32 in registers) -> h16; final state after the last chunk
+            if (!wait(B_C4, ph)) break;
+            fence_after_sync();
+            {
+                const float eL = expf(gam[kChunk - 1]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int hrow = 128 * h + row;
+                    if (h >= halves) break;
+                    float a[32];
+                    tmem_ld32(tDH + 64 * h, a);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) Hreg[h][q] = fmaf(eL, Hreg[h][q], a[q]);
+                    if (hrow < dk) {
+                        store_half_row_f16(h16, hrow, c0, Hreg[h]);
+                        if (cidx == nchunks - 1 && p.hT) {
+                            float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
+                        }
+                    }
+                }
+            }
+            if (tid < kChunk && cidx + 1 < nchunks) {
+                gam_s[(gs ^ 1) * kChunk + tid] = g_next;
+                bet_s[(gs ^ 1) * kChunk + tid] = b_next;
+                if (cidx + 2 < nchunks) load_gb(cidx + 2, g_next, b_next);
+            }
+            warp_arrive(B_H);
+        }
+        if (nchunks == 0 && p.hT) {      // empty sequence: final state = initial state
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int hrow = 128 * h + row;
+                if (h >= halves || hrow >= dk) continue;
+                float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
+            }
+        }
+    }
+    __syncthreads();
+    if (s_err && tid == kEpiWarps * 32) {
+        // drain: bounded waits for this CTA's own copies and MMAs before freeing TMEM
         set_timeout(p);
-        for (int s = 0; s < 2; ++s)
-            if (loads_in_flight & (1 << s)) mbar_wait(&bar_load[s], load_uses[s] & 1);
-        mbar_wait(bar_mma, mma_phase & 1);
+        for (int b = B_LOAD0; b <= B_LOAD1; ++b) { mbar_wait(&bar[b], 0); mbar_wait(&bar[b], 1); }
+        mbar_wait(&bar[B_C4], 0);
+        mbar_wait(&bar[B_C4], 1);
     }
     fence_before_sync();
     __syncthreads();
