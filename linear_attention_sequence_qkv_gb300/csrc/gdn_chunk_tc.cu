@@ -225,24 +225,33 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
     for (int e = tid; e < kChunk * LDA; e += kThreads) Ts[e] = 0.f;
     fence_before_sync();
     __syncthreads();
-    // T = (I + A)^{-1}: 16x16 diagonal blocks by forward substitution ...
+    // T = (I + A)^{-1}: 16x16 diagonal blocks by forward substitution, one
+    // column per thread with the column in registers (x[m] = 0 above the
+    // diagonal makes the unrolled triangle exact) ...
     if (tid < kChunk) {
         const int blk = tid >> 4, cc = tid & 15, o0 = blk * 16;
-        for (int r = cc; r < 16; ++r) {
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
             float val = (r == cc) ? 1.f : 0.f;
-            for (int m = cc; m < r; ++m) val -= As[(o0 + r) * LDA + o0 + m] * Ts[(o0 + m) * LDA + o0 + cc];
-            Ts[(o0 + r) * LDA + o0 + cc] = val;
+#pragma unroll
+            for (int m = 0; m < r; ++m) val = fmaf(-As[(o0 + r) * LDA + o0 + m], x[m], val);
+            x[r] = val;
         }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Ts[(o0 + r) * LDA + o0 + cc] = x[r];
     }
     __syncthreads();
     // ... then one block diagonal at a time: T[bi][bj] = -T[bi][bi] sum_m A[bi][m] T[m][bj]
+#pragma unroll
     for (int dd = 1; dd < 4; ++dd) {
         const int npairs = 4 - dd;
         for (int e = tid; e < npairs * 256; e += kThreads) {
             const int pr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int bj = pr, bi = pr + dd;
             float x = 0.f;
-            for (int m = bj * 16; m < bi * 16; ++m) x += As[(bi * 16 + r) * LDA + m] * Ts[m * LDA + bj * 16 + cc];
+#pragma unroll
+            for (int m = 0; m < 16 * dd; ++m) x = fmaf(As[(bi * 16 + r) * LDA + bj * 16 + m], Ts[(bj * 16 + m) * LDA + bj * 16 + cc], x);
             Xs[pr * 256 + r * 16 + cc] = x;
         }
         __syncthreads();
@@ -250,7 +259,8 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
             const int pr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int bj = pr, bi = pr + dd;
             float t = 0.f;
-            for (int m = 0; m < 16; ++m) t += Ts[(bi * 16 + r) * LDA + bi * 16 + m] * Xs[pr * 256 + m * 16 + cc];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) t = fmaf(Ts[(bi * 16 + r) * LDA + bi * 16 + m], Xs[pr * 256 + m * 16 + cc], t);
             Ts[(bi * 16 + r) * LDA + bj * 16 + cc] = -t;
         }
         __syncthreads();
