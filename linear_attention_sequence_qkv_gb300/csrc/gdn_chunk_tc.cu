@@ -104,20 +104,24 @@ __device__ __forceinline__ void load_half_row_f16(const unsigned char *tile, int
 }
 
 // ================================================================ prep kernel
+constexpr int kPrepThreads = 256;   // 8 warps: warps w and w+4 share TMEM lanes, split columns
+
 struct PrepSmem {
     int blocks;            // dk / 64
+    int bpp;               // dk blocks per load phase (operand buffers hold bpp blocks)
     size_t hi, lo, As, Ts, Xs, tp, gam, bet, bars, total;
     __host__ __device__ PrepSmem(int dk) {
         blocks = dk / 64;
+        bpp = blocks < 2 ? blocks : 2;
         size_t o = 0;
-        hi = o; o += (size_t)blocks * 2 * kTileBytes;
-        lo = o;                                      // lo stack; reused by the solve after S1
-        As = lo;
+        hi = o; o += (size_t)bpp * 2 * kTileBytes;
+        lo = o; o += (size_t)bpp * 2 * kTileBytes;
+        // the solve's fp32 scratch reuses the operand buffers once S1 is done
+        As = 0;
         Ts = As + kChunk * LDA * 4;
         Xs = Ts + kChunk * LDA * 4;
-        size_t solve_end = Xs + 768 * 4;
-        size_t lo_end = lo + (size_t)blocks * 2 * kTileBytes;
-        o = (solve_end > lo_end ? solve_end : lo_end);
+        const size_t solve_end = Xs + 768 * 4;
+        if (solve_end > o) o = solve_end;
         o = (o + 1023) & ~(size_t)1023;
         tp = o; o += kTPTBytes;
         gam = o; o += kChunk * 4;
@@ -127,13 +131,15 @@ struct PrepSmem {
     }
 };
 
-__global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
-                                                              const Problem p, int64_t nslots,
-                                                              unsigned char *tpt) {
+__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
+                                                                     const Problem p, int64_t nslots,
+                                                                     unsigned char *tpt) {
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const gdn_desc &d = p.d;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int row = tid & 127;                 // TMEM lane = tile row
+    const int c0 = (tid >> 7) * 32;            // its 32 of the 64 columns
     const int j = blockIdx.y;
     const int64_t slot = blockIdx.x;
     if (p.cu != nullptr && *p.status != GDN_OK) return;
@@ -146,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
     float *gam = (float *)(sm + L.gam), *bet = (float *)(sm + L.bet);
     uint64_t *bar_load = (uint64_t *)(sm + L.bars), *bar_mma = bar_load + 1;
     uint32_t *tslot = (uint32_t *)(bar_load + 2);
-    __shared__ int s_err;
+    __shared__ volatile int s_err;
 
     if (tid == 0) {
         s_err = 0;
@@ -159,70 +165,83 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
-    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_addr = tbase + ((uint32_t)((warp & 3) * 32) << 16) + c0;
+    const int nphase = L.blocks / L.bpp;
+    uint32_t load_phase = 0, mma_phase = 0;
     bool load_out = false, mma_out = false;
 
-    if (tid == 0) {
-        mbar_expect_tx(bar_load, (uint32_t)L.blocks * 4 * kTileBytes);
-        const int y = (int)((int64_t)hk * p.ntok + c.tok0);
-        for (int b = 0; b < L.blocks; ++b) {
-            tma_load_2d(hi + b * 2 * kTileBytes, &maps.k_hi, 64 * b, y, bar_load);
-            tma_load_2d(hi + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, y, bar_load);
-            tma_load_2d(lo + b * 2 * kTileBytes, &maps.k_lo, 64 * b, y, bar_load);
-            tma_load_2d(lo + b * 2 * kTileBytes + kTileBytes, &maps.q_lo, 64 * b, y, bar_load);
-        }
-    }
-    load_out = true;
     if (tid < kChunk) {
         const float *gw = (const float *)p.gamma + (int64_t)j * p.ntok;
         const int i = tid < c.len ? tid : c.len - 1;
         gam[tid] = gw[c.tok0 + i];
         bet[tid] = tid < c.len ? p.beta[(int64_t)j * p.ntok + c.tok0 + tid] : 0.f;
     }
-    if (!mbar_wait(bar_load, 0)) s_err = 1;
-    __syncthreads();
-    if (s_err) goto cleanup;
-    load_out = false;
-
-    // S1 = [Kh;Qh] Kh^T + [Kh;Qh] Kl^T + [Kl;Ql] Kh^T  -> TMEM cols [0, 64)
-    if (tid == 0) {
-        const uint32_t id = idesc_f16(128, 64, false, false);
-        for (int b = 0; b < L.blocks; ++b)
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t oh = smem_u32(hi + b * 2 * kTileBytes) + 32 * ks;
-                const uint32_t ol = smem_u32(lo + b * 2 * kTileBytes) + 32 * ks;
-                const uint64_t ah = sw128_desc(oh, 16, 1024), al = sw128_desc(ol, 16, 1024);
-                mma_f16(tbase, ah, ah, id, (b | ks) != 0);
-                mma_f16(tbase, ah, al, id, 1);
-                mma_f16(tbase, al, ah, id, 1);
+    // S1 = [Kh;Qh] Kh^T + [Kh;Qh] Kl^T + [Kl;Ql] Kh^T  -> TMEM cols [0, 64),
+    // dk blocks streamed through the operand buffers bpp at a time
+    for (int ph = 0; ph < nphase; ++ph) {
+        if (tid == 0) {
+            mbar_expect_tx(bar_load, (uint32_t)L.bpp * 4 * kTileBytes);
+            const int y = (int)((int64_t)hk * p.ntok + c.tok0);
+            for (int q = 0; q < L.bpp; ++q) {
+                const int b = ph * L.bpp + q;
+                tma_load_2d(hi + q * 2 * kTileBytes, &maps.k_hi, 64 * b, y, bar_load);
+                tma_load_2d(hi + q * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, y, bar_load);
+                tma_load_2d(lo + q * 2 * kTileBytes, &maps.k_lo, 64 * b, y, bar_load);
+                tma_load_2d(lo + q * 2 * kTileBytes + kTileBytes, &maps.q_lo, 64 * b, y, bar_load);
             }
-        mma_commit(bar_mma);
+        }
+        load_out = true;
+        if (!mbar_wait(bar_load, load_phase & 1)) s_err = 1;
+        load_phase++;
+        __syncthreads();
+        if (s_err) goto cleanup;
+        load_out = false;
+        if (tid == 0) {
+            const uint32_t id = idesc_f16(128, 64, false, false);
+            for (int q = 0; q < L.bpp; ++q)
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t oh = smem_u32(hi + q * 2 * kTileBytes) + 32 * ks;
+                    const uint32_t ol = smem_u32(lo + q * 2 * kTileBytes) + 32 * ks;
+                    const uint64_t ah = sw128_desc(oh, 16, 1024), al = sw128_desc(ol, 16, 1024);
+                    mma_f16(tbase, ah, ah, id, (ph | q | ks) != 0);
+                    mma_f16(tbase, ah, al, id, 1);
+                    mma_f16(tbase, al, ah, id, 1);
+                }
+            mma_commit(bar_mma);
+        }
+        mma_out = true;
+        // the buffers are reused by the next phase (and by the solve) once these MMAs are done
+        if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
+        mma_phase++;
+        __syncthreads();
+        if (s_err) goto cleanup;
+        mma_out = false;
     }
-    mma_out = true;
-    if (!mbar_wait(bar_mma, 0)) s_err = 1;
-    __syncthreads();
-    if (s_err) goto cleanup;
-    mma_out = false;
     fence_after_sync();
 
     {   // decay masks: rows 0..63 -> A (fp32, solve input); rows 64..127 -> P (fp16 tile)
-        float v[64];
-        tmem_ld64(lane_addr, v);
-        if (tid < kChunk) {
-            const int i = tid;
+        float v[32];
+        tmem_ld32(lane_addr, v);
+        if (row < kChunk) {
+            const int i = row;
             const float gi = gam[i], bi = bet[i];
 #pragma unroll
-            for (int jj = 0; jj < kChunk; ++jj)
-                As[i * LDA + jj] = jj < i ? bi * expf(gi - gam[jj]) * v[jj] : 0.f;
+            for (int q = 0; q < 32; ++q) {
+                const int jj = c0 + q;
+                As[i * LDA + jj] = jj < i ? bi * __expf(gi - gam[jj]) * v[q] : 0.f;
+            }
         } else {
-            const int i = tid - kChunk;
+            const int i = row - kChunk;
             const float gi = gam[i];
 #pragma unroll
-            for (int jj = 0; jj < kChunk; ++jj) v[jj] = jj <= i ? expf(gi - gam[jj]) * v[jj] : 0.f;
-            store_row_f16(tp, tid, v);
+            for (int q = 0; q < 32; ++q) {
+                const int jj = c0 + q;
+                v[q] = jj <= i ? __expf(gi - gam[jj]) * v[q] : 0.f;
+            }
+            store_half_row_f16(tp, row, c0, v);
         }
     }
-    for (int e = tid; e < kChunk * LDA; e += kThreads) Ts[e] = 0.f;
+    for (int e = tid; e < kChunk * LDA; e += kPrepThreads) Ts[e] = 0.f;
     fence_before_sync();
     __syncthreads();
     // T = (I + A)^{-1}: 16x16 diagonal blocks by forward substitution, one
@@ -246,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
 #pragma unroll
     for (int dd = 1; dd < 4; ++dd) {
         const int npairs = 4 - dd;
-        for (int e = tid; e < npairs * 256; e += kThreads) {
+        for (int e = tid; e < npairs * 256; e += kPrepThreads) {
             const int pr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int bj = pr, bi = pr + dd;
             float x = 0.f;
@@ -255,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
             Xs[pr * 256 + r * 16 + cc] = x;
         }
         __syncthreads();
-        for (int e = tid; e < npairs * 256; e += kThreads) {
+        for (int e = tid; e < npairs * 256; e += kPrepThreads) {
             const int pr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int bj = pr, bi = pr + dd;
             float t = 0.f;
@@ -265,11 +284,12 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
         }
         __syncthreads();
     }
-    if (tid < kChunk) {   // T rows into the fp16 tile (rows 0..63)
-        float v[64];
+    if (tid < 2 * kChunk) {   // T rows into the fp16 tile (rows 0..63), 32 columns per thread
+        const int r = tid & 63, h = (tid >> 6) * 32;
+        float v[32];
 #pragma unroll
-        for (int jj = 0; jj < kChunk; ++jj) v[jj] = Ts[tid * LDA + jj];
-        store_row_f16(tp, tid, v);
+        for (int q = 0; q < 32; ++q) v[q] = Ts[r * LDA + h + q];
+        store_half_row_f16(tp, r, h, v);
     }
     fence_async_smem();
     __syncthreads();
@@ -282,29 +302,30 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const __grid_const
         mma_commit(bar_mma);
     }
     mma_out = true;
-    if (!mbar_wait(bar_mma, 1)) s_err = 1;
+    if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
+    mma_phase++;
     __syncthreads();
     if (s_err) goto cleanup;
     mma_out = false;
     fence_after_sync();
-    if (tid >= kChunk) {   // P T replaces P in rows 64..127
-        float v[64];
-        tmem_ld64(lane_addr + 64, v);
-        store_row_f16(tp, tid, v);
+    if (row >= kChunk) {   // P T replaces P in rows 64..127
+        float v[32];
+        tmem_ld32(lane_addr + 64, v);
+        store_half_row_f16(tp, row, c0, v);
     }
     __syncthreads();
     {
         uint4 *dst = reinterpret_cast<uint4 *>(tpt + ((int64_t)j * nslots + slot) * kTPTBytes);
         const uint4 *src = reinterpret_cast<const uint4 *>(tp);
-        for (int e = tid; e < (int)(kTPTBytes / 16); e += kThreads) dst[e] = src[e];
+        for (int e = tid; e < (int)(kTPTBytes / 16); e += kPrepThreads) dst[e] = src[e];
     }
 
 cleanup:
     if (s_err) {
         if (tid == 0) {
             set_timeout(p);
-            if (load_out) mbar_wait(bar_load, 0);
-            if (mma_out) { mbar_wait(bar_mma, 0); mbar_wait(bar_mma, 1); }
+            if (load_out) mbar_wait(bar_load, load_phase & 1);
+            if (mma_out) mbar_wait(bar_mma, mma_phase & 1);
         }
     }
     fence_before_sync();
@@ -694,7 +715,7 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
                                              (int)ps.total);
         if (e != cudaSuccess) return e;
         if (nslots > 0) {
-            chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hv), kThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt);
+            chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hv), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
