@@ -40,6 +40,8 @@ constexpr int kThreads = 128;
 constexpr int LDA = kChunk + 1;
 constexpr uint32_t kTileBytes = 64 * 128;      // one 64x64 fp16 tile (8 KB)
 constexpr uint32_t kTPTBytes = 2 * kTileBytes; // [T; P T] 128x64 fp16
+constexpr uint32_t kXBytes = 2 * kTileBytes;   // X = [K_c; Q_c] K_{c-1}^T, 128x64 fp16
+constexpr uint32_t kPrepOut = kTPTBytes + kXBytes;   // per (v head, chunk) in the workspace
 
 struct PrepMaps {
     CUtensorMap q_hi, q_lo, k_hi, k_lo;
@@ -109,13 +111,14 @@ constexpr int kPrepThreads = 256;   // 8 warps: warps w and w+4 share TMEM lanes
 struct PrepSmem {
     int blocks;            // dk / 64
     int bpp;               // dk blocks per load phase (operand buffers hold bpp blocks)
-    size_t hi, lo, As, Ts, Xs, tp, gam, bet, bars, total;
+    size_t hi, lo, kp, As, Ts, Xs, tp, gam, bet, bars, total;
     __host__ __device__ PrepSmem(int dk) {
         blocks = dk / 64;
         bpp = blocks < 2 ? blocks : 2;
         size_t o = 0;
         hi = o; o += (size_t)bpp * 2 * kTileBytes;
         lo = o; o += (size_t)bpp * 2 * kTileBytes;
+        kp = o; o += (size_t)bpp * kTileBytes;       // K of the previous chunk (hi)
         // the solve's fp32 scratch reuses the operand buffers once S1 is done
         As = 0;
         Ts = As + kChunk * LDA * 4;
@@ -147,12 +150,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
     if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, c)) return;
     const int hk = j / (d.Hv / d.Hk);
     const PrepSmem L(d.dk);
-    unsigned char *hi = sm + L.hi, *lo = sm + L.lo, *tp = sm + L.tp;
+    unsigned char *hi = sm + L.hi, *lo = sm + L.lo, *kp = sm + L.kp, *tp = sm + L.tp;
     float *As = (float *)(sm + L.As), *Ts = (float *)(sm + L.Ts), *Xs = (float *)(sm + L.Xs);
     float *gam = (float *)(sm + L.gam), *bet = (float *)(sm + L.bet);
     uint64_t *bar_load = (uint64_t *)(sm + L.bars), *bar_mma = bar_load + 1;
     uint32_t *tslot = (uint32_t *)(bar_load + 2);
     __shared__ volatile int s_err;
+    const bool has_prev = c.tok0 > c.seq0;     // not the first chunk of its sequence
+    unsigned char *out = tpt + ((int64_t)j * nslots + slot) * kPrepOut;
 
     if (tid == 0) {
         s_err = 0;
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
         mbar_init(bar_mma, 1);
         mbar_init_fence();
     }
-    if (warp == 0) tmem_alloc(tslot, 128);
+    if (warp == 0) tmem_alloc(tslot, 256);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -176,11 +181,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
         gam[tid] = gw[c.tok0 + i];
         bet[tid] = tid < c.len ? p.beta[(int64_t)j * p.ntok + c.tok0 + tid] : 0.f;
     }
-    // S1 = [Kh;Qh] Kh^T + [Kh;Qh] Kl^T + [Kl;Ql] Kh^T  -> TMEM cols [0, 64),
-    // dk blocks streamed through the operand buffers bpp at a time
+    // S1 = [Kh;Qh] Kh^T + [Kh;Qh] Kl^T + [Kl;Ql] Kh^T  -> TMEM cols [0, 64), and
+    // X = [Kh;Qh] Kh_prev^T -> cols [128, 192), dk blocks streamed through the
+    // operand buffers bpp at a time
     for (int ph = 0; ph < nphase; ++ph) {
         if (tid == 0) {
-            mbar_expect_tx(bar_load, (uint32_t)L.bpp * 4 * kTileBytes);
+            mbar_expect_tx(bar_load, (uint32_t)L.bpp * (has_prev ? 5 : 4) * kTileBytes);
             const int y = (int)((int64_t)hk * p.ntok + c.tok0);
             for (int q = 0; q < L.bpp; ++q) {
                 const int b = ph * L.bpp + q;
@@ -188,6 +194,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
                 tma_load_2d(hi + q * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, y, bar_load);
                 tma_load_2d(lo + q * 2 * kTileBytes, &maps.k_lo, 64 * b, y, bar_load);
                 tma_load_2d(lo + q * 2 * kTileBytes + kTileBytes, &maps.q_lo, 64 * b, y, bar_load);
+                if (has_prev) tma_load_2d(kp + q * kTileBytes, &maps.k_hi, 64 * b, y - kChunk, bar_load);
             }
         }
         load_out = true;
@@ -206,6 +213,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
                     mma_f16(tbase, ah, ah, id, (ph | q | ks) != 0);
                     mma_f16(tbase, ah, al, id, 1);
                     mma_f16(tbase, al, ah, id, 1);
+                    if (has_prev)
+                        mma_f16(tbase + 128, ah, sw128_desc(smem_u32(kp + q * kTileBytes) + 32 * ks, 16, 1024),
+                                id, (ph | q | ks) != 0);
                 }
             mma_commit(bar_mma);
         }
@@ -219,6 +229,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
     }
     fence_after_sync();
 
+    if (has_prev) {   // X -> workspace, fp16, already in the 128-byte-swizzled tile layout
+        float v[32];
+        tmem_ld32(lane_addr + 128, v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+            *reinterpret_cast<uint4 *>(out + kTPTBytes + sw128_off(row, c0 + 8 * q)) = u;
+        }
+    }
     {   // decay masks: rows 0..63 -> A (fp32, solve input); rows 64..127 -> P (fp16 tile)
         float v[32];
         tmem_ld32(lane_addr, v);
@@ -315,7 +337,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
     }
     __syncthreads();
     {
-        uint4 *dst = reinterpret_cast<uint4 *>(tpt + ((int64_t)j * nslots + slot) * kTPTBytes);
+        uint4 *dst = reinterpret_cast<uint4 *>(out);
         const uint4 *src = reinterpret_cast<const uint4 *>(tp);
         for (int e = tid; e < (int)(kTPTBytes / 16); e += kPrepThreads) dst[e] = src[e];
     }
@@ -330,49 +352,55 @@ cleanup:
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 128);
+    if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // =============================================================== chain kernel
+// Shared memory of the chain kernel: two stages of [K;Q] (dk/64 blocks of 16 KB)
+// plus X (16 KB); one [T; P T] tile; the fp16 state copy h16 (B operand of
+// [K;Q] h16); R and Vn' tiles.
 struct ChainSmem {
-    int blocks, stages;
-    size_t stage_bytes, stack, v, tpt, h16, r16, vn16, gam, bet, bars, total;
-    __host__ __device__ ChainSmem(int dk, int nstages) {
+    int blocks;
+    size_t stage_bytes, x, tpt, h16, r16, vn16, bars, total;
+    __host__ __device__ ChainSmem(int dk) {
         blocks = dk / 64;
-        stages = nstages;
-        stack = 0;
-        v = (size_t)blocks * 2 * kTileBytes;
-        tpt = v + kTileBytes;
-        stage_bytes = tpt + kTPTBytes;
-        size_t o = stage_bytes * stages;
+        x = (size_t)blocks * 2 * kTileBytes;        // inside a stage, after the stack
+        stage_bytes = x + kXBytes;
+        size_t o = 2 * stage_bytes;
+        tpt = o; o += kTPTBytes;
         h16 = o; o += (size_t)(dk < 128 ? 128 : dk) * 128;
         r16 = o; o += kTileBytes;
         vn16 = o; o += kTileBytes;
-        gam = o; o += 2 * kChunk * 4;
-        bet = o; o += 2 * kChunk * 4;
         bars = o; o += 128;
         total = o + 1024;
     }
 };
 
-// 8 epilogue warps (warps w and w+4 share tensor-memory lanes and split the 64
-// columns) plus one control warp that issues every TMA copy and MMA. The roles
-// meet on mbarriers, one arrival per warp, so the control thread issues the next
-// MMA as soon as its operands are written; the output store of rows 64..127 is
-// off the critical path.
-constexpr int kEpiWarps = 8;
-constexpr int kChainThreads = (kEpiWarps + 1) * 32;
-enum ChainBar { B_LOAD0 = 0, B_LOAD1, B_C1, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_COUNT };
+// Warp roles. Warps 0..7 ("row warps"): lanes = rows of the 128-row MMA
+// results, warps w and w+4 split the 64 columns; rows 0..63 produce R and Vn',
+// rows 64..127 the output. Warps 8..15 ("state warps", same lane split) carry
+// the fp32 state in registers and write its fp16 copy. Warp 16 issues every TMA
+// copy and MMA. Roles meet on mbarriers (one arrival per warp).
+//
+// With H_c = e^{gL_c} H_{c-1} + K_c^T Vn'_c, the first product of chunk c splits as
+//   [K_c; Q_c] H_{c-1} = [K_c; Q_c] (e^{gL_{c-1}} H_{c-2}) + X_c Vn'_{c-1},
+//   X_c = [K_c; Q_c] K_{c-1}^T (from the prep kernel),
+// so only X_c Vn'_{c-1} (4 MMAs) waits for the previous chunk; the dk-deep part
+// and the state update run beside the critical path.
+constexpr int kRowWarps = 8, kStateWarps = 8;
+constexpr int kCtrlWarp = kRowWarps + kStateWarps;
+constexpr int kChainThreads = (kCtrlWarp + 1) * 32;
+enum ChainBar { B_LOAD0 = 0, B_LOAD1, B_TPT, B_C1, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_COUNT };
 
 __global__ void __launch_bounds__(kChainThreads, 1)
-chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles, int nstages,
-                   int64_t nslots, const unsigned char *tpt) {
+chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles,
+                   int64_t nslots, const unsigned char *prep_out) {
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const gdn_desc &d = p.d;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool ctrl = warp == kEpiWarps;
-    const int row = tid & 127;                 // TMEM lane = tile row (epilogue warps)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;          // TMEM lane
     const int c0 = ((warp >> 2) & 1) * 32;     // its 32 of the 64 columns
     int bid = blockIdx.x;
     const int tile = bid % ntiles;
@@ -387,69 +415,76 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : seq0 + d.T;
     const int nchunks = (int)((seq1 - seq0 + kChunk - 1) / kChunk);
     const int64_t slot0 = p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk);
-    const ChainSmem L(dk, nstages);
+    const ChainSmem L(dk);
     const int halves = dk >= 128 ? dk / 128 : 1;  // M=128 row groups of the state
-    unsigned char *h16 = sm + L.h16, *r16 = sm + L.r16, *vn16 = sm + L.vn16;
-    float *gam_s = (float *)(sm + L.gam), *bet_s = (float *)(sm + L.bet);
+    unsigned char *tptb = sm + L.tpt, *h16 = sm + L.h16, *r16 = sm + L.r16, *vn16 = sm + L.vn16;
     uint64_t *bar = (uint64_t *)(sm + L.bars);
     uint32_t *tslot = (uint32_t *)(bar + B_COUNT);
     __shared__ volatile int s_err;
     const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
     const float *gw = (const float *)p.gamma + (int64_t)j * p.ntok;
     const float *bw = p.beta + (int64_t)j * p.ntok;
+    const __half *vw = (const __half *)p.v + (int64_t)j * p.ntok * dv;
     __half *o = (__half *)p.o;
 
     if (tid == 0) {
         s_err = 0;
         mbar_init(&bar[B_LOAD0], 1);
         mbar_init(&bar[B_LOAD1], 1);
+        mbar_init(&bar[B_TPT], 1);
         mbar_init(&bar[B_C1], 1);
         mbar_init(&bar[B_C2], 1);
         mbar_init(&bar[B_C4], 1);
-        mbar_init(&bar[B_R], 4);     // rows 0..63: warps 0, 1, 4, 5
+        mbar_init(&bar[B_R], 4);     // row warps of rows 0..63: 0, 1, 4, 5
         mbar_init(&bar[B_VN], 4);
-        mbar_init(&bar[B_O], 4);     // rows 64..127: warps 2, 3, 6, 7
-        mbar_init(&bar[B_H], kEpiWarps);
+        mbar_init(&bar[B_O], 4);     // row warps of rows 64..127: 2, 3, 6, 7
+        mbar_init(&bar[B_H], kStateWarps);
         mbar_init_fence();
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
+    if (warp == 0) tmem_alloc(tslot, 512);
+    // state warps: fp32 state slice in registers (rows 128h + row, columns
+    // c0..c0+31) and its fp16 copy h16 (the B operand of chunk 0's first product)
+    const bool state_warp = warp >= kRowWarps && warp < kCtrlWarp;
+    float Hreg[2][32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int hrow = 128 * h + row;
+        const bool ok = state_warp && h < halves && hrow < dk;
+        if (ok && p.h0) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)hrow * dv + v0 + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 f = src[q];
+                Hreg[h][4 * q] = f.x; Hreg[h][4 * q + 1] = f.y; Hreg[h][4 * q + 2] = f.z; Hreg[h][4 * q + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) Hreg[h][q] = 0.f;
+        }
+        if (ok) store_half_row_f16(h16, hrow, c0, Hreg[h]);
+    }
+    fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tD1 = tbase + lane_off + c0, tD2 = tbase + 64 + lane_off + c0;
-    const uint32_t tDH = tbase + 128 + lane_off + c0;   // + 64 h for row group h
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    // TMEM: D1 (two buffers) at 0 / 64, D2 at 128, dH (row group h) at 192 + 64 h
+    auto tD1 = [&](int c) { return tbase + lane_off + c0 + 64 * (c & 1); };
+    const uint32_t tD2 = tbase + 128 + lane_off + c0;
+    const uint32_t tDH = tbase + 192 + lane_off + c0;
 
-    auto issue_loads = [&](int cidx) {   // control thread
-        const int s = cidx % nstages;
-        unsigned char *st = sm + s * L.stage_bytes;
-        const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
-        const int yk = (int)((int64_t)hk * p.ntok + tok0);
-        const int yv = (int)((int64_t)j * p.ntok + tok0);
-        mbar_expect_tx(&bar[B_LOAD0 + s], (uint32_t)L.blocks * 2 * kTileBytes + kTileBytes + kTPTBytes);
-        for (int b = 0; b < L.blocks; ++b) {
-            tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
-            tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
-        }
-        tma_load_2d(st + L.v, &maps.v, v0, yv, &bar[B_LOAD0 + s]);
-        bulk_load(st + L.tpt, tpt + ((int64_t)j * nslots + slot0 + cidx) * kTPTBytes, kTPTBytes,
-                  &bar[B_LOAD0 + s]);
+    auto chunk_tok0 = [&](int c) { return seq0 + (int64_t)c * kChunk; };
+    auto chunk_len = [&](int c) {
+        const int64_t r = seq1 - chunk_tok0(c);
+        return r < kChunk ? (int)r : kChunk;
     };
-    auto load_gb = [&](int cidx, float &g, float &b) {   // threads < 64
-        const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
-        const int len = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
-        const int i = tid < len ? tid : len - 1;
-        g = gw[tok0 + i];
-        b = tid < len ? bw[tok0 + i] : 0.f;
-    };
-    // wait on an mbarrier phase; a timeout flags the CTA (every role then drains)
+    auto gamma_last = [&](int c) { return gw[chunk_tok0(c) + chunk_len(c) - 1]; };
     auto wait = [&](int b, uint32_t parity) -> bool {
         if (s_err) return false;
         if (!mbar_wait(&bar[b], parity)) { s_err = 1; return false; }
         return true;
     };
-    // one arrival per warp, after every lane's shared/tensor-memory accesses
     auto warp_arrive = [&](int b) {
         fence_async_smem();
         fence_before_sync();
@@ -457,130 +492,154 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         if (lane == 0) mbar_arrive(&bar[b]);
     };
 
-    // fp32 state slice in registers (epilogue warps): rows 128h + row, columns
-    // c0..c0+31; an fp16 copy in h16 is the B operand of the next chunk's C1
-    float Hreg[2][32];
-    if (!ctrl) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int hrow = 128 * h + row;
-            if (h < halves && hrow < dk && p.h0) {
-                const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)hrow * dv + v0 + c0);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 f = src[q];
-                    Hreg[h][4 * q] = f.x; Hreg[h][4 * q + 1] = f.y; Hreg[h][4 * q + 2] = f.z; Hreg[h][4 * q + 3] = f.w;
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 32; ++q) Hreg[h][q] = 0.f;
-            }
-            if (h < halves && hrow < dk) store_half_row_f16(h16, hrow, c0, Hreg[h]);
-        }
-    }
-    if (nchunks > 0 && tid < kChunk) load_gb(0, gam_s[tid], bet_s[tid]);
-    float g_next = 0.f, b_next = 0.f;
-    if (tid < kChunk && nchunks > 1) load_gb(1, g_next, b_next);
-    fence_async_smem();
-    __syncthreads();
-
-    if (ctrl) {
+    if (warp == kCtrlWarp) {
         // ------------------------------------------------------ control warp
         if (lane == 0) {
-            for (int cidx = 0; cidx < nstages && cidx < nchunks; ++cidx) issue_loads(cidx);
-            const uint32_t id_c1 = idesc_f16(128, 64, false, true);
-            const uint32_t id_c4 = idesc_f16(128, 64, true, true);
+            auto load_stage = [&](int c) {
+                const int s = c & 1;
+                unsigned char *st = sm + s * L.stage_bytes;
+                const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
+                const bool with_x = c > 0;
+                mbar_expect_tx(&bar[B_LOAD0 + s], (uint32_t)L.blocks * 2 * kTileBytes + (with_x ? kXBytes : 0));
+                for (int b = 0; b < L.blocks; ++b) {
+                    tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
+                    tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
+                }
+                if (with_x)
+                    bulk_load(st + L.x, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut + kTPTBytes,
+                              kXBytes, &bar[B_LOAD0 + s]);
+            };
+            auto load_tpt = [&](int c) {
+                mbar_expect_tx(&bar[B_TPT], kTPTBytes);
+                bulk_load(tptb, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut, kTPTBytes, &bar[B_TPT]);
+            };
+            const uint32_t id_k = idesc_f16(128, 64, false, true);   // A K-major, B MN-major
+            const uint32_t id_m = idesc_f16(128, 64, true, true);    // A MN-major (K^T), B MN-major
             // dk = 64 has a single 64-row block: LBO 0 repeats it as rows 64..127 (ignored)
             const uint32_t lbo4 = dk >= 128 ? 2 * kTileBytes : 0;
-            for (int cidx = 0; cidx < nchunks; ++cidx) {
-                const int s = cidx % nstages;
-                const uint32_t ph = cidx & 1;
-                unsigned char *st = sm + s * L.stage_bytes;
-                if (!wait(B_LOAD0 + s, (cidx / nstages) & 1)) break;
-                if (cidx > 0 && (!wait(B_H, ph ^ 1) || !wait(B_O, ph ^ 1))) break;
-                fence_after_sync();
-                // C1: D1 = [K; Q] H
-                for (int b = 0; b < L.blocks; ++b)
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tbase, sw128_desc(smem_u32(st + b * 2 * kTileBytes) + 32 * ks, 16, 1024),
-                                sw128_desc(smem_u32(h16) + (b * 4 + ks) * 2048, 8192, 1024), id_c1,
-                                (b | ks) != 0);
-                mma_commit(&bar[B_C1]);
-                // C2: D2 = [T; P T] R, once R is written
-                if (!wait(B_R, ph)) break;
-                fence_after_sync();
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tbase + 64, sw128_desc(smem_u32(st + L.tpt) + 32 * ks, 16, 1024),
-                            sw128_desc(smem_u32(r16) + 2048 * ks, 8192, 1024), id_c1, ks != 0);
-                mma_commit(&bar[B_C2]);
-                // C4: dH[h] = K^T Vn', once Vn' is written
-                if (!wait(B_VN, ph)) break;
-                fence_after_sync();
+            auto issue_c4 = [&](int c) {   // dH = K_c^T Vn'_c
+                unsigned char *st = sm + (c & 1) * L.stage_bytes;
                 for (int h = 0; h < halves; ++h)
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tbase + 128 + 64 * h,
+                        mma_f16(tbase + 192 + 64 * h,
                                 sw128_desc(smem_u32(st + (2 * h) * 2 * kTileBytes) + 2048 * ks, lbo4, 1024),
-                                sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id_c4, ks != 0);
+                                sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id_m, ks != 0);
                 mma_commit(&bar[B_C4]);
-                // refill this stage once C4 (its last reader) is done
-                if (cidx + nstages < nchunks) {
-                    if (!wait(B_C4, ph)) break;
-                    issue_loads(cidx + nstages);
+            };
+            if (nchunks > 0) { load_stage(0); load_tpt(0); }
+            if (nchunks > 1) load_stage(1);
+            int c = 0;
+            for (; c < nchunks; ++c) {
+                const int s = c & 1;
+                unsigned char *st = sm + s * L.stage_bytes;
+                if (!wait(B_LOAD0 + s, (c >> 1) & 1)) break;
+                if (c >= 1 && !wait(B_H, (c - 1) & 1)) break;     // h16 = e^{gL_{c-1}} H_{c-2}
+                fence_after_sync();
+                // C1a: D1 = [K; Q] h16
+                for (int b = 0; b < L.blocks; ++b)
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tD1(c) - lane_off - c0, sw128_desc(smem_u32(st + b * 2 * kTileBytes) + 32 * ks, 16, 1024),
+                                sw128_desc(smem_u32(h16) + (b * 4 + ks) * 2048, 8192, 1024), id_k,
+                                (b | ks) != 0);
+                if (c >= 1) {
+                    // C1b: D1 += X Vn'_{c-1}, then the state update of chunk c-1
+                    if (!wait(B_VN, (c - 1) & 1)) break;
+                    fence_after_sync();
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tD1(c) - lane_off - c0, sw128_desc(smem_u32(st + L.x) + 32 * ks, 16, 1024),
+                                sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id_k, 1);
+                }
+                mma_commit(&bar[B_C1]);
+                if (c >= 1) issue_c4(c - 1);
+                // C2: D2 = [T; P T] R
+                if (!wait(B_TPT, c & 1) || !wait(B_R, c & 1)) break;
+                if (c >= 1 && !wait(B_O, (c - 1) & 1)) break;     // D2 of chunk c-1 consumed
+                fence_after_sync();
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tbase + 128, sw128_desc(smem_u32(tptb) + 32 * ks, 16, 1024),
+                            sw128_desc(smem_u32(r16) + 2048 * ks, 8192, 1024), id_k, ks != 0);
+                mma_commit(&bar[B_C2]);
+                // refills: [T; P T] of chunk c+1 once C2 is done; stage of chunk c-1
+                // (now chunk c+1) once its state update is done
+                if (c + 1 < nchunks) {
+                    if (!wait(B_C2, c & 1)) break;
+                    load_tpt(c + 1);
+                    if (c >= 1) {
+                        if (!wait(B_C4, (c - 1) & 1)) break;
+                        load_stage(c + 1);
+                    }
+                }
+            }
+            if (c == nchunks && nchunks > 0) {   // state update of the last chunk
+                if (wait(B_VN, (nchunks - 1) & 1) && wait(B_H, (nchunks - 1) & 1)) {
+                    fence_after_sync();
+                    issue_c4(nchunks - 1);
                 }
             }
         }
         __syncwarp();
-    } else {
-        // ---------------------------------------------------- epilogue warps
-        const bool top = row < kChunk;         // rows 0..63 (R, Vn) vs 64..127 (O)
-        for (int cidx = 0; cidx < nchunks; ++cidx) {
-            const int s = cidx % nstages;
-            const uint32_t ph = cidx & 1;
-            const int gs = cidx & 1;
-            unsigned char *st = sm + s * L.stage_bytes;
-            const int64_t tok0 = seq0 + (int64_t)cidx * kChunk;
-            const int len = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
-            const float *gam = gam_s + gs * kChunk, *bet = bet_s + gs * kChunk;
-            // gam/bet of this chunk are read only after C1 (top rows) or C2 (the
-            // others) completed: both follow every warp's arrival for the last chunk
+    } else if (warp < kRowWarps) {
+        // ---------------------------------------------------------- row warps
+        const bool top = row < kChunk;
+        const int r = top ? row : row - kChunk;   // token within the chunk
+        // operands of the next chunk, prefetched into registers: V row slice,
+        // gamma and beta of this row, the chunk's last gamma
+        uint4 vq[4];
+        float g_r = 0.f, b_r = 0.f, g_l = 0.f;
+        auto prefetch = [&](int c) {
+            const int64_t t0 = chunk_tok0(c);
+            const int len = chunk_len(c);
+            const int i = r < len ? r : len - 1;
+            g_r = gw[t0 + i];
+            g_l = gw[t0 + len - 1];
             if (top) {
+                b_r = r < len ? bw[t0 + r] : 0.f;
+                const uint4 *src = reinterpret_cast<const uint4 *>(vw + (t0 + i) * dv + v0 + c0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) vq[q] = r < len ? src[q] : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        if (nchunks > 0) prefetch(0);
+        for (int c = 0; c < nchunks; ++c) {
+            const int64_t t0 = chunk_tok0(c);
+            const int len = chunk_len(c);
+            const float gr = g_r, br = b_r, gl = g_l;
+            float vv[32];
+            if (top) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) unpack16<__half>(vq[q], vv + 8 * q);
                 // E1: R = beta (V - e^gam K H) -> r16
-                if (!wait(B_LOAD0 + s, (cidx / nstages) & 1) || !wait(B_C1, ph)) break;
+                if (!wait(B_C1, c & 1)) break;
                 fence_after_sync();
-                {
-                    float kh[32], vv[32];
-                    tmem_ld32(tD1, kh);
-                    load_half_row_f16(st + L.v, row, c0, vv);
-                    const float eg = expf(gam[row]), bb = bet[row];
+                float a[32];
+                tmem_ld32(tD1(c), a);
+                const float eg = __expf(gr);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) kh[q] = bb * (vv[q] - eg * kh[q]);
-                    store_half_row_f16(r16, row, c0, kh);
-                }
+                for (int q = 0; q < 32; ++q) a[q] = br * (vv[q] - eg * a[q]);
+                store_half_row_f16(r16, r, c0, a);
                 warp_arrive(B_R);
+                if (c + 1 < nchunks) prefetch(c + 1);
                 // E2a: Vn' = e^{gam_L - gam} Vn -> vn16
-                if (!wait(B_C2, ph)) break;
+                if (!wait(B_C2, c & 1)) break;
                 fence_after_sync();
-                {
-                    float a[32];
-                    tmem_ld32(tD2, a);
-                    const float sc = expf(gam[kChunk - 1] - gam[row]);
+                tmem_ld32(tD2, a);
+                const float sc = __expf(gl - gr);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) a[q] *= sc;
-                    store_half_row_f16(vn16, row, c0, a);
-                }
+                for (int q = 0; q < 32; ++q) a[q] *= sc;
+                store_half_row_f16(vn16, r, c0, a);
                 warp_arrive(B_VN);
             } else {
                 // E2b: O = e^gam (Q H) + P Vn -> o   (off the critical path)
-                if (!wait(B_C2, ph)) break;
+                if (c + 1 < nchunks) prefetch(c + 1);
+                if (!wait(B_C2, c & 1)) break;
                 fence_after_sync();
-                const int i = row - kChunk;
                 float a[32], b2[32];
-                tmem_ld32(tD1, a);
+                tmem_ld32(tD1(c), a);
                 tmem_ld32(tD2, b2);
                 warp_arrive(B_O);
-                if (i < len) {
-                    const float eg = expf(gam[i]);
-                    uint4 *dst = reinterpret_cast<uint4 *>(o + ((tok0 + i) * Hv + j) * (int64_t)dv + v0 + c0);
+                if (r < len) {
+                    const float eg = __expf(gr);
+                    uint4 *dst = reinterpret_cast<uint4 *>(o + ((t0 + r) * Hv + j) * (int64_t)dv + v0 + c0);
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
                         uint4 u;
@@ -593,38 +652,58 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                     }
                 }
             }
-            // E4: H = e^{gam_L} H + dH (fp32 in registers) -> h16; final state after the last chunk
-            if (!wait(B_C4, ph)) break;
-            fence_after_sync();
-            {
-                const float eL = expf(gam[kChunk - 1]);
+        }
+    } else {
+        // -------------------------------------------------------- state warps
+        auto write_h16 = [&](float scale) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int hrow = 128 * h + row;
-                    if (h >= halves) break;
-                    float a[32];
-                    tmem_ld32(tDH + 64 * h, a);
+            for (int h = 0; h < 2; ++h) {
+                const int hrow = 128 * h + row;
+                if (h < halves && hrow < dk) {
+                    float t[32];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) Hreg[h][q] = fmaf(eL, Hreg[h][q], a[q]);
-                    if (hrow < dk) {
-                        store_half_row_f16(h16, hrow, c0, Hreg[h]);
-                        if (cidx == nchunks - 1 && p.hT) {
+                    for (int q = 0; q < 32; ++q) t[q] = scale * Hreg[h][q];
+                    store_half_row_f16(h16, hrow, c0, t);
+                }
+            }
+        };
+        if (nchunks > 0) {
+            // h16 for chunk 1: e^{gL_0} H_init, once chunk 0's first product is done
+            float gl_next = gamma_last(0);
+            if (wait(B_C1, 0)) {
+                write_h16(__expf(gl_next));
+                warp_arrive(B_H);
+                for (int c = 0; c < nchunks; ++c) {
+                    const float gl = gl_next;
+                    gl_next = c + 1 < nchunks ? gamma_last(c + 1) : 0.f;
+                    if (!wait(B_C4, c & 1)) break;
+                    fence_after_sync();
+                    const float eL = __expf(gl);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h >= halves) break;
+                        float a[32];
+                        tmem_ld32(tDH + 64 * h, a);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) Hreg[h][q] = fmaf(eL, Hreg[h][q], a[q]);
+                    }
+                    // h16 for chunk c+2: e^{gL_{c+1}} H_c
+                    if (c + 2 < nchunks) write_h16(__expf(gl_next));
+                    if (c == nchunks - 1 && p.hT) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int hrow = 128 * h + row;
+                            if (h >= halves || hrow >= dk) continue;
                             float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
                                 dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
                         }
                     }
+                    warp_arrive(B_H);
                 }
             }
-            if (tid < kChunk && cidx + 1 < nchunks) {
-                gam_s[(gs ^ 1) * kChunk + tid] = g_next;
-                bet_s[(gs ^ 1) * kChunk + tid] = b_next;
-                if (cidx + 2 < nchunks) load_gb(cidx + 2, g_next, b_next);
-            }
-            warp_arrive(B_H);
-        }
-        if (nchunks == 0 && p.hT) {      // empty sequence: final state = initial state
+        } else if (p.hT) {               // empty sequence: final state = initial state
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int hrow = 128 * h + row;
@@ -637,16 +716,16 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         }
     }
     __syncthreads();
-    if (s_err && tid == kEpiWarps * 32) {
+    if (s_err && tid == kCtrlWarp * 32) {
         // drain: bounded waits for this CTA's own copies and MMAs before freeing TMEM
         set_timeout(p);
-        for (int b = B_LOAD0; b <= B_LOAD1; ++b) { mbar_wait(&bar[b], 0); mbar_wait(&bar[b], 1); }
+        for (int b = B_LOAD0; b <= B_TPT; ++b) { mbar_wait(&bar[b], 0); mbar_wait(&bar[b], 1); }
         mbar_wait(&bar[B_C4], 0);
         mbar_wait(&bar[B_C4], 1);
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
 // ===================================================================== host
@@ -692,7 +771,7 @@ bool chunk_tc_supports(const gdn_desc &d) {
 
 size_t chunk_tc_workspace(const gdn_desc &d) {
     if (!chunk_tc_supports(d)) return 0;
-    return (size_t)d.Hv * (size_t)chunk_slot_bound(d) * kTPTBytes;
+    return (size_t)d.Hv * (size_t)chunk_slot_bound(d) * kPrepOut;
 }
 
 cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
@@ -729,17 +808,18 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
         memset(&cm, 0, sizeof(cm));
     }
     const int maxs = max_dyn_smem();
-    int nstages = 2;
-    if ((int)ChainSmem(d.dk, 2).total > maxs) nstages = 1;
-    const ChainSmem cs(d.dk, nstages);
-    if ((int)cs.total > maxs) return cudaErrorInvalidValue;
+    const ChainSmem cs(d.dk);
+    // the kernel holds all 512 TMEM columns: request enough shared memory that a
+    // second CTA never shares the SM (its allocation would wait for this one)
+    const size_t smem = cs.total > (size_t)(maxs / 2 + 1024) ? cs.total : (size_t)(maxs / 2 + 1024);
+    if ((int)smem > maxs) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)cs.total);
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     const int ntiles = d.dv / 64;
     const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
     if (blocks == 0) return cudaSuccess;
-    chunk_chain_kernel<<<(unsigned)blocks, kChainThreads, cs.total, s>>>(cm, p, ntiles, nstages, nslots_alloc, tpt);
+    chunk_chain_kernel<<<(unsigned)blocks, kChainThreads, smem, s>>>(cm, p, ntiles, nslots_alloc, tpt);
     return cudaGetLastError();
 }
 
