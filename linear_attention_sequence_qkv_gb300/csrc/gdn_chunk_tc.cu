@@ -559,15 +559,16 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                     mma_f16(tbase + 128, sw128_desc(smem_u32(tptb) + 32 * ks, 16, 1024),
                             sw128_desc(smem_u32(r16) + 2048 * ks, 8192, 1024), id_k, ks != 0);
                 mma_commit(&bar[B_C2]);
-                // refills: [T; P T] of chunk c+1 once C2 is done; stage of chunk c-1
-                // (now chunk c+1) once its state update is done
+                // refills: the stage of chunk c-1 takes chunk c+1 as soon as its state
+                // update (C4 of chunk c-1, issued before C2) is done; [T; P T] of
+                // chunk c+1 once C2 is done
                 if (c + 1 < nchunks) {
-                    if (!wait(B_C2, c & 1)) break;
-                    load_tpt(c + 1);
                     if (c >= 1) {
                         if (!wait(B_C4, (c - 1) & 1)) break;
                         load_stage(c + 1);
                     }
+                    if (!wait(B_C2, c & 1)) break;
+                    load_tpt(c + 1);
                 }
             }
             if (c == nchunks && nchunks > 0) {   // state update of the last chunk
