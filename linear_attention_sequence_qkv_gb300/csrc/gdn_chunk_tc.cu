@@ -378,9 +378,10 @@ struct ChainSmem {
 
 // Warp roles. Warps 0..7 ("row warps"): lanes = rows of the 128-row MMA
 // results, warps w and w+4 split the 64 columns; rows 0..63 produce R and Vn',
-// rows 64..127 the output. Warps 8..15 ("state warps", same lane split) carry
-// the fp32 state in registers and write its fp16 copy. Warp 16 issues every TMA
-// copy and MMA. Roles meet on mbarriers (one arrival per warp).
+// rows 64..127 the output. Warps 8..15 ("state warps", same lane split) update
+// the fp32 state kept in tensor memory and write its fp16 copy. Warp 16 issues
+// every MMA, warp 17 every TMA copy. Roles meet on mbarriers (one arrival per
+// warp).
 //
 // With H_c = e^{gL_c} H_{c-1} + K_c^T Vn'_c, the first product of chunk c splits as
 //   [K_c; Q_c] H_{c-1} = [K_c; Q_c] (e^{gL_{c-1}} H_{c-2}) + X_c Vn'_{c-1},
@@ -388,8 +389,9 @@ struct ChainSmem {
 // so only X_c Vn'_{c-1} (4 MMAs) waits for the previous chunk; the dk-deep part
 // and the state update run beside the critical path.
 constexpr int kRowWarps = 8, kStateWarps = 8;
-constexpr int kCtrlWarp = kRowWarps + kStateWarps;
-constexpr int kChainThreads = (kCtrlWarp + 1) * 32;
+constexpr int kMmaWarp = kRowWarps + kStateWarps;
+constexpr int kLoadWarp = kMmaWarp + 1;
+constexpr int kChainThreads = (kLoadWarp + 1) * 32;
 enum ChainBar { B_LOAD0 = 0, B_LOAD1, B_TPT, B_C1, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_COUNT };
 
 __global__ void __launch_bounds__(kChainThreads, 1)
@@ -426,6 +428,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     const float *bw = p.beta + (int64_t)j * p.ntok;
     const __half *vw = (const __half *)p.v + (int64_t)j * p.ntok * dv;
     __half *o = (__half *)p.o;
+    const bool state_warp = warp >= kRowWarps && warp < kMmaWarp;
 
     if (tid == 0) {
         s_err = 0;
@@ -442,37 +445,16 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         mbar_init_fence();
     }
     if (warp == 0) tmem_alloc(tslot, 512);
-    // state warps: fp32 state slice in registers (rows 128h + row, columns
-    // c0..c0+31) and its fp16 copy h16 (the B operand of chunk 0's first product)
-    const bool state_warp = warp >= kRowWarps && warp < kCtrlWarp;
-    float Hreg[2][32];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int hrow = 128 * h + row;
-        const bool ok = state_warp && h < halves && hrow < dk;
-        if (ok && p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)hrow * dv + v0 + c0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 f = src[q];
-                Hreg[h][4 * q] = f.x; Hreg[h][4 * q + 1] = f.y; Hreg[h][4 * q + 2] = f.z; Hreg[h][4 * q + 3] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) Hreg[h][q] = 0.f;
-        }
-        if (ok) store_half_row_f16(h16, hrow, c0, Hreg[h]);
-    }
-    fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    // TMEM: D1 (two buffers) at 0 / 64, D2 at 128, dH (row group h) at 192 + 64 h
+    // TMEM: D1 (two buffers) at 0 / 64, D2 at 128, dH at 192 + 64 h, H (fp32) at 320 + 64 h
     auto tD1 = [&](int c) { return tbase + lane_off + c0 + 64 * (c & 1); };
     const uint32_t tD2 = tbase + 128 + lane_off + c0;
     const uint32_t tDH = tbase + 192 + lane_off + c0;
+    const uint32_t tH = tbase + 320 + lane_off + c0;
 
     auto chunk_tok0 = [&](int c) { return seq0 + (int64_t)c * kChunk; };
     auto chunk_len = [&](int c) {
@@ -491,9 +473,35 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[b]);
     };
+    // state warps: fp32 state into TMEM and its fp16 copy (chunk 0's B operand)
+    if (state_warp) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int hrow = 128 * h + row;
+            if (h >= halves) break;
+            float t[32];
+            if (hrow < dk && p.h0) {
+                const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)hrow * dv + v0 + c0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 f = src[q];
+                    t[4 * q] = f.x; t[4 * q + 1] = f.y; t[4 * q + 2] = f.z; t[4 * q + 3] = f.w;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) t[q] = 0.f;
+            }
+            tmem_st32(tH + 64 * h, t);
+            if (hrow < dk) store_half_row_f16(h16, hrow, c0, t);
+        }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
 
-    if (warp == kCtrlWarp) {
-        // ------------------------------------------------------ control warp
+    if (warp == kLoadWarp) {
+        // -------------------------------------------------------- TMA warp
         if (lane == 0) {
             auto load_stage = [&](int c) {
                 const int s = c & 1;
@@ -513,41 +521,67 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 mbar_expect_tx(&bar[B_TPT], kTPTBytes);
                 bulk_load(tptb, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut, kTPTBytes, &bar[B_TPT]);
             };
-            const uint32_t id_k = idesc_f16(128, 64, false, true);   // A K-major, B MN-major
-            const uint32_t id_m = idesc_f16(128, 64, true, true);    // A MN-major (K^T), B MN-major
-            // dk = 64 has a single 64-row block: LBO 0 repeats it as rows 64..127 (ignored)
-            const uint32_t lbo4 = dk >= 128 ? 2 * kTileBytes : 0;
-            auto issue_c4 = [&](int c) {   // dH = K_c^T Vn'_c
-                unsigned char *st = sm + (c & 1) * L.stage_bytes;
-                for (int h = 0; h < halves; ++h)
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tbase + 192 + 64 * h,
-                                sw128_desc(smem_u32(st + (2 * h) * 2 * kTileBytes) + 2048 * ks, lbo4, 1024),
-                                sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id_m, ks != 0);
-                mma_commit(&bar[B_C4]);
-            };
             if (nchunks > 0) { load_stage(0); load_tpt(0); }
             if (nchunks > 1) load_stage(1);
+            for (int c = 0; c + 1 < nchunks; ++c) {
+                // [T; P T] of chunk c+1 once C2 of chunk c has read the buffer
+                if (!wait(B_C2, c & 1)) break;
+                load_tpt(c + 1);
+                // chunk c+2 into chunk c's stage once its last reader (C4 of chunk c) is done
+                if (c + 2 < nchunks) {
+                    if (!wait(B_C4, c & 1)) break;
+                    load_stage(c + 2);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------- MMA warp
+        if (lane == 0) {
+            const uint32_t id_k = idesc_f16(128, 64, false, true);   // A K-major, B MN-major
+            const uint32_t id_m = idesc_f16(128, 64, true, true);    // A MN-major (K^T), B MN-major
+            // descriptors are computed once; a K step adds a constant to the start field
+            const uint64_t d_st0 = sw128_desc(smem_u32(sm), 16, 1024);
+            const uint64_t d_h16 = sw128_desc(smem_u32(h16), 8192, 1024);
+            const uint64_t d_vn = sw128_desc(smem_u32(vn16), 8192, 1024);
+            const uint64_t d_r = sw128_desc(smem_u32(r16), 8192, 1024);
+            const uint64_t d_tpt = sw128_desc(smem_u32(tptb), 16, 1024);
+            // dk = 64 has a single 64-row block: LBO 0 repeats it as rows 64..127 (ignored)
+            const uint64_t d_kt0 = sw128_desc(smem_u32(sm), dk >= 128 ? 2 * kTileBytes : 0, 1024);
+            const uint32_t stage16 = (uint32_t)(L.stage_bytes >> 4), x16 = (uint32_t)(L.x >> 4);
+            auto issue_c4 = [&](int c) {   // dH = K_c^T Vn'_c
+                const uint64_t a0 = d_kt0 + (c & 1) * stage16;
+                for (int h = 0; h < halves; ++h)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tbase + 192 + 64 * h, a0 + (uint64_t)((h * 4 * kTileBytes + 2048 * ks) >> 4),
+                                d_vn + (uint64_t)((2048 * ks) >> 4), id_m, ks != 0);
+                mma_commit(&bar[B_C4]);
+            };
+            auto issue_c1a = [&](int c) {  // D1 = [K; Q] h16
+                const uint64_t a0 = d_st0 + (c & 1) * stage16;
+                for (int b = 0; b < L.blocks; ++b)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tbase + 64 * (c & 1), a0 + (uint64_t)((b * 2 * kTileBytes + 32 * ks) >> 4),
+                                d_h16 + (uint64_t)(((b * 4 + ks) * 2048) >> 4), id_k, (b | ks) != 0);
+            };
             int c = 0;
             for (; c < nchunks; ++c) {
                 const int s = c & 1;
-                unsigned char *st = sm + s * L.stage_bytes;
                 if (!wait(B_LOAD0 + s, (c >> 1) & 1)) break;
                 if (c >= 1 && !wait(B_H, (c - 1) & 1)) break;     // h16 = e^{gL_{c-1}} H_{c-2}
                 fence_after_sync();
-                // C1a: D1 = [K; Q] h16
-                for (int b = 0; b < L.blocks; ++b)
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tD1(c) - lane_off - c0, sw128_desc(smem_u32(st + b * 2 * kTileBytes) + 32 * ks, 16, 1024),
-                                sw128_desc(smem_u32(h16) + (b * 4 + ks) * 2048, 8192, 1024), id_k,
-                                (b | ks) != 0);
+                issue_c1a(c);
                 if (c >= 1) {
-                    // C1b: D1 += X Vn'_{c-1}, then the state update of chunk c-1
+                    // C1b: D1 += X Vn'_{c-1} (the only product that waits for chunk c-1)
                     if (!wait(B_VN, (c - 1) & 1)) break;
                     fence_after_sync();
+                    const uint64_t ax = d_st0 + s * stage16 + x16;
+#pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tD1(c) - lane_off - c0, sw128_desc(smem_u32(st + L.x) + 32 * ks, 16, 1024),
-                                sw128_desc(smem_u32(vn16) + 2048 * ks, 8192, 1024), id_k, 1);
+                        mma_f16(tbase + 64 * s, ax + (uint64_t)((32 * ks) >> 4),
+                                d_vn + (uint64_t)((2048 * ks) >> 4), id_k, 1);
                 }
                 mma_commit(&bar[B_C1]);
                 if (c >= 1) issue_c4(c - 1);
@@ -555,21 +589,11 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 if (!wait(B_TPT, c & 1) || !wait(B_R, c & 1)) break;
                 if (c >= 1 && !wait(B_O, (c - 1) & 1)) break;     // D2 of chunk c-1 consumed
                 fence_after_sync();
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tbase + 128, sw128_desc(smem_u32(tptb) + 32 * ks, 16, 1024),
-                            sw128_desc(smem_u32(r16) + 2048 * ks, 8192, 1024), id_k, ks != 0);
+                    mma_f16(tbase + 128, d_tpt + (uint64_t)((32 * ks) >> 4),
+                            d_r + (uint64_t)((2048 * ks) >> 4), id_k, ks != 0);
                 mma_commit(&bar[B_C2]);
-                // refills: the stage of chunk c-1 takes chunk c+1 as soon as its state
-                // update (C4 of chunk c-1, issued before C2) is done; [T; P T] of
-                // chunk c+1 once C2 is done
-                if (c + 1 < nchunks) {
-                    if (c >= 1) {
-                        if (!wait(B_C4, (c - 1) & 1)) break;
-                        load_stage(c + 1);
-                    }
-                    if (!wait(B_C2, c & 1)) break;
-                    load_tpt(c + 1);
-                }
             }
             if (c == nchunks && nchunks > 0) {   // state update of the last chunk
                 if (wait(B_VN, (nchunks - 1) & 1) && wait(B_H, (nchunks - 1) & 1)) {
@@ -605,8 +629,8 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             const int64_t t0 = chunk_tok0(c);
             const int len = chunk_len(c);
             const float gr = g_r, br = b_r, gl = g_l;
-            float vv[32];
             if (top) {
+                float vv[32];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) unpack16<__half>(vq[q], vv + 8 * q);
                 // E1: R = beta (V - e^gam K H) -> r16
@@ -654,70 +678,65 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 }
             }
         }
-    } else {
+    } else if (state_warp) {
         // -------------------------------------------------------- state warps
-        auto write_h16 = [&](float scale) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
+        // H (fp32, TMEM) <- e^{gL_c} H + dH_c; h16 <- e^{gL_{c+1}} H (B operand of chunk c+2)
+        auto final_state = [&]() {
+            for (int h = 0; h < halves; ++h) {
                 const int hrow = 128 * h + row;
-                if (h < halves && hrow < dk) {
-                    float t[32];
+                if (hrow >= dk) continue;
+                float t[32];
+                tmem_ld32(tH + 64 * h, t);
+                float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) t[q] = scale * Hreg[h][q];
-                    store_half_row_f16(h16, hrow, c0, t);
-                }
+                for (int q = 0; q < 8; ++q) dst[q] = make_float4(t[4 * q], t[4 * q + 1], t[4 * q + 2], t[4 * q + 3]);
             }
         };
         if (nchunks > 0) {
             // h16 for chunk 1: e^{gL_0} H_init, once chunk 0's first product is done
             float gl_next = gamma_last(0);
             if (wait(B_C1, 0)) {
-                write_h16(__expf(gl_next));
+                const float e0 = __expf(gl_next);
+                for (int h = 0; h < halves; ++h) {
+                    const int hrow = 128 * h + row;
+                    if (hrow >= dk) continue;
+                    float t[32];
+                    tmem_ld32(tH + 64 * h, t);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) t[q] *= e0;
+                    store_half_row_f16(h16, hrow, c0, t);
+                }
                 warp_arrive(B_H);
                 for (int c = 0; c < nchunks; ++c) {
                     const float gl = gl_next;
                     gl_next = c + 1 < nchunks ? gamma_last(c + 1) : 0.f;
                     if (!wait(B_C4, c & 1)) break;
                     fence_after_sync();
-                    const float eL = __expf(gl);
+                    const float eL = __expf(gl), eN = __expf(gl_next);
+                    for (int h = 0; h < halves; ++h) {
+                        float hv[32], dh[32];
+                        tmem_ld32(tH + 64 * h, hv);
+                        tmem_ld32(tDH + 64 * h, dh);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (h >= halves) break;
-                        float a[32];
-                        tmem_ld32(tDH + 64 * h, a);
+                        for (int q = 0; q < 32; ++q) hv[q] = fmaf(eL, hv[q], dh[q]);
+                        tmem_st32(tH + 64 * h, hv);
+                        const int hrow = 128 * h + row;
+                        if (c + 2 < nchunks && hrow < dk) {
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) Hreg[h][q] = fmaf(eL, Hreg[h][q], a[q]);
-                    }
-                    // h16 for chunk c+2: e^{gL_{c+1}} H_c
-                    if (c + 2 < nchunks) write_h16(__expf(gl_next));
-                    if (c == nchunks - 1 && p.hT) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int hrow = 128 * h + row;
-                            if (h >= halves || hrow >= dk) continue;
-                            float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
+                            for (int q = 0; q < 32; ++q) dh[q] = eN * hv[q];
+                            store_half_row_f16(h16, hrow, c0, dh);
                         }
                     }
                     warp_arrive(B_H);
                 }
+                if (p.hT && !s_err) final_state();
             }
         } else if (p.hT) {               // empty sequence: final state = initial state
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int hrow = 128 * h + row;
-                if (h >= halves || hrow >= dk) continue;
-                float4 *dst = reinterpret_cast<float4 *>(p.hT + sbase + (size_t)hrow * dv + v0 + c0);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = make_float4(Hreg[h][4 * q], Hreg[h][4 * q + 1], Hreg[h][4 * q + 2], Hreg[h][4 * q + 3]);
-            }
+            final_state();
         }
     }
     __syncthreads();
-    if (s_err && tid == kCtrlWarp * 32) {
+    if (s_err && tid == kMmaWarp * 32) {
         // drain: bounded waits for this CTA's own copies and MMAs before freeing TMEM
         set_timeout(p);
         for (int b = B_LOAD0; b <= B_TPT; ++b) { mbar_wait(&bar[b], 0); mbar_wait(&bar[b], 1); }
