@@ -84,6 +84,18 @@ __device__ __forceinline__ void store16_f_cs(T *p, const float *in) {
 
 __device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
+// silu(x) = x * (1 + tanh(x/2)) / 2 with one hardware tanh (relative error
+// ~2^-11): for values that are stored or consumed at 16-bit precision
+__device__ __forceinline__ float silu_fast(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return 0.5f * x * (1.0f + t);
+}
+// the accurate form for fp32 results, the one-instruction form for 16-bit ones
+template <typename T> __device__ __forceinline__ float silu_act(float x) {
+    return sizeof(T) == 4 ? silu_f(x) : silu_fast(x);
+}
+
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // softplus(x) = log(1 + e^x); above 20 the correction is below fp32 resolution

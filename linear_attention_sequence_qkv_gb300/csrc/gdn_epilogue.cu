@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
             const float rn = round_through<T>(wv[i] * (x[i] * inv));
-            y[i] = rn * silu_f(gv[i]);
+            y[i] = rn * silu_act<T>(gv[i]);
         }
         T *out = (T *)p.out + r * dv + cc;
 #pragma unroll

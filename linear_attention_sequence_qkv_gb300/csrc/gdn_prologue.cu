@@ -203,7 +203,8 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
             acc = fmaf(w[i][1], x2[i], acc);
             acc = fmaf(w[i][2], x1[i], acc);
             acc = fmaf(w[i][3], x0[i], acc);
-            y[i] = silu_f(acc);
+            // q/k keep ~fp32 precision (hi + lo planes); v is stored at 16 bits
+            y[i] = norm ? silu_f(acc) : silu_act<S>(acc);
             ss = fmaf(y[i], y[i], ss);
             x3[i] = x2[i];
             x2[i] = x1[i];
