@@ -17,11 +17,14 @@ namespace {
 
 constexpr int kThreads = 256;
 
+constexpr int kRowsPerThread = 2;   // independent rows per thread, loads issued together
+
 template <typename T, typename G, typename W, int NVEC, bool GVEC>
 __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     constexpr int VEC = Vec16<T>::N;
     constexpr int CPT = NVEC * VEC;            // columns per thread
     constexpr int GN = GVEC ? CPT * (int)sizeof(G) / 16 : 1;   // 16-byte gate vectors
+    constexpr int R = kRowsPerThread;
     using S = typename Inter<T>::S;            // storage of o
     // norm weights, one padding slot after every CPT of them: lane l reads
     // [l*(CPT+1), +CPT) without bank conflicts
@@ -32,72 +35,79 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     __syncthreads();
 
     const int lpr = dv / CPT;                  // lanes per row (power of two, <= 32)
-    const int rows_per_block = kThreads / lpr;
+    const int rows_per_pass = kThreads / lpr;
     const int sub = threadIdx.x / lpr;
     const int lane_in_row = threadIdx.x - sub * lpr;
     const int cc = lane_in_row * CPT;
     const int64_t nrows = p.ntok * d.Hv;
-    const int64_t r = (int64_t)blockIdx.x * rows_per_block + sub;
-    const bool valid = r < nrows;
+    const int64_t rbase = (int64_t)blockIdx.x * rows_per_pass * R + sub;
 
     // every load of this thread first
-    uint4 ox[NVEC];
-    uint4 gx[GN];
-    float gs[GVEC ? 1 : CPT];
-    if (valid) {
-        const int64_t tok = r / d.Hv;
-        const int h = (int)(r - tok * d.Hv);
-        const uint4 *op = reinterpret_cast<const uint4 *>((const S *)p.o + r * dv + cc);
+    uint4 ox[R][NVEC];
+    uint4 gx[R][GN];
+    float gs[R][GVEC ? 1 : CPT];
 #pragma unroll
-        for (int v = 0; v < NVEC; ++v) ox[v] = __ldcs(op + v);
-        const G *gp = (const G *)p.gate + tok_offset(tok, d.T, d.gate_stride_b, d.gate_stride_t) + h * dv + cc;
-        if (GVEC) {
+    for (int k = 0; k < R; ++k) {
+        const int64_t r = rbase + (int64_t)k * rows_per_pass;
+        if (r < nrows) {
+            const int64_t tok = r / d.Hv;
+            const int h = (int)(r - tok * d.Hv);
+            const uint4 *op = reinterpret_cast<const uint4 *>((const S *)p.o + r * dv + cc);
 #pragma unroll
-            for (int v = 0; v < GN; ++v) gx[v] = __ldcs(reinterpret_cast<const uint4 *>(gp) + v);
+            for (int v = 0; v < NVEC; ++v) ox[k][v] = __ldcs(op + v);
+            const G *gp = (const G *)p.gate + tok_offset(tok, d.T, d.gate_stride_b, d.gate_stride_t) + h * dv + cc;
+            if (GVEC) {
+#pragma unroll
+                for (int v = 0; v < GN; ++v) gx[k][v] = __ldcs(reinterpret_cast<const uint4 *>(gp) + v);
+            } else {
+#pragma unroll
+                for (int i = 0; i < (GVEC ? 1 : CPT); ++i) gs[k][i] = to_f<G>(gp[i]);
+            }
         } else {
 #pragma unroll
-            for (int i = 0; i < (GVEC ? 1 : CPT); ++i) gs[i] = to_f<G>(gp[i]);
+            for (int v = 0; v < NVEC; ++v) ox[k][v] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int v = 0; v < GN; ++v) gx[k][v] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < (GVEC ? 1 : CPT); ++i) gs[k][i] = 0.f;
         }
-    } else {
-#pragma unroll
-        for (int v = 0; v < NVEC; ++v) ox[v] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int v = 0; v < GN; ++v) gx[v] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int i = 0; i < (GVEC ? 1 : CPT); ++i) gs[i] = 0.f;
     }
-    float x[CPT];
-#pragma unroll
-    for (int v = 0; v < NVEC; ++v) unpack16<S>(ox[v], x + v * VEC);
-    float ss = 0.f;
+    const float *wv = nwp + lane_in_row * (CPT + 1);
     bool finite = true;
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-        ss = fmaf(x[i], x[i], ss);
-        finite = finite && isfinite(x[i]);
-    }
-    for (int off = lpr >> 1; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float inv = rsqrtf(ss * (1.0f / (float)dv) + d.norm_eps);
-    if (valid) {
-        float gv[CPT];
-        if (GVEC) {
-            constexpr int GE = 16 / sizeof(G);
+    for (int k = 0; k < R; ++k) {
+        const int64_t r = rbase + (int64_t)k * rows_per_pass;
+        float x[CPT];
 #pragma unroll
-            for (int v = 0; v < GN; ++v) unpack16<G>(gx[v], gv + v * GE);
-        } else {
-#pragma unroll
-            for (int i = 0; i < CPT; ++i) gv[i] = gs[GVEC ? 0 : i];
-        }
-        const float *wv = nwp + lane_in_row * (CPT + 1);
-        float y[CPT];
+        for (int v = 0; v < NVEC; ++v) unpack16<S>(ox[k][v], x + v * VEC);
+        float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
-            const float rn = round_through<T>(wv[i] * (x[i] * inv));
-            y[i] = rn * silu_act<T>(gv[i]);
+            ss = fmaf(x[i], x[i], ss);
+            finite = finite && isfinite(x[i]);
         }
-        T *out = (T *)p.out + r * dv + cc;
+        for (int off = lpr >> 1; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float inv = rsqrtf(ss * (1.0f / (float)dv) + d.norm_eps);
+        if (r < nrows) {
+            float gv[CPT];
+            if (GVEC) {
+                constexpr int GE = 16 / sizeof(G);
 #pragma unroll
-        for (int v = 0; v < NVEC; ++v) store16_f_cs<T>(out + v * VEC, y + v * VEC);
+                for (int v = 0; v < GN; ++v) unpack16<G>(gx[k][v], gv + v * GE);
+            } else {
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) gv[i] = gs[k][GVEC ? 0 : i];
+            }
+            float y[CPT];
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                const float rn = round_through<T>(wv[i] * (x[i] * inv));
+                y[i] = rn * silu_act<T>(gv[i]);
+            }
+            T *out = (T *)p.out + r * dv + cc;
+#pragma unroll
+            for (int v = 0; v < NVEC; ++v) store16_f_cs<T>(out + v * VEC, y + v * VEC);
+        }
     }
     // a non-finite gated-delta-rule output (unless an earlier stage already
     // reported a malformed cu_seqlens, after which o holds nothing meaningful)
@@ -109,7 +119,7 @@ template <typename T, typename G, typename W, int NVEC>
 cudaError_t launch_g(const Problem &p, cudaStream_t s) {
     constexpr int CPT = NVEC * Vec16<T>::N;
     const int lpr = p.d.dv / CPT;
-    const int rows_per_block = kThreads / lpr;
+    const int rows_per_block = kThreads / lpr * kRowsPerThread;
     const int64_t nrows = p.ntok * p.d.Hv;
     const int64_t blocks = (nrows + rows_per_block - 1) / rows_per_block;
     const size_t gs = sizeof(G);

@@ -105,7 +105,7 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool ok
                  : "memory");
 }
 
-template <typename T, int NVEC>
+template <typename T, int NVEC, bool NORM>
 __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc &c, int gy,
                                            uint4 *stage) {
     constexpr int VEC = Vec16<T>::N;
@@ -144,6 +144,7 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
     const int c0 = g * (kThreads * CPT) + tid * CPT;
     const bool active = c0 < nch;
     const int lanes_per_head = hd / CPT;      // <= 32 for q/k by construction
+    (void)norm;
 
     // rows into shared memory: stage[(r * NVEC + v) * kThreads + tid]
     const int64_t first = c.tok0 + t_begin - (kConvW - 1);
@@ -190,9 +191,10 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
     const int dd = c0 - head * hd;
     S *dbase = dst + ((int64_t)head * p.ntok + c.tok0 + t_begin) * hd + dd;
     // q/k of 2-byte activations: hi plane here, lo plane `plane` elements further
-    const bool split = norm && sizeof(S) == 2;
+    const bool split = NORM && sizeof(S) == 2;
     const int64_t plane = (int64_t)d.Hk * p.ntok * d.dk;
 
+#pragma unroll 4
     for (int u = 0; u < ntok; ++u) {          // uniform across the block
         float x0[CPT], y[CPT];
         row(u + kConvW - 1, x0);
@@ -204,13 +206,13 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
             acc = fmaf(w[i][2], x1[i], acc);
             acc = fmaf(w[i][3], x0[i], acc);
             // q/k keep ~fp32 precision (hi + lo planes); v is stored at 16 bits
-            y[i] = norm ? silu_f(acc) : silu_act<S>(acc);
+            y[i] = NORM ? silu_f(acc) : silu_act<S>(acc);
             ss = fmaf(y[i], y[i], ss);
             x3[i] = x2[i];
             x2[i] = x1[i];
             x1[i] = x0[i];
         }
-        if (norm) {
+        if (NORM) {
             for (int off = lanes_per_head >> 1; off >= 1; off >>= 1)
                 ss += __shfl_xor_sync(0xffffffffu, ss, off);
             const float inv = rsqrtf(ss + d.l2_eps);
@@ -294,7 +296,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueArgs A
     if (!locate_chunk(blockIdx.x, p.cu, p.chunk_off, p.d.N, p.d.T, c)) return;
     const int gy = blockIdx.y;
     if (gy == (2 * A.groups_qk + A.groups_v) * ConvShape<NVEC>::SLICES) gate_group<T>(p, c, (float *)stage);
-    else conv_group<T, NVEC>(A, c, gy, stage);
+    else if (gy < 2 * A.groups_qk * ConvShape<NVEC>::SLICES) conv_group<T, NVEC, true>(A, c, gy, stage);
+    else conv_group<T, NVEC, false>(A, c, gy, stage);
 }
 
 template <typename T, int NVEC>
