@@ -17,7 +17,7 @@ namespace {
 
 constexpr int kThreads = 256;
 
-constexpr int kRowsPerThread = 2;   // independent rows per thread, loads issued together
+constexpr int kRowsPerThread = 1;   // rows per thread (2 measured slower on the layer workload)
 
 template <typename T, typename G, typename W, int NVEC, bool GVEC>
 __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
