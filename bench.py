@@ -36,7 +36,13 @@ CHUNK = 64
 # ncu capture, keyed by kernel; each entry is only used while the kernel's
 # source file still hashes to the recorded value.
 # kernel -> (source file, sha256 of it, workload, bytes per launch)
-NCU_TRAFFIC: dict = {}
+# "chunk_rule" is the tensor-core chunk stage: chunk_prep_kernel + chunk_chain_kernel,
+# one launch each per step; the figure is the sum of the two launches.
+NCU_TRAFFIC: dict = {
+    "chunk_rule": ("linear_attention_sequence_qkv_gb300/csrc/gdn_chunk_tc.cu",
+                   "5e5f3f62aafad18974b04a33d7c8d6080a3dacc4e728532bcb7b5d7719d27ad6",
+                   "layer_bf16", 117_096_448),
+}
 
 
 def sha256(path):
@@ -320,9 +326,12 @@ def main():
     for name in ("prologue", "chunk_rule", "epilogue"):
         ms = sum(per[name]) / len(per[name])
         kernels[name] = roofline_entry(name, alg[name][0], alg[name][1], ms, pk, w.dtype)
+    tc = gdn.gdn_chunk_kernel_kind(d) == 1
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     roof = dict(kernels[dom])
     roof["kernel"] = dom
+    if dom == "chunk_rule":
+        roof["launches"] = ["chunk_prep_kernel", "chunk_chain_kernel"] if tc else ["chunk_simt_kernel"]
     tr = NCU_TRAFFIC.get(dom)
     roof["traffic"] = None
     if tr is not None:
@@ -380,7 +389,9 @@ def main():
         e2e = {"value": ntok * world / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
                "steps": ksteps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    launches_per_step = 3 + (1 if inp.cu_seqlens is not None else 0)
+    # prologue (+ the cu_seqlens scan for packed input), the chunk stage (prep + chain on
+    # the tensor-core path, one kernel on the fp32 path), the epilogue
+    launches_per_step = 1 + (1 if inp.cu_seqlens is not None else 0) + (2 if tc else 1) + 1
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -390,7 +401,7 @@ def main():
                    "dk": w.dk, "dv": w.dv, "tokens_per_step": ntok, "chunk": CHUNK,
                    "l2": "flushed before every timed step (512 MiB write, then 256 MiB read)",
                    "parallelism": f"replicas x{world}",
-                   "chunk_kernel": "tcgen05" if gdn.gdn_chunk_kernel_kind(d) == 1 else "cuda-core fp32"},
+                   "chunk_kernel": "tcgen05" if tc else "cuda-core fp32"},
         "roofline": roof,
         "kernels": kernels,
         "cpu_baseline": cpu,
