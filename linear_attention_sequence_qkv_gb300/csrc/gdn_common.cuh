@@ -96,6 +96,95 @@ template <typename T> __device__ __forceinline__ float silu_act(float x) {
     return sizeof(T) == 4 ? silu_f(x) : silu_fast(x);
 }
 
+// ------------------------------------------------------ packed fp32 pairs
+// sm_100-class SMs run fp32 add / mul / fma on a register pair as one
+// instruction; the streaming kernels keep their values as float2 pairs.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
+
+// 16 bytes of T as Vec16<T>::N / 2 pairs
+template <typename T> struct Pairs;
+template <> struct Pairs<float> {
+    static __device__ __forceinline__ void unpack(const uint4 &u, float2 *o) {
+        o[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        o[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+    }
+    static __device__ __forceinline__ uint4 pack(const float2 *in) {
+        return make_uint4(__float_as_uint(in[0].x), __float_as_uint(in[0].y), __float_as_uint(in[1].x),
+                          __float_as_uint(in[1].y));
+    }
+    static __device__ __forceinline__ float2 round(float2 x) { return x; }
+};
+template <> struct Pairs<__nv_bfloat16> {
+    // a bf16 is the upper half of the fp32 with the same value
+    static __device__ __forceinline__ float2 word(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    static __device__ __forceinline__ uint32_t pack1(float2 x) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    static __device__ __forceinline__ void unpack(const uint4 &u, float2 *o) {
+        o[0] = word(u.x); o[1] = word(u.y); o[2] = word(u.z); o[3] = word(u.w);
+    }
+    static __device__ __forceinline__ uint4 pack(const float2 *in) {
+        return make_uint4(pack1(in[0]), pack1(in[1]), pack1(in[2]), pack1(in[3]));
+    }
+    static __device__ __forceinline__ float2 round(float2 x) { return word(pack1(x)); }
+};
+template <> struct Pairs<__half> {
+    static __device__ __forceinline__ float2 word(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    }
+    static __device__ __forceinline__ uint32_t pack1(float2 x) {
+        __half2 h = __float22half2_rn(x);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    static __device__ __forceinline__ void unpack(const uint4 &u, float2 *o) {
+        o[0] = word(u.x); o[1] = word(u.y); o[2] = word(u.z); o[3] = word(u.w);
+    }
+    static __device__ __forceinline__ uint4 pack(const float2 *in) {
+        return make_uint4(pack1(in[0]), pack1(in[1]), pack1(in[2]), pack1(in[3]));
+    }
+    static __device__ __forceinline__ float2 round(float2 x) { return word(pack1(x)); }
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// silu(x) = x / (1 + e^-x) on a pair, e^-x = 2^(-x log2 e) from the hardware
+// base-2 exponential and the quotient from the hardware reciprocal (both a few
+// ulp): for values kept at fp32 precision
+__device__ __forceinline__ float2 silu2_acc(float2 x) {
+    const float2 m = mul2(x, splat2(-1.4426950408889634f));
+    const float2 d = add2(make_float2(ex2_approx(m.x), ex2_approx(m.y)), splat2(1.0f));
+    return mul2(x, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+// silu(x) = h + h tanh(h), h = x/2, with the hardware tanh (relative error
+// ~2^-11): for values stored or consumed at 16-bit precision
+__device__ __forceinline__ float2 silu2_fast(float2 x) {
+    const float2 h = mul2(x, splat2(0.5f));
+    return fma2(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+}
+template <typename T> __device__ __forceinline__ float2 silu2_act(float2 x) {
+    return sizeof(T) == 4 ? silu2_acc(x) : silu2_fast(x);
+}
+
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // softplus(x) = log(1 + e^x); above 20 the correction is below fp32 resolution

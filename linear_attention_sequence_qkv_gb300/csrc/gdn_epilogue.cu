@@ -6,10 +6,12 @@
 // input projection with separate batch and token strides, consumed in place;
 // "Execution and numerical behavior": the RMSNorm result is materialised in the
 // activation dtype before the fp32 SiLU-gating multiply).
-// HBM-bound streaming kernel: one row slice per thread, all of its loads issued
-// first; each row is read once (o, gate) and written once with 16-byte accesses
-// (scalar gate loads where the view's alignment does not allow 16 bytes). A row
-// spans at most one warp, so the mean of squares is a shuffle reduction.
+// HBM-bound streaming kernel: each thread owns the same column slice of a few
+// consecutive rows and issues all of their loads first; each row is read once
+// (o, gate) and written once with 16-byte accesses (scalar gate loads where the
+// view's alignment does not allow 16 bytes). A row spans at most one warp, so
+// the mean of squares is a shuffle reduction. The arithmetic runs on fp32
+// pairs (one packed instruction per two columns).
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -17,14 +19,17 @@ namespace {
 
 constexpr int kThreads = 256;
 
-constexpr int kRowsPerThread = 1;   // rows per thread (2 measured slower on the layer workload)
+// Rows (token, v head) of one thread: consecutive rows, so that one division
+// locates the first and the rest follow by carrying the head index.
+template <int NVEC> struct EpiRows { static constexpr int R = 2; };
 
 template <typename T, typename G, typename W, int NVEC, bool GVEC>
 __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     constexpr int VEC = Vec16<T>::N;
     constexpr int CPT = NVEC * VEC;            // columns per thread
+    constexpr int NP = CPT / 2;                // column pairs per thread
     constexpr int GN = GVEC ? CPT * (int)sizeof(G) / 16 : 1;   // 16-byte gate vectors
-    constexpr int R = kRowsPerThread;
+    constexpr int R = EpiRows<NVEC>::R;
     using S = typename Inter<T>::S;            // storage of o
     // norm weights, one padding slot after every CPT of them: lane l reads
     // [l*(CPT+1), +CPT) without bank conflicts
@@ -32,7 +37,6 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     const gdn_desc &d = p.d;
     const int dv = d.dv;
     for (int i = threadIdx.x; i < dv; i += kThreads) nwp[(i / CPT) * (CPT + 1) + i % CPT] = to_f<W>(((const W *)p.norm_w)[i]);
-    __syncthreads();
 
     const int lpr = dv / CPT;                  // lanes per row (power of two, <= 32)
     const int rows_per_pass = kThreads / lpr;
@@ -40,7 +44,24 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     const int lane_in_row = threadIdx.x - sub * lpr;
     const int cc = lane_in_row * CPT;
     const int64_t nrows = p.ntok * d.Hv;
-    const int64_t rbase = (int64_t)blockIdx.x * rows_per_pass * R + sub;
+    const int64_t r0 = ((int64_t)blockIdx.x * rows_per_pass + sub) * R;
+
+    // head of the first row, and its token as (batch row, token in the row) for
+    // the gate view; 32-bit divisions unless the row count needs more
+    int h, tt;
+    int64_t bt;
+    if (nrows <= 0x7fffffff) {
+        const uint32_t q = (uint32_t)r0 / (uint32_t)d.Hv;
+        h = (int)((uint32_t)r0 - q * (uint32_t)d.Hv);
+        const uint32_t b = q / (uint32_t)d.T;
+        tt = (int)(q - b * (uint32_t)d.T);
+        bt = b;
+    } else {
+        const int64_t tok = r0 / d.Hv;
+        h = (int)(r0 - tok * d.Hv);
+        bt = tok / d.T;
+        tt = (int)(tok - bt * d.T);
+    }
 
     // every load of this thread first
     uint4 ox[R][NVEC];
@@ -48,14 +69,11 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     float gs[R][GVEC ? 1 : CPT];
 #pragma unroll
     for (int k = 0; k < R; ++k) {
-        const int64_t r = rbase + (int64_t)k * rows_per_pass;
-        if (r < nrows) {
-            const int64_t tok = r / d.Hv;
-            const int h = (int)(r - tok * d.Hv);
-            const uint4 *op = reinterpret_cast<const uint4 *>((const S *)p.o + r * dv + cc);
+        if (r0 + k < nrows) {
+            const uint4 *op = reinterpret_cast<const uint4 *>((const S *)p.o + (r0 + k) * dv + cc);
 #pragma unroll
             for (int v = 0; v < NVEC; ++v) ox[k][v] = __ldcs(op + v);
-            const G *gp = (const G *)p.gate + tok_offset(tok, d.T, d.gate_stride_b, d.gate_stride_t) + h * dv + cc;
+            const G *gp = (const G *)p.gate + bt * d.gate_stride_b + tt * d.gate_stride_t + h * dv + cc;
             if (GVEC) {
 #pragma unroll
                 for (int v = 0; v < GN; ++v) gx[k][v] = __ldcs(reinterpret_cast<const uint4 *>(gp) + v);
@@ -71,42 +89,51 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
 #pragma unroll
             for (int i = 0; i < (GVEC ? 1 : CPT); ++i) gs[k][i] = 0.f;
         }
+        if (++h == d.Hv) {
+            h = 0;
+            if (++tt == d.T) { tt = 0; ++bt; }
+        }
     }
-    const float *wv = nwp + lane_in_row * (CPT + 1);
+    __syncthreads();
+    float2 w[NP];
+    {
+        const float *wv = nwp + lane_in_row * (CPT + 1);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) w[i] = make_float2(wv[2 * i], wv[2 * i + 1]);
+    }
     bool finite = true;
 #pragma unroll
     for (int k = 0; k < R; ++k) {
-        const int64_t r = rbase + (int64_t)k * rows_per_pass;
-        float x[CPT];
+        float2 x[NP];
 #pragma unroll
-        for (int v = 0; v < NVEC; ++v) unpack16<S>(ox[k][v], x + v * VEC);
-        float ss = 0.f;
+        for (int v = 0; v < NVEC; ++v) Pairs<S>::unpack(ox[k][v], x + v * (VEC / 2));
+        float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-            ss = fmaf(x[i], x[i], ss);
-            finite = finite && isfinite(x[i]);
-        }
+        for (int i = 0; i < NP; ++i) ss2 = fma2(x[i], x[i], ss2);
+        float ss = ss2.x + ss2.y;
         for (int off = lpr >> 1; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float inv = rsqrtf(ss * (1.0f / (float)dv) + d.norm_eps);
-        if (r < nrows) {
-            float gv[CPT];
+        // a non-finite element makes the sum of squares non-finite
+        finite = finite && isfinite(ss);
+        const float2 inv = splat2(rsqrtf(ss * (1.0f / (float)dv) + d.norm_eps));
+        if (r0 + k < nrows) {
+            float2 g[NP];
             if (GVEC) {
                 constexpr int GE = 16 / sizeof(G);
 #pragma unroll
-                for (int v = 0; v < GN; ++v) unpack16<G>(gx[k][v], gv + v * GE);
+                for (int v = 0; v < GN; ++v) Pairs<G>::unpack(gx[k][v], g + v * (GE / 2));
             } else {
 #pragma unroll
-                for (int i = 0; i < CPT; ++i) gv[i] = gs[k][GVEC ? 0 : i];
+                for (int i = 0; i < NP; ++i) g[i] = make_float2(gs[k][GVEC ? 0 : 2 * i], gs[k][GVEC ? 0 : 2 * i + 1]);
             }
-            float y[CPT];
+            float2 y[NP];
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) {
-                const float rn = round_through<T>(wv[i] * (x[i] * inv));
-                y[i] = rn * silu_act<T>(gv[i]);
+            for (int i = 0; i < NP; ++i) {
+                const float2 rn = Pairs<T>::round(mul2(w[i], mul2(x[i], inv)));
+                y[i] = mul2(rn, silu2_act<T>(g[i]));
             }
-            T *out = (T *)p.out + r * dv + cc;
+            uint4 *out = reinterpret_cast<uint4 *>((T *)p.out + (r0 + k) * dv + cc);
 #pragma unroll
-            for (int v = 0; v < NVEC; ++v) store16_f_cs<T>(out + v * VEC, y + v * VEC);
+            for (int v = 0; v < NVEC; ++v) __stcs(out + v, Pairs<T>::pack(y + v * (VEC / 2)));
         }
     }
     // a non-finite gated-delta-rule output (unless an earlier stage already
@@ -119,7 +146,7 @@ template <typename T, typename G, typename W, int NVEC>
 cudaError_t launch_g(const Problem &p, cudaStream_t s) {
     constexpr int CPT = NVEC * Vec16<T>::N;
     const int lpr = p.d.dv / CPT;
-    const int rows_per_block = kThreads / lpr * kRowsPerThread;
+    const int rows_per_block = kThreads / lpr * EpiRows<NVEC>::R;
     const int64_t nrows = p.ntok * p.d.Hv;
     const int64_t blocks = (nrows + rows_per_block - 1) / rows_per_block;
     const size_t gs = sizeof(G);

@@ -17,6 +17,8 @@
 // last y = beta/decay group. Every input row is read once plus a 3-token halo per
 // slice (L2 hits), with coalesced 16-byte loads all issued up front; q/k/v are
 // written head-major [H][Ntok][d] for the chunk kernels.
+#include <type_traits>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -104,12 +106,26 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool ok
                  :: "r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem), "r"(ok ? 16 : 0)
                  : "memory");
 }
+// wait until at most N of this thread's copy groups are still in flight
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
+// f(integral_constant<int, U>) for U = 0 .. N-1, unrolled at compile time
+template <int U, int N, typename F> __device__ __forceinline__ void static_for(F &&f) {
+    if constexpr (U < N) {
+        f(std::integral_constant<int, U>{});
+        static_for<U + 1, N>(f);
+    }
+}
 
 template <typename T, int NVEC, bool NORM>
 __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc &c, int gy,
                                            uint4 *stage) {
     constexpr int VEC = Vec16<T>::N;
     constexpr int CPT = NVEC * VEC;           // channels per thread
+    constexpr int NP = CPT / 2;               // channel pairs per thread
+    constexpr int PV = VEC / 2;               // pairs per 16-byte vector
     using Shape = ConvShape<NVEC>;
     constexpr int TOKS = Shape::TOKS;
     constexpr int ROWS = Shape::ROWS;
@@ -128,25 +144,26 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
     S *dst;
     int64_t sb, st;
     int nch, hd, w_base;
-    bool norm;
     const int ch_qk = d.Hk * d.dk;
     if (g < A.groups_qk) {
         src = (const T *)p.q_raw; dst = (S *)p.q; sb = d.q_stride_b; st = d.q_stride_t;
-        nch = ch_qk; hd = d.dk; w_base = 0; norm = true;
+        nch = ch_qk; hd = d.dk; w_base = 0;
     } else if ((g -= A.groups_qk) < A.groups_qk) {
         src = (const T *)p.k_raw; dst = (S *)p.k; sb = d.k_stride_b; st = d.k_stride_t;
-        nch = ch_qk; hd = d.dk; w_base = ch_qk; norm = true;
+        nch = ch_qk; hd = d.dk; w_base = ch_qk;
     } else {
         g -= A.groups_qk;
         src = (const T *)p.v_raw; dst = (S *)p.v; sb = d.v_stride_b; st = d.v_stride_t;
-        nch = d.Hv * d.dv; hd = d.dv; w_base = 2 * ch_qk; norm = false;
+        nch = d.Hv * d.dv; hd = d.dv; w_base = 2 * ch_qk;
     }
     const int c0 = g * (kThreads * CPT) + tid * CPT;
     const bool active = c0 < nch;
+    // a warp with no channel has nothing to do (no block barrier follows)
+    if (!__any_sync(0xffffffffu, active)) return;
     const int lanes_per_head = hd / CPT;      // <= 32 for q/k by construction
-    (void)norm;
 
-    // rows into shared memory: stage[(r * NVEC + v) * kThreads + tid]
+    // rows into shared memory, one copy group per row:
+    // stage[(r * NVEC + v) * kThreads + tid]
     const int64_t first = c.tok0 + t_begin - (kConvW - 1);
     const int64_t brow = p.cu ? 0 : c.n;     // batch row of this sequence
     const T *rp = src + brow * sb + (first - brow * (int64_t)d.T) * st + (active ? c0 : 0);
@@ -157,81 +174,93 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
         for (int v = 0; v < NVEC; ++v)
             cp_async16(&stage[(r * NVEC + v) * kThreads + tid], ok ? (const void *)(rp + r * st + v * VEC)
                                                                    : (const void *)src, ok);
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    // conv taps of my channels (overlaps the copies)
-    float w[CPT][kConvW];
+    // conv taps of my channels as pairs (overlaps the copies)
+    float2 w[NP][kConvW];
     if (active) {
         const T *wp = (const T *)p.conv_w + (int64_t)(w_base + c0) * kConvW;
+        float wf[CPT * kConvW];
 #pragma unroll
-        for (int i = 0; i < CPT * kConvW; i += VEC) {
-            float tmp[VEC];
-            load16_f<T>(wp + i, tmp);
+        for (int i = 0; i < CPT * kConvW; i += VEC) load16_f<T>(wp + i, wf + i);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) w[(i + j) / kConvW][(i + j) % kConvW] = tmp[j];
-        }
+        for (int i = 0; i < NP; ++i)
+#pragma unroll
+            for (int j = 0; j < kConvW; ++j)
+                w[i][j] = make_float2(wf[(2 * i) * kConvW + j], wf[(2 * i + 1) * kConvW + j]);
     } else {
 #pragma unroll
-        for (int i = 0; i < CPT; ++i)
+        for (int i = 0; i < NP; ++i)
 #pragma unroll
-            for (int j = 0; j < kConvW; ++j) w[i][j] = 0.f;
+            for (int j = 0; j < kConvW; ++j) w[i][j] = make_float2(0.f, 0.f);
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");   // each thread reads only its own rows
 
-    auto row = [&](int r, float *out) {
+    auto row = [&](int r, float2 *out) {   // each thread reads only its own rows
 #pragma unroll
-        for (int v = 0; v < NVEC; ++v) unpack16<T>(stage[(r * NVEC + v) * kThreads + tid], out + v * VEC);
+        for (int v = 0; v < NVEC; ++v) Pairs<T>::unpack(stage[(r * NVEC + v) * kThreads + tid], out + v * PV);
     };
-    float x3[CPT], x2[CPT], x1[CPT];
-    row(0, x3);
-    row(1, x2);
-    row(2, x1);
-
     const int head = c0 / hd;
     const int dd = c0 - head * hd;
     S *dbase = dst + ((int64_t)head * p.ntok + c.tok0 + t_begin) * hd + dd;
     // q/k of 2-byte activations: hi plane here, lo plane `plane` elements further
-    const bool split = NORM && sizeof(S) == 2;
+    constexpr bool split = NORM && sizeof(S) == 2;
     const int64_t plane = (int64_t)d.Hk * p.ntok * d.dk;
 
-#pragma unroll 4
-    for (int u = 0; u < ntok; ++u) {          // uniform across the block
-        float x0[CPT], y[CPT];
+    float2 x3[NP], x2[NP], x1[NP];
+    // token u of the slice: the window (x3, x2, x1) plus row u + 3
+    auto body = [&](auto uc) {
+        constexpr int u = decltype(uc)::value;
+        float2 x0[NP], y[NP];
         row(u + kConvW - 1, x0);
-        float ss = 0.f;
+        float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-            float acc = w[i][0] * x3[i];
-            acc = fmaf(w[i][1], x2[i], acc);
-            acc = fmaf(w[i][2], x1[i], acc);
-            acc = fmaf(w[i][3], x0[i], acc);
+        for (int i = 0; i < NP; ++i) {
+            float2 acc = mul2(w[i][0], x3[i]);
+            acc = fma2(w[i][1], x2[i], acc);
+            acc = fma2(w[i][2], x1[i], acc);
+            acc = fma2(w[i][3], x0[i], acc);
             // q/k keep ~fp32 precision (hi + lo planes); v is stored at 16 bits
-            y[i] = NORM ? silu_f(acc) : silu_act<S>(acc);
-            ss = fmaf(y[i], y[i], ss);
+            y[i] = NORM ? silu2_acc(acc) : silu2_act<S>(acc);
+            if (NORM) ss2 = fma2(y[i], y[i], ss2);
             x3[i] = x2[i];
             x2[i] = x1[i];
             x1[i] = x0[i];
         }
         if (NORM) {
-            for (int off = lanes_per_head >> 1; off >= 1; off >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float inv = rsqrtf(ss + d.l2_eps);
+            float ss = ss2.x + ss2.y;
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) y[i] *= inv;
+            for (int off = 16; off >= 1; off >>= 1)
+                if (off < lanes_per_head) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float2 inv = splat2(rsqrtf(ss + d.l2_eps));
+#pragma unroll
+            for (int i = 0; i < NP; ++i) y[i] = mul2(y[i], inv);
         }
         if (active) {
-            S *op = dbase + (int64_t)u * hd;
+            uint4 *op = reinterpret_cast<uint4 *>(dbase + (int64_t)u * hd);
 #pragma unroll
-            for (int v = 0; v < NVEC; ++v) store16_f<S>(op + v * VEC, y + v * VEC);
+            for (int v = 0; v < NVEC; ++v) op[v] = Pairs<S>::pack(y + v * PV);
             if (split) {   // lo plane: what fp16 rounding of y left out
-                float lo[CPT];
+                float2 lo[NP];
 #pragma unroll
-                for (int i = 0; i < CPT; ++i) lo[i] = y[i] - round_through<S>(y[i]);
+                for (int i = 0; i < NP; ++i) lo[i] = fma2(Pairs<S>::round(y[i]), splat2(-1.0f), y[i]);
+                uint4 *lp = reinterpret_cast<uint4 *>(dbase + (int64_t)u * hd + plane);
 #pragma unroll
-                for (int v = 0; v < NVEC; ++v) store16_f<S>(op + plane + v * VEC, lo + v * VEC);
+                for (int v = 0; v < NVEC; ++v) lp[v] = Pairs<S>::pack(lo + v * PV);
             }
         }
-    }
+    };
+    // rows 0..2, then token u as soon as row u + 3 has landed
+    cp_async_wait<ROWS - 3>();
+    row(0, x3);
+    row(1, x2);
+    row(2, x1);
+    static_for<0, TOKS>([&](auto uc) {
+        constexpr int u = decltype(uc)::value;
+        if (u < ntok) {                       // uniform across the block
+            cp_async_wait<TOKS - 1 - u>();
+            body(uc);
+        }
+    });
 }
 
 // ------------------------------------------------------- beta/decay group
