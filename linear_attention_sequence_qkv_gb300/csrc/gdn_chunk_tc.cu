@@ -450,10 +450,9 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     fence_after_sync();
     const uint32_t tbase = *tslot;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    // TMEM: D1 (two buffers) at 0 / 64, D2 at 128, dH at 192 + 64 h, H (fp32) at 320 + 64 h
+    // TMEM: D1 (two buffers) at 0 / 64, D2 at 128, H (fp32) at 320 + 64 h
     auto tD1 = [&](int c) { return tbase + lane_off + c0 + 64 * (c & 1); };
     const uint32_t tD2 = tbase + 128 + lane_off + c0;
-    const uint32_t tDH = tbase + 192 + lane_off + c0;
     const uint32_t tH = tbase + 320 + lane_off + c0;
 
     auto chunk_tok0 = [&](int c) { return seq0 + (int64_t)c * kChunk; };
@@ -549,13 +548,14 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             // dk = 64 has a single 64-row block: LBO 0 repeats it as rows 64..127 (ignored)
             const uint64_t d_kt0 = sw128_desc(smem_u32(sm), dk >= 128 ? 2 * kTileBytes : 0, 1024);
             const uint32_t stage16 = (uint32_t)(L.stage_bytes >> 4), x16 = (uint32_t)(L.x >> 4);
-            auto issue_c4 = [&](int c) {   // dH = K_c^T Vn'_c
+            // H += K_c^T Vn'_c, into the state the state warps already scaled by e^{gL_c}
+            auto issue_c4 = [&](int c) {
                 const uint64_t a0 = d_kt0 + (c & 1) * stage16;
                 for (int h = 0; h < halves; ++h)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tbase + 192 + 64 * h, a0 + (uint64_t)((h * 4 * kTileBytes + 2048 * ks) >> 4),
-                                d_vn + (uint64_t)((2048 * ks) >> 4), id_m, ks != 0);
+                        mma_f16(tbase + 320 + 64 * h, a0 + (uint64_t)((h * 4 * kTileBytes + 2048 * ks) >> 4),
+                                d_vn + (uint64_t)((2048 * ks) >> 4), id_m, 1);
                 mma_commit(&bar[B_C4]);
             };
             auto issue_c1a = [&](int c) {  // D1 = [K; Q] h16
@@ -643,7 +643,6 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 for (int q = 0; q < 32; ++q) a[q] = br * (vv[q] - eg * a[q]);
                 store_half_row_f16(r16, r, c0, a);
                 warp_arrive(B_R);
-                if (c + 1 < nchunks) prefetch(c + 1);
                 // E2a: Vn' = e^{gam_L - gam} Vn -> vn16
                 if (!wait(B_C2, c & 1)) break;
                 fence_after_sync();
@@ -653,6 +652,10 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 for (int q = 0; q < 32; ++q) a[q] *= sc;
                 store_half_row_f16(vn16, r, c0, a);
                 warp_arrive(B_VN);
+                // the next chunk's operands only now: the proxy fence of an arrival
+                // waits for this thread's loads in flight, so none may be pending
+                // at the two arrivals on the serial path
+                if (c + 1 < nchunks) prefetch(c + 1);
             } else {
                 // E2b: O = e^gam (Q H) + P Vn -> o   (off the critical path)
                 if (c + 1 < nchunks) prefetch(c + 1);
@@ -661,7 +664,10 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 float a[32], b2[32];
                 tmem_ld32(tD1(c), a);
                 tmem_ld32(tD2, b2);
-                warp_arrive(B_O);
+                // no shared-memory writes to publish: order the tensor-memory reads only
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_O]);
                 if (r < len) {
                     const float eg = __expf(gr);
                     uint4 *dst = reinterpret_cast<uint4 *>(o + ((t0 + r) * Hv + j) * (int64_t)dv + v0 + c0);
@@ -680,7 +686,9 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         }
     } else if (state_warp) {
         // -------------------------------------------------------- state warps
-        // H (fp32, TMEM) <- e^{gL_c} H + dH_c; h16 <- e^{gL_{c+1}} H (B operand of chunk c+2)
+        // Once H_c is complete (C4 of chunk c done): H <- e^{gL_{c+1}} H_c in place,
+        // so that C4 of chunk c+1 accumulates onto it, and its fp16 copy h16 (the
+        // B operand of chunk c+2's first product).
         auto final_state = [&]() {
             for (int h = 0; h < halves; ++h) {
                 const int hrow = 128 * h + row;
@@ -692,42 +700,32 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 for (int q = 0; q < 8; ++q) dst[q] = make_float4(t[4 * q], t[4 * q + 1], t[4 * q + 2], t[4 * q + 3]);
             }
         };
-        if (nchunks > 0) {
-            // h16 for chunk 1: e^{gL_0} H_init, once chunk 0's first product is done
-            float gl_next = gamma_last(0);
-            if (wait(B_C1, 0)) {
-                const float e0 = __expf(gl_next);
-                for (int h = 0; h < halves; ++h) {
-                    const int hrow = 128 * h + row;
-                    if (hrow >= dk) continue;
-                    float t[32];
-                    tmem_ld32(tH + 64 * h, t);
+        auto scale_state = [&](float e, bool copy) {
+            for (int h = 0; h < halves; ++h) {
+                const int hrow = 128 * h + row;
+                if (hrow >= dk) continue;
+                float t[32];
+                tmem_ld32(tH + 64 * h, t);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) t[q] *= e0;
-                    store_half_row_f16(h16, hrow, c0, t);
-                }
+                for (int q = 0; q < 32; ++q) t[q] *= e;
+                tmem_st32(tH + 64 * h, t);
+                if (copy) store_half_row_f16(h16, hrow, c0, t);
+            }
+        };
+        if (nchunks > 0) {
+            // chunk 0's first product has read h16 = H_init: scale for chunk 0's
+            // update and publish e^{gL_0} H_init for chunk 1
+            if (wait(B_C1, 0)) {
+                scale_state(__expf(gamma_last(0)), nchunks > 1);
                 warp_arrive(B_H);
                 for (int c = 0; c < nchunks; ++c) {
-                    const float gl = gl_next;
-                    gl_next = c + 1 < nchunks ? gamma_last(c + 1) : 0.f;
+                    const float gl_next = c + 1 < nchunks ? gamma_last(c + 1) : 0.f;
                     if (!wait(B_C4, c & 1)) break;
                     fence_after_sync();
-                    const float eL = __expf(gl), eN = __expf(gl_next);
-                    for (int h = 0; h < halves; ++h) {
-                        float hv[32], dh[32];
-                        tmem_ld32(tH + 64 * h, hv);
-                        tmem_ld32(tDH + 64 * h, dh);
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) hv[q] = fmaf(eL, hv[q], dh[q]);
-                        tmem_st32(tH + 64 * h, hv);
-                        const int hrow = 128 * h + row;
-                        if (c + 2 < nchunks && hrow < dk) {
-#pragma unroll
-                            for (int q = 0; q < 32; ++q) dh[q] = eN * hv[q];
-                            store_half_row_f16(h16, hrow, c0, dh);
-                        }
+                    if (c + 1 < nchunks) {
+                        scale_state(__expf(gl_next), c + 2 < nchunks);
+                        warp_arrive(B_H);
                     }
-                    warp_arrive(B_H);
                 }
                 if (p.hT && !s_err) final_state();
             }
