@@ -392,7 +392,10 @@ constexpr int kRowWarps = 8, kStateWarps = 8;
 constexpr int kMmaWarp = kRowWarps + kStateWarps;
 constexpr int kLoadWarp = kMmaWarp + 1;
 constexpr int kChainThreads = (kLoadWarp + 1) * 32;
-enum ChainBar { B_LOAD0 = 0, B_LOAD1, B_TPT, B_C1, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_COUNT };
+// B_LOAD s / B_LQ s: the K part / the Q + X part of stage s landed; B_QF s: the
+// products reading stage s's Q + X part are done (its refill may start).
+enum ChainBar { B_LOAD0 = 0, B_LOAD1, B_LQ0, B_LQ1, B_TPT, B_QF0, B_QF1, B_C1, B_R, B_C2, B_VN, B_O, B_C4, B_H,
+                B_COUNT };
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles,
@@ -434,6 +437,10 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         s_err = 0;
         mbar_init(&bar[B_LOAD0], 1);
         mbar_init(&bar[B_LOAD1], 1);
+        mbar_init(&bar[B_LQ0], 1);
+        mbar_init(&bar[B_LQ1], 1);
+        mbar_init(&bar[B_QF0], 1);
+        mbar_init(&bar[B_QF1], 1);
         mbar_init(&bar[B_TPT], 1);
         mbar_init(&bar[B_C1], 1);
         mbar_init(&bar[B_C2], 1);
@@ -502,34 +509,52 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     if (warp == kLoadWarp) {
         // -------------------------------------------------------- TMA warp
         if (lane == 0) {
-            auto load_stage = [&](int c) {
+            // a stage is [K_b; Q_b] for each 64-column block b, then X; its K part is
+            // read until C4 of the chunk, its Q and X parts only until C1
+            auto load_k = [&](int c) {
+                const int s = c & 1;
+                unsigned char *st = sm + s * L.stage_bytes;
+                const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
+                mbar_expect_tx(&bar[B_LOAD0 + s], (uint32_t)L.blocks * kTileBytes);
+                for (int b = 0; b < L.blocks; ++b)
+                    tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
+            };
+            auto load_qx = [&](int c) {
                 const int s = c & 1;
                 unsigned char *st = sm + s * L.stage_bytes;
                 const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
                 const bool with_x = c > 0;
-                mbar_expect_tx(&bar[B_LOAD0 + s], (uint32_t)L.blocks * 2 * kTileBytes + (with_x ? kXBytes : 0));
-                for (int b = 0; b < L.blocks; ++b) {
-                    tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
-                    tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
-                }
+                mbar_expect_tx(&bar[B_LQ0 + s], (uint32_t)L.blocks * kTileBytes + (with_x ? kXBytes : 0));
+                for (int b = 0; b < L.blocks; ++b)
+                    tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar[B_LQ0 + s]);
                 if (with_x)
                     bulk_load(st + L.x, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut + kTPTBytes,
-                              kXBytes, &bar[B_LOAD0 + s]);
+                              kXBytes, &bar[B_LQ0 + s]);
             };
             auto load_tpt = [&](int c) {
                 mbar_expect_tx(&bar[B_TPT], kTPTBytes);
                 bulk_load(tptb, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut, kTPTBytes, &bar[B_TPT]);
             };
-            if (nchunks > 0) { load_stage(0); load_tpt(0); }
-            if (nchunks > 1) load_stage(1);
+            if (nchunks > 0) { load_k(0); load_qx(0); load_tpt(0); }
+            if (nchunks > 1) { load_k(1); load_qx(1); }
+            // Each wait below is for the phase right after the one this thread last
+            // consumed, and the barrier cannot complete the next one before this
+            // thread's refill: B_QF s is re-armed only by chunk c+2's C1, B_C2 only
+            // by chunk c+1's C2 (after its [T; P T] load), B_C4 only by chunk c+1's
+            // C4 (issued after chunk c+2's first product, which needs its K part).
             for (int c = 0; c + 1 < nchunks; ++c) {
+                // Q and X of chunk c+2 into chunk c's stage once C1 of chunk c is done
+                if (c + 2 < nchunks) {
+                    if (!wait(B_QF0 + (c & 1), (c >> 1) & 1)) break;
+                    load_qx(c + 2);
+                }
                 // [T; P T] of chunk c+1 once C2 of chunk c has read the buffer
                 if (!wait(B_C2, c & 1)) break;
                 load_tpt(c + 1);
-                // chunk c+2 into chunk c's stage once its last reader (C4 of chunk c) is done
+                // K of chunk c+2 once its last reader (C4 of chunk c) is done
                 if (c + 2 < nchunks) {
                     if (!wait(B_C4, c & 1)) break;
-                    load_stage(c + 2);
+                    load_k(c + 2);
                 }
             }
         }
@@ -569,7 +594,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             int c = 0;
             for (; c < nchunks; ++c) {
                 const int s = c & 1;
-                if (!wait(B_LOAD0 + s, (c >> 1) & 1)) break;
+                if (!wait(B_LOAD0 + s, (c >> 1) & 1) || !wait(B_LQ0 + s, (c >> 1) & 1)) break;
                 if (c >= 1 && !wait(B_H, (c - 1) & 1)) break;     // h16 = e^{gL_{c-1}} H_{c-2}
                 fence_after_sync();
                 issue_c1a(c);
@@ -584,6 +609,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                                 d_vn + (uint64_t)((2048 * ks) >> 4), id_k, 1);
                 }
                 mma_commit(&bar[B_C1]);
+                mma_commit(&bar[B_QF0 + s]);      // stage s's Q and X parts are free
                 if (c >= 1) issue_c4(c - 1);
                 // C2: D2 = [T; P T] R
                 if (!wait(B_TPT, c & 1) || !wait(B_R, c & 1)) break;
