@@ -106,12 +106,17 @@ __device__ __forceinline__ void load_half_row_f16(const unsigned char *tile, int
 }
 
 // ================================================================ prep kernel
+// One CTA per (q/k head, chunk slot): the products of the chunk's keys and
+// queries are shared by the v heads of the q/k head (GQA), so they are loaded
+// and multiplied once; the decay masks, the solve and P T are per v head.
 constexpr int kPrepThreads = 256;   // 8 warps: warps w and w+4 share TMEM lanes, split columns
+constexpr int kLdc = kChunk + 4;    // column stride of A (column-major, 16-byte aligned columns)
+constexpr int kPassHeads = 2;       // v heads solved side by side (warps 0-1 and 2-3)
 
 struct PrepSmem {
     int blocks;            // dk / 64
     int bpp;               // dk blocks per load phase (operand buffers hold bpp blocks)
-    size_t hi, lo, kp, As, Ts, Xs, tp, gam, bet, bars, total;
+    size_t hi, lo, kp, Ac, Ts, Ws, tp, gam, bet, bars, total;
     __host__ __device__ PrepSmem(int dk) {
         blocks = dk / 64;
         bpp = blocks < 2 ? blocks : 2;
@@ -119,16 +124,17 @@ struct PrepSmem {
         hi = o; o += (size_t)bpp * 2 * kTileBytes;
         lo = o; o += (size_t)bpp * 2 * kTileBytes;
         kp = o; o += (size_t)bpp * kTileBytes;       // K of the previous chunk (hi)
-        // the solve's fp32 scratch reuses the operand buffers once S1 is done
-        As = 0;
-        Ts = As + kChunk * LDA * 4;
-        Xs = Ts + kChunk * LDA * 4;
-        const size_t solve_end = Xs + 768 * 4;
+        // the solve's fp32 scratch reuses the operand buffers once S1 and X are done:
+        // A (column-major), T (row-major), W = A21 T11 (row-major 32x33), per v head
+        Ac = 0;
+        Ts = Ac + (size_t)kPassHeads * kChunk * kLdc * 4;
+        Ws = Ts + (size_t)kPassHeads * kChunk * LDA * 4;
+        const size_t solve_end = Ws + (size_t)kPassHeads * 32 * 33 * 4;
         if (solve_end > o) o = solve_end;
         o = (o + 1023) & ~(size_t)1023;
         tp = o; o += kTPTBytes;
-        gam = o; o += kChunk * 4;
-        bet = o; o += kChunk * 4;
+        gam = o; o += kPassHeads * kChunk * 4;
+        bet = o; o += kPassHeads * kChunk * 4;
         bars = o; o += 64;
         total = o + 1024;    // slack for aligning the base to 1024 B
     }
@@ -143,21 +149,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
     const int tid = threadIdx.x, warp = tid >> 5;
     const int row = tid & 127;                 // TMEM lane = tile row
     const int c0 = (tid >> 7) * 32;            // its 32 of the 64 columns
-    const int j = blockIdx.y;
+    const int hk = blockIdx.y;
+    const int G = d.Hv / d.Hk;
     const int64_t slot = blockIdx.x;
     if (p.cu != nullptr && *p.status != GDN_OK) return;
     ChunkLoc c;
     if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, c)) return;
-    const int hk = j / (d.Hv / d.Hk);
     const PrepSmem L(d.dk);
     unsigned char *hi = sm + L.hi, *lo = sm + L.lo, *kp = sm + L.kp, *tp = sm + L.tp;
-    float *As = (float *)(sm + L.As), *Ts = (float *)(sm + L.Ts), *Xs = (float *)(sm + L.Xs);
+    float *Ac = (float *)(sm + L.Ac), *Ts = (float *)(sm + L.Ts), *Ws = (float *)(sm + L.Ws);
     float *gam = (float *)(sm + L.gam), *bet = (float *)(sm + L.bet);
     uint64_t *bar_load = (uint64_t *)(sm + L.bars), *bar_mma = bar_load + 1;
     uint32_t *tslot = (uint32_t *)(bar_load + 2);
     __shared__ volatile int s_err;
     const bool has_prev = c.tok0 > c.seq0;     // not the first chunk of its sequence
-    unsigned char *out = tpt + ((int64_t)j * nslots + slot) * kPrepOut;
+    // per v head: [T; P T] then X (X is written for the first v head of the group only)
+    auto out_of = [&](int jv) { return tpt + ((int64_t)jv * nslots + slot) * kPrepOut; };
 
     if (tid == 0) {
         s_err = 0;
@@ -174,13 +181,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
     const int nphase = L.blocks / L.bpp;
     uint32_t load_phase = 0, mma_phase = 0;
     bool load_out = false, mma_out = false;
+    // cumulative decay and beta of v heads g0, g0 + 1 of the group (their global
+    // loads overlap the operand copies for the first pass)
+    auto load_gb = [&](int g0) {
+        if (tid < kPassHeads * kChunk) {
+            const int h = tid >> 6, i = tid & (kChunk - 1);
+            if (g0 + h < G) {
+                const int64_t base = (int64_t)(hk * G + g0 + h) * p.ntok + c.tok0;
+                gam[tid] = ((const float *)p.gamma)[base + (i < c.len ? i : c.len - 1)];
+                bet[tid] = i < c.len ? p.beta[base + i] : 0.f;
+            }
+        }
+    };
+    load_gb(0);
 
-    if (tid < kChunk) {
-        const float *gw = (const float *)p.gamma + (int64_t)j * p.ntok;
-        const int i = tid < c.len ? tid : c.len - 1;
-        gam[tid] = gw[c.tok0 + i];
-        bet[tid] = tid < c.len ? p.beta[(int64_t)j * p.ntok + c.tok0 + tid] : 0.f;
-    }
     // S1 = [Kh;Qh] Kh^T + [Kh;Qh] Kl^T + [Kl;Ql] Kh^T  -> TMEM cols [0, 64), and
     // X = [Kh;Qh] Kh_prev^T -> cols [128, 192), dk blocks streamed through the
     // operand buffers bpp at a time
@@ -232,114 +246,168 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
     if (has_prev) {   // X -> workspace, fp16, already in the 128-byte-swizzled tile layout
         float v[32];
         tmem_ld32(lane_addr + 128, v);
+        unsigned char *xo = out_of(hk * G) + kTPTBytes;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint4 u;
             __half2 *h = reinterpret_cast<__half2 *>(&u);
 #pragma unroll
             for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
-            *reinterpret_cast<uint4 *>(out + kTPTBytes + sw128_off(row, c0 + 8 * q)) = u;
+            *reinterpret_cast<uint4 *>(xo + sw128_off(row, c0 + 8 * q)) = u;
         }
     }
-    {   // decay masks: rows 0..63 -> A (fp32, solve input); rows 64..127 -> P (fp16 tile)
-        float v[32];
-        tmem_ld32(lane_addr, v);
+    // S1 stays in TMEM cols [0, 64) for every v head of the group
+
+    for (int g0 = 0; g0 < G; g0 += kPassHeads) {
+        const int nh = G - g0 < kPassHeads ? G - g0 : kPassHeads;
+        if (g0 > 0) load_gb(g0);
+        __syncthreads();
+        // A = beta_i e^{gam_i - gam_j} k_i.k_j below the diagonal, stored column-major
         if (row < kChunk) {
-            const int i = row;
-            const float gi = gam[i], bi = bet[i];
+            float s1[32];
+            tmem_ld32(lane_addr, s1);
+            for (int h = 0; h < nh; ++h) {
+                const float gi = gam[h * kChunk + row], bi = bet[h * kChunk + row];
+                float *Ah = Ac + h * kChunk * kLdc;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int jj = c0 + q;
-                As[i * LDA + jj] = jj < i ? bi * __expf(gi - gam[jj]) * v[q] : 0.f;
+                for (int q = 0; q < 32; ++q) {
+                    const int jj = c0 + q;
+                    Ah[jj * kLdc + row] = jj < row ? bi * __expf(gi - gam[h * kChunk + jj]) * s1[q] : 0.f;
+                }
             }
-        } else {
-            const int i = row - kChunk;
-            const float gi = gam[i];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int jj = c0 + q;
-                v[q] = jj <= i ? __expf(gi - gam[jj]) * v[q] : 0.f;
-            }
-            store_half_row_f16(tp, row, c0, v);
-        }
-    }
-    for (int e = tid; e < kChunk * LDA; e += kPrepThreads) Ts[e] = 0.f;
-    fence_before_sync();
-    __syncthreads();
-    // T = (I + A)^{-1}: 16x16 diagonal blocks by forward substitution, one
-    // column per thread with the column in registers (x[m] = 0 above the
-    // diagonal makes the unrolled triangle exact) ...
-    if (tid < kChunk) {
-        const int blk = tid >> 4, cc = tid & 15, o0 = blk * 16;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float val = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < r; ++m) val = fmaf(-As[(o0 + r) * LDA + o0 + m], x[m], val);
-            x[r] = val;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Ts[(o0 + r) * LDA + o0 + cc] = x[r];
-    }
-    __syncthreads();
-    // ... then one block diagonal at a time: T[bi][bj] = -T[bi][bi] sum_m A[bi][m] T[m][bj]
-#pragma unroll
-    for (int dd = 1; dd < 4; ++dd) {
-        const int npairs = 4 - dd;
-        for (int e = tid; e < npairs * 256; e += kPrepThreads) {
-            const int pr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int bj = pr, bi = pr + dd;
-            float x = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16 * dd; ++m) x = fmaf(As[(bi * 16 + r) * LDA + bj * 16 + m], Ts[(bj * 16 + m) * LDA + bj * 16 + cc], x);
-            Xs[pr * 256 + r * 16 + cc] = x;
         }
         __syncthreads();
-        for (int e = tid; e < npairs * 256; e += kPrepThreads) {
-            const int pr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int bj = pr, bi = pr + dd;
-            float t = 0.f;
+        // T = (I + A)^{-1} in two levels. The 32x32 diagonal blocks first: one warp
+        // per (v head, block), thread jc solving column jc by forward substitution
+        // with the column in registers; after step m, row m is final and updates
+        // the rows below it with column m of A (the same address for every thread).
+        if (tid < nh * kChunk) {
+            const int h = tid >> 6, b = (tid >> 5) & 1, jc = tid & 31;
+            const float *Ab = Ac + h * kChunk * kLdc + 32 * b * kLdc + 32 * b;
+            float2 acc[16];                    // rows 2k, 2k + 1 of the block
 #pragma unroll
-            for (int m = 0; m < 16; ++m) t = fmaf(Ts[(bi * 16 + r) * LDA + bi * 16 + m], Xs[pr * 256 + m * 16 + cc], t);
-            Ts[(bi * 16 + r) * LDA + bj * 16 + cc] = -t;
+            for (int k = 0; k < 16; ++k) acc[k] = make_float2(2 * k == jc ? 1.f : 0.f, 2 * k + 1 == jc ? 1.f : 0.f);
+#pragma unroll
+            for (int m = 0; m < 31; ++m) {
+                const float tm = (m & 1) ? acc[m >> 1].y : acc[m >> 1].x;
+                const float2 nt = make_float2(-tm, -tm);
+                const float4 *col = reinterpret_cast<const float4 *>(Ab + m * kLdc);
+                // rows up to m hold A = 0 in this column, so whole float4 groups are safe
+#pragma unroll
+                for (int q = (m + 1) >> 2; q < 8; ++q) {
+                    const float4 a = col[q];
+                    acc[2 * q] = fma2(make_float2(a.x, a.y), nt, acc[2 * q]);
+                    acc[2 * q + 1] = fma2(make_float2(a.z, a.w), nt, acc[2 * q + 1]);
+                }
+            }
+            float *Th = Ts + h * kChunk * LDA + 32 * b * LDA + 32 * b;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                Th[(2 * k) * LDA + jc] = acc[k].x;
+                Th[(2 * k + 1) * LDA + jc] = acc[k].y;
+                if (b == 0) {                  // the upper right block of T is zero
+                    Th[(2 * k) * LDA + 32 + jc] = 0.f;
+                    Th[(2 * k + 1) * LDA + 32 + jc] = 0.f;
+                }
+            }
         }
         __syncthreads();
-    }
-    if (tid < 2 * kChunk) {   // T rows into the fp16 tile (rows 0..63), 32 columns per thread
-        const int r = tid & 63, h = (tid >> 6) * 32;
-        float v[32];
+        // ... then T21 = -T22 (A21 T11): two 32x32x32 products, each thread a 4x2 tile
+        const int mt = tid & 127, mh = tid >> 7;
+        const int i0 = (mt >> 4) * 4, j0 = (mt & 15) * 2;
+        if (mh < nh) {                         // W = A21 T11 (T11 is zero above its diagonal)
+            const float *Ah = Ac + mh * kChunk * kLdc;
+            const float *Th = Ts + mh * kChunk * LDA;
+            float2 w[4] = {};
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float4 a = *reinterpret_cast<const float4 *>(Ah + k * kLdc + 32 + i0);
+                const float2 t = make_float2(Th[k * LDA + j0], Th[k * LDA + j0 + 1]);
+                w[0] = fma2(make_float2(a.x, a.x), t, w[0]);
+                w[1] = fma2(make_float2(a.y, a.y), t, w[1]);
+                w[2] = fma2(make_float2(a.z, a.z), t, w[2]);
+                w[3] = fma2(make_float2(a.w, a.w), t, w[3]);
+            }
+            float *Wh = Ws + mh * 32 * 33;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = Ts[r * LDA + h + q];
-        store_half_row_f16(tp, r, h, v);
-    }
-    fence_async_smem();
-    __syncthreads();
-    // P T: A = [T; P] (K-major), B = T (MN-major, rows 0..63 of the same tile) -> cols [64, 128)
-    if (tid == 0) {
-        const uint32_t id = idesc_f16(128, 64, false, true);
-        for (int ks = 0; ks < 4; ++ks)
-            mma_f16(tbase + 64, sw128_desc(smem_u32(tp) + 32 * ks, 16, 1024),
-                    sw128_desc(smem_u32(tp) + 2048 * ks, 8192, 1024), id, ks != 0);
-        mma_commit(bar_mma);
-    }
-    mma_out = true;
-    if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
-    mma_phase++;
-    __syncthreads();
-    if (s_err) goto cleanup;
-    mma_out = false;
-    fence_after_sync();
-    if (row >= kChunk) {   // P T replaces P in rows 64..127
-        float v[32];
-        tmem_ld32(lane_addr + 64, v);
-        store_half_row_f16(tp, row, c0, v);
-    }
-    __syncthreads();
-    {
-        uint4 *dst = reinterpret_cast<uint4 *>(out);
-        const uint4 *src = reinterpret_cast<const uint4 *>(tp);
-        for (int e = tid; e < (int)(kTPTBytes / 16); e += kPrepThreads) dst[e] = src[e];
+            for (int r = 0; r < 4; ++r) {
+                Wh[(i0 + r) * 33 + j0] = w[r].x;
+                Wh[(i0 + r) * 33 + j0 + 1] = w[r].y;
+            }
+        }
+        __syncthreads();
+        if (mh < nh) {                         // T21 = -T22 W (T22 is zero above its diagonal)
+            const float *Wh = Ws + mh * 32 * 33;
+            float *Th = Ts + mh * kChunk * LDA;
+            float2 t21[4] = {};
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float2 wk = make_float2(Wh[k * 33 + j0], Wh[k * 33 + j0 + 1]);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float t22 = Th[(32 + i0 + r) * LDA + 32 + k];
+                    t21[r] = fma2(make_float2(t22, t22), wk, t21[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                Th[(32 + i0 + r) * LDA + j0] = -t21[r].x;
+                Th[(32 + i0 + r) * LDA + j0 + 1] = -t21[r].y;
+            }
+        }
+        __syncthreads();
+        for (int h = 0; h < nh; ++h) {
+            // [T; P] tile: T rows from the solve, P = e^{gam_i - gam_j} q_i.k_j (j <= i)
+            {
+                float v[32];
+                if (row < kChunk) {
+                    const float *Th = Ts + h * kChunk * LDA + row * LDA + c0;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] = Th[q];
+                } else {
+                    const int i = row - kChunk;
+                    const float gi = gam[h * kChunk + i];
+                    float s1[32];
+                    tmem_ld32(lane_addr, s1);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int jj = c0 + q;
+                        v[q] = jj <= i ? __expf(gi - gam[h * kChunk + jj]) * s1[q] : 0.f;
+                    }
+                }
+                store_half_row_f16(tp, row, c0, v);
+            }
+            fence_async_smem();
+            __syncthreads();
+            // P T: A = [T; P] (K-major), B = T (MN-major, rows 0..63 of the same tile) -> cols [64, 128)
+            if (tid == 0) {
+                const uint32_t id = idesc_f16(128, 64, false, true);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tbase + 64, sw128_desc(smem_u32(tp) + 32 * ks, 16, 1024),
+                            sw128_desc(smem_u32(tp) + 2048 * ks, 8192, 1024), id, ks != 0);
+                mma_commit(bar_mma);
+            }
+            mma_out = true;
+            if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
+            mma_phase++;
+            __syncthreads();
+            if (s_err) goto cleanup;
+            mma_out = false;
+            fence_after_sync();
+            if (row >= kChunk) {   // P T replaces P in rows 64..127
+                float v[32];
+                tmem_ld32(lane_addr + 64, v);
+                store_half_row_f16(tp, row, c0, v);
+            }
+            fence_before_sync();
+            __syncthreads();
+            {
+                uint4 *dst = reinterpret_cast<uint4 *>(out_of(hk * G + g0 + h));
+                const uint4 *src = reinterpret_cast<const uint4 *>(tp);
+                for (int e = tid; e < (int)(kTPTBytes / 16); e += kPrepThreads) dst[e] = src[e];
+            }
+            __syncthreads();   // tp is rewritten for the next v head
+        }
     }
 
 cleanup:
@@ -414,7 +482,8 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     const int n = bid / d.Hv;
     if (p.cu != nullptr && *p.status != GDN_OK) return;
     const int dk = d.dk, dv = d.dv, Hv = d.Hv;
-    const int hk = j / (Hv / d.Hk);
+    const int G = Hv / d.Hk;                   // v heads per q/k head
+    const int hk = j / G;
     const int v0 = tile * 64;
     const int64_t seq0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
     const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : seq0 + d.T;
@@ -528,7 +597,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 for (int b = 0; b < L.blocks; ++b)
                     tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar[B_LQ0 + s]);
                 if (with_x)
-                    bulk_load(st + L.x, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut + kTPTBytes,
+                    bulk_load(st + L.x, prep_out + ((int64_t)(hk * G) * nslots + slot0 + c) * kPrepOut + kTPTBytes,
                               kXBytes, &bar[B_LQ0 + s]);
             };
             auto load_tpt = [&](int c) {
@@ -838,7 +907,7 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
                                              (int)ps.total);
         if (e != cudaSuccess) return e;
         if (nslots > 0) {
-            chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hv), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt);
+            chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
