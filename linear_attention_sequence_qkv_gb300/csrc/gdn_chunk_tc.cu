@@ -111,15 +111,18 @@ __device__ __forceinline__ void load_half_row_f16(const unsigned char *tile, int
 // and multiplied once; the decay masks, the solve and P T are per v head.
 constexpr int kPrepThreads = 256;   // 8 warps: warps w and w+4 share TMEM lanes, split columns
 constexpr int kLdc = kChunk + 4;    // column stride of A (column-major, 16-byte aligned columns)
-constexpr int kPassHeads = 2;       // v heads solved side by side (warps 0-1 and 2-3)
+// v heads solved per pass (the solve scratch holds this many); one keeps the
+// shared memory of a CTA at ~58 KB and the TMEM at 128 columns, so that three
+// CTAs share an SM and hide each other's copy and barrier latency
+constexpr int kPassHeads = 1;
 
 struct PrepSmem {
     int blocks;            // dk / 64
-    int bpp;               // dk blocks per load phase (operand buffers hold bpp blocks)
+    int bpp;               // dk blocks per load phase (operand buffers hold bpp blocks: one)
     size_t hi, lo, kp, Ac, Ts, Ws, tp, gam, bet, bars, total;
     __host__ __device__ PrepSmem(int dk) {
         blocks = dk / 64;
-        bpp = blocks < 2 ? blocks : 2;
+        bpp = 1;                                     // 40 KB of operands per phase
         size_t o = 0;
         hi = o; o += (size_t)bpp * 2 * kTileBytes;
         lo = o; o += (size_t)bpp * 2 * kTileBytes;
@@ -140,7 +143,7 @@ struct PrepSmem {
     }
 };
 
-__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
+__global__ void __launch_bounds__(kPrepThreads, 3) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
                                                                      const Problem p, int64_t nslots,
                                                                      unsigned char *tpt) {
     extern __shared__ unsigned char smraw[];
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
         mbar_init(bar_mma, 1);
         mbar_init_fence();
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
+    if (warp == 0) tmem_alloc(tslot, 128);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
     load_gb(0);
 
     // S1 = [Kh;Qh] Kh^T + [Kh;Qh] Kl^T + [Kl;Ql] Kh^T  -> TMEM cols [0, 64), and
-    // X = [Kh;Qh] Kh_prev^T -> cols [128, 192), dk blocks streamed through the
+    // X = [Kh;Qh] Kh_prev^T -> cols [64, 128) (later reused by P T), dk blocks streamed through the
     // operand buffers bpp at a time
     for (int ph = 0; ph < nphase; ++ph) {
         if (tid == 0) {
@@ -228,7 +231,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
                     mma_f16(tbase, ah, al, id, 1);
                     mma_f16(tbase, al, ah, id, 1);
                     if (has_prev)
-                        mma_f16(tbase + 128, ah, sw128_desc(smem_u32(kp + q * kTileBytes) + 32 * ks, 16, 1024),
+                        mma_f16(tbase + 64, ah, sw128_desc(smem_u32(kp + q * kTileBytes) + 32 * ks, 16, 1024),
                                 id, (ph | q | ks) != 0);
                 }
             mma_commit(bar_mma);
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const __gri
 
     if (has_prev) {   // X -> workspace, fp16, already in the 128-byte-swizzled tile layout
         float v[32];
-        tmem_ld32(lane_addr + 128, v);
+        tmem_ld32(lane_addr + 64, v);
         unsigned char *xo = out_of(hk * G) + kTPTBytes;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -420,7 +423,7 @@ cleanup:
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
 // =============================================================== chain kernel
