@@ -323,3 +323,60 @@ done:
     free(qh); free(kh); free(vh); free(ob); free(beta); free(g); free(h0); free(hT);
     return rc;
 }
+
+/* One decode step per sequence: the window of the last W-1 raw inputs (from
+ * the conv cache) and the new token gives the token's conv outputs (the conv
+ * definition applied to a W-row sequence, last row kept); then the same
+ * L2 norm, beta / decay, one step of the token-by-token rule from the carried
+ * state, and the gated RMSNorm as in the forward. */
+int gdn_oracle_decode(const gdn_oracle_decode_problem *p) {
+    if (!p || p->n_seq < 0 || p->Hk <= 0 || p->Hv <= 0 || p->Hv % p->Hk != 0 || p->dk <= 0 ||
+        p->dv <= 0 || p->conv_width < 2)
+        return -1;
+    const int W = p->conv_width, dk = p->dk, dv = p->dv, G = p->Hv / p->Hk;
+    const int ch_qk = p->Hk * dk, ch_v = p->Hv * dv, ch = 2 * ch_qk + ch_v;
+    float *win = (float *)malloc(sizeof(float) * (size_t)W * ch);
+    double *y = (double *)malloc(sizeof(double) * (size_t)W * ch);
+    double *o = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *h0 = (double *)malloc(sizeof(double) * (size_t)dk * dv);
+    double *hT = (double *)malloc(sizeof(double) * (size_t)dk * dv);
+    int rc = 0;
+    if (!win || !y || !o || !h0 || !hT) { rc = -1; goto done; }
+    const int64_t s[2] = {0, W};
+    for (int n = 0; n < p->n_seq; ++n) {
+        /* window rows 0..W-2: cached raw inputs (oldest first); row W-1: the token */
+        const float *cs = p->conv_state + (int64_t)n * ch * (W - 1);
+        for (int r = 0; r < W - 1; ++r)
+            for (int c = 0; c < ch; ++c) win[(int64_t)r * ch + c] = cs[(int64_t)c * (W - 1) + r];
+        float *last = win + (int64_t)(W - 1) * ch;
+        for (int c = 0; c < ch_qk; ++c) {
+            last[c] = p->q_raw[(int64_t)n * ch_qk + c];
+            last[ch_qk + c] = p->k_raw[(int64_t)n * ch_qk + c];
+        }
+        for (int c = 0; c < ch_v; ++c) last[2 * ch_qk + c] = p->v_raw[(int64_t)n * ch_v + c];
+        gdn_oracle_conv_silu(1, s, ch, W, win, ch, p->conv_w, y);
+        double *yq = y + (int64_t)(W - 1) * ch, *yk = yq + ch_qk, *yv = yq + 2 * ch_qk;
+        gdn_oracle_l2norm(1, p->Hk, dk, p->l2_eps, yq);
+        gdn_oracle_l2norm(1, p->Hk, dk, p->l2_eps, yk);
+        /* the cache advanced by this token */
+        double *cso = p->conv_state_out + (int64_t)n * ch * (W - 1);
+        for (int r = 0; r < W - 1; ++r)
+            for (int c = 0; c < ch; ++c) cso[(int64_t)c * (W - 1) + r] = win[(int64_t)(r + 1) * ch + c];
+        for (int h = 0; h < p->Hv; ++h) {
+            const int hk = h / G;
+            double beta, g;
+            beta_decay_one(p->a[(int64_t)n * p->Hv + h], p->b[(int64_t)n * p->Hv + h], p->A_log[h],
+                           p->dt_bias[h], &beta, &g);
+            memcpy(h0, p->state + ((int64_t)n * p->Hv + h) * dk * dv, (size_t)dk * dv * sizeof(double));
+            gdn_oracle_delta_rule(1, dk, dv, yq + (int64_t)hk * dk, dk, yk + (int64_t)hk * dk, dk,
+                                  yv + (int64_t)h * dv, dv, &beta, &g, 1, p->scale, h0, o, dv, hT);
+            memcpy(p->state_out + ((int64_t)n * p->Hv + h) * dk * dv, hT, (size_t)dk * dv * sizeof(double));
+            gdn_oracle_gated_rmsnorm(1, dv, o, dv, p->gate + (int64_t)n * ch_v + (int64_t)h * dv, ch_v,
+                                     p->norm_w, p->norm_eps, p->act,
+                                     p->out + ((int64_t)n * p->Hv + h) * dv, dv);
+        }
+    }
+done:
+    free(win); free(y); free(o); free(h0); free(hT);
+    return rc;
+}

@@ -115,6 +115,29 @@ typedef struct {
 
 int gdn_oracle_forward(const gdn_oracle_problem *p, int head_begin, int head_end);
 
+/* One decode step: a single new token for each of n_seq sequences, given each
+ * sequence's conv cache and state (the forward of one more token of those
+ * sequences; the decode entry of the GPU library has no counterpart on the
+ * pages beyond the forward it must agree with).
+ *   q_raw, k_raw [n_seq][Hk*dk], v_raw [n_seq][Hv*dv], a, b [n_seq][Hv],
+ *   gate [n_seq][Hv*dv], conv_w, A_log, dt_bias, norm_w as in the forward;
+ *   conv_state [n_seq][ch][width-1]: the raw inputs of the sequence's last
+ *   width-1 tokens per channel, oldest first (ch = 2*Hk*dk + Hv*dv, q|k|v
+ *   order; zeros where the sequence is shorter);
+ *   state [n_seq][Hv][dk][dv]: S^T as in the forward, in double precision
+ *   (so that a chain of steps carries the state as the forward does).
+ * Outputs (double): out [n_seq][Hv][dv]; conv_state_out and state_out in the
+ * layouts of conv_state and state, advanced by the token. Returns 0, or -1. */
+typedef struct {
+    int n_seq, Hk, Hv, dk, dv, conv_width, act;
+    double l2_eps, norm_eps, scale;
+    const float *q_raw, *k_raw, *v_raw, *a, *b, *gate, *conv_w;
+    const float *A_log, *dt_bias, *norm_w, *conv_state;
+    const double *state;
+    double *out, *conv_state_out, *state_out;
+} gdn_oracle_decode_problem;
+int gdn_oracle_decode(const gdn_oracle_decode_problem *p);
+
 #ifdef __cplusplus
 }
 #endif

@@ -48,6 +48,18 @@ class _Problem(ctypes.Structure):
     ]
 
 
+class _DecodeProblem(ctypes.Structure):
+    _fields_ = [
+        ("n_seq", ctypes.c_int), ("Hk", ctypes.c_int), ("Hv", ctypes.c_int),
+        ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("conv_width", ctypes.c_int), ("act", ctypes.c_int),
+        ("l2_eps", ctypes.c_double), ("norm_eps", ctypes.c_double), ("scale", ctypes.c_double),
+        ("q_raw", _f32p), ("k_raw", _f32p), ("v_raw", _f32p), ("a", _f32p), ("b", _f32p),
+        ("gate", _f32p), ("conv_w", _f32p), ("A_log", _f32p), ("dt_bias", _f32p),
+        ("norm_w", _f32p), ("conv_state", _f32p), ("state", _f64p),
+        ("out", _f64p), ("conv_state_out", _f64p), ("state_out", _f64p),
+    ]
+
+
 def build(force: bool = False) -> str:
     """Compile ``libgdn_oracle.so`` next to its source if it is missing or stale."""
     with _lock:
@@ -92,6 +104,8 @@ def lib():
                                                ctypes.c_int, _f64p, ctypes.c_int64]
         L.gdn_oracle_forward.restype = ctypes.c_int
         L.gdn_oracle_forward.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int, ctypes.c_int]
+        L.gdn_oracle_decode.restype = ctypes.c_int
+        L.gdn_oracle_decode.argtypes = [ctypes.POINTER(_DecodeProblem)]
         _lib = L
     return _lib
 
@@ -217,3 +231,29 @@ def forward(*, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
         with cf.ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(run, heads))
     return out, fin
+
+
+def decode(*, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
+           conv_state, state, Hk, Hv, dk, dv, dtype,
+           l2_eps=1e-6, norm_eps=1e-5, scale=1.0, conv_width=4):
+    """One decode step (float32 values, one token per sequence):
+    q_raw/k_raw [N, Hk*dk], v_raw [N, Hv*dv], a/b [N, Hv], gate [N, Hv*dv],
+    conv_state [N, ch, width-1] (raw inputs of the last tokens, oldest first),
+    state [N, Hv, dk, dv] (taken in float64). Returns (out [N, Hv, dv],
+    conv_state_out, state_out), all float64."""
+    arrs = dict(q_raw=_f32(q_raw), k_raw=_f32(k_raw), v_raw=_f32(v_raw), a=_f32(a), b=_f32(b),
+                gate=_f32(gate), conv_w=_f32(conv_w), A_log=_f32(A_log),
+                dt_bias=_f32(dt_bias), norm_w=_f32(norm_w), conv_state=_f32(conv_state))
+    st = _f64(state)
+    n = arrs["q_raw"].shape[0]
+    ch = 2 * Hk * dk + Hv * dv
+    out = np.zeros((n, Hv, dv))
+    cso = np.zeros((n, ch, conv_width - 1))
+    so = np.zeros((n, Hv, dk, dv))
+    prob = _DecodeProblem(
+        n_seq=n, Hk=Hk, Hv=Hv, dk=dk, dv=dv, conv_width=conv_width, act=ACT_CODES[dtype],
+        l2_eps=l2_eps, norm_eps=norm_eps, scale=scale, **{k: _p32(v) for k, v in arrs.items()},
+        state=_p64(st), out=_p64(out), conv_state_out=_p64(cso), state_out=_p64(so))
+    if lib().gdn_oracle_decode(ctypes.byref(prob)) != 0:
+        raise RuntimeError("gdn_oracle_decode failed")
+    return out, cso, so
