@@ -208,6 +208,44 @@ int gdn_forward_static_ws(const gdn_desc *d,
  * 1 = tcgen05 tensor-core kernel (bf16/fp16). */
 int gdn_chunk_kernel_kind(const gdn_desc *d);
 
+/*
+ * Decode: one new token for each of d->B sequences. The result is what
+ * gdn_forward gives for one more token of each sequence (same definitions,
+ * same readings): the width-4 causal conv takes the sequence's last three raw
+ * inputs from a conv cache, then SiLU, the q/k L2 norm, beta and the decay, one
+ * step of S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T with
+ * o_t = scale * S_t q_t from the carried state, and the gated RMSNorm. The pages
+ * define the forward; a decode cache appears there only as the conv input that a
+ * fused prefill conv has to leave out ("fused q/k/v short conv",
+ * flash-linear-attention PR #972, "Risk / scope").
+ *
+ * d           d->T == 1, not packed (N == B), everything else as for gdn_forward;
+ *             the token tensors are [B, 1, *] views (only the batch strides and
+ *             the contiguous channels matter).
+ * q_raw ... norm_w   as for gdn_forward, one token per sequence.
+ * conv_state  act dtype [B][ch][3] contiguous, ch = 2*Hk*dk + Hv*dv in q|k|v
+ *             order: per channel the raw inputs of the sequence's last three
+ *             tokens, oldest first (zeros where the sequence has fewer). Read,
+ *             then overwritten with the window advanced by this token. After a
+ *             gdn_forward prefill it holds that call's last three raw tokens.
+ * state       fp32 [B][Hv][dk][dv] (S^T per sequence and v head, the layout of
+ *             gdn_forward's initial_state / final_state), 16-byte aligned; read
+ *             and overwritten in place.
+ * out         act dtype [B, 1, Hv, dv] contiguous, 16-byte aligned.
+ * workspace   gdn_decode_workspace_bytes(d) bytes, 256-byte aligned; its first
+ *             word is the device status (gdn_device_status).
+ * Returns GDN_OK or a negative status as gdn_forward (GDN_ERR_INVALID_ARG for
+ * d->T != 1 or a packed descriptor). conv_state, state, out and workspace must
+ * not overlap each other or the inputs.
+ */
+int gdn_decode_workspace_bytes(const gdn_desc *d, size_t *bytes);
+int gdn_decode_step(const gdn_desc *d,
+                    const void *q_raw, const void *k_raw, const void *v_raw,
+                    const void *a, const void *b, const void *gate,
+                    const void *conv_w, const float *A_log, const float *dt_bias,
+                    const void *norm_w, void *conv_state, float *state, void *out,
+                    void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -243,6 +243,68 @@ int gdn_forward(const gdn_desc *d, const void *q_raw, const void *k_raw, const v
     return run_epilogue(p, s);
 }
 
+int gdn_decode_workspace_bytes(const gdn_desc *d, size_t *bytes) {
+    if (!bytes) return GDN_ERR_INVALID_ARG;
+    int rc = check_desc(d, false);
+    if (rc != GDN_OK) return rc;
+    if (d->T != 1) return GDN_ERR_INVALID_ARG;
+    *bytes = gdn::make_decode_layout(*d).total;
+    return GDN_OK;
+}
+
+int gdn_decode_step(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw,
+                    const void *a, const void *b, const void *gate, const void *conv_w,
+                    const float *A_log, const float *dt_bias, const void *norm_w, void *conv_state,
+                    float *state, void *out, void *workspace, size_t workspace_bytes,
+                    gdn_stream_t stream) {
+    int rc = check_desc(d, false);
+    if (rc != GDN_OK) return rc;
+    if (d->T != 1) return GDN_ERR_INVALID_ARG;
+    if (!q_raw || !k_raw || !v_raw || !a || !b || !gate || !conv_w || !A_log || !dt_bias || !norm_w ||
+        !conv_state || !state || !out)
+        return GDN_ERR_INVALID_ARG;
+    const size_t es = gdn::act_size(d->dtype);
+    if (!aligned(q_raw, es) || !aligned(k_raw, es) || !aligned(v_raw, es) || !aligned(conv_w, es) ||
+        !aligned(conv_state, es) || !aligned(state, 16) || !aligned(out, 16) || !aligned(norm_w, 4))
+        return GDN_ERR_INVALID_ARG;
+    const gdn::DecodeLayout L = gdn::make_decode_layout(*d);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return GDN_ERR_WORKSPACE;
+    char *w = (char *)workspace;
+    gdn::DecodeProblem p;
+    memset(&p, 0, sizeof(p));
+    p.d = *d;
+    p.q_raw = q_raw;
+    p.k_raw = k_raw;
+    p.v_raw = v_raw;
+    p.a = a;
+    p.b = b;
+    p.conv_w = conv_w;
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.conv_state = conv_state;
+    p.state = state;
+    p.status = (int32_t *)(w + L.status);
+    p.q = (float *)(w + L.q);
+    p.k = (float *)(w + L.k);
+    p.v = (float *)(w + L.v);
+    p.beta = (float *)(w + L.beta);
+    p.g = (float *)(w + L.g);
+    p.o = w + L.o;
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((rc = cuda_status(gdn::launch_decode(p, s))) != GDN_OK) return rc;
+    // the forward's gated RMSNorm over the B new tokens
+    Problem e;
+    memset(&e, 0, sizeof(e));
+    e.d = *d;
+    e.ntok = d->B;
+    e.gate = gate;
+    e.norm_w = norm_w;
+    e.out = out;
+    e.status = p.status;
+    e.o = p.o;
+    return run_epilogue(e, s);
+}
+
 int gdn_device_status(const void *workspace, int *status, gdn_stream_t stream) {
     if (!workspace || !status) return GDN_ERR_INVALID_ARG;
     int32_t v = 0;

@@ -91,4 +91,34 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s);
 bool chunk_tc_supports(const gdn_desc &d);
 cudaError_t launch_epilogue(const Problem &p, cudaStream_t s);
 
+// Decode (one token per sequence, d.T == 1): workspace regions, all fp32 but o.
+struct DecodeLayout {
+    size_t status, q, k, v, beta, g, o, total;
+};
+inline DecodeLayout make_decode_layout(const gdn_desc &d) {
+    const size_t B = (size_t)d.B;
+    DecodeLayout L;
+    size_t off = 0;
+    L.status = off; off = align_up(off + 256, 256);
+    L.q = off;      off = align_up(off + 4 * B * d.Hk * d.dk, 256);   // [Hk][B][dk]
+    L.k = off;      off = align_up(off + 4 * B * d.Hk * d.dk, 256);   // [Hk][B][dk]
+    L.v = off;      off = align_up(off + 4 * B * d.Hv * d.dv, 256);   // [B][Hv*dv]
+    L.beta = off;   off = align_up(off + 4 * B * d.Hv, 256);          // [B][Hv]
+    L.g = off;      off = align_up(off + 4 * B * d.Hv, 256);          // [B][Hv]
+    L.o = off;      off = align_up(off + act_size(d.dtype) * B * d.Hv * d.dv, 256);   // [B][Hv][dv], as o
+    L.total = off;
+    return L;
+}
+struct DecodeProblem {
+    gdn_desc d;
+    const void *q_raw, *k_raw, *v_raw, *a, *b, *conv_w;
+    const float *A_log, *dt_bias;
+    void *conv_state;
+    float *state;
+    int32_t *status;
+    float *q, *k, *v, *beta, *g;
+    void *o;
+};
+cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t s);
+
 }  // namespace gdn

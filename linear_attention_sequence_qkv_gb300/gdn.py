@@ -34,7 +34,8 @@ ACT_TORCH = {GDN_F32: torch.float32, GDN_BF16: torch.bfloat16, GDN_F16: torch.fl
 # every entry point declared in include/gdn.h
 EXPORTS = ("gdn_desc_init", "gdn_workspace_bytes", "gdn_workspace_offsets", "gdn_forward",
            "gdn_prologue", "gdn_chunk_rule", "gdn_epilogue", "gdn_device_status",
-           "gdn_status_string", "gdn_chunk_kernel_kind", "gdn_forward_static_ws")
+           "gdn_status_string", "gdn_chunk_kernel_kind", "gdn_forward_static_ws",
+           "gdn_decode_workspace_bytes", "gdn_decode_step")
 
 # bytes of the library's fixed device scratch used by gdn_forward_static_ws
 GDN_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
@@ -94,6 +95,8 @@ def load(path: str = LIB_PATH):
     L.gdn_status_string.restype = ctypes.c_char_p
     L.gdn_chunk_kernel_kind.argtypes = [dp]
     L.gdn_forward_static_ws.argtypes = [dp] + [vp] * 14 + [vp]
+    L.gdn_decode_workspace_bytes.argtypes = [dp, ctypes.POINTER(sz)]
+    L.gdn_decode_step.argtypes = [dp] + [vp] * 13 + [vp, sz, vp]
     for name in EXPORTS:
         if name != "gdn_status_string":
             getattr(L, name).restype = i32
@@ -212,6 +215,25 @@ def gdn_device_status(workspace, stream=None) -> int:
 
 def gdn_chunk_kernel_kind(d: gdn_desc) -> int:
     return load().gdn_chunk_kernel_kind(ctypes.byref(d))
+
+
+def gdn_decode_workspace_bytes(d: gdn_desc) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().gdn_decode_workspace_bytes(ctypes.byref(d), ctypes.byref(n)),
+           "gdn_decode_workspace_bytes")
+    return n.value
+
+
+def gdn_decode_step(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
+                    conv_state, state, out, workspace, workspace_bytes, stream=None,
+                    check=True) -> int:
+    rc = load().gdn_decode_step(ctypes.byref(d), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(a),
+                                _ptr(b), _ptr(gate), _ptr(conv_w), _ptr(A_log), _ptr(dt_bias),
+                                _ptr(norm_w), _ptr(conv_state), _ptr(state), _ptr(out),
+                                _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if check:
+        _check(rc, "gdn_decode_step")
+    return rc
 
 
 # --------------------------------------------------- tensors -> descriptor

@@ -125,3 +125,40 @@ def test_chunk_kernel_kind(lib):
     assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(2, 100, 0, 6, 6, 64, 128, gdn.GDN_F16)) == 1
     assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(1, 70, 0, 1, 1, 512, 512, gdn.GDN_BF16)) == 0
     assert gdn.gdn_chunk_kernel_kind(gdn.gdn_desc_init(1, 70, 0, 1, 1, 64, 32, gdn.GDN_BF16)) == 0
+
+
+def test_decode_checks(lib):
+    """The decode entry rejects non-decode descriptors and bad pointers before any launch."""
+    fake = 1 << 20   # never dereferenced: every call below fails its checks first
+    d = gdn.gdn_desc_init(4, 1, 0, 2, 4, 64, 128, gdn.GDN_BF16)
+    need = gdn.gdn_decode_workspace_bytes(d)
+    # fp32 q, k, v of the token, beta and g, fp16 o, after a 256-byte status block
+    B, Hk, Hv, dk, dv = 4, 2, 4, 64, 128
+    assert need >= 256 + 4 * B * (2 * Hk * dk + Hv * dv + 2 * Hv) + 2 * B * Hv * dv
+    args = [fake] * 13   # q_raw .. out
+
+    def call(desc, a=None, ws=fake, nbytes=None):
+        a = args if a is None else a
+        return lib.gdn_decode_step(ctypes.byref(desc), *a, ws, need if nbytes is None else nbytes, None)
+
+    multi = gdn.gdn_desc_init(4, 8, 0, 2, 4, 64, 128, gdn.GDN_BF16)   # T = 8: not a decode step
+    n = ctypes.c_size_t(0)
+    assert lib.gdn_decode_workspace_bytes(ctypes.byref(multi), ctypes.byref(n)) == gdn.GDN_ERR_INVALID_ARG
+    assert call(multi) == gdn.GDN_ERR_INVALID_ARG
+    packed = gdn.gdn_desc_init(1, 1, 4, 2, 4, 64, 128, gdn.GDN_BF16)  # cu_seqlens-style descriptor
+    assert call(packed) == gdn.GDN_ERR_INVALID_ARG
+    for i in range(13):                     # each pointer null in turn
+        a = list(args)
+        a[i] = None
+        assert call(d, a) == gdn.GDN_ERR_INVALID_ARG, i
+    a = list(args)
+    a[12] = fake + 4                        # out not 16-byte aligned
+    assert call(d, a) == gdn.GDN_ERR_INVALID_ARG
+    a = list(args)
+    a[11] = fake + 8                        # state not 16-byte aligned
+    assert call(d, a) == gdn.GDN_ERR_INVALID_ARG
+    assert call(d, nbytes=need - 1) == gdn.GDN_ERR_WORKSPACE
+    assert call(d, ws=fake + 16) == gdn.GDN_ERR_WORKSPACE
+    bad = gdn.gdn_desc_init(4, 1, 0, 2, 4, 64, 128, gdn.GDN_BF16)
+    bad.dk = 48                             # not a power of two
+    assert call(bad) == gdn.GDN_ERR_UNSUPPORTED
