@@ -13,17 +13,17 @@
 //
 // Two kernels: decode_prep (conv + cache, norms, beta / decay; every channel is
 // read and rewritten by one thread) and decode_state (one CTA per (sequence,
-// v head, 32 columns of dv): each thread keeps up to 32 rows of one column in
-// registers, so the state is read once and written once, both coalesced). The
-// step is bound by the state traffic, 8 bytes per element of S per token.
+// v head, stripe of up to 128 columns of dv): each thread keeps 16 rows of 4
+// adjacent columns in registers, so the state is read once and written once
+// with 16-byte accesses). The step is bound by the state traffic, 8 bytes per
+// element of S per token.
 #include "gdn_common.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kPrepThreads = 512;   // >= dk: one q or k head per CTA
-constexpr int kStateCols = 32;      // dv columns per state CTA
-constexpr int kStateRows = 32;      // state rows per thread
+constexpr int kQuadRows = 16;       // state rows per thread (4 columns each)
 
 // y = silu(conv) of channel c from the cache and the token x; advances the cache
 template <typename T>
@@ -83,56 +83,82 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const DecodeP
     }
 }
 
-// grid (B * Hv, dv / ncol); block ncol x (dk / rows) threads: column `col`,
-// rows [slice * rows, +rows) of the state of (n, j)
+// grid (B * Hv, dv / (4 nq)); block nq x (dk / kQuadRows) threads: thread
+// (qd, slice) owns columns [4 qd, +4) of the CTA's stripe and rows
+// [slice * kQuadRows, +kQuadRows) of the state of (n, j), in registers
 template <typename S>
-__global__ void __launch_bounds__(512) decode_state_kernel(const DecodeProblem p, int ncol, int rows) {
+__global__ void __launch_bounds__(256, 2) decode_state_kernel(const DecodeProblem p, int nq) {
     extern __shared__ float dsm[];
     const gdn_desc &d = p.d;
     const int dk = d.dk, dv = d.dv;
-    const int col = threadIdx.x % ncol, slice = threadIdx.x / ncol;
-    const int slices = blockDim.x / ncol;
+    const int qd = threadIdx.x % nq, slice = threadIdx.x / nq;
+    const int slices = blockDim.x / nq;
     const int nj = blockIdx.x;                // n * Hv + j
     const int n = nj / d.Hv, j = nj - n * d.Hv;
     const int hk = j / (d.Hv / d.Hk);
-    const int c = blockIdx.y * ncol + col;
-    float *qs = dsm, *ks = dsm + dk, *red = dsm + 2 * dk;
+    const int c = (blockIdx.y * nq + qd) * 4;
+    float *qs = dsm, *ks = dsm + dk;
+    float4 *red = reinterpret_cast<float4 *>(dsm + 2 * dk);   // [slices][nq]
     for (int i = threadIdx.x; i < dk; i += blockDim.x) {
         qs[i] = p.q[((int64_t)hk * d.B + n) * dk + i];
         ks[i] = p.k[((int64_t)hk * d.B + n) * dk + i];
     }
     __syncthreads();
-    float *H = p.state + (int64_t)nj * dk * dv + c;
-    const int r0 = slice * rows;
-    float h[kStateRows];
-    float u = 0.f;
+    const int r0 = slice * kQuadRows;
+    const int rs = dv / 4;                    // row stride in float4
+    float4 *H = reinterpret_cast<float4 *>(p.state + (int64_t)nj * dk * dv + (int64_t)r0 * dv + c);
+    float4 h[kQuadRows];
 #pragma unroll
-    for (int i = 0; i < kStateRows; ++i)
-        if (i < rows) h[i] = H[(int64_t)(r0 + i) * dv];
+    for (int i = 0; i < kQuadRows; ++i) h[i] = H[i * rs];
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kStateRows; ++i)
-        if (i < rows) u = fmaf(h[i], ks[r0 + i], u);
-    red[slice * ncol + col] = u;
+    for (int i = 0; i < kQuadRows; ++i) {
+        const float kk = ks[r0 + i];
+        u.x = fmaf(h[i].x, kk, u.x);
+        u.y = fmaf(h[i].y, kk, u.y);
+        u.z = fmaf(h[i].z, kk, u.z);
+        u.w = fmaf(h[i].w, kk, u.w);
+    }
+    red[slice * nq + qd] = u;
     __syncthreads();
-    float ut = 0.f;
-    for (int s = 0; s < slices; ++s) ut += red[s * ncol + col];
-    const float eg = expf(p.g[nj]);
-    const float r = p.beta[nj] * (p.v[(int64_t)n * d.Hv * dv + (int64_t)j * dv + c] - eg * ut);
-    float o = 0.f;
+    float4 ut = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < slices; ++s) {
+        const float4 t = red[s * nq + qd];
+        ut.x += t.x; ut.y += t.y; ut.z += t.z; ut.w += t.w;
+    }
+    const float eg = expf(p.g[nj]), bt = p.beta[nj];
+    const float4 v = *reinterpret_cast<const float4 *>(p.v + (int64_t)n * d.Hv * dv + (int64_t)j * dv + c);
+    const float4 r = make_float4(bt * (v.x - eg * ut.x), bt * (v.y - eg * ut.y), bt * (v.z - eg * ut.z),
+                                 bt * (v.w - eg * ut.w));
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kStateRows; ++i)
-        if (i < rows) {
-            const float hn = fmaf(eg, h[i], ks[r0 + i] * r);
-            H[(int64_t)(r0 + i) * dv] = hn;
-            o = fmaf(hn, qs[r0 + i], o);
-        }
+    for (int i = 0; i < kQuadRows; ++i) {
+        const float kk = ks[r0 + i], qq = qs[r0 + i];
+        float4 hn;
+        hn.x = fmaf(eg, h[i].x, kk * r.x);
+        hn.y = fmaf(eg, h[i].y, kk * r.y);
+        hn.z = fmaf(eg, h[i].z, kk * r.z);
+        hn.w = fmaf(eg, h[i].w, kk * r.w);
+        H[i * rs] = hn;
+        o.x = fmaf(hn.x, qq, o.x);
+        o.y = fmaf(hn.y, qq, o.y);
+        o.z = fmaf(hn.z, qq, o.z);
+        o.w = fmaf(hn.w, qq, o.w);
+    }
     __syncthreads();                          // every thread has read u's partial sums
-    red[slice * ncol + col] = o;
+    red[slice * nq + qd] = o;
     __syncthreads();
     if (slice == 0) {
-        float ot = 0.f;
-        for (int s = 0; s < slices; ++s) ot += red[s * ncol + col];
-        ((S *)p.o)[(int64_t)nj * dv + c] = from_f<S>(ot * d.scale);
+        float4 ot = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < slices; ++s) {
+            const float4 t = red[s * nq + qd];
+            ot.x += t.x; ot.y += t.y; ot.z += t.z; ot.w += t.w;
+        }
+        S *dst = (S *)p.o + (int64_t)nj * dv + c;
+        dst[0] = from_f<S>(ot.x * d.scale);
+        dst[1] = from_f<S>(ot.y * d.scale);
+        dst[2] = from_f<S>(ot.z * d.scale);
+        dst[3] = from_f<S>(ot.w * d.scale);
     }
 }
 
@@ -144,12 +170,16 @@ cudaError_t launch_t(const DecodeProblem &p, cudaStream_t s) {
     decode_prep_kernel<T><<<dim3((unsigned)d.B, 2 * d.Hk + units_v + 1), kPrepThreads, 0, s>>>(p, units_v);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int ncol = d.dv < kStateCols ? d.dv : kStateCols;
-    const int rows = d.dk < kStateRows ? d.dk : kStateRows;
-    const int threads = ncol * (d.dk / rows);
-    const size_t smem = (size_t)(2 * d.dk + threads) * sizeof(float);
+    // column quads per CTA: up to 128 columns, and at most 256 threads (two CTAs
+    // per SM, so that one's stores overlap the other's loads)
+    const int slices = d.dk / kQuadRows;
+    int nq = d.dv / 4;
+    if (nq > 32) nq = 32;
+    if (nq * slices > 256) nq = 256 / slices;
+    const int threads = nq * slices;
+    const size_t smem = (size_t)2 * d.dk * sizeof(float) + (size_t)threads * sizeof(float4);
     using S = typename Inter<T>::S;
-    decode_state_kernel<S><<<dim3((unsigned)((int64_t)d.B * d.Hv), d.dv / ncol), threads, smem, s>>>(p, ncol, rows);
+    decode_state_kernel<S><<<dim3((unsigned)((int64_t)d.B * d.Hv), d.dv / (4 * nq)), threads, smem, s>>>(p, nq);
     return cudaGetLastError();
 }
 
