@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the decode step (one token per sequence) instead of the forward")
+    ap.add_argument("--decode-batch", type=int, default=256, help="sequences per decode step")
     return ap.parse_args()
 
 
@@ -220,12 +223,83 @@ def reference_arm(args, w):
 
 
 # ----------------------------------------------------------------- our arm
+# -------------------------------------------------------------- decode step
+def decode_main(args, w):
+    """One decode step per timed iteration: args.decode_batch sequences with the
+    workload's head shape, each with a conv cache and a state resident in HBM."""
+    import torch
+    from linear_attention_sequence_qkv_gb300 import build, gdn
+    from linear_attention_sequence_qkv_gb300.workloads import make_inputs_device, replace
+
+    build.build()
+    gdn.load()
+    dev = torch.device("cuda", 0)
+    B = args.decode_batch
+    wd = replace(w, B=B, T=1, n_packed=0)
+    inp = make_inputs_device(wd, dev)
+    d = gdn.desc_for(inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.gate, inp.norm_w,
+                     Hk=wd.Hk, Hv=wd.Hv, dk=wd.dk, dv=wd.dv)
+    ws = torch.empty(gdn.gdn_decode_workspace_bytes(d), dtype=torch.uint8, device=dev)
+    ch = 2 * wd.Hk * wd.dk + wd.Hv * wd.dv
+    cache = torch.zeros((B, ch, 3), dtype=inp.q_raw.dtype, device=dev)
+    state = torch.randn((B, wd.Hv, wd.dk, wd.dv), device=dev) * 0.1
+    out = torch.empty((B, 1, wd.Hv, wd.dv), dtype=inp.q_raw.dtype, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gdn.gdn_decode_step(d, inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.gate, inp.conv_w,
+                            inp.A_log, inp.dt_bias, inp.norm_w, cache, state, out, ws, ws.numel(), stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status(ws) == gdn.GDN_OK
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = None if args.no_clocks else ClockSampler(None)
+    torch.cuda.synchronize()
+    for e in evs:
+        flush.zero_()
+        e[0].record()
+        step()
+        e[1].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    s = 4 if wd.dtype == "fp32" else 2
+    # algorithmic bytes of a step: the state read and written (fp32), the conv cache
+    # read and written, the token's raw inputs, a, b, gate, and the output
+    per_seq = (8 * wd.Hv * wd.dk * wd.dv + 2 * 3 * ch * s + ch * s + 2 * wd.Hv * s
+               + 2 * wd.Hv * wd.dv * s)
+    pk = peaks()
+    ach = B * per_seq / (ms / 1e3) / 1e9
+    line = {
+        "metric": "GDN decode step tokens/s at 1 GB300 and % of HBM roofline", "value": B / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp32": "f32", "bf16": "bf16", "fp16": "f16"}[wd.dtype], "data": "synthetic",
+        "config": {"workload": f"decode_{w.name}", "sequences": B, "Hk": wd.Hk, "Hv": wd.Hv,
+                   "dk": wd.dk, "dv": wd.dv, "l2": "flushed before every timed step (512 MiB write)"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / pk["hbm_gbs"], "algorithmic_bytes": B * per_seq, "traffic": None,
+                     "kernel": "decode step (decode_prep + decode_state + epilogue)",
+                     "peak_source": pk["source"]},
+        "gpu_launches": 3 * args.steps, "gpu_launches_per_step": 3, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from linear_attention_sequence_qkv_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         reference_arm(args, w)
+        return
+    if args.decode:
+        decode_main(args, w)
         return
 
     import torch
