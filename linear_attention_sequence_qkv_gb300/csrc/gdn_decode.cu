@@ -22,7 +22,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kPrepThreads = 512;   // >= dk: one q or k head per CTA
+constexpr int kPrepThreads = 512;   // most threads of a prep CTA: max(dk, 128) are launched
 constexpr int kQuadRows = 16;       // state rows per thread (4 columns each)
 
 // y = silu(conv) of channel c from the cache and the token x; advances the cache
@@ -68,13 +68,13 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const DecodeP
         for (int i = 0; i < (d.dk + 31) / 32; ++i) tot += red[i];
         if (tid < d.dk) (isk ? p.k : p.q)[((int64_t)h * d.B + n) * d.dk + tid] = y * rsqrtf(tot + d.l2_eps);
     } else if (u < 2 * d.Hk + units_v) {      // a group of v channels
-        const int cv = (u - 2 * d.Hk) * kPrepThreads + tid;
+        const int cv = (u - 2 * d.Hk) * (int)blockDim.x + tid;
         if (cv < ch_v) {
             const T *x = (const T *)p.v_raw + (int64_t)n * d.v_stride_b + cv;
             p.v[(int64_t)n * ch_v + cv] = conv_token<T>(cs, w, 2 * ch_qk + cv, *x);
         }
     } else {                                  // beta and decay of every v head
-        for (int h = tid; h < d.Hv; h += kPrepThreads) {
+        for (int h = tid; h < d.Hv; h += blockDim.x) {
             const float av = to_f<T>(((const T *)p.a)[(int64_t)n * d.a_stride_b + h]);
             const float bv = to_f<T>(((const T *)p.b)[(int64_t)n * d.b_stride_b + h]);
             p.beta[(int64_t)n * d.Hv + h] = sigmoid_f(bv);
@@ -166,8 +166,10 @@ template <typename T>
 cudaError_t launch_t(const DecodeProblem &p, cudaStream_t s) {
     const gdn_desc &d = p.d;
     const int ch_v = d.Hv * d.dv;
-    const int units_v = (ch_v + kPrepThreads - 1) / kPrepThreads;
-    decode_prep_kernel<T><<<dim3((unsigned)d.B, 2 * d.Hk + units_v + 1), kPrepThreads, 0, s>>>(p, units_v);
+    // a q or k head per CTA (dk threads, at least 128 so that the v groups are not tiny)
+    const int pt = d.dk > 128 ? d.dk : 128;
+    const int units_v = (ch_v + pt - 1) / pt;
+    decode_prep_kernel<T><<<dim3((unsigned)d.B, 2 * d.Hk + units_v + 1), pt, 0, s>>>(p, units_v);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // column quads per CTA: up to 128 columns, and at most 256 threads (two CTAs
