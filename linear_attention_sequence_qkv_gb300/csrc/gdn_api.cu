@@ -86,7 +86,10 @@ int run_prologue(const Problem &p, cudaStream_t s) {
 }
 
 int run_chunk(const Problem &p, cudaStream_t s) {
-    if (gdn::chunk_tc_supports(p.d)) return cuda_status(gdn::launch_chunk_tc(p, s));
+    if (gdn::chunk_tc_supports(p.d)) {
+        if (gdn::chunk_tc_segmented(p)) return cuda_status(gdn::launch_chunk_tc_segmented(p, s));
+        return cuda_status(gdn::launch_chunk_tc(p, s));
+    }
     return cuda_status(gdn::launch_chunk_simt(p, s));
 }
 
@@ -205,12 +208,15 @@ int gdn_epilogue(const gdn_desc *d, const void *gate, const void *norm_w, void *
     return run_epilogue(p, (cudaStream_t)stream);
 }
 
-int gdn_forward(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw,
-                const void *a, const void *b, const void *gate, const void *conv_w,
-                const float *A_log, const float *dt_bias, const void *norm_w,
-                const int32_t *cu_seqlens, const float *initial_state, void *out,
-                float *final_state, void *workspace, size_t workspace_bytes,
-                gdn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+int forward_impl(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw,
+                 const void *a, const void *b, const void *gate, const void *conv_w,
+                 const float *A_log, const float *dt_bias, const void *norm_w,
+                 const int32_t *cu_seqlens, const float *initial_state, void *out,
+                 float *final_state, void *workspace, size_t workspace_bytes,
+                 gdn_stream_t stream, bool single_stream) {
     int rc = check_desc(d, cu_seqlens != nullptr);
     if (rc != GDN_OK) return rc;
     const bool tok = (int64_t)d->B * d->T > 0;   // token tensors may be empty (null)
@@ -237,10 +243,35 @@ int gdn_forward(const gdn_desc *d, const void *q_raw, const void *k_raw, const v
     p.h0 = initial_state;
     p.hT = final_state;
     p.out = out;
+    p.single_stream = single_stream;
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_prologue(p, s)) != GDN_OK) return rc;
     if ((rc = run_chunk(p, s)) != GDN_OK) return rc;
     return run_epilogue(p, s);
+}
+}  // namespace
+
+namespace gdn {
+int forward_single_stream(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw,
+                          const void *a, const void *b, const void *gate, const void *conv_w,
+                          const float *A_log, const float *dt_bias, const void *norm_w,
+                          const int32_t *cu_seqlens, const float *initial_state, void *out,
+                          float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return forward_impl(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w, cu_seqlens,
+                        initial_state, out, final_state, workspace, workspace_bytes, (gdn_stream_t)stream, true);
+}
+}  // namespace gdn
+
+extern "C" {
+
+int gdn_forward(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw,
+                const void *a, const void *b, const void *gate, const void *conv_w,
+                const float *A_log, const float *dt_bias, const void *norm_w,
+                const int32_t *cu_seqlens, const float *initial_state, void *out,
+                float *final_state, void *workspace, size_t workspace_bytes,
+                gdn_stream_t stream) {
+    return forward_impl(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w, cu_seqlens,
+                        initial_state, out, final_state, workspace, workspace_bytes, stream, false);
 }
 
 int gdn_decode_workspace_bytes(const gdn_desc *d, size_t *bytes) {

@@ -28,6 +28,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
 
@@ -145,7 +147,7 @@ struct PrepSmem {
 
 __global__ void __launch_bounds__(kPrepThreads, 3) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
                                                                      const Problem p, int64_t nslots,
-                                                                     unsigned char *tpt) {
+                                                                     unsigned char *tpt, int64_t slot_base) {
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const gdn_desc &d = p.d;
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) chunk_prep_kernel(const __gri
     const int c0 = (tid >> 7) * 32;            // its 32 of the 64 columns
     const int hk = blockIdx.y;
     const int G = d.Hv / d.Hk;
-    const int64_t slot = blockIdx.x;
+    const int64_t slot = blockIdx.x + slot_base;   // a segment's slots start at slot_base
     if (p.cu != nullptr && *p.status != GDN_OK) return;
     ChunkLoc c;
     if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, c)) return;
@@ -470,7 +472,7 @@ enum ChainBar { B_LOAD0 = 0, B_LOAD1, B_LQ0, B_LQ1, B_TPT, B_QF0, B_QF1, B_C1, B
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles,
-                   int64_t nslots, const unsigned char *prep_out) {
+                   int64_t nslots, const unsigned char *prep_out, int cbase, int cmax) {
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const gdn_desc &d = p.d;
@@ -488,10 +490,14 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     const int G = Hv / d.Hk;                   // v heads per q/k head
     const int hk = j / G;
     const int v0 = tile * 64;
-    const int64_t seq0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
-    const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : seq0 + d.T;
-    const int nchunks = (int)((seq1 - seq0 + kChunk - 1) / kChunk);
-    const int64_t slot0 = p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk);
+    // chunks [cbase, cbase + cmax) of the sequence: a segment of it, or all of it;
+    // h0 / hT are the state before / after the segment
+    const int64_t sstart = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
+    const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : sstart + d.T;
+    const int64_t seq0 = sstart + (int64_t)cbase * kChunk;
+    const int64_t left = seq1 > seq0 ? (seq1 - seq0 + kChunk - 1) / kChunk : 0;
+    const int nchunks = (int)(left < cmax ? left : cmax);
+    const int64_t slot0 = (p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk)) + cbase;
     const ChainSmem L(dk);
     const int halves = dk >= 128 ? dk / 128 : 1;  // M=128 row groups of the state
     unsigned char *tptb = sm + L.tpt, *h16 = sm + L.h16, *r16 = sm + L.r16, *vn16 = sm + L.vn16;
@@ -871,6 +877,33 @@ bool encode_tile_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t c
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Segmented schedule of a long single sequence: one high-priority stream per
+// device for the chain segments and the events that order them against the
+// prep segments on the caller's stream, created on first use and kept (events
+// are re-recorded by every call; the enqueue runs under the mutex, so one
+// call's records are waited on before another call records them again).
+constexpr int kMaxSegments = 16;
+struct SideStream {
+    cudaStream_t hp = nullptr;
+    cudaEvent_t ev[kMaxSegments + 2] = {};
+    bool ready = false;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+SideStream *side_stream(int dev) {   // caller holds g_side_mu
+    if (dev < 0 || dev >= 64) return nullptr;
+    SideStream &ss = g_side[dev];
+    if (ss.ready) return &ss;
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithPriority(&ss.hp, cudaStreamNonBlocking, hi) != cudaSuccess) return nullptr;
+    for (auto &e : ss.ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    ss.ready = true;
+    return &ss;
+}
+
 int max_dyn_smem() {
     int dev = 0, v = 232448;
     if (cudaGetDevice(&dev) == cudaSuccess)
@@ -885,9 +918,12 @@ bool chunk_tc_supports(const gdn_desc &d) {
            d.dv >= 64 && d.dv % 64 == 0;
 }
 
+// The prep tiles, and for a single sequence the state between two segments of
+// its chain (see launch_chunk_tc).
 size_t chunk_tc_workspace(const gdn_desc &d) {
     if (!chunk_tc_supports(d)) return 0;
-    return (size_t)d.Hv * (size_t)chunk_slot_bound(d) * kPrepOut;
+    const size_t seg_state = d.N == 1 ? (size_t)d.Hv * d.dk * d.dv * sizeof(float) : 0;
+    return (size_t)d.Hv * (size_t)chunk_slot_bound(d) * kPrepOut + seg_state;
 }
 
 cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
@@ -910,7 +946,8 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
                                              (int)ps.total);
         if (e != cudaSuccess) return e;
         if (nslots > 0) {
-            chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt);
+            chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt,
+                                                                                           (int64_t)0);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
@@ -935,8 +972,87 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
     const int ntiles = d.dv / 64;
     const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
     if (blocks == 0) return cudaSuccess;
-    chunk_chain_kernel<<<(unsigned)blocks, kChainThreads, smem, s>>>(cm, p, ntiles, nslots_alloc, tpt);
+    chunk_chain_kernel<<<(unsigned)blocks, kChainThreads, smem, s>>>(cm, p, ntiles, nslots_alloc, tpt, 0,
+                                                                   0x7fffffff);
     return cudaGetLastError();
+}
+
+// One long sequence whose chain occupies at most half of the SMs: the chunks are
+// cut into segments; the prep of every segment runs on the caller's stream, the
+// chain of segment k on a high-priority side stream once the prep of segment k
+// is done, so that the prep of segment k+1 uses the SMs the chain leaves idle.
+// The state crosses segments through the workspace (the chain's h0 / hT).
+bool chunk_tc_segmented(const Problem &p) {
+    const gdn_desc &d = p.d;
+    if (p.single_stream || p.cu != nullptr || d.N != 1 || p.ntok == 0) return false;
+    const int64_t nch = (d.T + kChunk - 1) / kChunk;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    return nch >= 256 && (int64_t)d.Hv * (d.dv / 64) * 2 <= nsm;
+}
+
+cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
+    const gdn_desc &d = p.d;
+    const int64_t nslots_alloc = chunk_slot_bound(d);
+    const int nch = (int)((d.T + kChunk - 1) / kChunk);
+    const int seg = (nch + kMaxSegments - 1) / kMaxSegments > 64 ? (nch + kMaxSegments - 1) / kMaxSegments : 64;
+    const int nseg = (nch + seg - 1) / seg;
+    unsigned char *tpt = (unsigned char *)p.tpt;
+    float *seg_state = (float *)(tpt + (size_t)d.Hv * nslots_alloc * kPrepOut);
+    const int64_t plane = (int64_t)d.Hk * p.ntok * d.dk;
+    PrepMaps pm;
+    ChainMaps cm;
+    const __half *q = (const __half *)p.q, *k = (const __half *)p.k;
+    if (!encode_tile_map(&pm.q_hi, q, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&pm.q_lo, q + plane, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&pm.k_hi, k, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&pm.k_lo, k + plane, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&cm.q_hi, p.q, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&cm.k_hi, p.k, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&cm.v, p.v, (uint64_t)d.Hv * p.ntok, d.dv))
+        return cudaErrorInvalidValue;
+    const PrepSmem ps(d.dk);
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)ps.total);
+    if (e != cudaSuccess) return e;
+    const int maxs = max_dyn_smem();
+    const ChainSmem cs(d.dk);
+    const size_t smem = cs.total > (size_t)(maxs / 2 + 1024) ? cs.total : (size_t)(maxs / 2 + 1024);
+    if ((int)smem > maxs) return cudaErrorInvalidValue;
+    if ((e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+        return e;
+    const int ntiles = d.dv / 64;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream *ss = side_stream(dev);
+    if (!ss) return cudaErrorInvalidValue;
+    // the side stream starts after everything already queued on the caller's
+    if ((e = cudaEventRecord(ss->ev[0], s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->hp, ss->ev[0], 0)) != cudaSuccess) return e;
+    for (int g = 0; g < nseg; ++g) {
+        const int cb = g * seg, cn = nch - cb < seg ? nch - cb : seg;
+        chunk_prep_kernel<<<dim3((unsigned)cn, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt,
+                                                                                   (int64_t)cb);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(ss->ev[1 + g], s)) != cudaSuccess) return e;
+    }
+    for (int g = 0; g < nseg; ++g) {
+        const int cb = g * seg, cn = nch - cb < seg ? nch - cb : seg;
+        if ((e = cudaStreamWaitEvent(ss->hp, ss->ev[1 + g], 0)) != cudaSuccess) return e;
+        Problem pg = p;
+        pg.h0 = g == 0 ? p.h0 : seg_state;
+        pg.hT = g == nseg - 1 ? p.hT : seg_state;
+        chunk_chain_kernel<<<(unsigned)(d.Hv * ntiles), kChainThreads, smem, ss->hp>>>(cm, pg, ntiles,
+                                                                                      nslots_alloc, tpt, cb, cn);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // the caller's stream continues once the last chain segment is done
+    if ((e = cudaEventRecord(ss->ev[1 + nseg], ss->hp)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(s, ss->ev[1 + nseg], 0);
 }
 
 }  // namespace gdn

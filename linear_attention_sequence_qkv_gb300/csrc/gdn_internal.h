@@ -75,6 +75,7 @@ struct Problem {
     float *beta;
     void *gamma;                  // float, or double for fp32 activations
     void *tpt;                    // [T; P T] tiles of the tensor-core kernels
+    bool single_stream;           // no side stream (the no-allocation entry point)
 };
 
 // Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one
@@ -88,6 +89,15 @@ cudaError_t launch_seqlens_scan(const Problem &p, cudaStream_t s);
 cudaError_t launch_prologue(const Problem &p, cudaStream_t s);
 cudaError_t launch_chunk_simt(const Problem &p, cudaStream_t s);
 cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s);
+// a long single sequence: prep and chain in segments on two streams
+bool chunk_tc_segmented(const Problem &p);
+cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s);
+// gdn_forward on one stream only (used by gdn_forward_static_ws)
+int forward_single_stream(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw,
+                          const void *a, const void *b, const void *gate, const void *conv_w,
+                          const float *A_log, const float *dt_bias, const void *norm_w,
+                          const int32_t *cu_seqlens, const float *initial_state, void *out,
+                          float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 bool chunk_tc_supports(const gdn_desc &d);
 cudaError_t launch_epilogue(const Problem &p, cudaStream_t s);
 

@@ -55,7 +55,9 @@ extern "C" int gdn_forward_static_ws(const gdn_desc *d, const void *q_raw, const
     // Every region of the workspace (status word, chunk table, intermediates) is
     // written by this call before it is read, so the contents left by the last
     // call need no clearing.
-    return gdn_forward(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
-                       cu_seqlens, initial_state, out, final_state, ws,
-                       (size_t)GDN_STATIC_WORKSPACE_BYTES, stream);
+    // one stream only: the segmented schedule of long sequences would create a
+    // side stream on first use
+    return gdn::forward_single_stream(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
+                                      cu_seqlens, initial_state, out, final_state, ws,
+                                      (size_t)GDN_STATIC_WORKSPACE_BYTES, (cudaStream_t)stream);
 }
