@@ -434,17 +434,19 @@ cleanup:
 // [K;Q] h16); R and Vn' tiles.
 struct ChainSmem {
     int blocks;
+    int stages;            // 3 where they fit (dk <= 128), else 2
     size_t stage_bytes, x, tpt, h16, r16, vn16, bars, total;
     __host__ __device__ ChainSmem(int dk) {
         blocks = dk / 64;
         x = (size_t)blocks * 2 * kTileBytes;        // inside a stage, after the stack
         stage_bytes = x + kXBytes;
-        size_t o = 2 * stage_bytes;
+        stages = dk <= 128 ? 3 : 2;
+        size_t o = (size_t)stages * stage_bytes;
         tpt = o; o += kTPTBytes;
         h16 = o; o += (size_t)(dk < 128 ? 128 : dk) * 128;
         r16 = o; o += kTileBytes;
         vn16 = o; o += kTileBytes;
-        bars = o; o += 128;
+        bars = o; o += 256;   // B_COUNT barriers and the TMEM slot
         total = o + 1024;
     }
 };
@@ -465,11 +467,13 @@ constexpr int kRowWarps = 8, kStateWarps = 8;
 constexpr int kMmaWarp = kRowWarps + kStateWarps;
 constexpr int kLoadWarp = kMmaWarp + 1;
 constexpr int kChainThreads = (kLoadWarp + 1) * 32;
-// B_LOAD s / B_LQ s: the K part / the Q + X part of stage s landed; B_QF s: the
-// products reading stage s's Q + X part are done (its refill may start).
-enum ChainBar { B_LOAD0 = 0, B_LOAD1, B_LQ0, B_LQ1, B_TPT, B_QF0, B_QF1, B_C1, B_R, B_C2, B_VN, B_O, B_C4, B_H,
-                B_COUNT };
+// B_LOAD s / B_LQ s: the K part / the Q + X part of stage s landed; B_QF s / B_KF s:
+// the products reading stage s's Q + X part / K part are done (its refill may start).
+constexpr int kMaxStages = 3;
+enum ChainBar { B_LOAD0 = 0, B_LQ0 = B_LOAD0 + kMaxStages, B_TPT = B_LQ0 + kMaxStages, B_QF0, B_KF0 = B_QF0 + kMaxStages,
+                B_C1 = B_KF0 + kMaxStages, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_COUNT };
 
+template <int NS>   // stages: 3 where they fit (dk <= 128), else 2
 __global__ void __launch_bounds__(kChainThreads, 1)
 chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles,
                    int64_t nslots, const unsigned char *prep_out, int cbase, int cmax) {
@@ -513,12 +517,12 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
 
     if (tid == 0) {
         s_err = 0;
-        mbar_init(&bar[B_LOAD0], 1);
-        mbar_init(&bar[B_LOAD1], 1);
-        mbar_init(&bar[B_LQ0], 1);
-        mbar_init(&bar[B_LQ1], 1);
-        mbar_init(&bar[B_QF0], 1);
-        mbar_init(&bar[B_QF1], 1);
+        for (int i = 0; i < kMaxStages; ++i) {
+            mbar_init(&bar[B_LOAD0 + i], 1);
+            mbar_init(&bar[B_LQ0 + i], 1);
+            mbar_init(&bar[B_QF0 + i], 1);
+            mbar_init(&bar[B_KF0 + i], 1);
+        }
         mbar_init(&bar[B_TPT], 1);
         mbar_init(&bar[B_C1], 1);
         mbar_init(&bar[B_C2], 1);
@@ -590,7 +594,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             // a stage is [K_b; Q_b] for each 64-column block b, then X; its K part is
             // read until C4 of the chunk, its Q and X parts only until C1
             auto load_k = [&](int c) {
-                const int s = c & 1;
+                const int s = c % NS;
                 unsigned char *st = sm + s * L.stage_bytes;
                 const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
                 mbar_expect_tx(&bar[B_LOAD0 + s], (uint32_t)L.blocks * kTileBytes);
@@ -598,7 +602,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                     tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
             };
             auto load_qx = [&](int c) {
-                const int s = c & 1;
+                const int s = c % NS;
                 unsigned char *st = sm + s * L.stage_bytes;
                 const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
                 const bool with_x = c > 0;
@@ -613,26 +617,32 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 mbar_expect_tx(&bar[B_TPT], kTPTBytes);
                 bulk_load(tptb, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut, kTPTBytes, &bar[B_TPT]);
             };
-            if (nchunks > 0) { load_k(0); load_qx(0); load_tpt(0); }
-            if (nchunks > 1) { load_k(1); load_qx(1); }
+            constexpr int ns = NS;
+            for (int c = 0; c < ns && c < nchunks; ++c) {
+                load_k(c);
+                load_qx(c);
+                if (c == 0) load_tpt(0);
+            }
             // Each wait below is for the phase right after the one this thread last
             // consumed, and the barrier cannot complete the next one before this
-            // thread's refill: B_QF s is re-armed only by chunk c+2's C1, B_C2 only
-            // by chunk c+1's C2 (after its [T; P T] load), B_C4 only by chunk c+1's
-            // C4 (issued after chunk c+2's first product, which needs its K part).
+            // thread's refill: B_QF s / B_KF s are re-armed only by the products of
+            // chunk c + ns, which need the parts loaded here; B_C2 only by chunk
+            // c+1's C2, which needs its [T; P T] load.
             for (int c = 0; c + 1 < nchunks; ++c) {
-                // Q and X of chunk c+2 into chunk c's stage once C1 of chunk c is done
-                if (c + 2 < nchunks) {
-                    if (!wait(B_QF0 + (c & 1), (c >> 1) & 1)) break;
-                    load_qx(c + 2);
+                const int s = c % ns;
+                const uint32_t ph = (uint32_t)(c / ns) & 1;
+                // Q and X of chunk c+ns into chunk c's stage once C1 of chunk c is done
+                if (c + ns < nchunks) {
+                    if (!wait(B_QF0 + s, ph)) break;
+                    load_qx(c + ns);
                 }
                 // [T; P T] of chunk c+1 once C2 of chunk c has read the buffer
                 if (!wait(B_C2, c & 1)) break;
                 load_tpt(c + 1);
-                // K of chunk c+2 once its last reader (C4 of chunk c) is done
-                if (c + 2 < nchunks) {
-                    if (!wait(B_C4, c & 1)) break;
-                    load_k(c + 2);
+                // K of chunk c+ns once its last reader (C4 of chunk c) is done
+                if (c + ns < nchunks) {
+                    if (!wait(NS == 2 ? B_C4 : B_KF0 + s, NS == 2 ? (uint32_t)(c & 1) : ph)) break;
+                    load_k(c + ns);
                 }
             }
         }
@@ -653,16 +663,17 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             const uint32_t stage16 = (uint32_t)(L.stage_bytes >> 4), x16 = (uint32_t)(L.x >> 4);
             // H += K_c^T Vn'_c, into the state the state warps already scaled by e^{gL_c}
             auto issue_c4 = [&](int c) {
-                const uint64_t a0 = d_kt0 + (c & 1) * stage16;
+                const uint64_t a0 = d_kt0 + (c % NS) * stage16;
                 for (int h = 0; h < halves; ++h)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_f16(tbase + 320 + 64 * h, a0 + (uint64_t)((h * 4 * kTileBytes + 2048 * ks) >> 4),
                                 d_vn + (uint64_t)((2048 * ks) >> 4), id_m, 1);
                 mma_commit(&bar[B_C4]);
+                if (NS > 2) mma_commit(&bar[B_KF0 + c % NS]);   // the stage's K part is free
             };
             auto issue_c1a = [&](int c) {  // D1 = [K; Q] h16
-                const uint64_t a0 = d_st0 + (c & 1) * stage16;
+                const uint64_t a0 = d_st0 + (c % NS) * stage16;
                 for (int b = 0; b < L.blocks; ++b)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
@@ -671,8 +682,9 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             };
             int c = 0;
             for (; c < nchunks; ++c) {
-                const int s = c & 1;
-                if (!wait(B_LOAD0 + s, (c >> 1) & 1) || !wait(B_LQ0 + s, (c >> 1) & 1)) break;
+                const int s = c % NS;
+                const uint32_t ph = (uint32_t)(c / NS) & 1;
+                if (!wait(B_LOAD0 + s, ph) || !wait(B_LQ0 + s, ph)) break;
                 if (c >= 1 && !wait(B_H, (c - 1) & 1)) break;     // h16 = e^{gL_{c-1}} H_{c-2}
                 fence_after_sync();
                 issue_c1a(c);
@@ -683,7 +695,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                     const uint64_t ax = d_st0 + s * stage16 + x16;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tbase + 64 * s, ax + (uint64_t)((32 * ks) >> 4),
+                        mma_f16(tbase + 64 * (c & 1), ax + (uint64_t)((32 * ks) >> 4),
                                 d_vn + (uint64_t)((2048 * ks) >> 4), id_k, 1);
                 }
                 mma_commit(&bar[B_C1]);
@@ -841,7 +853,10 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     if (s_err && tid == kMmaWarp * 32) {
         // drain: bounded waits for this CTA's own copies and MMAs before freeing TMEM
         set_timeout(p);
-        for (int b = B_LOAD0; b <= B_TPT; ++b) { mbar_wait(&bar[b], 0); mbar_wait(&bar[b], 1); }
+        for (int i = 0; i < NS; ++i)
+            for (int b : {B_LOAD0 + i, B_LQ0 + i}) { mbar_wait(&bar[b], 0); mbar_wait(&bar[b], 1); }
+        mbar_wait(&bar[B_TPT], 0);
+        mbar_wait(&bar[B_TPT], 1);
         mbar_wait(&bar[B_C4], 0);
         mbar_wait(&bar[B_C4], 1);
     }
@@ -966,13 +981,13 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
     // second CTA never shares the SM (its allocation would wait for this one)
     const size_t smem = cs.total > (size_t)(maxs / 2 + 1024) ? cs.total : (size_t)(maxs / 2 + 1024);
     if ((int)smem > maxs) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    auto chain = cs.stages == 3 ? chunk_chain_kernel<3> : chunk_chain_kernel<2>;
+    cudaError_t e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int ntiles = d.dv / 64;
     const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
     if (blocks == 0) return cudaSuccess;
-    chunk_chain_kernel<<<(unsigned)blocks, kChainThreads, smem, s>>>(cm, p, ntiles, nslots_alloc, tpt, 0,
+    chain<<<(unsigned)blocks, kChainThreads, smem, s>>>(cm, p, ntiles, nslots_alloc, tpt, 0,
                                                                    0x7fffffff);
     return cudaGetLastError();
 }
@@ -1021,7 +1036,8 @@ cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
     const ChainSmem cs(d.dk);
     const size_t smem = cs.total > (size_t)(maxs / 2 + 1024) ? cs.total : (size_t)(maxs / 2 + 1024);
     if ((int)smem > maxs) return cudaErrorInvalidValue;
-    if ((e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+    auto chain = cs.stages == 3 ? chunk_chain_kernel<3> : chunk_chain_kernel<2>;
+    if ((e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
         cudaSuccess)
         return e;
     const int ntiles = d.dv / 64;
@@ -1046,7 +1062,7 @@ cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
         Problem pg = p;
         pg.h0 = g == 0 ? p.h0 : seg_state;
         pg.hT = g == nseg - 1 ? p.hT : seg_state;
-        chunk_chain_kernel<<<(unsigned)(d.Hv * ntiles), kChainThreads, smem, ss->hp>>>(cm, pg, ntiles,
+        chain<<<(unsigned)(d.Hv * ntiles), kChainThreads, smem, ss->hp>>>(cm, pg, ntiles,
                                                                                       nslots_alloc, tpt, cb, cn);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
