@@ -41,6 +41,8 @@ double gdn_oracle_round_act(double x, int act) {
         return round_format(x, 8, -126, ldexp(255.0, 120));   /* (2-2^-7)*2^127 */
     case GDN_ORACLE_F16:
         return round_format(x, 11, -14, 65504.0);
+    case GDN_ORACLE_F64:
+        return x;
     default:
         return round_format(x, 24, -126, ldexp(16777215.0, 104)); /* FLT_MAX */
     }

@@ -38,8 +38,9 @@
 extern "C" {
 #endif
 
-/* activation dtype codes (rounding of the RMSNorm output) */
-enum { GDN_ORACLE_F32 = 0, GDN_ORACLE_BF16 = 1, GDN_ORACLE_F16 = 2 };
+/* activation dtype codes (rounding of the RMSNorm output); GDN_ORACLE_F64
+ * leaves it unrounded (the real-valued forward that the backward differentiates) */
+enum { GDN_ORACLE_F32 = 0, GDN_ORACLE_BF16 = 1, GDN_ORACLE_F16 = 2, GDN_ORACLE_F64 = 3 };
 
 /* Round x to the nearest value of the activation dtype, ties to even. */
 double gdn_oracle_round_act(double x, int act);
@@ -137,6 +138,30 @@ typedef struct {
     double *out, *conv_state_out, *state_out;
 } gdn_oracle_decode_problem;
 int gdn_oracle_decode(const gdn_oracle_decode_problem *p);
+
+/* Backward of the whole core (gdn_oracle_bwd.c): the gradients of
+ *   L = sum(grad_out * out) + sum(grad_final * final_state)
+ * with respect to every input of gdn_oracle_forward, the RMSNorm rounding taken
+ * as the identity. Inputs as in the forward plus grad_out [ntok][Hv][dv] and
+ * grad_final [n_seq][Hv][dk][dv] (or NULL for zeros). Outputs (double, each
+ * written in full for the heads of the call):
+ *   dq_raw, dk_raw [ntok][Hk*dk], dv_raw [ntok][Hv*dv], da, db [ntok][Hv],
+ *   dgate [ntok][Hv*dv], dconv_w [ch][width], dA_log, ddt_bias [Hv],
+ *   dnorm_w [Hv][dv] (each v head's share; the gradient is their sum),
+ *   dinitial_state [n_seq][Hv][dk][dv] or NULL.
+ * gdn_oracle_backward(p, b, e) covers q/k heads [b, e) and their v heads. */
+typedef struct {
+    int n_seq;
+    const int64_t *seq_start;
+    int Hk, Hv, dk, dv, conv_width;
+    double l2_eps, norm_eps, scale;
+    const float *q_raw, *k_raw, *v_raw, *a, *b, *gate, *conv_w;
+    const float *A_log, *dt_bias, *norm_w, *initial_state;
+    const float *grad_out, *grad_final;
+    double *dq_raw, *dk_raw, *dv_raw, *da, *db, *dgate, *dconv_w;
+    double *dA_log, *ddt_bias, *dnorm_w, *dinitial_state;
+} gdn_oracle_bwd_problem;
+int gdn_oracle_backward(const gdn_oracle_bwd_problem *p, int hk_begin, int hk_end);
 
 #ifdef __cplusplus
 }

@@ -22,12 +22,14 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_oracle.c")
+_SRC_BWD = os.path.join(_HERE, "gdn_oracle_bwd.c")
 _HDR = os.path.join(_HERE, "gdn_oracle.h")
 _LIB = os.path.join(_HERE, "libgdn_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-ACT_CODES = {"fp32": 0, "bf16": 1, "fp16": 2}
+# "fp64": the RMSNorm result is not rounded (the real-valued forward)
+ACT_CODES = {"fp32": 0, "bf16": 1, "fp16": 2, "fp64": 3}
 
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
@@ -60,15 +62,30 @@ class _DecodeProblem(ctypes.Structure):
     ]
 
 
+class _BwdProblem(ctypes.Structure):
+    _fields_ = [
+        ("n_seq", ctypes.c_int), ("seq_start", _i64p),
+        ("Hk", ctypes.c_int), ("Hv", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+        ("conv_width", ctypes.c_int),
+        ("l2_eps", ctypes.c_double), ("norm_eps", ctypes.c_double), ("scale", ctypes.c_double),
+        ("q_raw", _f32p), ("k_raw", _f32p), ("v_raw", _f32p), ("a", _f32p), ("b", _f32p),
+        ("gate", _f32p), ("conv_w", _f32p), ("A_log", _f32p), ("dt_bias", _f32p),
+        ("norm_w", _f32p), ("initial_state", _f32p), ("grad_out", _f32p), ("grad_final", _f32p),
+        ("dq_raw", _f64p), ("dk_raw", _f64p), ("dv_raw", _f64p), ("da", _f64p), ("db", _f64p),
+        ("dgate", _f64p), ("dconv_w", _f64p), ("dA_log", _f64p), ("dt_bias_grad", _f64p),
+        ("dnorm_w", _f64p), ("dinitial_state", _f64p),
+    ]
+
+
 def build(force: bool = False) -> str:
     """Compile ``libgdn_oracle.so`` next to its source if it is missing or stale."""
     with _lock:
         stale = (not os.path.exists(_LIB) or
-                 os.path.getmtime(_LIB) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+                 os.path.getmtime(_LIB) < max(os.path.getmtime(f) for f in (_SRC, _SRC_BWD, _HDR)))
         if force or stale:
             tmp = _LIB + f".tmp{os.getpid()}"
             cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-                   "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+                   "-fno-fast-math", "-o", tmp, _SRC, _SRC_BWD, "-lm"]
             subprocess.run(cmd, check=True)
             os.replace(tmp, _LIB)
     return _LIB
@@ -104,6 +121,8 @@ def lib():
                                                ctypes.c_int, _f64p, ctypes.c_int64]
         L.gdn_oracle_forward.restype = ctypes.c_int
         L.gdn_oracle_forward.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int, ctypes.c_int]
+        L.gdn_oracle_backward.restype = ctypes.c_int
+        L.gdn_oracle_backward.argtypes = [ctypes.POINTER(_BwdProblem), ctypes.c_int, ctypes.c_int]
         L.gdn_oracle_decode.restype = ctypes.c_int
         L.gdn_oracle_decode.argtypes = [ctypes.POINTER(_DecodeProblem)]
         _lib = L
@@ -257,3 +276,50 @@ def decode(*, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
     if lib().gdn_oracle_decode(ctypes.byref(prob)) != 0:
         raise RuntimeError("gdn_oracle_decode failed")
     return out, cso, so
+
+
+def backward(*, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
+             seq_start, Hk, Hv, dk, dv, grad_out, grad_final=None, initial_state=None,
+             l2_eps=1e-6, norm_eps=1e-5, scale=1.0, conv_width=4, threads: int = 1):
+    """Gradients of sum(grad_out * out) + sum(grad_final * final_state) with
+    respect to every input of ``forward`` (float32 values in the forward's
+    shapes; grad_out [ntok, Hv, dv], grad_final [N, Hv, dk, dv] or None). The
+    RMSNorm rounding is taken as the identity. Returns a dict of float64 arrays:
+    dq_raw, dk_raw, dv_raw, da, db, dgate, dconv_w, dA_log, ddt_bias, dnorm_w,
+    dinitial_state. ``threads`` spreads q/k heads over host threads."""
+    arrs = dict(q_raw=_f32(q_raw), k_raw=_f32(k_raw), v_raw=_f32(v_raw), a=_f32(a), b=_f32(b),
+                gate=_f32(gate), conv_w=_f32(conv_w), A_log=_f32(A_log),
+                dt_bias=_f32(dt_bias), norm_w=_f32(norm_w), grad_out=_f32(grad_out))
+    init = _f32(initial_state) if initial_state is not None else None
+    gfin = _f32(grad_final) if grad_final is not None else None
+    s = np.ascontiguousarray(np.asarray(seq_start, dtype=np.int64))
+    n_seq = len(s) - 1
+    ntok = int(s[-1])
+    ch = 2 * Hk * dk + Hv * dv
+    out = dict(dq_raw=np.zeros((ntok, Hk * dk)), dk_raw=np.zeros((ntok, Hk * dk)),
+               dv_raw=np.zeros((ntok, Hv * dv)), da=np.zeros((ntok, Hv)), db=np.zeros((ntok, Hv)),
+               dgate=np.zeros((ntok, Hv * dv)), dconv_w=np.zeros((ch, conv_width)),
+               dA_log=np.zeros(Hv), ddt_bias=np.zeros(Hv), dnorm_w=np.zeros((Hv, dv)),
+               dinitial_state=np.zeros((n_seq, Hv, dk, dv)))
+    prob = _BwdProblem(
+        n_seq=n_seq, seq_start=s.ctypes.data_as(_i64p), Hk=Hk, Hv=Hv, dk=dk, dv=dv,
+        conv_width=conv_width, l2_eps=l2_eps, norm_eps=norm_eps, scale=scale,
+        **{k: _p32(v) for k, v in arrs.items()}, initial_state=_p32(init), grad_final=_p32(gfin),
+        dq_raw=_p64(out["dq_raw"]), dk_raw=_p64(out["dk_raw"]), dv_raw=_p64(out["dv_raw"]),
+        da=_p64(out["da"]), db=_p64(out["db"]), dgate=_p64(out["dgate"]),
+        dconv_w=_p64(out["dconv_w"]), dA_log=_p64(out["dA_log"]), dt_bias_grad=_p64(out["ddt_bias"]),
+        dnorm_w=_p64(out["dnorm_w"]), dinitial_state=_p64(out["dinitial_state"]))
+    L = lib()
+
+    def run(hk):
+        if L.gdn_oracle_backward(ctypes.byref(prob), hk, hk + 1) != 0:
+            raise RuntimeError(f"gdn_oracle_backward failed for q/k head {hk}")
+
+    if threads <= 1 or Hk <= 1:
+        for hk in range(Hk):
+            run(hk)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(run, range(Hk)))
+    out["dnorm_w"] = out["dnorm_w"].sum(axis=0)
+    return out
