@@ -246,6 +246,57 @@ int gdn_decode_step(const gdn_desc *d,
                     const void *norm_w, void *conv_state, float *state, void *out,
                     void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/*
+ * Backward of the core: the gradients of
+ *     L = sum(grad_out * out) + sum(grad_final * final_state)
+ * with respect to every input of gdn_forward, first order. The pages define
+ * the forward; training needs its first-order gradients ("GDN Elementwise
+ * Fusion", Megatron Core developer guide, "Execution and numerical behavior":
+ * the fused post-GDR kernels support first-order autograd; "fused q/k/v short
+ * conv", flash-linear-attention PR #972, "Test plan": input and parameter
+ * gradients of the fused path checked against the unfused one, and the
+ * benchmark table timing forward + backward). Reading: the rounding of the
+ * RMSNorm result to the activation dtype is taken as the identity (the
+ * straight-through derivative of the rounded forward).
+ *
+ * The call recomputes the forward (prologue and the fp32 CUDA-core chunk
+ * kernel, storing each chunk's start state) and then runs the reverse pass on
+ * CUDA cores in fp32 for every dtype. Every sum has a fixed order: results are
+ * run-to-run identical.
+ *
+ * d, q_raw ... initial_state   exactly as for gdn_forward (same descriptor,
+ *             strides, packing and alignment rules).
+ * grad_out    act dtype [B*T][Hv][dv] contiguous (the gradient of out).
+ * grad_final  fp32 [N][Hv][dk][dv] (S^T layout of final_state), or NULL = zeros.
+ * dq_raw, dk_raw  act dtype, dense [B*T][Hk*dk]; dv_raw act dtype [B*T][Hv*dv];
+ * da, db      act dtype [B*T][Hv]; dgate gate dtype [B*T][Hv*dv] (all dense,
+ *             whatever the strides of the inputs);
+ * dconv_w     fp32 [2*Hk*dk+Hv*dv][4]; dA_log, ddt_bias fp32 [Hv];
+ * dnorm_w     fp32 [dv]; dinitial_state fp32 [N][Hv][dk][dv] or NULL (skip).
+ *             All outputs are written in full (not accumulated into).
+ * workspace   gdn_backward_workspace_bytes(d) bytes, 256-byte aligned; it
+ *             begins with gdn_forward's layout (status word first, so
+ *             gdn_device_status reads it), followed by the backward's fp32
+ *             regions: per token and v head about 2*dk*dv/64 + 3*dv + 2*dk + 196
+ *             floats, plus 2*Hk*dk + Hv*dv floats per token (about 180 KB per
+ *             token at 6 heads, dk 256, dv 512).
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG (null or misaligned pointer),
+ * GDN_ERR_UNSUPPORTED (as gdn_forward), GDN_ERR_WORKSPACE or GDN_ERR_CUDA; a
+ * malformed cu_seqlens sets GDN_ERR_DEVICE_SEQLENS in the workspace and the
+ * kernels skip their work. Outputs must not overlap the inputs or workspace.
+ */
+int gdn_backward_workspace_bytes(const gdn_desc *d, size_t *bytes);
+int gdn_backward(const gdn_desc *d,
+                 const void *q_raw, const void *k_raw, const void *v_raw,
+                 const void *a, const void *b, const void *gate,
+                 const void *conv_w, const float *A_log, const float *dt_bias,
+                 const void *norm_w, const int32_t *cu_seqlens,
+                 const float *initial_state, const void *grad_out,
+                 const float *grad_final, void *dq_raw, void *dk_raw, void *dv_raw,
+                 void *da, void *db, void *dgate, float *dconv_w, float *dA_log,
+                 float *ddt_bias, float *dnorm_w, float *dinitial_state,
+                 void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -367,3 +367,90 @@ int gdn_chunk_kernel_kind(const gdn_desc *d) {
 }
 
 }  // extern "C"
+
+extern "C" {
+
+int gdn_backward_workspace_bytes(const gdn_desc *d, size_t *bytes) {
+    if (!d || !bytes) return GDN_ERR_INVALID_ARG;
+    *bytes = gdn::make_bwd_layout(*d).total;
+    return GDN_OK;
+}
+
+int gdn_backward(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw, const void *a,
+                 const void *b, const void *gate, const void *conv_w, const float *A_log, const float *dt_bias,
+                 const void *norm_w, const int32_t *cu_seqlens, const float *initial_state,
+                 const void *grad_out, const float *grad_final, void *dq_raw, void *dk_raw, void *dv_raw,
+                 void *da, void *db, void *dgate, float *dconv_w, float *dA_log, float *ddt_bias,
+                 float *dnorm_w, float *dinitial_state, void *workspace, size_t workspace_bytes,
+                 gdn_stream_t stream) {
+    int rc = check_desc(d, cu_seqlens != nullptr);
+    if (rc != GDN_OK) return rc;
+    const bool tok = (int64_t)d->B * d->T > 0;   // token tensors may be empty (null)
+    if ((tok && (!q_raw || !k_raw || !v_raw || !a || !b || !gate || !grad_out || !dq_raw || !dk_raw ||
+                 !dv_raw || !da || !db || !dgate)) ||
+        !conv_w || !A_log || !dt_bias || !norm_w || !dconv_w || !dA_log || !ddt_bias || !dnorm_w)
+        return GDN_ERR_INVALID_ARG;
+    if (!aligned(q_raw, 16) || !aligned(k_raw, 16) || !aligned(v_raw, 16) || !aligned(conv_w, 16) ||
+        !aligned(norm_w, 4))
+        return GDN_ERR_INVALID_ARG;
+    if ((initial_state && !aligned(initial_state, 16)) || (grad_final && !aligned(grad_final, 16)) ||
+        (dinitial_state && !aligned(dinitial_state, 16)))
+        return GDN_ERR_INVALID_ARG;
+    const gdn::BwdLayout L = gdn::make_bwd_layout(*d);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return GDN_ERR_WORKSPACE;
+    Problem p = base_problem(d, cu_seqlens, workspace);
+    p.q_raw = q_raw;
+    p.k_raw = k_raw;
+    p.v_raw = v_raw;
+    p.a = a;
+    p.b = b;
+    p.gate = gate;
+    p.conv_w = conv_w;
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.norm_w = norm_w;
+    p.h0 = initial_state;
+    p.hT = nullptr;
+    p.single_stream = true;
+    char *w = (char *)workspace;
+    p.bw_h0 = (float *)(w + L.h0);
+    p.bw_mats = (float *)(w + L.mats);
+    p.bw_vn = (float *)(w + L.vn);
+    cudaStream_t s = (cudaStream_t)stream;
+    // the forward's prologue, then its CUDA-core chunk kernel with the backward's stores
+    if ((rc = run_prologue(p, s)) != GDN_OK) return rc;
+    if ((rc = cuda_status(gdn::launch_chunk_simt(p, s))) != GDN_OK) return rc;
+    gdn::BwdProblem bp;
+    memset(&bp, 0, sizeof(bp));
+    bp.f = p;
+    bp.grad_out = grad_out;
+    bp.grad_final = grad_final;
+    bp.dq_raw = dq_raw;
+    bp.dk_raw = dk_raw;
+    bp.dv_raw = dv_raw;
+    bp.da = da;
+    bp.db = db;
+    bp.dgate = dgate;
+    bp.dconv_w = dconv_w;
+    bp.dA_log = dA_log;
+    bp.ddt_bias = ddt_bias;
+    bp.dnorm_w = dnorm_w;
+    bp.dinit = dinitial_state;
+    bp.h0 = p.bw_h0;
+    bp.mats = p.bw_mats;
+    bp.vn = p.bw_vn;
+    bp.dh1 = (float *)(w + L.dh1);
+    bp.dO = (float *)(w + L.dO);
+    bp.dR = (float *)(w + L.dR);
+    bp.dq = (float *)(w + L.dq);
+    bp.dk = (float *)(w + L.dk);
+    bp.dbeta = (float *)(w + L.dbeta);
+    bp.dgam = (float *)(w + L.dgam);
+    bp.dz = (float *)(w + L.dz);
+    bp.pa = (float *)(w + L.pa);
+    bp.pnorm = (float *)(w + L.pnorm);
+    bp.pconv = (float *)(w + L.pconv);
+    return cuda_status(gdn::launch_backward(bp, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,861 @@
+// gdn_backward.cu -- backward of the GDN layer core on CUDA cores in fp32.
+//
+// The pages define the forward (the gated delta rule S_t = e^{g_t} S_{t-1}
+// (I - beta_t k_t k_t^T) + beta_t v_t k_t^T, o_t = S_t q_t, with the
+// "GDN Elementwise Fusion" pre- and post-GDR steps); this file computes the
+// gradient of sum(grad_out * out) + sum(grad_final * final_state) with respect
+// to every input, the RMSNorm rounding taken as the identity. The forward's
+// prologue and its CUDA-core chunk kernel run first (in gdn_api.cu) and leave,
+// per chunk slot and v head, the state at the chunk's start H0, the matrices
+// T = (I + A)^{-1}, Pm = lower(e^{gam_i - gam_j} q_i.k_j) and Ak = strict_lower(
+// e^{gam_i - gam_j} k_i.k_j), and per token the new values Vn.
+//
+// Chunk form (H = S^T, dk x dv; gam the in-chunk cumulative decay, L its last
+// valid token, E_ij = e^{gam_i - gam_j}, Kd = diag(e^{gam_L - gam}) K):
+//   R0 = diag(beta)(V - diag(e^gam) K H0),  Vn = T R0,
+//   O  = scale (diag(e^gam) Q H0 + Pm Vn),  H1 = e^{gam_L} H0 + Kd^T Vn.
+// Reverse, with dO' = scale dO and dH1 the gradient of the chunk's end state:
+//   dVn = Pm^T dO' + Kd dH1,  dR0 = T^T dVn,  dV = beta dR0,
+//   dH0 = e^{gam_L} dH1 + Q^T diag(e^gam) dO' - K^T diag(beta e^gam) dR0,
+//   dA  = -dR0 Vn^T (strictly lower),  dPm = dO' Vn^T (lower),
+//   dQ  = diag(e^gam) dO' H0^T + (dPm . E) K,
+//   dK  = (dPm . E)^T Q + F K + F^T K - diag(beta e^gam) dR0 H0^T + diag(e^{gam_L - gam}) Vn dH1^T,
+//         F = dA . beta_i E (strictly lower),
+//   dbeta_i = dR0_i . V_i - e^{gam_i} K_i . (dR0 H0^T)_i + sum_j dA_ij Ak_ij,
+//   dgam_i from every e^{...} factor, and dg = reverse cumulative sum of dgam.
+//
+// Kernels, in launch order: rms_bwd (gated RMSNorm), chain_bwd (serial over the
+// chunks of a sequence in reverse, per dv tile: carries dH, writes dH1 and dR0),
+// chunk_grad (all chunks in parallel: dq, dk per v head, dbeta, dg),
+// prologue_bwd (L2 norm, SiLU, beta / decay), conv_bwd (the causal conv:
+// input gradients and per-block weight sums) and sum_rows (fixed-order sums of
+// the partials: dnorm_w, dconv_w, ddt_bias, dA_log). Every sum has a fixed
+// order, so results are run-to-run identical.
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int DS = 32;              // dk slice staged in shared memory
+constexpr int LDA = kChunk + 1;     // padded row length of 64x64 tiles
+constexpr int LDS = DS + 1;
+constexpr int kC2 = kChunk * kChunk;
+
+__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float dsilu(float z) {
+    const float s = sigm(z);
+    return s * (1.0f + z * (1.0f - s));
+}
+
+// q / k of the forward's workspace: fp32, or fp16 hi + lo planes
+template <typename S>
+__device__ __forceinline__ float load_qk(const S *base, int64_t idx, int64_t plane) {
+    if (sizeof(S) == 4) return to_f<S>(base[idx]);
+    return to_f<S>(base[idx]) + to_f<S>(base[idx + plane]);
+}
+
+// flattened token t -> (batch row b, position tau) of the strided inputs
+__device__ __forceinline__ void tok_pos(const gdn_desc &d, int64_t t, int64_t &b, int64_t &tau) {
+    b = d.T > 0 ? t / d.T : 0;
+    tau = t - b * d.T;
+}
+
+// sequence [s0, s1) holding flattened token t
+__device__ __forceinline__ void seq_of(const gdn_desc &d, const int32_t *cu, int64_t t, int64_t &s0,
+                                       int64_t &s1) {
+    if (cu == nullptr) {
+        s0 = (t / d.T) * d.T;
+        s1 = s0 + d.T;
+        return;
+    }
+    int lo = 0, hi = d.N;   // cu[lo] <= t < cu[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= t) lo = mid; else hi = mid;
+    }
+    s0 = cu[lo];
+    s1 = cu[lo + 1];
+}
+
+// ------------------------------------------------------------ gated RMSNorm
+// One warp per (token, v head) row, NE columns per lane. Forward:
+// y = w * o * rstd * silu(gate). Writes dgate, dO' = scale * dL/do ([Hv][ntok][dv])
+// and the warp's partial sums of dnorm_w.
+template <typename T, typename GTy, typename WT, int NE>
+__global__ void __launch_bounds__(kThreads) rms_bwd_kernel(const BwdProblem bp, int64_t rows, int64_t nwarps) {
+    using S = typename Inter<T>::S;
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dv = d.dv, Hv = d.Hv;
+    const int lane = threadIdx.x & 31;
+    const int64_t w = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    float accw[NE];
+#pragma unroll
+    for (int e = 0; e < NE; ++e) accw[e] = 0.f;
+    for (int64_t r = w; r < rows; r += nwarps) {
+        const int64_t t = r / Hv;
+        const int h = (int)(r - t * Hv);
+        int64_t b, tau;
+        tok_pos(d, t, b, tau);
+        const S *orow = (const S *)p.o + r * dv;
+        const GTy *grow = (const GTy *)p.gate + b * d.gate_stride_b + tau * d.gate_stride_t + (int64_t)h * dv;
+        const T *dyrow = (const T *)bp.grad_out + r * dv;
+        float o[NE], dn[NE], nn[NE];
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const int c = lane + 32 * e;
+            o[e] = c < dv ? to_f<S>(orow[c]) : 0.f;
+            ss = fmaf(o[e], o[e], ss);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float rstd = 1.0f / sqrtf(ss / dv + d.norm_eps);
+        float dot = 0.f;
+        GTy *dgrow = (GTy *)bp.dgate + r * dv;
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const int c = lane + 32 * e;
+            nn[e] = o[e] * rstd;
+            dn[e] = 0.f;
+            if (c < dv) {
+                const float g = to_f<GTy>(grow[c]), dy = to_f<T>(dyrow[c]), wc = to_f<WT>(((const WT *)p.norm_w)[c]);
+                const float sg = sigm(g);
+                dgrow[c] = from_f<GTy>(dy * wc * nn[e] * (sg * (1.0f + g * (1.0f - sg))));
+                const float dr = dy * g * sg;
+                accw[e] = fmaf(dr, nn[e], accw[e]);
+                dn[e] = dr * wc;
+                dot = fmaf(dn[e], nn[e], dot);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        float *drow = bp.dO + ((int64_t)h * p.ntok + t) * dv;
+        const float k = d.scale * rstd, m = dot / dv;
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const int c = lane + 32 * e;
+            if (c < dv) drow[c] = k * (dn[e] - nn[e] * m);
+        }
+    }
+    if (w < nwarps) {
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const int c = lane + 32 * e;
+            if (c < dv) bp.pnorm[w * dv + c] = accw[e];
+        }
+    }
+}
+
+// ------------------------------------------------------------ reverse chain
+// One CTA per (sequence, v head, dv tile of NV columns), chunks in reverse.
+// Carries dH [dk][NV] in shared memory; per chunk stores dH1 (the gradient of
+// the chunk's end state) and dR0, then steps dH to the chunk's start.
+template <int NV>
+size_t chain_smem_bytes(int dk) {
+    return sizeof(float) * ((size_t)dk * NV + 2 * kChunk * LDA + 2 * kChunk * LDS + 3 * kChunk * NV + kChunk) +
+           sizeof(double) * kChunk;
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads) chain_bwd_kernel(const BwdProblem bp, int ntiles) {
+    using S = typename Inter<T>::S;
+    using GT = typename Inter<T>::G;
+    constexpr int NB = NV / 16;
+    extern __shared__ float sm[];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    int bid = blockIdx.x;
+    const int tile = bid % ntiles;
+    bid /= ntiles;
+    const int j = bid % Hv;
+    const int n = bid / Hv;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    const int64_t seq0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
+    const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : seq0 + d.T;
+    const int64_t slot0 = p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk);
+    const int nch = (int)((seq1 - seq0 + kChunk - 1) / kChunk);
+    const int hk = j / (Hv / d.Hk);
+    const int v0 = tile * NV;
+
+    GT *gam = (GT *)sm;                        // [64]
+    float *dHs = (float *)(gam + kChunk);      // [dk][NV]
+    float *Ts = dHs + (size_t)dk * NV;         // [64][LDA]
+    float *Ps = Ts + kChunk * LDA;             // [64][LDA]
+    float *Ks = Ps + kChunk * LDA;             // [64][LDS]
+    float *Qs = Ks + kChunk * LDS;             // [64][LDS]
+    float *dOs = Qs + kChunk * LDS;            // [64][NV]
+    float *dVs = dOs + kChunk * NV;            // [64][NV]
+    float *dRs = dVs + kChunk * NV;            // [64][NV]
+    float *bet = dRs + kChunk * NV;            // [64]
+
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
+    const S *qq = (const S *)p.q + (int64_t)hk * p.ntok * dk;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    const GT *gw = (const GT *)p.gamma + (int64_t)j * p.ntok;
+    const float *bw = p.beta + (int64_t)j * p.ntok;
+    const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
+
+    for (int idx = tid; idx < dk * NV; idx += kThreads) {
+        const int r = idx / NV, c = idx - r * NV;
+        dHs[idx] = bp.grad_final ? bp.grad_final[sbase + (size_t)r * dv + v0 + c] : 0.f;
+    }
+    for (int cc = nch - 1; cc >= 0; --cc) {
+        const int64_t tok0 = seq0 + (int64_t)cc * kChunk, slot = slot0 + cc;
+        const int L = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
+        __syncthreads();
+        // ---- dH1 of this chunk; T, Pm; decay, beta; dO' tile
+        float *dst = bp.dh1 + ((size_t)slot * Hv + j) * dk * dv + v0;
+        for (int idx = tid; idx < dk * NV; idx += kThreads) {
+            const int r = idx / NV, c = idx - r * NV;
+            dst[(size_t)r * dv + c] = dHs[idx];
+        }
+        const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
+        for (int idx = tid; idx < kC2; idx += kThreads) {
+            const int i = idx / kChunk, m = idx - i * kChunk;
+            Ts[i * LDA + m] = mats[idx];
+            Ps[i * LDA + m] = mats[kC2 + idx];
+        }
+        if (tid < kChunk) {
+            const int i = tid < L ? tid : L - 1;
+            gam[tid] = gw[tok0 + i];
+            bet[tid] = tid < L ? bw[tok0 + i] : 0.f;
+        }
+        for (int idx = tid; idx < kChunk * NV; idx += kThreads) {
+            const int i = idx / NV, c = idx - i * NV;
+            dOs[idx] = i < L ? bp.dO[((size_t)j * p.ntok + tok0 + i) * dv + v0 + c] : 0.f;
+        }
+        __syncthreads();
+        const GT gL = gam[kChunk - 1];
+        // ---- dVn = Pm^T dO' + Kd dH1
+        float acc[4][NB];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int i = ty + 16 * a;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) acc[a][b] = 0.f;
+            for (int m = i; m < kChunk; ++m) {
+                const float pv = Ps[m * LDA + i];
+#pragma unroll
+                for (int b = 0; b < NB; ++b) acc[a][b] = fmaf(pv, dOs[m * NV + tx + 16 * b], acc[a][b]);
+            }
+        }
+        for (int d0 = 0; d0 < dk; d0 += DS) {
+            __syncthreads();
+            for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
+                const int i = idx / DS, c = idx - i * DS;
+                const bool ok = i < L && d0 + c < dk;
+                Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) * expf((float)(gL - gam[i])) : 0.f;
+            }
+            __syncthreads();
+            const int dn = min(DS, dk - d0);
+            for (int c = 0; c < dn; ++c) {
+                float hv[NB];
+#pragma unroll
+                for (int b = 0; b < NB; ++b) hv[b] = dHs[(d0 + c) * NV + tx + 16 * b];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float kv = Ks[(ty + 16 * a) * LDS + c];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) acc[a][b] = fmaf(kv, hv[b], acc[a][b]);
+                }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) dVs[(ty + 16 * a) * NV + tx + 16 * b] = acc[a][b];
+        __syncthreads();
+        // ---- dR0 = T^T dVn (stored for the per-chunk kernels)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int i = ty + 16 * a;
+            float r[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) r[b] = 0.f;
+            for (int m = i; m < kChunk; ++m) {
+                const float tv = Ts[m * LDA + i];
+#pragma unroll
+                for (int b = 0; b < NB; ++b) r[b] = fmaf(tv, dVs[m * NV + tx + 16 * b], r[b]);
+            }
+#pragma unroll
+            for (int b = 0; b < NB; ++b) dRs[i * NV + tx + 16 * b] = r[b];
+            if (i < L) {
+                float *row = bp.dR + ((size_t)j * p.ntok + tok0 + i) * dv + v0;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) row[tx + 16 * b] = r[b];
+            }
+        }
+        // ---- dH0 = e^{gam_L} dH1 + (e^gam Q)^T dO' - (beta e^gam K)^T dR0
+        const float eL = expf((float)gL);
+        for (int d0 = 0; d0 < dk; d0 += DS) {
+            __syncthreads();
+            for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
+                const int i = idx / DS, c = idx - i * DS;
+                const bool ok = i < L && d0 + c < dk;
+                const float eg = expf((float)gam[i]);
+                Qs[i * LDS + c] = ok ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) * eg : 0.f;
+                Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) * eg * bet[i] : 0.f;
+            }
+            __syncthreads();
+            const int dn = min(DS, dk - d0);
+            for (int r = ty; r < dn; r += 16) {
+                float h[NB];
+#pragma unroll
+                for (int b = 0; b < NB; ++b) h[b] = 0.f;
+                for (int i = 0; i < kChunk; ++i) {
+                    const float qv = Qs[i * LDS + r], kv = Ks[i * LDS + r];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        h[b] = fmaf(qv, dOs[i * NV + tx + 16 * b], fmaf(-kv, dRs[i * NV + tx + 16 * b], h[b]));
+                }
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    float *hp = &dHs[(d0 + r) * NV + tx + 16 * b];
+                    *hp = fmaf(eL, *hp, h[b]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (bp.dinit) {
+        for (int idx = tid; idx < dk * NV; idx += kThreads) {
+            const int r = idx / NV, c = idx - r * NV;
+            bp.dinit[sbase + (size_t)r * dv + v0 + c] = dHs[idx];
+        }
+    }
+}
+
+// ------------------------------------------------------------ per-chunk gradients
+// One CTA per (chunk slot, v head). Phase A sums dPm = dO' Vn^T and dA = -dR0 Vn^T
+// over dv; phase B, per dk slice, forms dO' H0^T, dR0 H0^T and Vn dH1^T over dv
+// and the q / k gradients of the slice; phase C finishes dbeta and dg.
+constexpr int TW = 33;              // padded row of a 32-column dv tile
+constexpr int kTileV = 32;
+
+size_t grad_smem_bytes() {
+    return sizeof(double) * kChunk +
+           sizeof(float) * (5 * kChunk * LDA + 3 * kChunk * TW + 2 * DS * TW + 2 * kChunk * LDS + 5 * kChunk + 64);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) chunk_grad_kernel(const BwdProblem bp) {
+    using S = typename Inter<T>::S;
+    using GT = typename Inter<T>::G;
+    extern __shared__ float sm[];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    const int j = blockIdx.y;
+    const int64_t slot = blockIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    ChunkLoc loc;
+    if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, loc)) return;
+    const int64_t tok0 = loc.tok0;
+    const int L = loc.len;
+    const int hk = j / (Hv / d.Hk);
+
+    GT *gam = (GT *)sm;                        // [64]
+    float *Ps = (float *)(gam + kChunk);       // [64][LDA] Pm
+    float *Aks = Ps + kChunk * LDA;            // [64][LDA] Ak
+    float *dPs = Aks + kChunk * LDA;           // [64][LDA] dPm, then dPm . E
+    float *dAs = dPs + kChunk * LDA;           // [64][LDA] dA, then dA . beta_i E
+    float *Gs = dAs + kChunk * LDA;            // [64][LDA] dPm . Pm + dA . A
+    float *tO = Gs + kChunk * LDA;             // [64][TW]
+    float *tR = tO + kChunk * TW;              // [64][TW]
+    float *tV = tR + kChunk * TW;              // [64][TW]
+    float *hs = tV + kChunk * TW;              // [DS][TW]
+    float *dhs = hs + DS * TW;                 // [DS][TW]
+    float *Ks = dhs + DS * TW;                 // [64][LDS]
+    float *Qs = Ks + kChunk * LDS;             // [64][LDS]
+    float *bet = Qs + kChunk * LDS;            // [64]
+    float *eg = bet + kChunk;                  // [64] e^gam
+    float *ed = eg + kChunk;                   // [64] e^{gam_L - gam}
+    float *dbet = ed + kChunk;                 // [64]
+    float *dgm = dbet + kChunk;                // [64] dL/dgam
+    float *red = dgm + kChunk;                 // [64] block reduction scratch
+
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
+    const S *qq = (const S *)p.q + (int64_t)hk * p.ntok * dk;
+    const S *vv = (const S *)p.v + (int64_t)j * p.ntok * dv;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
+    const float *H0 = bp.h0 + ((size_t)slot * Hv + j) * dk * dv;
+    const float *dH1 = bp.dh1 + ((size_t)slot * Hv + j) * dk * dv;
+    const float *dOg = bp.dO + ((size_t)j * p.ntok + tok0) * dv;
+    const float *dRg = bp.dR + ((size_t)j * p.ntok + tok0) * dv;
+    const float *Vng = bp.vn + ((size_t)j * p.ntok + tok0) * dv;
+
+    if (tid < kChunk) {
+        const int i = tid < L ? tid : L - 1;
+        gam[tid] = ((const GT *)p.gamma)[(int64_t)j * p.ntok + tok0 + i];
+        bet[tid] = tid < L ? p.beta[(int64_t)j * p.ntok + tok0 + i] : 0.f;
+    }
+    for (int idx = tid; idx < kC2; idx += kThreads) {
+        const int i = idx / kChunk, m = idx - i * kChunk;
+        Ps[i * LDA + m] = mats[kC2 + idx];
+        Aks[i * LDA + m] = mats[2 * kC2 + idx];
+    }
+    __syncthreads();
+    if (tid < kChunk) {
+        eg[tid] = expf((float)gam[tid]);
+        ed[tid] = expf((float)(gam[kChunk - 1] - gam[tid]));
+    }
+    // dv tile loader: rows i < L of dO', dR0, Vn, columns [c0, c0 + 32)
+    auto load_tiles = [&](int c0) {
+        for (int idx = tid; idx < kChunk * kTileV; idx += kThreads) {
+            const int i = idx / kTileV, c = idx - i * kTileV;
+            const bool ok = i < L && c0 + c < dv;
+            tO[i * TW + c] = ok ? dOg[(int64_t)i * dv + c0 + c] : 0.f;
+            tR[i * TW + c] = ok ? dRg[(int64_t)i * dv + c0 + c] : 0.f;
+            tV[i * TW + c] = ok ? Vng[(int64_t)i * dv + c0 + c] : 0.f;
+        }
+    };
+
+    // ---- phase A: dPm, dA over dv; dbeta's dR0 . V term
+    float dP[4][4], dA[4][4], pb[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        pb[a] = 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) dP[a][b] = dA[a][b] = 0.f;
+    }
+    for (int c0 = 0; c0 < dv; c0 += kTileV) {
+        __syncthreads();
+        load_tiles(c0);
+        __syncthreads();
+        for (int c = 0; c < kTileV; ++c) {
+            float o[4], r[4], vj[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                o[a] = tO[(ty + 16 * a) * TW + c];
+                r[a] = tR[(ty + 16 * a) * TW + c];
+                vj[a] = tV[(tx + 16 * a) * TW + c];
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    dP[a][b] = fmaf(o[a], vj[b], dP[a][b]);
+                    dA[a][b] = fmaf(-r[a], vj[b], dA[a][b]);
+                }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int i = ty + 16 * a;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = tx + 16 * h;
+                if (i < L && c0 + c < dv) pb[a] = fmaf(tR[i * TW + c], to_f<S>(vv[(tok0 + i) * dv + c0 + c]), pb[a]);
+            }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int i = ty + 16 * a;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int m = tx + 16 * b;
+            dPs[i * LDA + m] = m <= i ? dP[a][b] : 0.f;
+            dAs[i * LDA + m] = m < i ? dA[a][b] : 0.f;
+        }
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) pb[a] += __shfl_xor_sync(0xffffffffu, pb[a], off);
+        if (tx == 0) dbet[i] = pb[a];
+    }
+    __syncthreads();
+    // G = dPm . Pm + dA . beta_i Ak: its row sums minus column sums are dgam's
+    // share from the decay factors inside Pm and A
+    for (int idx = tid; idx < kC2; idx += kThreads) {
+        const int i = idx / kChunk, m = idx - i * kChunk;
+        Gs[i * LDA + m] = dPs[i * LDA + m] * Ps[i * LDA + m] + dAs[i * LDA + m] * bet[i] * Aks[i * LDA + m];
+    }
+    __syncthreads();
+    if (tid < kChunk) {
+        const int i = tid;
+        float g = 0.f, bA = 0.f;
+        for (int m = 0; m < kChunk; ++m) {
+            g += Gs[i * LDA + m] - Gs[m * LDA + i];
+            bA = fmaf(dAs[i * LDA + m], Aks[i * LDA + m], bA);
+        }
+        dgm[i] = g;
+        dbet[i] += bA;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < kC2; idx += kThreads) {
+        const int i = idx / kChunk, m = idx - i * kChunk;
+        const float e = m <= i ? expf((float)(gam[i] - gam[m])) : 0.f;
+        dPs[i * LDA + m] *= e;
+        dAs[i * LDA + m] *= bet[i] * e;
+    }
+    // ---- phase B: per dk slice, X1 = dO' H0^T, X2 = dR0 H0^T, X3 = Vn dH1^T
+    float rg[4], rb[4], kap = 0.f, hd = 0.f;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) rg[a] = rb[a] = 0.f;
+    float *dqo = bp.dq + ((size_t)j * p.ntok + tok0) * dk;
+    float *dko = bp.dk + ((size_t)j * p.ntok + tok0) * dk;
+    for (int d0 = 0; d0 < dk; d0 += DS) {
+        float X1[4][2], X2[4][2], X3[4][2];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) X1[a][b] = X2[a][b] = X3[a][b] = 0.f;
+        for (int c0 = 0; c0 < dv; c0 += kTileV) {
+            __syncthreads();
+            load_tiles(c0);
+            for (int idx = tid; idx < DS * kTileV; idx += kThreads) {
+                const int r = idx / kTileV, c = idx - r * kTileV;
+                const bool ok = d0 + r < dk && c0 + c < dv;
+                hs[r * TW + c] = ok ? H0[(int64_t)(d0 + r) * dv + c0 + c] : 0.f;
+                dhs[r * TW + c] = ok ? dH1[(int64_t)(d0 + r) * dv + c0 + c] : 0.f;
+            }
+            __syncthreads();
+            for (int c = 0; c < kTileV; ++c) {
+                float o[4], r[4], vn[4], h[2], dh[2];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    o[a] = tO[(ty + 16 * a) * TW + c];
+                    r[a] = tR[(ty + 16 * a) * TW + c];
+                    vn[a] = tV[(ty + 16 * a) * TW + c];
+                }
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    h[b] = hs[(tx + 16 * b) * TW + c];
+                    dh[b] = dhs[(tx + 16 * b) * TW + c];
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        X1[a][b] = fmaf(o[a], h[b], X1[a][b]);
+                        X2[a][b] = fmaf(r[a], h[b], X2[a][b]);
+                        X3[a][b] = fmaf(vn[a], dh[b], X3[a][b]);
+                    }
+            }
+            for (int idx = tid; idx < DS * kTileV; idx += kThreads) {
+                const int r = idx / kTileV, c = idx - r * kTileV;
+                hd = fmaf(hs[r * TW + c], dhs[r * TW + c], hd);
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
+            const int i = idx / DS, c = idx - i * DS;
+            const bool ok = i < L && d0 + c < dk;
+            Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
+            Qs[i * LDS + c] = ok ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int i = ty + 16 * a;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int dd = tx + 16 * b;
+                float gq = eg[i] * X1[a][b], gk = -bet[i] * eg[i] * X2[a][b] + ed[i] * X3[a][b];
+                for (int m = 0; m <= i; ++m) gq = fmaf(dPs[i * LDA + m], Ks[m * LDS + dd], gq);
+                for (int m = i; m < kChunk; ++m) gk = fmaf(dPs[m * LDA + i], Qs[m * LDS + dd], gk);
+                for (int m = 0; m < i; ++m) gk = fmaf(dAs[i * LDA + m], Ks[m * LDS + dd], gk);
+                for (int m = i + 1; m < kChunk; ++m) gk = fmaf(dAs[m * LDA + i], Ks[m * LDS + dd], gk);
+                const float qv = Qs[i * LDS + dd], kv = Ks[i * LDS + dd];
+                rg[a] += qv * eg[i] * X1[a][b] - kv * bet[i] * eg[i] * X2[a][b] - kv * ed[i] * X3[a][b];
+                kap = fmaf(kv * ed[i], X3[a][b], kap);
+                rb[a] = fmaf(-eg[i] * kv, X2[a][b], rb[a]);
+                if (i < L && d0 + dd < dk) {
+                    dqo[(int64_t)i * dk + d0 + dd] = gq;
+                    dko[(int64_t)i * dk + d0 + dd] = gk;
+                }
+            }
+        }
+    }
+    // ---- phase C: dbeta, dgam, then dg = reverse cumulative sum of dgam
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) {
+            rg[a] += __shfl_xor_sync(0xffffffffu, rg[a], off);
+            rb[a] += __shfl_xor_sync(0xffffffffu, rb[a], off);
+        }
+    }
+    // kappa and <H0, dH1>: fixed-order block sums
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        kap += __shfl_xor_sync(0xffffffffu, kap, off);
+        hd += __shfl_xor_sync(0xffffffffu, hd, off);
+    }
+    __syncthreads();
+    if ((tid & 31) == 0) {
+        red[tid >> 5] = kap;
+        red[32 + (tid >> 5)] = hd;
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+        if (tx == 0) {
+            const int i = ty + 16 * a;
+            dgm[i] += rg[a];
+            dbet[i] += rb[a];
+        }
+    __syncthreads();
+    if (tid == 0) {
+        float ks = 0.f, hs_ = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            ks += red[w];
+            hs_ += red[32 + w];
+        }
+        dgm[L - 1] += ks + expf((float)gam[kChunk - 1]) * hs_;
+        float acc = 0.f;
+        float *dbo = bp.dbeta + (size_t)j * p.ntok + tok0;
+        float *dgo = bp.dgam + (size_t)j * p.ntok + tok0;
+        for (int i = L - 1; i >= 0; --i) {
+            acc += dgm[i];
+            dgo[i] = acc;
+            dbo[i] = dbet[i];
+        }
+    }
+}
+
+// ------------------------------------------------------------ prologue backward
+// Sum of v over the CTA, the same total in every thread (fixed order).
+__device__ __forceinline__ float block_sum(float v, float *red) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+    return t;
+}
+
+// grid (token, 2*Hk q/k heads + v channel groups + 1 beta/decay unit). Recomputes
+// the conv pre-activation z of the token and writes dz = dL/dz ([ntok][ch]);
+// the beta / decay unit writes db, da and the per-token terms of ddt_bias and dA_log.
+template <typename T>
+__global__ void __launch_bounds__(512) prologue_bwd_kernel(const BwdProblem bp, int units_v) {
+    __shared__ float red[16];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int64_t t = blockIdx.x;
+    const int u = blockIdx.y, tid = threadIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    int64_t s0, s1, b, tau;
+    seq_of(d, p.cu, t, s0, s1);
+    tok_pos(d, t, b, tau);
+    const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
+    const T *w = (const T *)p.conv_w;
+    // z of channel c_in of input x (batch row b), conv weights of row cw
+    auto conv_z = [&](const T *x, int64_t sb, int64_t st, int c_in, int cw) {
+        float z = 0.f;
+#pragma unroll
+        for (int m = 0; m < kConvW; ++m) {
+            const int64_t back = kConvW - 1 - m;
+            if (t - back >= s0) z = fmaf(to_f<T>(w[(int64_t)cw * kConvW + m]), to_f<T>(x[b * sb + (tau - back) * st + c_in]), z);
+        }
+        return z;
+    };
+    if (u < 2 * d.Hk) {
+        const bool isk = u >= d.Hk;
+        const int h = isk ? u - d.Hk : u;
+        const int i = tid;
+        const bool act = i < d.dk;
+        float z = 0.f, y = 0.f;
+        if (act) {
+            z = isk ? conv_z((const T *)p.k_raw, d.k_stride_b, d.k_stride_t, h * d.dk + i, ch_qk + h * d.dk + i)
+                    : conv_z((const T *)p.q_raw, d.q_stride_b, d.q_stride_t, h * d.dk + i, h * d.dk + i);
+            y = z * sigm(z);
+        }
+        const float rho = 1.0f / sqrtf(block_sum(y * y, red) + d.l2_eps);
+        const float xn = y * rho;
+        float dxn = 0.f;
+        if (act) {
+            const int G = d.Hv / d.Hk;
+            const float *src = isk ? bp.dk : bp.dq;
+            for (int jj = h * G; jj < (h + 1) * G; ++jj) dxn += src[((int64_t)jj * p.ntok + t) * d.dk + i];
+        }
+        const float dot = block_sum(xn * dxn, red);
+        if (act) bp.dz[t * ch + (isk ? ch_qk : 0) + h * d.dk + i] = rho * (dxn - xn * dot) * dsilu(z);
+    } else if (u < 2 * d.Hk + units_v) {
+        const int cv = (u - 2 * d.Hk) * (int)blockDim.x + tid;
+        if (cv < ch_v) {
+            const float z = conv_z((const T *)p.v_raw, d.v_stride_b, d.v_stride_t, cv, 2 * ch_qk + cv);
+            const int jh = cv / d.dv;
+            const int64_t r = (int64_t)jh * p.ntok + t;
+            bp.dz[t * ch + 2 * ch_qk + cv] = p.beta[r] * bp.dR[r * d.dv + (cv - jh * d.dv)] * dsilu(z);
+        }
+    } else {
+        for (int h = tid; h < d.Hv; h += blockDim.x) {
+            const float av = to_f<T>(((const T *)p.a)[b * d.a_stride_b + tau * d.a_stride_t + h]);
+            const float bv = to_f<T>(((const T *)p.b)[b * d.b_stride_b + tau * d.b_stride_t + h]);
+            const int64_t r = (int64_t)h * p.ntok + t;
+            const float be = sigm(bv);
+            ((T *)bp.db)[t * d.Hv + h] = from_f<T>(bp.dbeta[r] * be * (1.0f - be));
+            const float x = av + p.dt_bias[h], eA = expf(p.A_log[h]);
+            const float dg = bp.dgam[r];
+            const float dx = -dg * eA * sigm(x);
+            ((T *)bp.da)[t * d.Hv + h] = from_f<T>(dx);
+            bp.pa[r] = dx;
+            bp.pa[(int64_t)d.Hv * p.ntok + r] = dg * (-eA * softplus_f(x));
+        }
+    }
+}
+
+// ------------------------------------------------------------ conv backward
+// grid (blocks of kBwdConvTokens tokens, channel groups of 256): per channel,
+// dx_t = sum_m w_m dz_{t+3-m} within the sequence, and the block's partial
+// sums of dw_m = sum_t dz_t x_{t-3+m}.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) conv_bwd_kernel(const BwdProblem bp) {
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
+    const int c = blockIdx.y * kThreads + threadIdx.x;
+    if (c >= ch) return;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    const T *x;
+    T *dx;
+    int64_t sb, st, ostride;
+    int c_in;
+    if (c < ch_qk) {
+        x = (const T *)p.q_raw; sb = d.q_stride_b; st = d.q_stride_t; c_in = c;
+        dx = (T *)bp.dq_raw; ostride = ch_qk;
+    } else if (c < 2 * ch_qk) {
+        x = (const T *)p.k_raw; sb = d.k_stride_b; st = d.k_stride_t; c_in = c - ch_qk;
+        dx = (T *)bp.dk_raw; ostride = ch_qk;
+    } else {
+        x = (const T *)p.v_raw; sb = d.v_stride_b; st = d.v_stride_t; c_in = c - 2 * ch_qk;
+        dx = (T *)bp.dv_raw; ostride = ch_v;
+    }
+    float wm[kConvW], dw[kConvW];
+#pragma unroll
+    for (int m = 0; m < kConvW; ++m) {
+        wm[m] = to_f<T>(((const T *)p.conv_w)[(int64_t)c * kConvW + m]);
+        dw[m] = 0.f;
+    }
+    const int64_t t0 = (int64_t)blockIdx.x * kBwdConvTokens;
+    const int64_t t1 = t0 + kBwdConvTokens < p.ntok ? t0 + kBwdConvTokens : p.ntok;
+    int64_t s0 = 0, s1 = 0;
+    for (int64_t t = t0; t < t1; ++t) {
+        if (t >= s1) seq_of(d, p.cu, t, s0, s1);
+        int64_t b, tau;
+        tok_pos(d, t, b, tau);
+        float g = 0.f;
+#pragma unroll
+        for (int m = 0; m < kConvW; ++m) {
+            const int64_t tt = t + (kConvW - 1 - m);
+            if (tt < s1) g = fmaf(wm[m], bp.dz[tt * ch + c], g);
+        }
+        dx[t * ostride + c_in] = from_f<T>(g);
+        const float dzt = bp.dz[t * ch + c];
+#pragma unroll
+        for (int m = 0; m < kConvW; ++m) {
+            const int64_t back = kConvW - 1 - m;
+            if (t - back >= s0) dw[m] = fmaf(dzt, to_f<T>(x[b * sb + (tau - back) * st + c_in]), dw[m]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kConvW; ++m) bp.pconv[((int64_t)blockIdx.x * ch + c) * kConvW + m] = dw[m];
+}
+
+// out[i] = sum_{r < R} part[r * rs + i * cs], one CTA per i, fixed order
+__global__ void __launch_bounds__(kThreads) sum_kernel(const float *part, int64_t R, int64_t rs, int64_t cs,
+                                                       float *out) {
+    __shared__ float red[kThreads];
+    const int64_t i = blockIdx.x;
+    float acc = 0.f;
+    for (int64_t r = threadIdx.x; r < R; r += kThreads) acc += part[r * rs + i * cs];
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int s = kThreads / 2; s > 0; s >>= 1) {
+        if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[i] = red[0];
+}
+
+// ------------------------------------------------------------ launches
+template <typename T, typename GTy, typename WT>
+cudaError_t launch_rms(const BwdProblem &bp, cudaStream_t s) {
+    const gdn_desc &d = bp.f.d;
+    const int64_t rows = bp.f.ntok * d.Hv;
+    if (rows == 0) return cudaSuccess;
+    const int64_t nwarps = bwd_epi_warps(d);
+    const unsigned blocks = (unsigned)((nwarps + kThreads / 32 - 1) / (kThreads / 32));
+    switch (d.dv <= 32 ? 1 : d.dv / 32) {
+    case 1: rms_bwd_kernel<T, GTy, WT, 1><<<blocks, kThreads, 0, s>>>(bp, rows, nwarps); break;
+    case 2: rms_bwd_kernel<T, GTy, WT, 2><<<blocks, kThreads, 0, s>>>(bp, rows, nwarps); break;
+    case 4: rms_bwd_kernel<T, GTy, WT, 4><<<blocks, kThreads, 0, s>>>(bp, rows, nwarps); break;
+    case 8: rms_bwd_kernel<T, GTy, WT, 8><<<blocks, kThreads, 0, s>>>(bp, rows, nwarps); break;
+    default: rms_bwd_kernel<T, GTy, WT, 16><<<blocks, kThreads, 0, s>>>(bp, rows, nwarps); break;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T, typename GTy>
+cudaError_t launch_rms_w(const BwdProblem &bp, cudaStream_t s) {
+    return bp.f.d.norm_w_dtype == GDN_F32 ? launch_rms<T, GTy, float>(bp, s) : launch_rms<T, GTy, T>(bp, s);
+}
+
+template <typename T, int NV>
+cudaError_t launch_chain(const BwdProblem &bp, cudaStream_t s) {
+    const gdn_desc &d = bp.f.d;
+    const int ntiles = d.dv / NV;
+    const size_t bytes = chain_smem_bytes<NV>(d.dk);
+    cudaError_t e = cudaFuncSetAttribute(chain_bwd_kernel<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
+    chain_bwd_kernel<T, NV><<<(unsigned)blocks, kThreads, bytes, s>>>(bp, ntiles);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const BwdProblem &bp, cudaStream_t s) {
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    cudaError_t e = d.gate_dtype == GDN_F32 ? launch_rms_w<T, float>(bp, s) : launch_rms_w<T, T>(bp, s);
+    if (e != cudaSuccess) return e;
+    // reverse chain: the CUDA-core forward's dv tiling
+    if (d.dv >= 64 && d.dk <= 256) e = launch_chain<T, 64>(bp, s);
+    else if (d.dv >= 32) e = launch_chain<T, 32>(bp, s);
+    else e = launch_chain<T, 16>(bp, s);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = chunk_slots(p);
+    if (slots > 0) {
+        const size_t bytes = grad_smem_bytes();
+        e = cudaFuncSetAttribute(chunk_grad_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        chunk_grad_kernel<T><<<dim3((unsigned)slots, d.Hv), kThreads, bytes, s>>>(bp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
+    if (p.ntok > 0) {
+        const int pt = d.dk > 128 ? d.dk : 128;
+        const int units_v = (ch_v + pt - 1) / pt;
+        prologue_bwd_kernel<T><<<dim3((unsigned)p.ntok, 2 * d.Hk + units_v + 1), pt, 0, s>>>(bp, units_v);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        conv_bwd_kernel<T><<<dim3((unsigned)bwd_conv_blocks(d), (ch + kThreads - 1) / kThreads), kThreads, 0, s>>>(bp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // parameter gradients: fixed-order sums of the partials (zero without tokens)
+    const int64_t rows = p.ntok * d.Hv;
+    sum_kernel<<<d.dv, kThreads, 0, s>>>(bp.pnorm, rows > 0 ? bwd_epi_warps(d) : 0, d.dv, 1, bp.dnorm_w);
+    sum_kernel<<<ch * kConvW, kThreads, 0, s>>>(bp.pconv, p.ntok > 0 ? bwd_conv_blocks(d) : 0, (int64_t)ch * kConvW,
+                                                 1, bp.dconv_w);
+    sum_kernel<<<d.Hv, kThreads, 0, s>>>(bp.pa, p.ntok, 1, p.ntok, bp.ddt_bias);
+    sum_kernel<<<d.Hv, kThreads, 0, s>>>(bp.pa + (int64_t)d.Hv * p.ntok, p.ntok, 1, p.ntok, bp.dA_log);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdProblem &p, cudaStream_t s) {
+    switch (p.f.d.dtype) {
+    case GDN_F32: return launch_t<float>(p, s);
+    case GDN_BF16: return launch_t<__nv_bfloat16>(p, s);
+    default: return launch_t<__half>(p, s);
+    }
+}
+
+}  // namespace gdn

@@ -76,6 +76,12 @@ struct Problem {
     void *gamma;                  // float, or double for fp32 activations
     void *tpt;                    // [T; P T] tiles of the tensor-core kernels
     bool single_stream;           // no side stream (the no-allocation entry point)
+    // Backward recompute only (null in the forward; the CUDA-core chunk kernel
+    // writes them): per (chunk slot, v head) the state at the chunk's start
+    // [dk][dv] and the chunk's matrices [3][64][64] (T = (I + A)^{-1}, the
+    // masked decayed Q K^T, and the strictly lower decayed K K^T without beta);
+    // per (v head, token) the new values Vn [dv]. All fp32.
+    float *bw_h0, *bw_mats, *bw_vn;
 };
 
 // Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one
@@ -100,6 +106,69 @@ int forward_single_stream(const gdn_desc *d, const void *q_raw, const void *k_ra
                           float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 bool chunk_tc_supports(const gdn_desc &d);
 cudaError_t launch_epilogue(const Problem &p, cudaStream_t s);
+
+// Backward: the forward's regions, then the backward's (all fp32), each on a
+// 256-byte boundary. Slots are chunk slots (chunk_slot_bound), tokens the
+// flattened B*T axis.
+constexpr int kBwdEpiWarps = 4864;    // warps of the RMSNorm backward (152 SMs x 32)
+constexpr int kBwdConvTokens = 256;   // tokens per block of the conv backward
+struct BwdLayout {
+    Layout f;                // the forward's regions (q, k, v, beta, gamma, o, ...)
+    size_t h0;               // [slot][Hv][dk][dv]  state at each chunk's start
+    size_t dh1;              // [slot][Hv][dk][dv]  gradient of the state at each chunk's end
+    size_t mats;             // [slot][Hv][3][64][64] T, decayed Q K^T, decayed K K^T
+    size_t vn, dO, dR;       // [Hv][ntok][dv]      new values, scale * dL/do, dL/d(beta (v - e^g K H))
+    size_t dq, dk;           // [Hv][ntok][dk]      gradients of the normalised q, k per v head
+    size_t dbeta, dgam;      // [Hv][ntok]          gradients of beta and of the per-token decay g
+    size_t dz;               // [ntok][ch]          gradient of the pre-activation conv output
+    size_t pa;               // [2][Hv][ntok]       per-token terms of ddt_bias and dA_log
+    size_t pnorm;            // [kBwdEpiWarps][dv]  per-warp partial sums of dnorm_w
+    size_t pconv;            // [blocks][ch][4]     per-block partial sums of dconv_w
+    size_t total;
+};
+inline int64_t bwd_epi_warps(const gdn_desc &d) {
+    const int64_t rows = (int64_t)d.B * d.T * d.Hv;
+    return rows < kBwdEpiWarps ? (rows > 0 ? rows : 1) : kBwdEpiWarps;
+}
+inline int64_t bwd_conv_blocks(const gdn_desc &d) {
+    const int64_t ntok = (int64_t)d.B * d.T;
+    return ntok > 0 ? (ntok + kBwdConvTokens - 1) / kBwdConvTokens : 1;
+}
+inline BwdLayout make_bwd_layout(const gdn_desc &d) {
+    BwdLayout L;
+    L.f = make_layout(d);
+    const size_t ntok = (size_t)d.B * (size_t)d.T, slots = (size_t)chunk_slot_bound(d);
+    const size_t ch = 2 * (size_t)d.Hk * d.dk + (size_t)d.Hv * d.dv;
+    const size_t st = (size_t)d.Hv * d.dk * d.dv * 4;
+    size_t off = L.f.total;
+    L.h0 = off;    off = align_up(off + slots * st, 256);
+    L.dh1 = off;   off = align_up(off + slots * st, 256);
+    L.mats = off;  off = align_up(off + slots * d.Hv * 3 * 64 * 64 * 4, 256);
+    L.vn = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dv * 4, 256);
+    L.dO = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dv * 4, 256);
+    L.dR = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dv * 4, 256);
+    L.dq = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dk * 4, 256);
+    L.dk = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dk * 4, 256);
+    L.dbeta = off; off = align_up(off + (size_t)d.Hv * ntok * 4, 256);
+    L.dgam = off;  off = align_up(off + (size_t)d.Hv * ntok * 4, 256);
+    L.dz = off;    off = align_up(off + ntok * ch * 4, 256);
+    L.pa = off;    off = align_up(off + 2 * (size_t)d.Hv * ntok * 4, 256);
+    L.pnorm = off; off = align_up(off + (size_t)bwd_epi_warps(d) * d.dv * 4, 256);
+    L.pconv = off; off = align_up(off + (size_t)bwd_conv_blocks(d) * ch * 4 * 4, 256);
+    L.total = off;
+    return L;
+}
+struct BwdProblem {
+    Problem f;                          // the forward's inputs and workspace pointers
+    const void *grad_out;               // act dtype [B*T][Hv][dv]
+    const float *grad_final;            // [N][Hv][dk][dv] or null
+    void *dq_raw, *dk_raw, *dv_raw;     // act dtype, dense [B*T][Hk*dk] / [B*T][Hv*dv]
+    void *da, *db;                      // act dtype [B*T][Hv]
+    void *dgate;                        // gate dtype [B*T][Hv*dv]
+    float *dconv_w, *dA_log, *ddt_bias, *dnorm_w, *dinit;
+    float *h0, *dh1, *mats, *vn, *dO, *dR, *dq, *dk, *dbeta, *dgam, *dz, *pa, *pnorm, *pconv;
+};
+cudaError_t launch_backward(const BwdProblem &p, cudaStream_t s);
 
 // Decode (one token per sequence, d.T == 1): workspace regions, all fp32 but o.
 struct DecodeLayout {

@@ -35,7 +35,8 @@ ACT_TORCH = {GDN_F32: torch.float32, GDN_BF16: torch.bfloat16, GDN_F16: torch.fl
 EXPORTS = ("gdn_desc_init", "gdn_workspace_bytes", "gdn_workspace_offsets", "gdn_forward",
            "gdn_prologue", "gdn_chunk_rule", "gdn_epilogue", "gdn_device_status",
            "gdn_status_string", "gdn_chunk_kernel_kind", "gdn_forward_static_ws",
-           "gdn_decode_workspace_bytes", "gdn_decode_step")
+           "gdn_decode_workspace_bytes", "gdn_decode_step", "gdn_backward_workspace_bytes",
+           "gdn_backward")
 
 # bytes of the library's fixed device scratch used by gdn_forward_static_ws
 GDN_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
@@ -97,6 +98,8 @@ def load(path: str = LIB_PATH):
     L.gdn_forward_static_ws.argtypes = [dp] + [vp] * 14 + [vp]
     L.gdn_decode_workspace_bytes.argtypes = [dp, ctypes.POINTER(sz)]
     L.gdn_decode_step.argtypes = [dp] + [vp] * 13 + [vp, sz, vp]
+    L.gdn_backward_workspace_bytes.argtypes = [dp, ctypes.POINTER(sz)]
+    L.gdn_backward.argtypes = [dp] + [vp] * 25 + [vp, sz, vp]
     for name in EXPORTS:
         if name != "gdn_status_string":
             getattr(L, name).restype = i32
@@ -236,6 +239,28 @@ def gdn_decode_step(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, 
     return rc
 
 
+def gdn_backward_workspace_bytes(d: gdn_desc) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().gdn_backward_workspace_bytes(ctypes.byref(d), ctypes.byref(n)),
+           "gdn_backward_workspace_bytes")
+    return n.value
+
+
+def gdn_backward(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w, cu_seqlens,
+                 initial_state, grad_out, grad_final, dq_raw, dk_raw, dv_raw, da, db, dgate, dconv_w,
+                 dA_log, ddt_bias, dnorm_w, dinitial_state, workspace, workspace_bytes, stream=None,
+                 check=True) -> int:
+    rc = load().gdn_backward(ctypes.byref(d), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(a), _ptr(b),
+                             _ptr(gate), _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w),
+                             _ptr(cu_seqlens), _ptr(initial_state), _ptr(grad_out), _ptr(grad_final),
+                             _ptr(dq_raw), _ptr(dk_raw), _ptr(dv_raw), _ptr(da), _ptr(db), _ptr(dgate),
+                             _ptr(dconv_w), _ptr(dA_log), _ptr(ddt_bias), _ptr(dnorm_w),
+                             _ptr(dinitial_state), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if check:
+        _check(rc, "gdn_backward")
+    return rc
+
+
 # --------------------------------------------------- tensors -> descriptor
 def desc_for(q_raw, k_raw, v_raw, a, b, gate, norm_w, *, Hk, Hv, dk, dv,
              cu_seqlens=None, l2_eps=1e-6, norm_eps=1e-5, scale=1.0) -> gdn_desc:
@@ -313,3 +338,53 @@ def forward(inp, bufs: Optional[Buffers] = None, stream=None, want_final_state=T
                 inp.A_log, inp.dt_bias, inp.norm_w, inp.cu_seqlens, inp.initial_state,
                 bufs.out, bufs.final_state, bufs.workspace, bufs.ws_bytes, stream)
     return bufs
+
+
+@dataclass
+class Grads:
+    dq_raw: torch.Tensor
+    dk_raw: torch.Tensor
+    dv_raw: torch.Tensor
+    da: torch.Tensor
+    db: torch.Tensor
+    dgate: torch.Tensor
+    dconv_w: torch.Tensor
+    dA_log: torch.Tensor
+    ddt_bias: torch.Tensor
+    dnorm_w: torch.Tensor
+    dinitial_state: Optional[torch.Tensor]
+    workspace: torch.Tensor
+
+
+def alloc_grads(desc: gdn_desc, device, want_dinitial=True) -> Grads:
+    """Gradient buffers (dense, see gdn_backward in include/gdn.h) and the workspace."""
+    act = ACT_TORCH[desc.dtype]
+    ntok = desc.B * desc.T
+    ch_qk, ch_v = desc.Hk * desc.dk, desc.Hv * desc.dv
+    f32 = dict(dtype=torch.float32, device=device)
+    return Grads(
+        dq_raw=torch.empty((ntok, ch_qk), dtype=act, device=device),
+        dk_raw=torch.empty((ntok, ch_qk), dtype=act, device=device),
+        dv_raw=torch.empty((ntok, ch_v), dtype=act, device=device),
+        da=torch.empty((ntok, desc.Hv), dtype=act, device=device),
+        db=torch.empty((ntok, desc.Hv), dtype=act, device=device),
+        dgate=torch.empty((ntok, ch_v), dtype=ACT_TORCH[desc.gate_dtype], device=device),
+        dconv_w=torch.empty((2 * ch_qk + ch_v, 4), **f32), dA_log=torch.empty(desc.Hv, **f32),
+        ddt_bias=torch.empty(desc.Hv, **f32), dnorm_w=torch.empty(desc.dv, **f32),
+        dinitial_state=torch.empty((desc.N, desc.Hv, desc.dk, desc.dv), **f32) if want_dinitial else None,
+        workspace=torch.empty(gdn_backward_workspace_bytes(desc), dtype=torch.uint8, device=device))
+
+
+def backward(inp, grad_out, grad_final=None, grads: Optional[Grads] = None, stream=None) -> Grads:
+    """Gradients of sum(grad_out * out) + sum(grad_final * final_state) for an
+    ``Inputs``-like object on the GPU (grad_out [B, T, Hv, dv] act dtype,
+    contiguous; grad_final [N, Hv, dk, dv] fp32 or None)."""
+    d = make_desc(inp)
+    if grads is None:
+        grads = alloc_grads(d, inp.q_raw.device)
+    gdn_backward(d, inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.gate, inp.conv_w, inp.A_log,
+                 inp.dt_bias, inp.norm_w, inp.cu_seqlens, inp.initial_state, grad_out, grad_final,
+                 grads.dq_raw, grads.dk_raw, grads.dv_raw, grads.da, grads.db, grads.dgate, grads.dconv_w,
+                 grads.dA_log, grads.ddt_bias, grads.dnorm_w, grads.dinitial_state, grads.workspace,
+                 grads.workspace.numel(), stream)
+    return grads

@@ -235,3 +235,16 @@ def head_subproblem(inp: Inputs, heads: list) -> Inputs:
                   take(inp.gate, dv, heads), conv_w, inp.A_log[heads].contiguous(),
                   inp.dt_bias[heads].contiguous(), inp.norm_w, inp.cu_seqlens,
                   None if inp.initial_state is None else inp.initial_state[:, heads].contiguous())
+
+
+def make_cotangents(inp: Inputs, seed: int = 1, final: bool = True):
+    """Seeded gradients of the outputs for the backward: grad_out ~ N(0, 1) in
+    the act dtype [B, T, Hv, dv], grad_final ~ N(0, 1) fp32 [N, Hv, dk, dv]
+    (or None)."""
+    w = inp.w
+    g = torch.Generator().manual_seed(seed * 104729 + w.seed)
+    B, T = inp.q_raw.shape[0], inp.q_raw.shape[1]
+    grad_out = torch.randn((B, T, w.Hv, w.dv), generator=g, dtype=torch.float32).to(ACT_DTYPES[w.dtype])
+    grad_final = (torch.randn((inp.n_seq, w.Hv, w.dk, w.dv), generator=g, dtype=torch.float32)
+                  if final else None)
+    return grad_out, grad_final

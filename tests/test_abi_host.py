@@ -162,3 +162,43 @@ def test_decode_checks(lib):
     bad = gdn.gdn_desc_init(4, 1, 0, 2, 4, 64, 128, gdn.GDN_BF16)
     bad.dk = 48                             # not a power of two
     assert call(bad) == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_backward_checks(lib):
+    """The backward entry rejects bad pointers and workspaces before any launch."""
+    fake = 1 << 20   # never dereferenced: every call below fails its checks first
+    d = gdn.gdn_desc_init(2, 100, 0, 2, 4, 64, 128, gdn.GDN_BF16)
+    need = gdn.gdn_backward_workspace_bytes(d)
+    B, T, Hk, Hv, dk, dv = 2, 100, 2, 4, 64, 128
+    ntok, slots = B * T, (B * T + 63) // 64 + B
+    # the forward's workspace, then per chunk slot two states and three 64x64
+    # matrices, and per token the fp32 rows of the reverse pass
+    assert need >= gdn.gdn_workspace_bytes(d) + slots * Hv * (2 * dk * dv + 3 * 64 * 64) * 4 + \
+        ntok * Hv * (3 * dv + 2 * dk + 4) * 4 + ntok * (2 * Hk * dk + Hv * dv) * 4
+    args = [fake] * 25   # q_raw .. dinitial_state
+    args[10] = None      # cu_seqlens: not packed
+    optional = {10, 11, 13, 24}   # cu_seqlens, initial_state, grad_final, dinitial_state
+
+    def call(desc, a=None, ws=fake, nbytes=None):
+        a = args if a is None else a
+        return lib.gdn_backward(ctypes.byref(desc), *a, ws, need if nbytes is None else nbytes, None)
+
+    for i in range(25):
+        if i in optional:
+            continue
+        a = list(args)
+        a[i] = None
+        assert call(d, a) == gdn.GDN_ERR_INVALID_ARG, i
+    for i in (0, 1, 2, 6):                  # vector-loaded inputs must be 16-byte aligned
+        a = list(args)
+        a[i] = fake + 2
+        assert call(d, a) == gdn.GDN_ERR_INVALID_ARG, i
+    for i in (11, 13, 24):                  # fp32 states must be 16-byte aligned
+        a = list(args)
+        a[i] = fake + 4
+        assert call(d, a) == gdn.GDN_ERR_INVALID_ARG, i
+    assert call(d, nbytes=need - 1) == gdn.GDN_ERR_WORKSPACE
+    assert call(d, ws=fake + 16) == gdn.GDN_ERR_WORKSPACE
+    bad = gdn.gdn_desc_init(2, 100, 0, 2, 4, 64, 128, gdn.GDN_BF16)
+    bad.dv = 96                             # not a power of two
+    assert call(bad) == gdn.GDN_ERR_UNSUPPORTED
