@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--decode", action="store_true",
                     help="time the decode step (one token per sequence) instead of the forward")
     ap.add_argument("--decode-batch", type=int, default=256, help="sequences per decode step")
+    ap.add_argument("--backward", action="store_true",
+                    help="time forward + backward (gdn_forward then gdn_backward) per step")
     return ap.parse_args()
 
 
@@ -291,6 +293,199 @@ def decode_main(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- forward + backward
+def fp32_alu_peak_tflops():
+    """FP32 FMA peak of the CUDA cores: 152 SMs x 128 FP32 lanes x 2 flops x the
+    maximum SM clock (MEASURED_PEAKS.json's sm_max_mhz, else 2070 MHz)."""
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except (OSError, ValueError):
+        pass
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def backward_flops(w, ntok):
+    """Algorithmic flops of gdn_backward (its forward recompute included), per
+    token and v head: 18 dk dv + 12 C dv + 12 C dk (C = 64): the recompute
+    (K H0, Q H0, the state update; T R0, P Vn; K K^T, Q K^T), the reverse chain
+    (Kd dH1, the two dH0 terms; P^T dO', T^T dVn) and the per-chunk gradients
+    (dO' H0^T, dR0 H0^T, Vn dH1^T; dO' Vn^T, dR0 Vn^T; four 64x64 by 64xdk
+    products)."""
+    C = CHUNK
+    return ntok * w.Hv * (18 * w.dk * w.dv + 12 * C * w.dv + 12 * C * w.dk)
+
+
+def oracle_bwd_sample(w):
+    from linear_attention_sequence_qkv_gb300.workloads import head_subproblem, make_inputs, replace
+    if w.n_packed:
+        w1 = replace(w, n_packed=0, B=1, T=min(w.max_len, 1024))
+    else:
+        w1 = replace(w, B=1, T=min(w.T, 1024))
+    inp = make_inputs(w1)
+    hk = list(range(w1.Hk))
+    if w1.Hv * w1.dk * w1.dv * w1.T > 6 * 256 * 512 * 1024:
+        hk = hk[:1]
+        inp = head_subproblem(inp, list(range(w1.Hv // w1.Hk)))
+    return inp, w1, len(hk) * (w1.Hv // w1.Hk)
+
+
+def run_oracle_fwd_bwd(inp, threads):
+    from linear_attention_sequence_qkv_gb300.workloads import make_cotangents
+    from oracle import oracle as O
+    w = inp.w
+    flat = lambda x: x.float().reshape(-1, x.shape[-1]).numpy()
+    gout, gfin = make_cotangents(inp)
+    args = dict(q_raw=flat(inp.q_raw), k_raw=flat(inp.k_raw), v_raw=flat(inp.v_raw), a=flat(inp.a),
+                b=flat(inp.b), gate=flat(inp.gate.contiguous()), conv_w=inp.conv_w.float().numpy(),
+                A_log=inp.A_log.numpy(), dt_bias=inp.dt_bias.numpy(), norm_w=inp.norm_w.float().numpy(),
+                seq_start=inp.seq_starts(), Hk=w.Hk, Hv=w.Hv, dk=w.dk, dv=w.dv,
+                initial_state=None if inp.initial_state is None else inp.initial_state.numpy(),
+                threads=threads)
+    t0 = time.perf_counter()
+    O.forward(**args, dtype=w.dtype)
+    O.backward(**args, grad_out=gout.float().reshape(-1, w.Hv, w.dv).numpy(), grad_final=gfin.numpy())
+    return time.perf_counter() - t0
+
+
+def backward_main(args, w):
+    """One step = gdn_forward + gdn_backward over the workload, inputs and
+    cotangents resident in HBM."""
+    import torch
+    from linear_attention_sequence_qkv_gb300 import build, gdn
+    from linear_attention_sequence_qkv_gb300.workloads import make_inputs_device
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import oracle as O
+        O.build()
+        sinp, w1, nheads = oracle_bwd_sample(w)
+        threads = max(1, min(os.cpu_count() or 1, sinp.w.Hk))   # the oracle spreads q/k heads
+        dt = run_oracle_fwd_bwd(sinp, threads)
+        cpu = {"value": w1.B * w1.T / dt * (nheads / w.Hv), "unit": "tokens/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{w1.B * w1.T} tokens x {nheads}/{w.Hv} v heads of {w.name}, oracle forward + "
+                         f"backward, {dt:.2f} s wall, scaled to all heads"}
+    build.build()
+    gdn.load()
+    dev = torch.device("cuda", 0)
+    inp = make_inputs_device(w, dev)
+    d = gdn.make_desc(inp)
+    bufs = gdn.alloc(d, dev)
+    grads = gdn.alloc_grads(d, dev)
+    B, T = inp.q_raw.shape[0], inp.q_raw.shape[1]
+    ntok = B * T
+    g = torch.Generator(device=dev).manual_seed(1)
+    gout = torch.randn((B, T, w.Hv, w.dv), generator=g, device=dev).to(inp.q_raw.dtype)
+    gfin = torch.randn((d.N, w.Hv, w.dk, w.dv), generator=g, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        gdn.forward(inp, bufs, stream)
+        if ev:
+            ev[1].record()
+        gdn.backward(inp, gout, gfin, grads, stream)
+        if ev:
+            ev[2].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status(grads.workspace) == gdn.GDN_OK
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = None if args.no_clocks else ClockSampler(None)
+    torch.cuda.synchronize()
+    for e in evs:
+        flush.zero_()
+        step(e)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms_f = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
+    ms_b = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
+    ms = ms_f + ms_b
+    pk_alu = fp32_alu_peak_tflops()
+    fl = backward_flops(w, ntok)
+    ach = fl / (ms_b / 1e3) / 1e12
+    tc = gdn.gdn_chunk_kernel_kind(d) == 1
+    # forward: prologue (+ scan), chunk stage, epilogue; backward: prologue, scan,
+    # the fp32 chunk kernel with stores, rms, chain, per-chunk, prologue and conv
+    # backward, four sums
+    scan = 1 if inp.cu_seqlens is not None else 0
+    launches = (2 + scan + (2 if tc else 1)) + (1 + scan + 1 + 3 + 2 + 4)
+
+    e2e = None
+    if not args.no_e2e:
+        names = ["q_raw", "k_raw", "v_raw", "a", "b", "gate_buf", "conv_w", "A_log", "dt_bias", "norm_w"]
+        if inp.cu_seqlens is not None:
+            names.append("cu_seqlens")
+        host = {nm: getattr(inp, nm).cpu().pin_memory() for nm in names}
+        host["grad_out"] = gout.cpu().pin_memory()
+        host["grad_final"] = gfin.cpu().pin_memory()
+        dvc = {nm: torch.empty_like(t, device=dev) for nm, t in host.items()}
+        outs = [bufs.out, grads.dq_raw, grads.dk_raw, grads.dv_raw, grads.da, grads.db, grads.dgate,
+                grads.dconv_w, grads.dA_log, grads.ddt_bias, grads.dnorm_w, grads.dinitial_state]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+
+        class Dev:
+            pass
+        di = Dev()
+        for nm in names:
+            setattr(di, nm, dvc[nm])
+        di.gate = dvc["gate_buf"][..., : w.Hv * w.dv]
+        di.cu_seqlens = dvc.get("cu_seqlens")
+        di.initial_state = None
+        di.w = w
+
+        def e2e_step():
+            for nm, t in host.items():
+                dvc[nm].copy_(t, non_blocking=True)
+            gdn.forward(di, bufs, stream)
+            gdn.backward(di, dvc["grad_out"], dvc["grad_final"], grads, stream)
+            for a_, b_ in zip(outs_h, outs):
+                a_.copy_(b_, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        k = min(args.steps, 20)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(k):
+            e2e_step()
+        t1.record()
+        torch.cuda.synchronize()
+        ms_e2e = t0.elapsed_time(t1) / k
+        e2e = {"value": ntok / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e, "steps": k,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "mode": "serial: pinned host inputs and cotangents copied in, forward + backward, "
+                       "output and every gradient copied back, per step"}
+    line = {
+        "metric": "GDN core fwd+bwd tokens/s at 1 GB300", "value": ntok / (ms / 1e3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp32": "f32", "bf16": "bf16", "fp16": "f16"}[w.dtype], "data": "synthetic",
+        "config": {"workload": f"fwd_bwd_{w.name}", "B": d.B, "T": d.T, "N": d.N, "Hk": w.Hk, "Hv": w.Hv,
+                   "dk": w.dk, "dv": w.dv, "tokens_per_step": ntok, "chunk": CHUNK,
+                   "l2": "flushed before every timed step (512 MiB write)",
+                   "fwd_ms": ms_f, "bwd_ms": ms_b, "bwd_arith": "fp32 CUDA cores"},
+        "roofline": {"bound": "alu", "achieved": ach, "peak": pk_alu, "unit": "TFLOP/s", "frac": ach / pk_alu,
+                     "algorithmic_flops": fl, "ms": ms_b, "traffic": None,
+                     "kernel": "gdn_backward (recompute, rms, chain, per-chunk, prologue, conv, sums)",
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"},
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches * args.steps, "gpu_launches_per_step": launches, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from linear_attention_sequence_qkv_gb300.workloads import WORKLOADS
@@ -300,6 +495,9 @@ def main():
         return
     if args.decode:
         decode_main(args, w)
+        return
+    if args.backward:
+        backward_main(args, w)
         return
 
     import torch

@@ -413,13 +413,9 @@ int gdn_backward(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
     p.hT = nullptr;
     p.single_stream = true;
     char *w = (char *)workspace;
-    p.bw_h0 = (float *)(w + L.h0);
-    p.bw_mats = (float *)(w + L.mats);
-    p.bw_vn = (float *)(w + L.vn);
     cudaStream_t s = (cudaStream_t)stream;
-    // the forward's prologue, then its CUDA-core chunk kernel with the backward's stores
+    // the forward's prologue (q, k, v, beta and the in-chunk decay in the workspace)
     if ((rc = run_prologue(p, s)) != GDN_OK) return rc;
-    if ((rc = cuda_status(gdn::launch_chunk_simt(p, s))) != GDN_OK) return rc;
     gdn::BwdProblem bp;
     memset(&bp, 0, sizeof(bp));
     bp.f = p;
@@ -436,10 +432,12 @@ int gdn_backward(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
     bp.ddt_bias = ddt_bias;
     bp.dnorm_w = dnorm_w;
     bp.dinit = dinitial_state;
-    bp.h0 = p.bw_h0;
-    bp.mats = p.bw_mats;
-    bp.vn = p.bw_vn;
+    bp.h0 = (float *)(w + L.h0);
+    bp.mats = (float *)(w + L.mats);
+    bp.vn = (float *)(w + L.vn);
     bp.dh1 = (float *)(w + L.dh1);
+    bp.uq = (float *)(w + L.uq);
+    bp.wv = (float *)(w + L.wv);
     bp.dO = (float *)(w + L.dO);
     bp.dR = (float *)(w + L.dR);
     bp.dq = (float *)(w + L.dq);

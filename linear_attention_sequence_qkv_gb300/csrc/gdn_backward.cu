@@ -5,13 +5,12 @@
 // "GDN Elementwise Fusion" pre- and post-GDR steps); this file computes the
 // gradient of sum(grad_out * out) + sum(grad_final * final_state) with respect
 // to every input, the RMSNorm rounding taken as the identity. The forward's
-// prologue and its CUDA-core chunk kernel run first (in gdn_api.cu) and leave,
-// per chunk slot and v head, the state at the chunk's start H0, the matrices
-// T = (I + A)^{-1}, Pm = lower(e^{gam_i - gam_j} q_i.k_j) and Ak = strict_lower(
-// e^{gam_i - gam_j} k_i.k_j), and per token the new values Vn.
+// prologue runs first (gdn_api.cu) and leaves q, k, v, beta and the in-chunk
+// cumulative decay gam in the workspace.
 //
-// Chunk form (H = S^T, dk x dv; gam the in-chunk cumulative decay, L its last
-// valid token, E_ij = e^{gam_i - gam_j}, Kd = diag(e^{gam_L - gam}) K):
+// Chunk form (H = S^T, dk x dv; L the chunk's last valid token, E_ij =
+// e^{gam_i - gam_j}, Kd = diag(e^{gam_L - gam}) K, Ak = strict_lower(E . K K^T),
+// A = diag(beta) Ak, T = (I + A)^{-1}, Pm = lower(E . Q K^T)):
 //   R0 = diag(beta)(V - diag(e^gam) K H0),  Vn = T R0,
 //   O  = scale (diag(e^gam) Q H0 + Pm Vn),  H1 = e^{gam_L} H0 + Kd^T Vn.
 // Reverse, with dO' = scale dO and dH1 the gradient of the chunk's end state:
@@ -24,13 +23,16 @@
 //   dbeta_i = dR0_i . V_i - e^{gam_i} K_i . (dR0 H0^T)_i + sum_j dA_ij Ak_ij,
 //   dgam_i from every e^{...} factor, and dg = reverse cumulative sum of dgam.
 //
-// Kernels, in launch order: rms_bwd (gated RMSNorm), chain_bwd (serial over the
-// chunks of a sequence in reverse, per dv tile: carries dH, writes dH1 and dR0),
-// chunk_grad (all chunks in parallel: dq, dk per v head, dbeta, dg),
-// prologue_bwd (L2 norm, SiLU, beta / decay), conv_bwd (the causal conv:
-// input gradients and per-block weight sums) and sum_rows (fixed-order sums of
-// the partials: dnorm_w, dconv_w, ddt_bias, dA_log). Every sum has a fixed
-// order, so results are run-to-run identical.
+// Kernels, in launch order. Serial over the chunks of a sequence (one CTA per
+// (sequence, v head, dv tile)): states (H0 of every chunk and Vn) and chain_bwd
+// (dH1 of every chunk and dR0, chunks in reverse). Everything else runs over all
+// chunks or tokens in parallel: mats (T, Pm, Ak), out (O), rms_bwd (gated
+// RMSNorm: dgate, dO'), dterms (Pm^T dO' and Q^T diag(e^gam) dO', the parts of
+// the reverse step that do not depend on dH), chunk_grad (dq, dk per v head,
+// dbeta, dg), prologue_bwd (L2 norm, SiLU, beta / decay), conv_bwd (input
+// gradients and per-block weight sums) and sum_kernel (fixed-order sums of the
+// partials: dnorm_w, dconv_w, ddt_bias, dA_log). Every sum has a fixed order,
+// so results are run-to-run identical.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -80,11 +82,10 @@ __device__ __forceinline__ void seq_of(const gdn_desc &d, const int32_t *cu, int
 
 // ------------------------------------------------------------ gated RMSNorm
 // One warp per (token, v head) row, NE columns per lane. Forward:
-// y = w * o * rstd * silu(gate). Writes dgate, dO' = scale * dL/do ([Hv][ntok][dv])
-// and the warp's partial sums of dnorm_w.
+// y = w * o * rstd * silu(gate). Reads o (fp32, [Hv][ntok][dv], from out_kernel),
+// writes dgate, dO' = scale * dL/do over o, and the warp's partial sums of dnorm_w.
 template <typename T, typename GTy, typename WT, int NE>
 __global__ void __launch_bounds__(kThreads) rms_bwd_kernel(const BwdProblem bp, int64_t rows, int64_t nwarps) {
-    using S = typename Inter<T>::S;
     const Problem &p = bp.f;
     const gdn_desc &d = p.d;
     const int dv = d.dv, Hv = d.Hv;
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) rms_bwd_kernel(const BwdProblem bp, 
         const int h = (int)(r - t * Hv);
         int64_t b, tau;
         tok_pos(d, t, b, tau);
-        const S *orow = (const S *)p.o + r * dv;
+        float *orow = bp.dO + ((int64_t)h * p.ntok + t) * dv;   // o in, dO' out (same row)
         const GTy *grow = (const GTy *)p.gate + b * d.gate_stride_b + tau * d.gate_stride_t + (int64_t)h * dv;
         const T *dyrow = (const T *)bp.grad_out + r * dv;
         float o[NE], dn[NE], nn[NE];
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) rms_bwd_kernel(const BwdProblem bp, 
 #pragma unroll
         for (int e = 0; e < NE; ++e) {
             const int c = lane + 32 * e;
-            o[e] = c < dv ? to_f<S>(orow[c]) : 0.f;
+            o[e] = c < dv ? orow[c] : 0.f;
             ss = fmaf(o[e], o[e], ss);
         }
 #pragma unroll
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) rms_bwd_kernel(const BwdProblem bp, 
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        float *drow = bp.dO + ((int64_t)h * p.ntok + t) * dv;
+        float *drow = orow;
         const float k = d.scale * rstd, m = dot / dv;
 #pragma unroll
         for (int e = 0; e < NE; ++e) {
@@ -148,21 +149,168 @@ __global__ void __launch_bounds__(kThreads) rms_bwd_kernel(const BwdProblem bp, 
     }
 }
 
-// ------------------------------------------------------------ reverse chain
-// One CTA per (sequence, v head, dv tile of NV columns), chunks in reverse.
-// Carries dH [dk][NV] in shared memory; per chunk stores dH1 (the gradient of
-// the chunk's end state) and dR0, then steps dH to the chunk's start.
+constexpr int LDK = 68;             // row of a 64-column slice (float4-aligned rows)
+constexpr int DK = 64;              // dk slice of the 4x4-tiled kernels
+
+// acc[x][y] += a[x] * b[y]
+__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float (&a)[4], const float4 b) {
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        acc[x][0] = fmaf(a[x], b.x, acc[x][0]);
+        acc[x][1] = fmaf(a[x], b.y, acc[x][1]);
+        acc[x][2] = fmaf(a[x], b.z, acc[x][2]);
+        acc[x][3] = fmaf(a[x], b.w, acc[x][3]);
+    }
+}
+__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const float4 b) {
+    const float av[4] = {a.x, a.y, a.z, a.w};
+    fma4x4(acc, av, b);
+}
+__device__ __forceinline__ void zero4x4(float (&acc)[4][4]) {
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+}
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+
+// ------------------------------------------------------------ chunk matrices
+// One CTA per (chunk slot, v head): K K^T and Q K^T over dk slices, the decay
+// masks, and T = (I + A)^{-1} by forward substitution on 16 x 16 diagonal blocks
+// then block diagonals. Writes [T, Pm, Ak] of the chunk.
+size_t mats_smem_bytes() { return sizeof(float) * (2 * kChunk * LDA + 2 * kChunk * LDS + 3 * 256); }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) mats_kernel(const BwdProblem bp) {
+    using S = typename Inter<T>::S;
+    using GT = typename Inter<T>::G;
+    __shared__ GT gam[kChunk];
+    __shared__ float bet[kChunk];
+    extern __shared__ float sm[];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, Hv = d.Hv;
+    const int j = blockIdx.y;
+    const int64_t slot = blockIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    ChunkLoc loc;
+    if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, loc)) return;
+    const int64_t tok0 = loc.tok0;
+    const int L = loc.len;
+    const int hk = j / (Hv / d.Hk);
+    float *As = sm;                           // [64][LDA]
+    float *Ts = As + kChunk * LDA;            // [64][LDA]
+    float *Ks = Ts + kChunk * LDA;            // [64][LDS]
+    float *Qs = Ks + kChunk * LDS;            // [64][LDS]
+    float *Xs = Qs + kChunk * LDS;            // [3][16][16]
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
+    const S *qq = (const S *)p.q + (int64_t)hk * p.ntok * dk;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
+    if (tid < kChunk) {
+        const int i = tid < L ? tid : L - 1;
+        gam[tid] = ((const GT *)p.gamma)[(int64_t)j * p.ntok + tok0 + i];
+        bet[tid] = tid < L ? p.beta[(int64_t)j * p.ntok + tok0 + i] : 0.f;
+    }
+    float kk[4][4], qk[4][4];
+    zero4x4(kk);
+    zero4x4(qk);
+    for (int d0 = 0; d0 < dk; d0 += DS) {
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
+            const int i = idx / DS, c = idx - i * DS;
+            const bool ok = i < L && d0 + c < dk;
+            Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
+            Qs[i * LDS + c] = ok ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
+        }
+        __syncthreads();
+        const int dn = min(DS, dk - d0);
+        for (int c = 0; c < dn; ++c) {
+            float ki[4], qi[4], kj[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                ki[a] = Ks[(ty + 16 * a) * LDS + c];
+                qi[a] = Qs[(ty + 16 * a) * LDS + c];
+                kj[a] = Ks[(tx + 16 * a) * LDS + c];
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    kk[a][b] = fmaf(ki[a], kj[b], kk[a][b]);
+                    qk[a][b] = fmaf(qi[a], kj[b], qk[a][b]);
+                }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int i = ty + 16 * a;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int m = tx + 16 * b;
+            const float dec = m <= i ? expf((float)(gam[i] - gam[m])) : 0.f;
+            const float ak = m < i ? dec * kk[a][b] : 0.f;
+            mats[kC2 + i * kChunk + m] = dec * qk[a][b];
+            mats[2 * kC2 + i * kChunk + m] = ak;
+            As[i * LDA + m] = bet[i] * ak;
+            Ts[i * LDA + m] = 0.f;
+        }
+    }
+    __syncthreads();
+    // diagonal 16 x 16 blocks: column c of block b by forward substitution
+    if (tid < kChunk) {
+        const int o0 = (tid >> 4) * 16, c = tid & 15;
+        for (int r = c; r < 16; ++r) {
+            float val = (r == c) ? 1.f : 0.f;
+            for (int m = c; m < r; ++m) val -= As[(o0 + r) * LDA + o0 + m] * Ts[(o0 + m) * LDA + o0 + c];
+            Ts[(o0 + r) * LDA + o0 + c] = val;
+        }
+    }
+    __syncthreads();
+    // block (bi, bj), bi > bj, one block diagonal at a time:
+    // T[bi][bj] = -T[bi][bi] sum_{m in blocks bj .. bi-1} A[bi][m] T[m][bj]
+    for (int dd = 1; dd < 4; ++dd) {
+        const int npairs = 4 - dd;
+        for (int e = tid; e < npairs * 256; e += kThreads) {
+            const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int bj = pr, bi = pr + dd;
+            float x = 0.f;
+            for (int m = bj * 16; m < bi * 16; ++m) x += As[(bi * 16 + r) * LDA + m] * Ts[m * LDA + bj * 16 + c];
+            Xs[pr * 256 + r * 16 + c] = x;
+        }
+        __syncthreads();
+        for (int e = tid; e < npairs * 256; e += kThreads) {
+            const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int bj = pr, bi = pr + dd;
+            float t = 0.f;
+            for (int m = 0; m < 16; ++m) t += Ts[(bi * 16 + r) * LDA + bi * 16 + m] * Xs[pr * 256 + m * 16 + c];
+            Ts[(bi * 16 + r) * LDA + bj * 16 + c] = -t;
+        }
+        __syncthreads();
+    }
+    for (int idx = tid; idx < kC2; idx += kThreads) mats[idx] = Ts[(idx / kChunk) * LDA + (idx % kChunk)];
+}
+
+// ------------------------------------------------------------ state recompute
+// One CTA of 4 * NV threads per (sequence, v head, dv tile of NV columns),
+// chunks in order: stores the state at each chunk's start and the new values
+// Vn = T diag(beta)(V - diag(e^gam) K H), then H <- e^{gam_L} H + Kd^T Vn.
+// Thread (ti, ci) owns rows ti + 16x (token tiles) or 4 ti + x (state slices)
+// and columns 4 ci + y, x, y < 4.
 template <int NV>
-size_t chain_smem_bytes(int dk) {
-    return sizeof(float) * ((size_t)dk * NV + 2 * kChunk * LDA + 2 * kChunk * LDS + 3 * kChunk * NV + kChunk) +
-           sizeof(double) * kChunk;
+size_t states_smem_bytes(int dk) {
+    return sizeof(double) * kChunk + sizeof(float) * (kChunk + (size_t)dk * NV + kChunk * LDA + kChunk * LDK + 2 * kChunk * NV);
 }
 
 template <typename T, int NV>
-__global__ void __launch_bounds__(kThreads) chain_bwd_kernel(const BwdProblem bp, int ntiles) {
+__global__ void __launch_bounds__(256) states_kernel(const BwdProblem bp, int ntiles) {
     using S = typename Inter<T>::S;
     using GT = typename Inter<T>::G;
-    constexpr int NB = NV / 16;
+    constexpr int NQ = NV / 4;
     extern __shared__ float sm[];
     const Problem &p = bp.f;
     const gdn_desc &d = p.d;
@@ -179,150 +327,429 @@ __global__ void __launch_bounds__(kThreads) chain_bwd_kernel(const BwdProblem bp
     const int nch = (int)((seq1 - seq0 + kChunk - 1) / kChunk);
     const int hk = j / (Hv / d.Hk);
     const int v0 = tile * NV;
-
     GT *gam = (GT *)sm;                        // [64]
-    float *dHs = (float *)(gam + kChunk);      // [dk][NV]
-    float *Ts = dHs + (size_t)dk * NV;         // [64][LDA]
-    float *Ps = Ts + kChunk * LDA;             // [64][LDA]
-    float *Ks = Ps + kChunk * LDA;             // [64][LDS]
-    float *Qs = Ks + kChunk * LDS;             // [64][LDS]
-    float *dOs = Qs + kChunk * LDS;            // [64][NV]
-    float *dVs = dOs + kChunk * NV;            // [64][NV]
-    float *dRs = dVs + kChunk * NV;            // [64][NV]
-    float *bet = dRs + kChunk * NV;            // [64]
-
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    float *bet = (float *)(gam + kChunk);      // [64]
+    float *Hs = bet + kChunk;                  // [dk][NV]
+    float *Ts = Hs + (size_t)dk * NV;          // [64][LDA]
+    float *Ks = Ts + kChunk * LDA;             // [64][LDK]
+    float *Vs = Ks + kChunk * LDK;             // [64][NV]  V, then R0
+    float *Vn = Vs + kChunk * NV;              // [64][NV]
+    constexpr int nt = 4 * NV;
+    const int tid = threadIdx.x;
+    const int ci = tid % NQ, ti = tid / NQ;
     const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
-    const S *qq = (const S *)p.q + (int64_t)hk * p.ntok * dk;
+    const S *vv = (const S *)p.v + (int64_t)j * p.ntok * dv;
     const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
     const GT *gw = (const GT *)p.gamma + (int64_t)j * p.ntok;
     const float *bw = p.beta + (int64_t)j * p.ntok;
     const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
-
-    for (int idx = tid; idx < dk * NV; idx += kThreads) {
+    for (int idx = tid; idx < dk * NV; idx += nt) {
         const int r = idx / NV, c = idx - r * NV;
-        dHs[idx] = bp.grad_final ? bp.grad_final[sbase + (size_t)r * dv + v0 + c] : 0.f;
+        Hs[idx] = p.h0 ? p.h0[sbase + (size_t)r * dv + v0 + c] : 0.f;
     }
-    for (int cc = nch - 1; cc >= 0; --cc) {
+    float acc[4][4], a[4];
+    for (int cc = 0; cc < nch; ++cc) {
         const int64_t tok0 = seq0 + (int64_t)cc * kChunk, slot = slot0 + cc;
         const int L = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
         __syncthreads();
-        // ---- dH1 of this chunk; T, Pm; decay, beta; dO' tile
-        float *dst = bp.dh1 + ((size_t)slot * Hv + j) * dk * dv + v0;
-        for (int idx = tid; idx < dk * NV; idx += kThreads) {
-            const int r = idx / NV, c = idx - r * NV;
-            dst[(size_t)r * dv + c] = dHs[idx];
+        float *dst = bp.h0 + ((size_t)slot * Hv + j) * dk * dv + v0;
+        for (int idx = tid; idx < dk * NQ; idx += nt) {
+            const int r = idx / NQ, q = idx - r * NQ;
+            *reinterpret_cast<float4 *>(dst + (size_t)r * dv + 4 * q) = ld4(Hs + r * NV + 4 * q);
         }
         const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
-        for (int idx = tid; idx < kC2; idx += kThreads) {
-            const int i = idx / kChunk, m = idx - i * kChunk;
-            Ts[i * LDA + m] = mats[idx];
-            Ps[i * LDA + m] = mats[kC2 + idx];
-        }
+#pragma unroll 8
+        for (int idx = tid; idx < kC2; idx += nt) Ts[(idx / kChunk) * LDA + (idx % kChunk)] = mats[idx];
         if (tid < kChunk) {
             const int i = tid < L ? tid : L - 1;
             gam[tid] = gw[tok0 + i];
             bet[tid] = tid < L ? bw[tok0 + i] : 0.f;
         }
-        for (int idx = tid; idx < kChunk * NV; idx += kThreads) {
+        for (int idx = tid; idx < kChunk * NV; idx += nt) {
             const int i = idx / NV, c = idx - i * NV;
-            dOs[idx] = i < L ? bp.dO[((size_t)j * p.ntok + tok0 + i) * dv + v0 + c] : 0.f;
+            Vs[idx] = i < L ? to_f<S>(vv[(tok0 + i) * dv + v0 + c]) : 0.f;
         }
-        __syncthreads();
-        const GT gL = gam[kChunk - 1];
-        // ---- dVn = Pm^T dO' + Kd dH1
-        float acc[4][NB];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int i = ty + 16 * a;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) acc[a][b] = 0.f;
-            for (int m = i; m < kChunk; ++m) {
-                const float pv = Ps[m * LDA + i];
-#pragma unroll
-                for (int b = 0; b < NB; ++b) acc[a][b] = fmaf(pv, dOs[m * NV + tx + 16 * b], acc[a][b]);
-            }
-        }
-        for (int d0 = 0; d0 < dk; d0 += DS) {
+        // ---- K H over dk slices
+        zero4x4(acc);
+        for (int d0 = 0; d0 < dk; d0 += DK) {
             __syncthreads();
-            for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
-                const int i = idx / DS, c = idx - i * DS;
-                const bool ok = i < L && d0 + c < dk;
-                Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) * expf((float)(gL - gam[i])) : 0.f;
+#pragma unroll 8
+            for (int idx = tid; idx < kChunk * DK; idx += nt) {
+                const int i = idx / DK, c = idx - i * DK;
+                Ks[i * LDK + c] = (i < L && d0 + c < dk) ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
             }
             __syncthreads();
-            const int dn = min(DS, dk - d0);
+            const int dn = min(DK, dk - d0);
             for (int c = 0; c < dn; ++c) {
-                float hv[NB];
 #pragma unroll
-                for (int b = 0; b < NB; ++b) hv[b] = dHs[(d0 + c) * NV + tx + 16 * b];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    const float kv = Ks[(ty + 16 * a) * LDS + c];
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) acc[a][b] = fmaf(kv, hv[b], acc[a][b]);
-                }
+                for (int x = 0; x < 4; ++x) a[x] = Ks[(ti + 16 * x) * LDK + c];
+                fma4x4(acc, a, ld4(Hs + (d0 + c) * NV + 4 * ci));
             }
         }
+        // ---- R0 = beta (V - e^gam K H)
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int x = 0; x < 4; ++x) {
+            const int i = ti + 16 * x;
+            const float eg = expf((float)gam[i]);
 #pragma unroll
-            for (int b = 0; b < NB; ++b) dVs[(ty + 16 * a) * NV + tx + 16 * b] = acc[a][b];
+            for (int y = 0; y < 4; ++y) {
+                float *v = &Vs[i * NV + 4 * ci + y];
+                *v = bet[i] * (*v - eg * acc[x][y]);
+            }
+        }
         __syncthreads();
-        // ---- dR0 = T^T dVn (stored for the per-chunk kernels)
+        // ---- Vn = T R0
+        zero4x4(acc);
+        for (int m = 0; m < kChunk; ++m) {
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int i = ty + 16 * a;
-            float r[NB];
+            for (int x = 0; x < 4; ++x) a[x] = Ts[(ti + 16 * x) * LDA + m];
+            fma4x4(acc, a, ld4(Vs + m * NV + 4 * ci));
+        }
 #pragma unroll
-            for (int b = 0; b < NB; ++b) r[b] = 0.f;
-            for (int m = i; m < kChunk; ++m) {
-                const float tv = Ts[m * LDA + i];
-#pragma unroll
-                for (int b = 0; b < NB; ++b) r[b] = fmaf(tv, dVs[m * NV + tx + 16 * b], r[b]);
+        for (int x = 0; x < 4; ++x) {
+            const int i = ti + 16 * x;
+            st4(Vn + i * NV + 4 * ci, acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+            if (i < L)
+                st4(bp.vn + ((size_t)j * p.ntok + tok0 + i) * dv + v0 + 4 * ci, acc[x][0], acc[x][1], acc[x][2],
+                    acc[x][3]);
+        }
+        // ---- H <- e^{gam_L} H + Kd^T Vn over dk slices
+        const GT gL = gam[kChunk - 1];
+        const float eL = expf((float)gL);
+        for (int d0 = 0; d0 < dk; d0 += DK) {
+            __syncthreads();
+#pragma unroll 8
+            for (int idx = tid; idx < kChunk * DK; idx += nt) {
+                const int i = idx / DK, c = idx - i * DK;
+                Ks[i * LDK + c] = (i < L && d0 + c < dk)
+                                      ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) * expf((float)(gL - gam[i]))
+                                      : 0.f;
+            }
+            __syncthreads();
+            zero4x4(acc);
+            for (int i = 0; i < kChunk; ++i) {
+                fma4x4(acc, ld4(Ks + i * LDK + 4 * ti), ld4(Vn + i * NV + 4 * ci));
             }
 #pragma unroll
-            for (int b = 0; b < NB; ++b) dRs[i * NV + tx + 16 * b] = r[b];
-            if (i < L) {
-                float *row = bp.dR + ((size_t)j * p.ntok + tok0 + i) * dv + v0;
-#pragma unroll
-                for (int b = 0; b < NB; ++b) row[tx + 16 * b] = r[b];
+            for (int x = 0; x < 4; ++x) {
+                const int r = d0 + 4 * ti + x;
+                if (r < dk) {
+                    float *h = Hs + r * NV + 4 * ci;
+                    st4(h, fmaf(eL, h[0], acc[x][0]), fmaf(eL, h[1], acc[x][1]), fmaf(eL, h[2], acc[x][2]),
+                        fmaf(eL, h[3], acc[x][3]));
+                }
             }
         }
-        // ---- dH0 = e^{gam_L} dH1 + (e^gam Q)^T dO' - (beta e^gam K)^T dR0
-        const float eL = expf((float)gL);
-        for (int d0 = 0; d0 < dk; d0 += DS) {
+    }
+}
+
+// ------------------------------------------------------------ outputs
+// One CTA per (chunk slot, v head): O = scale (diag(e^gam) Q H0 + Pm Vn) in fp32,
+// [Hv][ntok][dv] (the RMSNorm backward's input), 64 dv columns at a time.
+size_t out_smem_bytes() { return sizeof(float) * (kChunk * LDA + kChunk * LDK + 2 * kChunk * 64); }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) out_kernel(const BwdProblem bp) {
+    using S = typename Inter<T>::S;
+    using GT = typename Inter<T>::G;
+    __shared__ GT gam[kChunk];
+    extern __shared__ float sm[];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    const int j = blockIdx.y;
+    const int64_t slot = blockIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    ChunkLoc loc;
+    if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, loc)) return;
+    const int64_t tok0 = loc.tok0;
+    const int L = loc.len;
+    const int hk = j / (Hv / d.Hk);
+    float *Ps = sm;                            // [64][LDA]
+    float *Qs = Ps + kChunk * LDA;             // [64][LDK]
+    float *Hs = Qs + kChunk * LDK;             // [64][64] rows of H0, 64 columns
+    float *Vs = Hs + kChunk * 64;              // [64][64] Vn
+    const int tid = threadIdx.x, ci = tid & 15, ti = tid >> 4;
+    const S *qq = (const S *)p.q + (int64_t)hk * p.ntok * dk;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
+    const float *H0 = bp.h0 + ((size_t)slot * Hv + j) * dk * dv;
+    if (tid < kChunk) {
+        const int i = tid < L ? tid : L - 1;
+        gam[tid] = ((const GT *)p.gamma)[(int64_t)j * p.ntok + tok0 + i];
+    }
+    for (int idx = tid; idx < kC2; idx += kThreads) Ps[(idx / kChunk) * LDA + (idx % kChunk)] = mats[kC2 + idx];
+    float acc[4][4], a[4];
+    for (int c0 = 0; c0 < dv; c0 += 64) {
+        zero4x4(acc);
+        for (int d0 = 0; d0 < dk; d0 += DK) {
             __syncthreads();
-            for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
-                const int i = idx / DS, c = idx - i * DS;
-                const bool ok = i < L && d0 + c < dk;
-                const float eg = expf((float)gam[i]);
-                Qs[i * LDS + c] = ok ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) * eg : 0.f;
-                Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) * eg * bet[i] : 0.f;
+            for (int idx = tid; idx < kChunk * DK; idx += kThreads) {
+                const int i = idx / DK, c = idx - i * DK;
+                Qs[i * LDK + c] = (i < L && d0 + c < dk) ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
+                Hs[idx] = (d0 + i < dk && c0 + c < dv) ? H0[(size_t)(d0 + i) * dv + c0 + c] : 0.f;
             }
             __syncthreads();
-            const int dn = min(DS, dk - d0);
-            for (int r = ty; r < dn; r += 16) {
-                float h[NB];
+            const int dn = min(DK, dk - d0);
+            for (int c = 0; c < dn; ++c) {
 #pragma unroll
-                for (int b = 0; b < NB; ++b) h[b] = 0.f;
-                for (int i = 0; i < kChunk; ++i) {
-                    const float qv = Qs[i * LDS + r], kv = Ks[i * LDS + r];
+                for (int x = 0; x < 4; ++x) a[x] = Qs[(ti + 16 * x) * LDK + c];
+                fma4x4(acc, a, ld4(Hs + c * 64 + 4 * ci));
+            }
+        }
 #pragma unroll
-                    for (int b = 0; b < NB; ++b)
-                        h[b] = fmaf(qv, dOs[i * NV + tx + 16 * b], fmaf(-kv, dRs[i * NV + tx + 16 * b], h[b]));
-                }
+        for (int x = 0; x < 4; ++x) {
+            const float eg = expf((float)gam[ti + 16 * x]);
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    float *hp = &dHs[(d0 + r) * NV + tx + 16 * b];
-                    *hp = fmaf(eL, *hp, h[b]);
+            for (int y = 0; y < 4; ++y) acc[x][y] *= eg;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
+            const int i = idx >> 6, c = idx & 63;
+            Vs[idx] = (i < L && c0 + c < dv) ? bp.vn[((size_t)j * p.ntok + tok0 + i) * dv + c0 + c] : 0.f;
+        }
+        __syncthreads();
+        for (int m = 0; m < kChunk; ++m) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) a[x] = Ps[(ti + 16 * x) * LDA + m];
+            fma4x4(acc, a, ld4(Vs + m * 64 + 4 * ci));
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int i = ti + 16 * x;
+            if (i < L && c0 + 4 * ci < dv)
+                st4(bp.dO + ((size_t)j * p.ntok + tok0 + i) * dv + c0 + 4 * ci, d.scale * acc[x][0],
+                    d.scale * acc[x][1], d.scale * acc[x][2], d.scale * acc[x][3]);
+        }
+    }
+}
+
+// ------------------------------------------------------------ dO' terms
+// One CTA per (chunk slot, v head): the parts of the reverse step that do not
+// depend on the carried gradient, W = Pm^T dO' ([Hv][ntok][dv]) and
+// U = Q^T diag(e^gam) dO' ([slot][Hv][dk][dv]).
+size_t dterms_smem_bytes() { return sizeof(float) * (kChunk * LDA + kChunk * 64 + kChunk * LDK); }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) dterms_kernel(const BwdProblem bp) {
+    using S = typename Inter<T>::S;
+    using GT = typename Inter<T>::G;
+    __shared__ GT gam[kChunk];
+    extern __shared__ float sm[];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    const int j = blockIdx.y;
+    const int64_t slot = blockIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    ChunkLoc loc;
+    if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, loc)) return;
+    const int64_t tok0 = loc.tok0;
+    const int L = loc.len;
+    const int hk = j / (Hv / d.Hk);
+    float *Ps = sm;                            // [64][LDA]
+    float *Os = Ps + kChunk * LDA;             // [64][64] dO' tile
+    float *Qs = Os + kChunk * 64;              // [64][LDK] e^gam Q slice
+    const int tid = threadIdx.x, ci = tid & 15, ti = tid >> 4;
+    const S *qq = (const S *)p.q + (int64_t)hk * p.ntok * dk;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
+    float *U = bp.uq + ((size_t)slot * Hv + j) * dk * dv;
+    if (tid < kChunk) {
+        const int i = tid < L ? tid : L - 1;
+        gam[tid] = ((const GT *)p.gamma)[(int64_t)j * p.ntok + tok0 + i];
+    }
+    for (int idx = tid; idx < kC2; idx += kThreads) Ps[(idx / kChunk) * LDA + (idx % kChunk)] = mats[kC2 + idx];
+    float acc[4][4], a[4];
+    for (int c0 = 0; c0 < dv; c0 += 64) {
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
+            const int i = idx >> 6, c = idx & 63;
+            Os[idx] = (i < L && c0 + c < dv) ? bp.dO[((size_t)j * p.ntok + tok0 + i) * dv + c0 + c] : 0.f;
+        }
+        __syncthreads();
+        // W = Pm^T dO'
+        zero4x4(acc);
+        for (int m = 0; m < kChunk; ++m) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) a[x] = Ps[m * LDA + ti + 16 * x];
+            fma4x4(acc, a, ld4(Os + m * 64 + 4 * ci));
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int i = ti + 16 * x;
+            if (i < L && c0 + 4 * ci < dv)
+                st4(bp.wv + ((size_t)j * p.ntok + tok0 + i) * dv + c0 + 4 * ci, acc[x][0], acc[x][1], acc[x][2],
+                    acc[x][3]);
+        }
+        // U = (e^gam Q)^T dO' over dk slices
+        for (int d0 = 0; d0 < dk; d0 += DK) {
+            __syncthreads();
+            for (int idx = tid; idx < kChunk * DK; idx += kThreads) {
+                const int i = idx / DK, c = idx - i * DK;
+                Qs[i * LDK + c] = (i < L && d0 + c < dk)
+                                      ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) * expf((float)gam[i])
+                                      : 0.f;
+            }
+            __syncthreads();
+            zero4x4(acc);
+            for (int i = 0; i < kChunk; ++i) {
+                fma4x4(acc, ld4(Qs + i * LDK + 4 * ti), ld4(Os + i * 64 + 4 * ci));
+            }
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const int r = d0 + 4 * ti + x;
+                if (r < dk && c0 + 4 * ci < dv)
+                    st4(U + (size_t)r * dv + c0 + 4 * ci, acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ reverse chain
+// One CTA of 4 * NV threads per (sequence, v head, dv tile of NV columns),
+// chunks in reverse. Carries dH [dk][NV]; per chunk stores dH1 (the gradient of
+// the chunk's end state) and dR0 = T^T (W + Kd dH1), then steps
+// dH <- e^{gam_L} dH + U - (diag(beta e^gam) K)^T dR0.
+template <int NV>
+size_t chain_smem_bytes(int dk) {
+    return sizeof(double) * kChunk + sizeof(float) * (kChunk + (size_t)dk * NV + kChunk * LDA + kChunk * LDK + 2 * kChunk * NV);
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(256) chain_bwd_kernel(const BwdProblem bp, int ntiles) {
+    using S = typename Inter<T>::S;
+    using GT = typename Inter<T>::G;
+    constexpr int NQ = NV / 4;
+    extern __shared__ float sm[];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    int bid = blockIdx.x;
+    const int tile = bid % ntiles;
+    bid /= ntiles;
+    const int j = bid % Hv;
+    const int n = bid / Hv;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    const int64_t seq0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
+    const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : seq0 + d.T;
+    const int64_t slot0 = p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk);
+    const int nch = (int)((seq1 - seq0 + kChunk - 1) / kChunk);
+    const int hk = j / (Hv / d.Hk);
+    const int v0 = tile * NV;
+    GT *gam = (GT *)sm;                        // [64]
+    float *bet = (float *)(gam + kChunk);      // [64]
+    float *dHs = bet + kChunk;                 // [dk][NV]
+    float *Ts = dHs + (size_t)dk * NV;         // [64][LDA]
+    float *Ks = Ts + kChunk * LDA;             // [64][LDK]
+    float *dVs = Ks + kChunk * LDK;            // [64][NV]  W, then dVn
+    float *dRs = dVs + kChunk * NV;            // [64][NV]
+    constexpr int nt = 4 * NV;
+    const int tid = threadIdx.x;
+    const int ci = tid % NQ, ti = tid / NQ;
+    const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    const GT *gw = (const GT *)p.gamma + (int64_t)j * p.ntok;
+    const float *bw = p.beta + (int64_t)j * p.ntok;
+    const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
+    for (int idx = tid; idx < dk * NV; idx += nt) {
+        const int r = idx / NV, c = idx - r * NV;
+        dHs[idx] = bp.grad_final ? bp.grad_final[sbase + (size_t)r * dv + v0 + c] : 0.f;
+    }
+    float acc[4][4], a[4];
+    for (int cc = nch - 1; cc >= 0; --cc) {
+        const int64_t tok0 = seq0 + (int64_t)cc * kChunk, slot = slot0 + cc;
+        const int L = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
+        __syncthreads();
+        float *dst = bp.dh1 + ((size_t)slot * Hv + j) * dk * dv + v0;
+        for (int idx = tid; idx < dk * NQ; idx += nt) {
+            const int r = idx / NQ, q = idx - r * NQ;
+            *reinterpret_cast<float4 *>(dst + (size_t)r * dv + 4 * q) = ld4(dHs + r * NV + 4 * q);
+        }
+        const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
+#pragma unroll 8
+        for (int idx = tid; idx < kC2; idx += nt) Ts[(idx / kChunk) * LDA + (idx % kChunk)] = mats[idx];
+        if (tid < kChunk) {
+            const int i = tid < L ? tid : L - 1;
+            gam[tid] = gw[tok0 + i];
+            bet[tid] = tid < L ? bw[tok0 + i] : 0.f;
+        }
+        for (int idx = tid; idx < kChunk * NV; idx += nt) {
+            const int i = idx / NV, c = idx - i * NV;
+            dVs[idx] = i < L ? bp.wv[((size_t)j * p.ntok + tok0 + i) * dv + v0 + c] : 0.f;
+        }
+        // ---- dVn = W + Kd dH1
+        zero4x4(acc);
+        for (int d0 = 0; d0 < dk; d0 += DK) {
+            __syncthreads();
+#pragma unroll 8
+            for (int idx = tid; idx < kChunk * DK; idx += nt) {
+                const int i = idx / DK, c = idx - i * DK;
+                Ks[i * LDK + c] = (i < L && d0 + c < dk) ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) *
+                                                               expf((float)(gam[kChunk - 1] - gam[i]))
+                                                         : 0.f;
+            }
+            __syncthreads();
+            const int dn = min(DK, dk - d0);
+            for (int c = 0; c < dn; ++c) {
+#pragma unroll
+                for (int x = 0; x < 4; ++x) a[x] = Ks[(ti + 16 * x) * LDK + c];
+                fma4x4(acc, a, ld4(dHs + (d0 + c) * NV + 4 * ci));
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            float *v = dVs + (ti + 16 * x) * NV + 4 * ci;
+            st4(v, v[0] + acc[x][0], v[1] + acc[x][1], v[2] + acc[x][2], v[3] + acc[x][3]);
+        }
+        __syncthreads();
+        // ---- dR0 = T^T dVn
+        zero4x4(acc);
+        for (int m = 0; m < kChunk; ++m) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) a[x] = Ts[m * LDA + ti + 16 * x];
+            fma4x4(acc, a, ld4(dVs + m * NV + 4 * ci));
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int i = ti + 16 * x;
+            st4(dRs + i * NV + 4 * ci, acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+            if (i < L)
+                st4(bp.dR + ((size_t)j * p.ntok + tok0 + i) * dv + v0 + 4 * ci, acc[x][0], acc[x][1], acc[x][2],
+                    acc[x][3]);
+        }
+        // ---- dH0 = e^{gam_L} dH1 + U - (diag(beta e^gam) K)^T dR0
+        const float eL = expf((float)gam[kChunk - 1]);
+        const float *U = bp.uq + ((size_t)slot * Hv + j) * dk * dv + v0;
+        for (int d0 = 0; d0 < dk; d0 += DK) {
+            __syncthreads();
+#pragma unroll 8
+            for (int idx = tid; idx < kChunk * DK; idx += nt) {
+                const int i = idx / DK, c = idx - i * DK;
+                Ks[i * LDK + c] = (i < L && d0 + c < dk)
+                                      ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) * bet[i] * expf((float)gam[i])
+                                      : 0.f;
+            }
+            __syncthreads();
+            zero4x4(acc);
+            for (int i = 0; i < kChunk; ++i) {
+                fma4x4(acc, ld4(Ks + i * LDK + 4 * ti), ld4(dRs + i * NV + 4 * ci));
+            }
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const int r = d0 + 4 * ti + x;
+                if (r < dk) {
+                    float *h = dHs + r * NV + 4 * ci;
+                    const float4 u = ld4(U + (size_t)r * dv + 4 * ci);
+                    st4(h, fmaf(eL, h[0], u.x - acc[x][0]), fmaf(eL, h[1], u.y - acc[x][1]),
+                        fmaf(eL, h[2], u.z - acc[x][2]), fmaf(eL, h[3], u.w - acc[x][3]));
                 }
             }
         }
     }
     __syncthreads();
     if (bp.dinit) {
-        for (int idx = tid; idx < dk * NV; idx += kThreads) {
+        for (int idx = tid; idx < dk * NV; idx += nt) {
             const int r = idx / NV, c = idx - r * NV;
             bp.dinit[sbase + (size_t)r * dv + v0 + c] = dHs[idx];
         }
@@ -798,15 +1225,46 @@ cudaError_t launch_rms_w(const BwdProblem &bp, cudaStream_t s) {
     return bp.f.d.norm_w_dtype == GDN_F32 ? launch_rms<T, GTy, float>(bp, s) : launch_rms<T, GTy, T>(bp, s);
 }
 
+// the serial kernels' dv tile: 64 columns where dv allows (measured fastest at
+// the layer and long-sequence shapes; narrower tiles give more CTAs but each
+// CTA's chain is bound by its per-chunk loads and barriers, not by its work)
+int serial_tile(const gdn_desc &d) { return d.dv >= 64 ? 64 : (d.dv >= 32 ? 32 : 16); }
+
 template <typename T, int NV>
-cudaError_t launch_chain(const BwdProblem &bp, cudaStream_t s) {
+cudaError_t launch_serial(const BwdProblem &bp, bool reverse, cudaStream_t s) {
     const gdn_desc &d = bp.f.d;
     const int ntiles = d.dv / NV;
-    const size_t bytes = chain_smem_bytes<NV>(d.dk);
-    cudaError_t e = cudaFuncSetAttribute(chain_bwd_kernel<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e != cudaSuccess) return e;
     const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
-    chain_bwd_kernel<T, NV><<<(unsigned)blocks, kThreads, bytes, s>>>(bp, ntiles);
+    if (blocks == 0) return cudaSuccess;
+    cudaError_t e;
+    if (!reverse) {
+        const size_t bytes = states_smem_bytes<NV>(d.dk);
+        e = cudaFuncSetAttribute(states_kernel<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        states_kernel<T, NV><<<(unsigned)blocks, 4 * NV, bytes, s>>>(bp, ntiles);
+    } else {
+        const size_t bytes = chain_smem_bytes<NV>(d.dk);
+        e = cudaFuncSetAttribute(chain_bwd_kernel<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        chain_bwd_kernel<T, NV><<<(unsigned)blocks, 4 * NV, bytes, s>>>(bp, ntiles);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_serial_nv(const BwdProblem &bp, bool reverse, cudaStream_t s) {
+    switch (serial_tile(bp.f.d)) {
+    case 64: return launch_serial<T, 64>(bp, reverse, s);
+    case 32: return launch_serial<T, 32>(bp, reverse, s);
+    default: return launch_serial<T, 16>(bp, reverse, s);
+    }
+}
+
+template <typename K>
+cudaError_t launch_per_chunk(K kernel, size_t bytes, const BwdProblem &bp, int64_t slots, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    kernel<<<dim3((unsigned)slots, bp.f.d.Hv), kThreads, bytes, s>>>(bp);
     return cudaGetLastError();
 }
 
@@ -814,21 +1272,18 @@ template <typename T>
 cudaError_t launch_t(const BwdProblem &bp, cudaStream_t s) {
     const Problem &p = bp.f;
     const gdn_desc &d = p.d;
-    cudaError_t e = d.gate_dtype == GDN_F32 ? launch_rms_w<T, float>(bp, s) : launch_rms_w<T, T>(bp, s);
-    if (e != cudaSuccess) return e;
-    // reverse chain: the CUDA-core forward's dv tiling
-    if (d.dv >= 64 && d.dk <= 256) e = launch_chain<T, 64>(bp, s);
-    else if (d.dv >= 32) e = launch_chain<T, 32>(bp, s);
-    else e = launch_chain<T, 16>(bp, s);
-    if (e != cudaSuccess) return e;
     const int64_t slots = chunk_slots(p);
-    if (slots > 0) {
-        const size_t bytes = grad_smem_bytes();
-        e = cudaFuncSetAttribute(chunk_grad_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        if (e != cudaSuccess) return e;
-        chunk_grad_kernel<T><<<dim3((unsigned)slots, d.Hv), kThreads, bytes, s>>>(bp);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    cudaError_t e = cudaSuccess;
+    if (slots > 0 && (e = launch_per_chunk(mats_kernel<T>, mats_smem_bytes(), bp, slots, s)) != cudaSuccess) return e;
+    if ((e = launch_serial_nv<T>(bp, false, s)) != cudaSuccess) return e;
+    if (slots > 0 && (e = launch_per_chunk(out_kernel<T>, out_smem_bytes(), bp, slots, s)) != cudaSuccess) return e;
+    e = d.gate_dtype == GDN_F32 ? launch_rms_w<T, float>(bp, s) : launch_rms_w<T, T>(bp, s);
+    if (e != cudaSuccess) return e;
+    if (slots > 0 && (e = launch_per_chunk(dterms_kernel<T>, dterms_smem_bytes(), bp, slots, s)) != cudaSuccess)
+        return e;
+    if ((e = launch_serial_nv<T>(bp, true, s)) != cudaSuccess) return e;
+    if (slots > 0 && (e = launch_per_chunk(chunk_grad_kernel<T>, grad_smem_bytes(), bp, slots, s)) != cudaSuccess)
+        return e;
     const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
     if (p.ntok > 0) {
         const int pt = d.dk > 128 ? d.dk : 128;

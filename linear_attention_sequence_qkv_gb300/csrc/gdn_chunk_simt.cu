@@ -85,20 +85,9 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
         Hs[idx] = p.h0 ? p.h0[sbase + (size_t)r * dv + v0 + c] : 0.f;
     }
 
-    // chunk slot of the sequence's first chunk (backward recompute stores)
-    int64_t slot = p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk);
-    for (int64_t tok0 = seq0; tok0 < seq1; tok0 += kChunk, ++slot) {
+    for (int64_t tok0 = seq0; tok0 < seq1; tok0 += kChunk) {
         const int L = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
         __syncthreads();
-        if (p.bw_h0) {
-            float *dst = p.bw_h0 + ((size_t)slot * Hv + j) * dk * dv + v0;
-            for (int idx = tid; idx < dk * NV; idx += kThreads) {
-                const int r = idx / NV, c = idx - r * NV;
-                dst[(size_t)r * dv + c] = Hs[idx];
-            }
-        }
-        float *mats = (p.bw_mats && tile == 0) ? p.bw_mats + ((size_t)slot * Hv + j) * 3 * kChunk * kChunk
-                                               : nullptr;
         // ---- decay, beta, V tile
         if (tid < kChunk) {
             const int i = tid < L ? tid : L - 1;
@@ -164,10 +153,6 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
                 As[i * LDA + jj] = jj < i ? bet[i] * dec * kk[a][b] : 0.f;
                 Ps[i * LDA + jj] = dec * qk[a][b];
                 Ts[i * LDA + jj] = 0.f;
-                if (mats) {
-                    mats[kChunk * kChunk + i * kChunk + jj] = dec * qk[a][b];
-                    mats[2 * kChunk * kChunk + i * kChunk + jj] = jj < i ? dec * kk[a][b] : 0.f;
-                }
             }
         }
         // R = beta (V - e^gam K H) ; keep e^gam Q H in registers
@@ -217,9 +202,6 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
             }
             __syncthreads();
         }
-        if (mats)
-            for (int idx = tid; idx < kChunk * kChunk; idx += kThreads)
-                mats[idx] = Ts[(idx / kChunk) * LDA + (idx % kChunk)];
         // ---- Vn = Tm R
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
@@ -234,11 +216,6 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const Problem p, i
             }
 #pragma unroll
             for (int b = 0; b < NB; ++b) Vn[i * NV + tx + 16 * b] = acc[b];
-            if (p.bw_vn && i < L) {
-                float *vrow = p.bw_vn + ((size_t)j * p.ntok + tok0 + i) * dv + v0;
-#pragma unroll
-                for (int b = 0; b < NB; ++b) vrow[tx + 16 * b] = acc[b];
-            }
         }
         __syncthreads();
         // ---- O = e^gam Q H + P Vn

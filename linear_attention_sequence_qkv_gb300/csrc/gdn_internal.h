@@ -76,12 +76,6 @@ struct Problem {
     void *gamma;                  // float, or double for fp32 activations
     void *tpt;                    // [T; P T] tiles of the tensor-core kernels
     bool single_stream;           // no side stream (the no-allocation entry point)
-    // Backward recompute only (null in the forward; the CUDA-core chunk kernel
-    // writes them): per (chunk slot, v head) the state at the chunk's start
-    // [dk][dv] and the chunk's matrices [3][64][64] (T = (I + A)^{-1}, the
-    // masked decayed Q K^T, and the strictly lower decayed K K^T without beta);
-    // per (v head, token) the new values Vn [dv]. All fp32.
-    float *bw_h0, *bw_mats, *bw_vn;
 };
 
 // Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one
@@ -116,8 +110,10 @@ struct BwdLayout {
     Layout f;                // the forward's regions (q, k, v, beta, gamma, o, ...)
     size_t h0;               // [slot][Hv][dk][dv]  state at each chunk's start
     size_t dh1;              // [slot][Hv][dk][dv]  gradient of the state at each chunk's end
+    size_t uq;               // [slot][Hv][dk][dv]  Q^T diag(e^gam) dO' of each chunk
     size_t mats;             // [slot][Hv][3][64][64] T, decayed Q K^T, decayed K K^T
-    size_t vn, dO, dR;       // [Hv][ntok][dv]      new values, scale * dL/do, dL/d(beta (v - e^g K H))
+    size_t vn, dO, dR, wv;   // [Hv][ntok][dv]      new values; o, then scale * dL/do;
+                             //                     dL/d(beta (v - e^g K H)); Pm^T dO'
     size_t dq, dk;           // [Hv][ntok][dk]      gradients of the normalised q, k per v head
     size_t dbeta, dgam;      // [Hv][ntok]          gradients of beta and of the per-token decay g
     size_t dz;               // [ntok][ch]          gradient of the pre-activation conv output
@@ -143,10 +139,12 @@ inline BwdLayout make_bwd_layout(const gdn_desc &d) {
     size_t off = L.f.total;
     L.h0 = off;    off = align_up(off + slots * st, 256);
     L.dh1 = off;   off = align_up(off + slots * st, 256);
+    L.uq = off;    off = align_up(off + slots * st, 256);
     L.mats = off;  off = align_up(off + slots * d.Hv * 3 * 64 * 64 * 4, 256);
     L.vn = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dv * 4, 256);
     L.dO = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dv * 4, 256);
     L.dR = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dv * 4, 256);
+    L.wv = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dv * 4, 256);
     L.dq = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dk * 4, 256);
     L.dk = off;    off = align_up(off + (size_t)d.Hv * ntok * d.dk * 4, 256);
     L.dbeta = off; off = align_up(off + (size_t)d.Hv * ntok * 4, 256);
@@ -166,7 +164,7 @@ struct BwdProblem {
     void *da, *db;                      // act dtype [B*T][Hv]
     void *dgate;                        // gate dtype [B*T][Hv*dv]
     float *dconv_w, *dA_log, *ddt_bias, *dnorm_w, *dinit;
-    float *h0, *dh1, *mats, *vn, *dO, *dR, *dq, *dk, *dbeta, *dgam, *dz, *pa, *pnorm, *pconv;
+    float *h0, *dh1, *uq, *mats, *vn, *dO, *dR, *wv, *dq, *dk, *dbeta, *dgam, *dz, *pa, *pnorm, *pconv;
 };
 cudaError_t launch_backward(const BwdProblem &p, cudaStream_t s);
 
