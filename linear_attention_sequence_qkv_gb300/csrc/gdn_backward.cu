@@ -757,21 +757,22 @@ __global__ void __launch_bounds__(256) chain_bwd_kernel(const BwdProblem bp, int
 }
 
 // ------------------------------------------------------------ per-chunk gradients
-// One CTA per (chunk slot, v head). Phase A sums dPm = dO' Vn^T and dA = -dR0 Vn^T
-// over dv; phase B, per dk slice, forms dO' H0^T, dR0 H0^T and Vn dH1^T over dv
-// and the q / k gradients of the slice; phase C finishes dbeta and dg.
-constexpr int TW = 33;              // padded row of a 32-column dv tile
-constexpr int kTileV = 32;
+// One CTA per (chunk slot, v head); thread (ti, ci) owns rows 4 ti + x and
+// columns 4 ci + y of every 64 x 64 block. Phase A sums dPm = dO' Vn^T and
+// dA = -dR0 Vn^T over dv; phase B, per 64-wide dk slice, forms X1 = dO' H0^T,
+// X2 = dR0 H0^T and X3 = Vn dH1^T over dv and the q / k gradients of the
+// slice; phase C finishes dbeta and dg. dv is staged 16 columns at a time,
+// transposed (row index contiguous) so that every operand is a float4.
+constexpr int kTileV = 16;
 
-size_t grad_smem_bytes() {
-    return sizeof(double) * kChunk +
-           sizeof(float) * (5 * kChunk * LDA + 3 * kChunk * TW + 2 * DS * TW + 2 * kChunk * LDS + 5 * kChunk + 64);
-}
+size_t grad_smem_bytes() { return sizeof(float) * (4 * kChunk * LDK + 5 * kTileV * LDK); }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) chunk_grad_kernel(const BwdProblem bp) {
+__global__ void __launch_bounds__(kThreads, 2) chunk_grad_kernel(const BwdProblem bp) {
     using S = typename Inter<T>::S;
     using GT = typename Inter<T>::G;
+    __shared__ GT gam[kChunk];
+    __shared__ float bet[kChunk], eg[kChunk], ed[kChunk], dbet[kChunk], dgm[kChunk], red[64];
     extern __shared__ float sm[];
     const Problem &p = bp.f;
     const gdn_desc &d = p.d;
@@ -785,27 +786,18 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(const BwdProblem b
     const int L = loc.len;
     const int hk = j / (Hv / d.Hk);
 
-    GT *gam = (GT *)sm;                        // [64]
-    float *Ps = (float *)(gam + kChunk);       // [64][LDA] Pm
-    float *Aks = Ps + kChunk * LDA;            // [64][LDA] Ak
-    float *dPs = Aks + kChunk * LDA;           // [64][LDA] dPm, then dPm . E
-    float *dAs = dPs + kChunk * LDA;           // [64][LDA] dA, then dA . beta_i E
-    float *Gs = dAs + kChunk * LDA;            // [64][LDA] dPm . Pm + dA . A
-    float *tO = Gs + kChunk * LDA;             // [64][TW]
-    float *tR = tO + kChunk * TW;              // [64][TW]
-    float *tV = tR + kChunk * TW;              // [64][TW]
-    float *hs = tV + kChunk * TW;              // [DS][TW]
-    float *dhs = hs + DS * TW;                 // [DS][TW]
-    float *Ks = dhs + DS * TW;                 // [64][LDS]
-    float *Qs = Ks + kChunk * LDS;             // [64][LDS]
-    float *bet = Qs + kChunk * LDS;            // [64]
-    float *eg = bet + kChunk;                  // [64] e^gam
-    float *ed = eg + kChunk;                   // [64] e^{gam_L - gam}
-    float *dbet = ed + kChunk;                 // [64]
-    float *dgm = dbet + kChunk;                // [64] dL/dgam
-    float *red = dgm + kChunk;                 // [64] block reduction scratch
+    float *Ps = sm;                            // [64][LDK] Pm, then Pg = dPm . E
+    float *As = Ps + kChunk * LDK;             // [64][LDK] Ak, then F = dA . beta_i E
+    float *Ks = As + kChunk * LDK;             // [64][LDK] k slice (token rows)
+    float *Qs = Ks + kChunk * LDK;             // [64][LDK] q slice
+    float *tO = Qs + kChunk * LDK;             // [16][LDK] dO'^T tile (column c: 64 token rows)
+    float *tR = tO + kTileV * LDK;             // [16][LDK] dR0^T
+    float *tV = tR + kTileV * LDK;             // [16][LDK] Vn^T
+    float *th = tV + kTileV * LDK;             // [16][LDK] H0^T slice (column c: 64 dk rows)
+    float *tdh = th + kTileV * LDK;            // [16][LDK] dH1^T slice
+    float *Gs = tO;                            // [64][LDK] after phase A (aliases the tiles)
 
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int tid = threadIdx.x, ci = tid & 15, ti = tid >> 4;
     const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
     const S *qq = (const S *)p.q + (int64_t)hk * p.ntok * dk;
     const S *vv = (const S *)p.v + (int64_t)j * p.ntok * dv;
@@ -823,191 +815,184 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(const BwdProblem b
         bet[tid] = tid < L ? p.beta[(int64_t)j * p.ntok + tok0 + i] : 0.f;
     }
     for (int idx = tid; idx < kC2; idx += kThreads) {
-        const int i = idx / kChunk, m = idx - i * kChunk;
-        Ps[i * LDA + m] = mats[kC2 + idx];
-        Aks[i * LDA + m] = mats[2 * kC2 + idx];
+        const int i = idx >> 6, m = idx & 63;
+        Ps[i * LDK + m] = mats[kC2 + idx];
+        As[i * LDK + m] = mats[2 * kC2 + idx];
     }
     __syncthreads();
     if (tid < kChunk) {
         eg[tid] = expf((float)gam[tid]);
         ed[tid] = expf((float)(gam[kChunk - 1] - gam[tid]));
     }
-    // dv tile loader: rows i < L of dO', dR0, Vn, columns [c0, c0 + 32)
-    auto load_tiles = [&](int c0) {
+    // transposed tiles of token rows: dst[c][i] = src[i][c0 + c] (rows i < L)
+    auto load_rows_t = [&](float *dst, const float *src, int c0) {
+#pragma unroll 4
         for (int idx = tid; idx < kChunk * kTileV; idx += kThreads) {
             const int i = idx / kTileV, c = idx - i * kTileV;
-            const bool ok = i < L && c0 + c < dv;
-            tO[i * TW + c] = ok ? dOg[(int64_t)i * dv + c0 + c] : 0.f;
-            tR[i * TW + c] = ok ? dRg[(int64_t)i * dv + c0 + c] : 0.f;
-            tV[i * TW + c] = ok ? Vng[(int64_t)i * dv + c0 + c] : 0.f;
+            dst[c * LDK + i] = (i < L && c0 + c < dv) ? src[(int64_t)i * dv + c0 + c] : 0.f;
         }
     };
 
-    // ---- phase A: dPm, dA over dv; dbeta's dR0 . V term
-    float dP[4][4], dA[4][4], pb[4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        pb[a] = 0.f;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) dP[a][b] = dA[a][b] = 0.f;
-    }
+    // ---- phase A
+    float dP[4][4], dA[4][4];
+    zero4x4(dP);
+    zero4x4(dA);
+    float pb[4] = {0.f, 0.f, 0.f, 0.f};
     for (int c0 = 0; c0 < dv; c0 += kTileV) {
         __syncthreads();
-        load_tiles(c0);
+        load_rows_t(tO, dOg, c0);
+        load_rows_t(tR, dRg, c0);
+        load_rows_t(tV, Vng, c0);
         __syncthreads();
+#pragma unroll 4
         for (int c = 0; c < kTileV; ++c) {
-            float o[4], r[4], vj[4];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                o[a] = tO[(ty + 16 * a) * TW + c];
-                r[a] = tR[(ty + 16 * a) * TW + c];
-                vj[a] = tV[(tx + 16 * a) * TW + c];
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    dP[a][b] = fmaf(o[a], vj[b], dP[a][b]);
-                    dA[a][b] = fmaf(-r[a], vj[b], dA[a][b]);
-                }
+            const float4 vm = ld4(tV + c * LDK + 4 * ci);
+            fma4x4(dP, ld4(tO + c * LDK + 4 * ti), vm);
+            fma4x4(dA, ld4(tR + c * LDK + 4 * ti), vm);
         }
+        // dbeta's dR0 . V: row 4 ti + x, columns ci (16 lanes per row)
+        if (c0 + ci < dv) {
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int i = ty + 16 * a;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c = tx + 16 * h;
-                if (i < L && c0 + c < dv) pb[a] = fmaf(tR[i * TW + c], to_f<S>(vv[(tok0 + i) * dv + c0 + c]), pb[a]);
+            for (int x = 0; x < 4; ++x) {
+                const int i = 4 * ti + x;
+                if (i < L) pb[x] = fmaf(tR[ci * LDK + i], to_f<S>(vv[(tok0 + i) * dv + c0 + ci]), pb[x]);
             }
         }
     }
+    // G = dPm . Pm + dA . beta_i Ak; Pg = dPm . E; F = dA . beta_i E (dA = -dR0 Vn^T)
+    float rowG[4], rowA[4], pg[4][4], fg[4][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int i = ty + 16 * a;
+    for (int x = 0; x < 4; ++x) {
+        const int i = 4 * ti + x;
+        rowG[x] = rowA[x] = 0.f;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int m = tx + 16 * b;
-            dPs[i * LDA + m] = m <= i ? dP[a][b] : 0.f;
-            dAs[i * LDA + m] = m < i ? dA[a][b] : 0.f;
+        for (int y = 0; y < 4; ++y) {
+            const int m = 4 * ci + y;
+            const float dAv = -dA[x][y];
+            const float e = m <= i ? expf((float)(gam[i] - gam[m])) : 0.f;
+            const float pm = Ps[i * LDK + m], ak = As[i * LDK + m];
+            const float g = (m <= i ? dP[x][y] * pm : 0.f) + (m < i ? dAv * bet[i] * ak : 0.f);
+            rowG[x] += g;
+            if (m < i) rowA[x] = fmaf(dAv, ak, rowA[x]);
+            pg[x][y] = m <= i ? dP[x][y] * e : 0.f;
+            fg[x][y] = m < i ? dAv * bet[i] * e : 0.f;
+            dP[x][y] = g;   // G, kept for the column sums
         }
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) pb[a] += __shfl_xor_sync(0xffffffffu, pb[a], off);
-        if (tx == 0) dbet[i] = pb[a];
     }
-    __syncthreads();
-    // G = dPm . Pm + dA . beta_i Ak: its row sums minus column sums are dgam's
-    // share from the decay factors inside Pm and A
-    for (int idx = tid; idx < kC2; idx += kThreads) {
-        const int i = idx / kChunk, m = idx - i * kChunk;
-        Gs[i * LDA + m] = dPs[i * LDA + m] * Ps[i * LDA + m] + dAs[i * LDA + m] * bet[i] * Aks[i * LDA + m];
+    __syncthreads();   // every thread has read Pm, Ak and the tiles
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int i = 4 * ti + x;
+        st4(Ps + i * LDK + 4 * ci, pg[x][0], pg[x][1], pg[x][2], pg[x][3]);
+        st4(As + i * LDK + 4 * ci, fg[x][0], fg[x][1], fg[x][2], fg[x][3]);
+        st4(Gs + i * LDK + 4 * ci, dP[x][0], dP[x][1], dP[x][2], dP[x][3]);
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) {
+            rowG[x] += __shfl_xor_sync(0xffffffffu, rowG[x], off);
+            rowA[x] += __shfl_xor_sync(0xffffffffu, rowA[x], off);
+            pb[x] += __shfl_xor_sync(0xffffffffu, pb[x], off);
+        }
+    }
+    if (ci == 0) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            dgm[4 * ti + x] = rowG[x];
+            dbet[4 * ti + x] = pb[x] + rowA[x];
+        }
     }
     __syncthreads();
     if (tid < kChunk) {
-        const int i = tid;
-        float g = 0.f, bA = 0.f;
-        for (int m = 0; m < kChunk; ++m) {
-            g += Gs[i * LDA + m] - Gs[m * LDA + i];
-            bA = fmaf(dAs[i * LDA + m], Aks[i * LDA + m], bA);
-        }
-        dgm[i] = g;
-        dbet[i] += bA;
+        float col = 0.f;
+        for (int i = 0; i < kChunk; ++i) col += Gs[i * LDK + tid];
+        dgm[tid] -= col;
     }
-    __syncthreads();
-    for (int idx = tid; idx < kC2; idx += kThreads) {
-        const int i = idx / kChunk, m = idx - i * kChunk;
-        const float e = m <= i ? expf((float)(gam[i] - gam[m])) : 0.f;
-        dPs[i * LDA + m] *= e;
-        dAs[i * LDA + m] *= bet[i] * e;
-    }
-    // ---- phase B: per dk slice, X1 = dO' H0^T, X2 = dR0 H0^T, X3 = Vn dH1^T
-    float rg[4], rb[4], kap = 0.f, hd = 0.f;
-#pragma unroll
-    for (int a = 0; a < 4; ++a) rg[a] = rb[a] = 0.f;
+    // ---- phase B
+    float rg[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f}, kap = 0.f, hd = 0.f;
     float *dqo = bp.dq + ((size_t)j * p.ntok + tok0) * dk;
     float *dko = bp.dk + ((size_t)j * p.ntok + tok0) * dk;
-    for (int d0 = 0; d0 < dk; d0 += DS) {
-        float X1[4][2], X2[4][2], X3[4][2];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 2; ++b) X1[a][b] = X2[a][b] = X3[a][b] = 0.f;
+    for (int d0 = 0; d0 < dk; d0 += DK) {
+        float X1[4][4], X2[4][4], X3[4][4];
+        zero4x4(X1);
+        zero4x4(X2);
+        zero4x4(X3);
         for (int c0 = 0; c0 < dv; c0 += kTileV) {
             __syncthreads();
-            load_tiles(c0);
-            for (int idx = tid; idx < DS * kTileV; idx += kThreads) {
+            load_rows_t(tO, dOg, c0);
+            load_rows_t(tR, dRg, c0);
+            load_rows_t(tV, Vng, c0);
+#pragma unroll 4
+            for (int idx = tid; idx < DK * kTileV; idx += kThreads) {
                 const int r = idx / kTileV, c = idx - r * kTileV;
                 const bool ok = d0 + r < dk && c0 + c < dv;
-                hs[r * TW + c] = ok ? H0[(int64_t)(d0 + r) * dv + c0 + c] : 0.f;
-                dhs[r * TW + c] = ok ? dH1[(int64_t)(d0 + r) * dv + c0 + c] : 0.f;
+                th[c * LDK + r] = ok ? H0[(int64_t)(d0 + r) * dv + c0 + c] : 0.f;
+                tdh[c * LDK + r] = ok ? dH1[(int64_t)(d0 + r) * dv + c0 + c] : 0.f;
             }
             __syncthreads();
+#pragma unroll 4
             for (int c = 0; c < kTileV; ++c) {
-                float o[4], r[4], vn[4], h[2], dh[2];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    o[a] = tO[(ty + 16 * a) * TW + c];
-                    r[a] = tR[(ty + 16 * a) * TW + c];
-                    vn[a] = tV[(ty + 16 * a) * TW + c];
-                }
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    h[b] = hs[(tx + 16 * b) * TW + c];
-                    dh[b] = dhs[(tx + 16 * b) * TW + c];
-                }
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        X1[a][b] = fmaf(o[a], h[b], X1[a][b]);
-                        X2[a][b] = fmaf(r[a], h[b], X2[a][b]);
-                        X3[a][b] = fmaf(vn[a], dh[b], X3[a][b]);
-                    }
+                const float4 h = ld4(th + c * LDK + 4 * ci), dh = ld4(tdh + c * LDK + 4 * ci);
+                fma4x4(X1, ld4(tO + c * LDK + 4 * ti), h);
+                fma4x4(X2, ld4(tR + c * LDK + 4 * ti), h);
+                fma4x4(X3, ld4(tV + c * LDK + 4 * ti), dh);
             }
-            for (int idx = tid; idx < DS * kTileV; idx += kThreads) {
-                const int r = idx / kTileV, c = idx - r * kTileV;
-                hd = fmaf(hs[r * TW + c], dhs[r * TW + c], hd);
-            }
+            for (int idx = tid; idx < DK * kTileV; idx += kThreads) hd = fmaf(th[idx % kTileV * LDK + idx / kTileV],
+                                                                             tdh[idx % kTileV * LDK + idx / kTileV], hd);
         }
         __syncthreads();
-        for (int idx = tid; idx < kChunk * DS; idx += kThreads) {
-            const int i = idx / DS, c = idx - i * DS;
+#pragma unroll 4
+        for (int idx = tid; idx < kChunk * DK; idx += kThreads) {
+            const int i = idx / DK, c = idx - i * DK;
             const bool ok = i < L && d0 + c < dk;
-            Ks[i * LDS + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
-            Qs[i * LDS + c] = ok ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
+            Ks[i * LDK + c] = ok ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
+            Qs[i * LDK + c] = ok ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
         }
         __syncthreads();
+        // dQ = e^gam X1 + Pg K;  dK = Pg^T Q + F K + F^T K - beta e^gam X2 + e^{gam_L - gam} X3
+        float gq[4][4], gk[4][4], a[4], b[4];
+        zero4x4(gq);
+        zero4x4(gk);
+        for (int m = 0; m < kChunk; ++m) {
+            const float4 km = ld4(Ks + m * LDK + 4 * ci), qm = ld4(Qs + m * LDK + 4 * ci);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int i = ty + 16 * a;
+            for (int x = 0; x < 4; ++x) {
+                a[x] = Ps[(4 * ti + x) * LDK + m];
+                b[x] = As[(4 * ti + x) * LDK + m];
+            }
+            fma4x4(gq, a, km);
+            fma4x4(gk, b, km);
+            fma4x4(gk, ld4(Ps + m * LDK + 4 * ti), qm);
+            fma4x4(gk, ld4(As + m * LDK + 4 * ti), km);
+        }
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                const int dd = tx + 16 * b;
-                float gq = eg[i] * X1[a][b], gk = -bet[i] * eg[i] * X2[a][b] + ed[i] * X3[a][b];
-                for (int m = 0; m <= i; ++m) gq = fmaf(dPs[i * LDA + m], Ks[m * LDS + dd], gq);
-                for (int m = i; m < kChunk; ++m) gk = fmaf(dPs[m * LDA + i], Qs[m * LDS + dd], gk);
-                for (int m = 0; m < i; ++m) gk = fmaf(dAs[i * LDA + m], Ks[m * LDS + dd], gk);
-                for (int m = i + 1; m < kChunk; ++m) gk = fmaf(dAs[m * LDA + i], Ks[m * LDS + dd], gk);
-                const float qv = Qs[i * LDS + dd], kv = Ks[i * LDS + dd];
-                rg[a] += qv * eg[i] * X1[a][b] - kv * bet[i] * eg[i] * X2[a][b] - kv * ed[i] * X3[a][b];
-                kap = fmaf(kv * ed[i], X3[a][b], kap);
-                rb[a] = fmaf(-eg[i] * kv, X2[a][b], rb[a]);
-                if (i < L && d0 + dd < dk) {
-                    dqo[(int64_t)i * dk + d0 + dd] = gq;
-                    dko[(int64_t)i * dk + d0 + dd] = gk;
-                }
+        for (int x = 0; x < 4; ++x) {
+            const int i = 4 * ti + x;
+            const float be = bet[i] * eg[i];
+            float oq[4], ok[4];
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+                const int dd = 4 * ci + y;
+                const float qv = Qs[i * LDK + dd], kv = Ks[i * LDK + dd];
+                oq[y] = fmaf(eg[i], X1[x][y], gq[x][y]);
+                ok[y] = gk[x][y] - be * X2[x][y] + ed[i] * X3[x][y];
+                rg[x] += qv * eg[i] * X1[x][y] - kv * be * X2[x][y] - kv * ed[i] * X3[x][y];
+                kap = fmaf(kv * ed[i], X3[x][y], kap);
+                rb[x] = fmaf(-eg[i] * kv, X2[x][y], rb[x]);
+            }
+            if (i < L && d0 + 4 * ci < dk) {
+                st4(dqo + (int64_t)i * dk + d0 + 4 * ci, oq[0], oq[1], oq[2], oq[3]);
+                st4(dko + (int64_t)i * dk + d0 + 4 * ci, ok[0], ok[1], ok[2], ok[3]);
             }
         }
     }
     // ---- phase C: dbeta, dgam, then dg = reverse cumulative sum of dgam
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int x = 0; x < 4; ++x) {
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) {
-            rg[a] += __shfl_xor_sync(0xffffffffu, rg[a], off);
-            rb[a] += __shfl_xor_sync(0xffffffffu, rb[a], off);
+            rg[x] += __shfl_xor_sync(0xffffffffu, rg[x], off);
+            rb[x] += __shfl_xor_sync(0xffffffffu, rb[x], off);
         }
     }
-    // kappa and <H0, dH1>: fixed-order block sums
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
         kap += __shfl_xor_sync(0xffffffffu, kap, off);
@@ -1018,13 +1003,13 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(const BwdProblem b
         red[tid >> 5] = kap;
         red[32 + (tid >> 5)] = hd;
     }
+    if (ci == 0) {
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-        if (tx == 0) {
-            const int i = ty + 16 * a;
-            dgm[i] += rg[a];
-            dbet[i] += rb[a];
+        for (int x = 0; x < 4; ++x) {
+            dgm[4 * ti + x] += rg[x];
+            dbet[4 * ti + x] += rb[x];
         }
+    }
     __syncthreads();
     if (tid == 0) {
         float ks = 0.f, hs_ = 0.f;
