@@ -295,154 +295,6 @@ __global__ void __launch_bounds__(kThreads) mats_kernel(const BwdProblem bp) {
     for (int idx = tid; idx < kC2; idx += kThreads) mats[idx] = Ts[(idx / kChunk) * LDA + (idx % kChunk)];
 }
 
-// ------------------------------------------------------------ state recompute
-// One CTA of 4 * NV threads per (sequence, v head, dv tile of NV columns),
-// chunks in order: stores the state at each chunk's start and the new values
-// Vn = T diag(beta)(V - diag(e^gam) K H), then H <- e^{gam_L} H + Kd^T Vn.
-// Thread (ti, ci) owns rows ti + 16x (token tiles) or 4 ti + x (state slices)
-// and columns 4 ci + y, x, y < 4.
-template <int NV>
-size_t states_smem_bytes(int dk) {
-    return sizeof(double) * kChunk + sizeof(float) * (kChunk + (size_t)dk * NV + kChunk * LDA + kChunk * LDK + 2 * kChunk * NV);
-}
-
-template <typename T, int NV>
-__global__ void __launch_bounds__(256) states_kernel(const BwdProblem bp, int ntiles) {
-    using S = typename Inter<T>::S;
-    using GT = typename Inter<T>::G;
-    constexpr int NQ = NV / 4;
-    extern __shared__ float sm[];
-    const Problem &p = bp.f;
-    const gdn_desc &d = p.d;
-    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
-    int bid = blockIdx.x;
-    const int tile = bid % ntiles;
-    bid /= ntiles;
-    const int j = bid % Hv;
-    const int n = bid / Hv;
-    if (p.cu != nullptr && *p.status != GDN_OK) return;
-    const int64_t seq0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
-    const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : seq0 + d.T;
-    const int64_t slot0 = p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk);
-    const int nch = (int)((seq1 - seq0 + kChunk - 1) / kChunk);
-    const int hk = j / (Hv / d.Hk);
-    const int v0 = tile * NV;
-    GT *gam = (GT *)sm;                        // [64]
-    float *bet = (float *)(gam + kChunk);      // [64]
-    float *Hs = bet + kChunk;                  // [dk][NV]
-    float *Ts = Hs + (size_t)dk * NV;          // [64][LDA]
-    float *Ks = Ts + kChunk * LDA;             // [64][LDK]
-    float *Vs = Ks + kChunk * LDK;             // [64][NV]  V, then R0
-    float *Vn = Vs + kChunk * NV;              // [64][NV]
-    constexpr int nt = 4 * NV;
-    const int tid = threadIdx.x;
-    const int ci = tid % NQ, ti = tid / NQ;
-    const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
-    const S *vv = (const S *)p.v + (int64_t)j * p.ntok * dv;
-    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
-    const GT *gw = (const GT *)p.gamma + (int64_t)j * p.ntok;
-    const float *bw = p.beta + (int64_t)j * p.ntok;
-    const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
-    for (int idx = tid; idx < dk * NV; idx += nt) {
-        const int r = idx / NV, c = idx - r * NV;
-        Hs[idx] = p.h0 ? p.h0[sbase + (size_t)r * dv + v0 + c] : 0.f;
-    }
-    float acc[4][4], a[4];
-    for (int cc = 0; cc < nch; ++cc) {
-        const int64_t tok0 = seq0 + (int64_t)cc * kChunk, slot = slot0 + cc;
-        const int L = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
-        __syncthreads();
-        float *dst = bp.h0 + ((size_t)slot * Hv + j) * dk * dv + v0;
-        for (int idx = tid; idx < dk * NQ; idx += nt) {
-            const int r = idx / NQ, q = idx - r * NQ;
-            *reinterpret_cast<float4 *>(dst + (size_t)r * dv + 4 * q) = ld4(Hs + r * NV + 4 * q);
-        }
-        const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
-#pragma unroll 8
-        for (int idx = tid; idx < kC2; idx += nt) Ts[(idx / kChunk) * LDA + (idx % kChunk)] = mats[idx];
-        if (tid < kChunk) {
-            const int i = tid < L ? tid : L - 1;
-            gam[tid] = gw[tok0 + i];
-            bet[tid] = tid < L ? bw[tok0 + i] : 0.f;
-        }
-        for (int idx = tid; idx < kChunk * NV; idx += nt) {
-            const int i = idx / NV, c = idx - i * NV;
-            Vs[idx] = i < L ? to_f<S>(vv[(tok0 + i) * dv + v0 + c]) : 0.f;
-        }
-        // ---- K H over dk slices
-        zero4x4(acc);
-        for (int d0 = 0; d0 < dk; d0 += DK) {
-            __syncthreads();
-#pragma unroll 8
-            for (int idx = tid; idx < kChunk * DK; idx += nt) {
-                const int i = idx / DK, c = idx - i * DK;
-                Ks[i * LDK + c] = (i < L && d0 + c < dk) ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
-            }
-            __syncthreads();
-            const int dn = min(DK, dk - d0);
-            for (int c = 0; c < dn; ++c) {
-#pragma unroll
-                for (int x = 0; x < 4; ++x) a[x] = Ks[(ti + 16 * x) * LDK + c];
-                fma4x4(acc, a, ld4(Hs + (d0 + c) * NV + 4 * ci));
-            }
-        }
-        // ---- R0 = beta (V - e^gam K H)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const int i = ti + 16 * x;
-            const float eg = expf((float)gam[i]);
-#pragma unroll
-            for (int y = 0; y < 4; ++y) {
-                float *v = &Vs[i * NV + 4 * ci + y];
-                *v = bet[i] * (*v - eg * acc[x][y]);
-            }
-        }
-        __syncthreads();
-        // ---- Vn = T R0
-        zero4x4(acc);
-        for (int m = 0; m < kChunk; ++m) {
-#pragma unroll
-            for (int x = 0; x < 4; ++x) a[x] = Ts[(ti + 16 * x) * LDA + m];
-            fma4x4(acc, a, ld4(Vs + m * NV + 4 * ci));
-        }
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const int i = ti + 16 * x;
-            st4(Vn + i * NV + 4 * ci, acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
-            if (i < L)
-                st4(bp.vn + ((size_t)j * p.ntok + tok0 + i) * dv + v0 + 4 * ci, acc[x][0], acc[x][1], acc[x][2],
-                    acc[x][3]);
-        }
-        // ---- H <- e^{gam_L} H + Kd^T Vn over dk slices
-        const GT gL = gam[kChunk - 1];
-        const float eL = expf((float)gL);
-        for (int d0 = 0; d0 < dk; d0 += DK) {
-            __syncthreads();
-#pragma unroll 8
-            for (int idx = tid; idx < kChunk * DK; idx += nt) {
-                const int i = idx / DK, c = idx - i * DK;
-                Ks[i * LDK + c] = (i < L && d0 + c < dk)
-                                      ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) * expf((float)(gL - gam[i]))
-                                      : 0.f;
-            }
-            __syncthreads();
-            zero4x4(acc);
-            for (int i = 0; i < kChunk; ++i) {
-                fma4x4(acc, ld4(Ks + i * LDK + 4 * ti), ld4(Vn + i * NV + 4 * ci));
-            }
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const int r = d0 + 4 * ti + x;
-                if (r < dk) {
-                    float *h = Hs + r * NV + 4 * ci;
-                    st4(h, fmaf(eL, h[0], acc[x][0]), fmaf(eL, h[1], acc[x][1]), fmaf(eL, h[2], acc[x][2]),
-                        fmaf(eL, h[3], acc[x][3]));
-                }
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------ outputs
 // One CTA per (chunk slot, v head): O = scale (diag(e^gam) Q H0 + Pm Vn) in fp32,
 // [Hv][ntok][dv] (the RMSNorm backward's input), 64 dv columns at a time.
@@ -606,25 +458,69 @@ __global__ void __launch_bounds__(kThreads) dterms_kernel(const BwdProblem bp) {
     }
 }
 
-// ------------------------------------------------------------ reverse chain
-// One CTA of 4 * NV threads per (sequence, v head, dv tile of NV columns),
-// chunks in reverse. Carries dH [dk][NV]; per chunk stores dH1 (the gradient of
-// the chunk's end state) and dR0 = T^T (W + Kd dH1), then steps
-// dH <- e^{gam_L} dH + U - (diag(beta e^gam) K)^T dR0.
+// ------------------------------------------------------------ serial kernels
+// One CTA of 4 * NV threads per (sequence, v head, dv tile of NV columns).
+// Each chunk step loads the chunk's K block once (64 x dk, fp32 in shared
+// memory, every load of a thread in flight together) and folds the per-row
+// decay factors into the accumulators or the other operand. Thread (ti, ci)
+// owns rows ti + 16x of token tiles, rows 64s + 4ti + x of the state, and
+// columns 4ci + y, x, y < 4.
 template <int NV>
-size_t chain_smem_bytes(int dk) {
-    return sizeof(double) * kChunk + sizeof(float) * (kChunk + (size_t)dk * NV + kChunk * LDA + kChunk * LDK + 2 * kChunk * NV);
+size_t serial_smem_bytes(int dk) {
+    return sizeof(double) * kChunk +
+           sizeof(float) * (2 * kChunk + (size_t)dk * NV + kChunk * LDA + (size_t)kChunk * (dk + 4) + 2 * kChunk * NV);
 }
 
+// Kc[i][d] = k of token i (rows i < L, zeros after), fp32, row length dk + 4
+template <typename S, int NT>
+__device__ __forceinline__ void load_k_block(float *Kc, const S *kq, int64_t tok0, int L, int dk, int64_t plane,
+                                             int tid) {
+    const int ldk = dk + 4;
+    if (sizeof(S) == 2) {
+        const int groups = kChunk * dk / 8;            // 8 halves = 16 bytes per plane
+#pragma unroll 8
+        for (int g = tid; g < groups; g += NT) {
+            const int i = g / (dk / 8), c = (g - i * (dk / 8)) * 8;
+            float v[8];
+            if (i < L) {
+                const int64_t e = (tok0 + i) * dk + c;
+                const uint4 hi = *reinterpret_cast<const uint4 *>(kq + e);
+                const uint4 lo = *reinterpret_cast<const uint4 *>(kq + e + plane);
+                float h[8], l[8];
+                unpack16<S>(hi, h);
+                unpack16<S>(lo, l);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = h[u] + l[u];
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = 0.f;
+            }
+            st4(Kc + i * ldk + c, v[0], v[1], v[2], v[3]);
+            st4(Kc + i * ldk + c + 4, v[4], v[5], v[6], v[7]);
+        }
+    } else {
+        const int groups = kChunk * dk / 4;
+#pragma unroll 8
+        for (int g = tid; g < groups; g += NT) {
+            const int i = g / (dk / 4), c = (g - i * (dk / 4)) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < L) v = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(kq) + (tok0 + i) * dk + c);
+            *reinterpret_cast<float4 *>(Kc + i * ldk + c) = v;
+        }
+    }
+}
+
+// Forward recompute: per chunk store H0, Vn = T diag(beta)(V - diag(e^gam) K H0)
+// (to the workspace), then H <- e^{gam_L} H + K^T (diag(e^{gam_L - gam}) Vn).
 template <typename T, int NV>
-__global__ void __launch_bounds__(256) chain_bwd_kernel(const BwdProblem bp, int ntiles) {
+__global__ void __launch_bounds__(256) states_kernel(const BwdProblem bp, int ntiles) {
     using S = typename Inter<T>::S;
     using GT = typename Inter<T>::G;
-    constexpr int NQ = NV / 4;
+    constexpr int NQ = NV / 4, NT = 4 * NV;
     extern __shared__ float sm[];
     const Problem &p = bp.f;
     const gdn_desc &d = p.d;
-    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv, ldk = dk + 4;
     int bid = blockIdx.x;
     const int tile = bid % ntiles;
     bid /= ntiles;
@@ -639,20 +535,148 @@ __global__ void __launch_bounds__(256) chain_bwd_kernel(const BwdProblem bp, int
     const int v0 = tile * NV;
     GT *gam = (GT *)sm;                        // [64]
     float *bet = (float *)(gam + kChunk);      // [64]
-    float *dHs = bet + kChunk;                 // [dk][NV]
+    float *dec = bet + kChunk;                 // [64] e^{gam_L - gam}
+    float *Hs = dec + kChunk;                  // [dk][NV]
+    float *Ts = Hs + (size_t)dk * NV;          // [64][LDA]
+    float *Kc = Ts + kChunk * LDA;             // [64][dk + 4]
+    float *Vs = Kc + (size_t)kChunk * ldk;     // [64][NV]  V, then R0
+    float *Vn = Vs + kChunk * NV;              // [64][NV]  e^{gam_L - gam} Vn
+    const int tid = threadIdx.x, ci = tid % NQ, ti = tid / NQ;
+    const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
+    const S *vv = (const S *)p.v + (int64_t)j * p.ntok * dv;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    const GT *gw = (const GT *)p.gamma + (int64_t)j * p.ntok;
+    const float *bw = p.beta + (int64_t)j * p.ntok;
+    const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
+    for (int idx = tid; idx < dk * NV; idx += NT) {
+        const int r = idx / NV, c = idx - r * NV;
+        Hs[idx] = p.h0 ? p.h0[sbase + (size_t)r * dv + v0 + c] : 0.f;
+    }
+    float acc[4][4], a[4];
+    for (int cc = 0; cc < nch; ++cc) {
+        const int64_t tok0 = seq0 + (int64_t)cc * kChunk, slot = slot0 + cc;
+        const int L = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
+        __syncthreads();
+        float *dst = bp.h0 + ((size_t)slot * Hv + j) * dk * dv + v0;
+        for (int idx = tid; idx < dk * NQ; idx += NT) {
+            const int r = idx / NQ, q = idx - r * NQ;
+            *reinterpret_cast<float4 *>(dst + (size_t)r * dv + 4 * q) = ld4(Hs + r * NV + 4 * q);
+        }
+        load_k_block<S, NT>(Kc, kq, tok0, L, dk, plane, tid);
+        const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
+#pragma unroll 4
+        for (int q = tid; q < kC2 / 4; q += NT) {
+            const float4 t4 = ld4(mats + 4 * q);
+            const int i = q / (kChunk / 4), m = (q - i * (kChunk / 4)) * 4;
+            Ts[i * LDA + m] = t4.x;
+            Ts[i * LDA + m + 1] = t4.y;
+            Ts[i * LDA + m + 2] = t4.z;
+            Ts[i * LDA + m + 3] = t4.w;
+        }
+        if (tid < kChunk) {
+            const int i = tid < L ? tid : L - 1;
+            gam[tid] = gw[tok0 + i];
+            bet[tid] = tid < L ? bw[tok0 + i] : 0.f;
+        }
+#pragma unroll 4
+        for (int idx = tid; idx < kChunk * NV; idx += NT) {
+            const int i = idx / NV, c = idx - i * NV;
+            Vs[idx] = i < L ? to_f<S>(vv[(tok0 + i) * dv + v0 + c]) : 0.f;
+        }
+        __syncthreads();
+        if (tid < kChunk) dec[tid] = expf((float)(gam[kChunk - 1] - gam[tid]));
+        // ---- K H
+        zero4x4(acc);
+        for (int c = 0; c < dk; ++c) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) a[x] = Kc[(ti + 16 * x) * ldk + c];
+            fma4x4(acc, a, ld4(Hs + c * NV + 4 * ci));
+        }
+        // ---- R0 = beta (V - e^gam K H)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int i = ti + 16 * x;
+            const float eg = expf((float)gam[i]);
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+                float *v = &Vs[i * NV + 4 * ci + y];
+                *v = bet[i] * (*v - eg * acc[x][y]);
+            }
+        }
+        __syncthreads();
+        // ---- Vn = T R0 (stored; kept scaled by e^{gam_L - gam} for the state step)
+        zero4x4(acc);
+        for (int m = 0; m < kChunk; ++m) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) a[x] = Ts[(ti + 16 * x) * LDA + m];
+            fma4x4(acc, a, ld4(Vs + m * NV + 4 * ci));
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int i = ti + 16 * x;
+            const float s = dec[i];
+            st4(Vn + i * NV + 4 * ci, s * acc[x][0], s * acc[x][1], s * acc[x][2], s * acc[x][3]);
+            if (i < L)
+                st4(bp.vn + ((size_t)j * p.ntok + tok0 + i) * dv + v0 + 4 * ci, acc[x][0], acc[x][1], acc[x][2],
+                    acc[x][3]);
+        }
+        __syncthreads();
+        // ---- H <- e^{gam_L} H + K^T (e^{gam_L - gam} Vn)
+        const float eL = expf((float)gam[kChunk - 1]);
+        for (int r0 = 0; r0 < dk; r0 += 64) {
+            zero4x4(acc);
+            if (r0 + 4 * ti < dk) {
+                for (int i = 0; i < kChunk; ++i) fma4x4(acc, ld4(Kc + i * ldk + r0 + 4 * ti), ld4(Vn + i * NV + 4 * ci));
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    float *h = Hs + (r0 + 4 * ti + x) * NV + 4 * ci;
+                    st4(h, fmaf(eL, h[0], acc[x][0]), fmaf(eL, h[1], acc[x][1]), fmaf(eL, h[2], acc[x][2]),
+                        fmaf(eL, h[3], acc[x][3]));
+                }
+            }
+        }
+    }
+}
+
+// Reverse chain: chunks in reverse, carrying dH [dk][NV]; per chunk store dH1,
+// dR0 = T^T (W + diag(e^{gam_L - gam}) K dH1) (to the workspace), then
+// dH <- e^{gam_L} dH + U - K^T (diag(beta e^gam) dR0).
+template <typename T, int NV>
+__global__ void __launch_bounds__(256) chain_bwd_kernel(const BwdProblem bp, int ntiles) {
+    using S = typename Inter<T>::S;
+    using GT = typename Inter<T>::G;
+    constexpr int NQ = NV / 4, NT = 4 * NV;
+    extern __shared__ float sm[];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv, ldk = dk + 4;
+    int bid = blockIdx.x;
+    const int tile = bid % ntiles;
+    bid /= ntiles;
+    const int j = bid % Hv;
+    const int n = bid / Hv;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    const int64_t seq0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
+    const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : seq0 + d.T;
+    const int64_t slot0 = p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk);
+    const int nch = (int)((seq1 - seq0 + kChunk - 1) / kChunk);
+    const int hk = j / (Hv / d.Hk);
+    const int v0 = tile * NV;
+    GT *gam = (GT *)sm;                        // [64]
+    float *bet = (float *)(gam + kChunk);      // [64]
+    float *dec = bet + kChunk;                 // [64] e^{gam_L - gam}
+    float *dHs = dec + kChunk;                 // [dk][NV]
     float *Ts = dHs + (size_t)dk * NV;         // [64][LDA]
-    float *Ks = Ts + kChunk * LDA;             // [64][LDK]
-    float *dVs = Ks + kChunk * LDK;            // [64][NV]  W, then dVn
-    float *dRs = dVs + kChunk * NV;            // [64][NV]
-    constexpr int nt = 4 * NV;
-    const int tid = threadIdx.x;
-    const int ci = tid % NQ, ti = tid / NQ;
+    float *Kc = Ts + kChunk * LDA;             // [64][dk + 4]
+    float *dVs = Kc + (size_t)kChunk * ldk;    // [64][NV]  W, then dVn
+    float *dRs = dVs + kChunk * NV;            // [64][NV]  beta e^gam dR0
+    const int tid = threadIdx.x, ci = tid % NQ, ti = tid / NQ;
     const S *kq = (const S *)p.k + (int64_t)hk * p.ntok * dk;
     const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
     const GT *gw = (const GT *)p.gamma + (int64_t)j * p.ntok;
     const float *bw = p.beta + (int64_t)j * p.ntok;
     const size_t sbase = ((size_t)n * Hv + j) * dk * dv;
-    for (int idx = tid; idx < dk * NV; idx += nt) {
+    for (int idx = tid; idx < dk * NV; idx += NT) {
         const int r = idx / NV, c = idx - r * NV;
         dHs[idx] = bp.grad_final ? bp.grad_final[sbase + (size_t)r * dv + v0 + c] : 0.f;
     }
@@ -662,48 +686,52 @@ __global__ void __launch_bounds__(256) chain_bwd_kernel(const BwdProblem bp, int
         const int L = (seq1 - tok0) < kChunk ? (int)(seq1 - tok0) : kChunk;
         __syncthreads();
         float *dst = bp.dh1 + ((size_t)slot * Hv + j) * dk * dv + v0;
-        for (int idx = tid; idx < dk * NQ; idx += nt) {
+        for (int idx = tid; idx < dk * NQ; idx += NT) {
             const int r = idx / NQ, q = idx - r * NQ;
             *reinterpret_cast<float4 *>(dst + (size_t)r * dv + 4 * q) = ld4(dHs + r * NV + 4 * q);
         }
+        load_k_block<S, NT>(Kc, kq, tok0, L, dk, plane, tid);
         const float *mats = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2;
-#pragma unroll 8
-        for (int idx = tid; idx < kC2; idx += nt) Ts[(idx / kChunk) * LDA + (idx % kChunk)] = mats[idx];
+#pragma unroll 4
+        for (int q = tid; q < kC2 / 4; q += NT) {
+            const float4 t4 = ld4(mats + 4 * q);
+            const int i = q / (kChunk / 4), m = (q - i * (kChunk / 4)) * 4;
+            Ts[i * LDA + m] = t4.x;
+            Ts[i * LDA + m + 1] = t4.y;
+            Ts[i * LDA + m + 2] = t4.z;
+            Ts[i * LDA + m + 3] = t4.w;
+        }
         if (tid < kChunk) {
             const int i = tid < L ? tid : L - 1;
             gam[tid] = gw[tok0 + i];
             bet[tid] = tid < L ? bw[tok0 + i] : 0.f;
         }
-        for (int idx = tid; idx < kChunk * NV; idx += nt) {
-            const int i = idx / NV, c = idx - i * NV;
-            dVs[idx] = i < L ? bp.wv[((size_t)j * p.ntok + tok0 + i) * dv + v0 + c] : 0.f;
+#pragma unroll 4
+        for (int q = tid; q < kChunk * NQ; q += NT) {
+            const int i = q / NQ, c = (q - i * NQ) * 4;
+            const float4 w4 = i < L ? ld4(bp.wv + ((size_t)j * p.ntok + tok0 + i) * dv + v0 + c)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4 *>(dVs + i * NV + c) = w4;
         }
-        // ---- dVn = W + Kd dH1
+        __syncthreads();
+        if (tid < kChunk) dec[tid] = expf((float)(gam[kChunk - 1] - gam[tid]));
+        __syncthreads();
+        // ---- dVn = W + diag(e^{gam_L - gam}) K dH1
         zero4x4(acc);
-        for (int d0 = 0; d0 < dk; d0 += DK) {
-            __syncthreads();
-#pragma unroll 8
-            for (int idx = tid; idx < kChunk * DK; idx += nt) {
-                const int i = idx / DK, c = idx - i * DK;
-                Ks[i * LDK + c] = (i < L && d0 + c < dk) ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) *
-                                                               expf((float)(gam[kChunk - 1] - gam[i]))
-                                                         : 0.f;
-            }
-            __syncthreads();
-            const int dn = min(DK, dk - d0);
-            for (int c = 0; c < dn; ++c) {
+        for (int c = 0; c < dk; ++c) {
 #pragma unroll
-                for (int x = 0; x < 4; ++x) a[x] = Ks[(ti + 16 * x) * LDK + c];
-                fma4x4(acc, a, ld4(dHs + (d0 + c) * NV + 4 * ci));
-            }
+            for (int x = 0; x < 4; ++x) a[x] = Kc[(ti + 16 * x) * ldk + c];
+            fma4x4(acc, a, ld4(dHs + c * NV + 4 * ci));
         }
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
+            const float s = dec[ti + 16 * x];
             float *v = dVs + (ti + 16 * x) * NV + 4 * ci;
-            st4(v, v[0] + acc[x][0], v[1] + acc[x][1], v[2] + acc[x][2], v[3] + acc[x][3]);
+            st4(v, fmaf(s, acc[x][0], v[0]), fmaf(s, acc[x][1], v[1]), fmaf(s, acc[x][2], v[2]),
+                fmaf(s, acc[x][3], v[3]));
         }
         __syncthreads();
-        // ---- dR0 = T^T dVn
+        // ---- dR0 = T^T dVn (stored), kept scaled by beta e^gam for the state step
         zero4x4(acc);
         for (int m = 0; m < kChunk; ++m) {
 #pragma unroll
@@ -713,43 +741,35 @@ __global__ void __launch_bounds__(256) chain_bwd_kernel(const BwdProblem bp, int
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
             const int i = ti + 16 * x;
-            st4(dRs + i * NV + 4 * ci, acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+            const float s = bet[i] * expf((float)gam[i]);
+            st4(dRs + i * NV + 4 * ci, s * acc[x][0], s * acc[x][1], s * acc[x][2], s * acc[x][3]);
             if (i < L)
                 st4(bp.dR + ((size_t)j * p.ntok + tok0 + i) * dv + v0 + 4 * ci, acc[x][0], acc[x][1], acc[x][2],
                     acc[x][3]);
         }
-        // ---- dH0 = e^{gam_L} dH1 + U - (diag(beta e^gam) K)^T dR0
+        __syncthreads();
+        // ---- dH0 = e^{gam_L} dH1 + U - K^T (beta e^gam dR0)
         const float eL = expf((float)gam[kChunk - 1]);
         const float *U = bp.uq + ((size_t)slot * Hv + j) * dk * dv + v0;
-        for (int d0 = 0; d0 < dk; d0 += DK) {
-            __syncthreads();
-#pragma unroll 8
-            for (int idx = tid; idx < kChunk * DK; idx += nt) {
-                const int i = idx / DK, c = idx - i * DK;
-                Ks[i * LDK + c] = (i < L && d0 + c < dk)
-                                      ? load_qk(kq, (tok0 + i) * dk + d0 + c, plane) * bet[i] * expf((float)gam[i])
-                                      : 0.f;
-            }
-            __syncthreads();
-            zero4x4(acc);
-            for (int i = 0; i < kChunk; ++i) {
-                fma4x4(acc, ld4(Ks + i * LDK + 4 * ti), ld4(dRs + i * NV + 4 * ci));
-            }
+        for (int r0 = 0; r0 < dk; r0 += 64) {
+            if (r0 + 4 * ti < dk) {
+                float4 u[4];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const int r = d0 + 4 * ti + x;
-                if (r < dk) {
-                    float *h = dHs + r * NV + 4 * ci;
-                    const float4 u = ld4(U + (size_t)r * dv + 4 * ci);
-                    st4(h, fmaf(eL, h[0], u.x - acc[x][0]), fmaf(eL, h[1], u.y - acc[x][1]),
-                        fmaf(eL, h[2], u.z - acc[x][2]), fmaf(eL, h[3], u.w - acc[x][3]));
+                for (int x = 0; x < 4; ++x) u[x] = ld4(U + (size_t)(r0 + 4 * ti + x) * dv + 4 * ci);
+                zero4x4(acc);
+                for (int i = 0; i < kChunk; ++i) fma4x4(acc, ld4(Kc + i * ldk + r0 + 4 * ti), ld4(dRs + i * NV + 4 * ci));
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    float *h = dHs + (r0 + 4 * ti + x) * NV + 4 * ci;
+                    st4(h, fmaf(eL, h[0], u[x].x - acc[x][0]), fmaf(eL, h[1], u[x].y - acc[x][1]),
+                        fmaf(eL, h[2], u[x].z - acc[x][2]), fmaf(eL, h[3], u[x].w - acc[x][3]));
                 }
             }
         }
     }
     __syncthreads();
     if (bp.dinit) {
-        for (int idx = tid; idx < dk * NV; idx += nt) {
+        for (int idx = tid; idx < dk * NV; idx += NT) {
             const int r = idx / NV, c = idx - r * NV;
             bp.dinit[sbase + (size_t)r * dv + v0 + c] = dHs[idx];
         }
@@ -1210,10 +1230,15 @@ cudaError_t launch_rms_w(const BwdProblem &bp, cudaStream_t s) {
     return bp.f.d.norm_w_dtype == GDN_F32 ? launch_rms<T, GTy, float>(bp, s) : launch_rms<T, GTy, T>(bp, s);
 }
 
-// the serial kernels' dv tile: 64 columns where dv allows (measured fastest at
-// the layer and long-sequence shapes; narrower tiles give more CTAs but each
-// CTA's chain is bound by its per-chunk loads and barriers, not by its work)
-int serial_tile(const gdn_desc &d) { return d.dv >= 64 ? 64 : (d.dv >= 32 ? 32 : 16); }
+// the serial kernels' dv tile: the widest of 64 / 32 / 16 columns within dv
+// whose shared memory fits a CTA (measured fastest at the layer and
+// long-sequence shapes: narrower tiles give more CTAs, but each CTA's chain is
+// bound by its per-chunk loads and barriers rather than by its work)
+int serial_tile(const gdn_desc &d) {
+    if (d.dv >= 64 && serial_smem_bytes<64>(d.dk) <= 227 * 1024) return 64;
+    if (d.dv >= 32 && serial_smem_bytes<32>(d.dk) <= 227 * 1024) return 32;
+    return 16;
+}
 
 template <typename T, int NV>
 cudaError_t launch_serial(const BwdProblem &bp, bool reverse, cudaStream_t s) {
@@ -1223,12 +1248,12 @@ cudaError_t launch_serial(const BwdProblem &bp, bool reverse, cudaStream_t s) {
     if (blocks == 0) return cudaSuccess;
     cudaError_t e;
     if (!reverse) {
-        const size_t bytes = states_smem_bytes<NV>(d.dk);
+        const size_t bytes = serial_smem_bytes<NV>(d.dk);
         e = cudaFuncSetAttribute(states_kernel<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
         if (e != cudaSuccess) return e;
         states_kernel<T, NV><<<(unsigned)blocks, 4 * NV, bytes, s>>>(bp, ntiles);
     } else {
-        const size_t bytes = chain_smem_bytes<NV>(d.dk);
+        const size_t bytes = serial_smem_bytes<NV>(d.dk);
         e = cudaFuncSetAttribute(chain_bwd_kernel<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
         if (e != cudaSuccess) return e;
         chain_bwd_kernel<T, NV><<<(unsigned)blocks, 4 * NV, bytes, s>>>(bp, ntiles);
