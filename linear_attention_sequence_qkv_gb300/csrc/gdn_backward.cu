@@ -330,12 +330,14 @@ __global__ void __launch_bounds__(kThreads) out_kernel(const BwdProblem bp) {
         const int i = tid < L ? tid : L - 1;
         gam[tid] = ((const GT *)p.gamma)[(int64_t)j * p.ntok + tok0 + i];
     }
+#pragma unroll 8
     for (int idx = tid; idx < kC2; idx += kThreads) Ps[(idx / kChunk) * LDA + (idx % kChunk)] = mats[kC2 + idx];
     float acc[4][4], a[4];
     for (int c0 = 0; c0 < dv; c0 += 64) {
         zero4x4(acc);
         for (int d0 = 0; d0 < dk; d0 += DK) {
             __syncthreads();
+#pragma unroll 8
             for (int idx = tid; idx < kChunk * DK; idx += kThreads) {
                 const int i = idx / DK, c = idx - i * DK;
                 Qs[i * LDK + c] = (i < L && d0 + c < dk) ? load_qk(qq, (tok0 + i) * dk + d0 + c, plane) : 0.f;
@@ -356,6 +358,7 @@ __global__ void __launch_bounds__(kThreads) out_kernel(const BwdProblem bp) {
             for (int y = 0; y < 4; ++y) acc[x][y] *= eg;
         }
         __syncthreads();
+#pragma unroll 8
         for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
             const int i = idx >> 6, c = idx & 63;
             Vs[idx] = (i < L && c0 + c < dv) ? bp.vn[((size_t)j * p.ntok + tok0 + i) * dv + c0 + c] : 0.f;
@@ -411,10 +414,12 @@ __global__ void __launch_bounds__(kThreads) dterms_kernel(const BwdProblem bp) {
         const int i = tid < L ? tid : L - 1;
         gam[tid] = ((const GT *)p.gamma)[(int64_t)j * p.ntok + tok0 + i];
     }
+#pragma unroll 8
     for (int idx = tid; idx < kC2; idx += kThreads) Ps[(idx / kChunk) * LDA + (idx % kChunk)] = mats[kC2 + idx];
     float acc[4][4], a[4];
     for (int c0 = 0; c0 < dv; c0 += 64) {
         __syncthreads();
+#pragma unroll 8
         for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
             const int i = idx >> 6, c = idx & 63;
             Os[idx] = (i < L && c0 + c < dv) ? bp.dO[((size_t)j * p.ntok + tok0 + i) * dv + c0 + c] : 0.f;
@@ -437,6 +442,7 @@ __global__ void __launch_bounds__(kThreads) dterms_kernel(const BwdProblem bp) {
         // U = (e^gam Q)^T dO' over dk slices
         for (int d0 = 0; d0 < dk; d0 += DK) {
             __syncthreads();
+#pragma unroll 8
             for (int idx = tid; idx < kChunk * DK; idx += kThreads) {
                 const int i = idx / DK, c = idx - i * DK;
                 Qs[i * LDK + c] = (i < L && d0 + c < dk)
