@@ -1071,14 +1071,12 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 // grid (token, 2*Hk q/k heads + v channel groups + 1 beta/decay unit). Recomputes
 // the conv pre-activation z of the token and writes dz = dL/dz ([ntok][ch]);
 // the beta / decay unit writes db, da and the per-token terms of ddt_bias and dA_log.
+// one token of the prologue backward (all threads of the CTA take part)
 template <typename T>
-__global__ void __launch_bounds__(512) prologue_bwd_kernel(const BwdProblem bp, int units_v) {
-    __shared__ float red[16];
+__device__ __forceinline__ void prologue_bwd_token(const BwdProblem &bp, int units_v, int64_t t, float *red) {
     const Problem &p = bp.f;
     const gdn_desc &d = p.d;
-    const int64_t t = blockIdx.x;
     const int u = blockIdx.y, tid = threadIdx.x;
-    if (p.cu != nullptr && *p.status != GDN_OK) return;
     int64_t s0, s1, b, tau;
     seq_of(d, p.cu, t, s0, s1);
     tok_pos(d, t, b, tau);
@@ -1140,6 +1138,18 @@ __global__ void __launch_bounds__(512) prologue_bwd_kernel(const BwdProblem bp, 
     }
 }
 
+constexpr int kProTokens = 8;   // tokens per CTA of the prologue backward
+
+template <typename T>
+__global__ void __launch_bounds__(512) prologue_bwd_kernel(const BwdProblem bp, int units_v) {
+    __shared__ float red[16];
+    const Problem &p = bp.f;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    const int64_t tb = (int64_t)blockIdx.x * kProTokens;
+    const int64_t te = tb + kProTokens < p.ntok ? tb + kProTokens : p.ntok;
+    for (int64_t t = tb; t < te; ++t)
+        prologue_bwd_token<T>(bp, units_v, t, red);
+}
 // ------------------------------------------------------------ conv backward
 // grid (blocks of kBwdConvTokens tokens, channel groups of 256): per channel,
 // dx_t = sum_m w_m dz_{t+3-m} within the sequence, and the block's partial
@@ -1174,11 +1184,15 @@ __global__ void __launch_bounds__(kThreads) conv_bwd_kernel(const BwdProblem bp)
     }
     const int64_t t0 = (int64_t)blockIdx.x * kBwdConvTokens;
     const int64_t t1 = t0 + kBwdConvTokens < p.ntok ? t0 + kBwdConvTokens : p.ntok;
-    int64_t s0 = 0, s1 = 0;
+    int64_t s0 = 0, s1 = 0, b = 0, bT = 0;
+#pragma unroll 4
     for (int64_t t = t0; t < t1; ++t) {
-        if (t >= s1) seq_of(d, p.cu, t, s0, s1);
-        int64_t b, tau;
-        tok_pos(d, t, b, tau);
+        if (t >= s1) {                        // entering the next sequence
+            seq_of(d, p.cu, t, s0, s1);
+            b = p.cu ? 0 : s0 / d.T;
+            bT = b * d.T;
+        }
+        const int64_t tau = t - bT;
         float g = 0.f;
 #pragma unroll
         for (int m = 0; m < kConvW; ++m) {
@@ -1304,7 +1318,8 @@ cudaError_t launch_t(const BwdProblem &bp, cudaStream_t s) {
     if (p.ntok > 0) {
         const int pt = d.dk > 128 ? d.dk : 128;
         const int units_v = (ch_v + pt - 1) / pt;
-        prologue_bwd_kernel<T><<<dim3((unsigned)p.ntok, 2 * d.Hk + units_v + 1), pt, 0, s>>>(bp, units_v);
+        prologue_bwd_kernel<T><<<dim3((unsigned)((p.ntok + kProTokens - 1) / kProTokens), 2 * d.Hk + units_v + 1), pt,
+                                 0, s>>>(bp, units_v);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         conv_bwd_kernel<T><<<dim3((unsigned)bwd_conv_blocks(d), (ch + kThreads - 1) / kThreads), kThreads, 0, s>>>(bp);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
