@@ -48,22 +48,36 @@ double gdn_oracle_round_act(double x, int act) {
     }
 }
 
-void gdn_oracle_conv_silu(int n_seq, const int64_t *seq_start, int nch, int width,
-                          const float *x, int64_t x_stride, const float *w,
-                          double *y) {
+void gdn_oracle_conv_silu_prefix(int n_seq, const int64_t *seq_start, int nch, int width,
+                                 const float *x, int64_t x_stride, const float *w,
+                                 const float *prefix, int64_t prefix_stride, double *y) {
     for (int n = 0; n < n_seq; ++n) {
         for (int64_t t = seq_start[n]; t < seq_start[n + 1]; ++t) {
             for (int c = 0; c < nch; ++c) {
                 double acc = 0.0;
                 for (int i = 0; i < width; ++i) {
                     int64_t tau = t - (width - 1) + i;   /* tap width-1 is the current token */
-                    if (tau < seq_start[n]) continue;    /* zero before the sequence start */
-                    acc += (double)w[(int64_t)c * width + i] * (double)x[tau * x_stride + c];
+                    double xv;
+                    if (tau >= seq_start[n]) {
+                        xv = (double)x[tau * x_stride + c];
+                    } else if (prefix) {                 /* the raw tokens before the start */
+                        int64_t r = tau - (seq_start[n] - (width - 1));   /* 0 = oldest */
+                        xv = (double)prefix[((int64_t)n * (width - 1) + r) * prefix_stride + c];
+                    } else {
+                        continue;                        /* zero before the sequence start */
+                    }
+                    acc += (double)w[(int64_t)c * width + i] * xv;
                 }
                 y[t * nch + c] = silu(acc);
             }
         }
     }
+}
+
+void gdn_oracle_conv_silu(int n_seq, const int64_t *seq_start, int nch, int width,
+                          const float *x, int64_t x_stride, const float *w,
+                          double *y) {
+    gdn_oracle_conv_silu_prefix(n_seq, seq_start, nch, width, x, x_stride, w, NULL, 0, y);
 }
 
 void gdn_oracle_l2norm(int64_t nrows, int nheads, int d, double eps, double *x) {
@@ -284,12 +298,18 @@ int gdn_oracle_forward(const gdn_oracle_problem *p, int head_begin, int head_end
     if (!qh || !kh || !vh || !ob || !beta || !g || !h0 || !hT) { rc = -1; goto done; }
     for (int h = head_begin; h < head_end; ++h) {
         const int hk = h / G;   /* GQA: v head h reads q/k head h / G */
-        gdn_oracle_conv_silu(p->n_seq, s, dk, W, p->q_raw + (int64_t)hk * dk, ch_qk,
-                             p->conv_w + (int64_t)hk * dk * W, qh);
-        gdn_oracle_conv_silu(p->n_seq, s, dk, W, p->k_raw + (int64_t)hk * dk, ch_qk,
-                             p->conv_w + (ch_qk + (int64_t)hk * dk) * W, kh);
-        gdn_oracle_conv_silu(p->n_seq, s, dv, W, p->v_raw + (int64_t)h * dv, ch_v,
-                             p->conv_w + (2 * ch_qk + (int64_t)h * dv) * W, vh);
+        /* conv_prefix rows hold all channels, q|k|v */
+        const float *pre = p->conv_prefix;
+        const int64_t ch = 2 * ch_qk + ch_v;
+        gdn_oracle_conv_silu_prefix(p->n_seq, s, dk, W, p->q_raw + (int64_t)hk * dk, ch_qk,
+                                    p->conv_w + (int64_t)hk * dk * W,
+                                    pre ? pre + (int64_t)hk * dk : NULL, ch, qh);
+        gdn_oracle_conv_silu_prefix(p->n_seq, s, dk, W, p->k_raw + (int64_t)hk * dk, ch_qk,
+                                    p->conv_w + (ch_qk + (int64_t)hk * dk) * W,
+                                    pre ? pre + ch_qk + (int64_t)hk * dk : NULL, ch, kh);
+        gdn_oracle_conv_silu_prefix(p->n_seq, s, dv, W, p->v_raw + (int64_t)h * dv, ch_v,
+                                    p->conv_w + (2 * ch_qk + (int64_t)h * dv) * W,
+                                    pre ? pre + 2 * ch_qk + (int64_t)h * dv : NULL, ch, vh);
         gdn_oracle_l2norm(ntok, 1, dk, p->l2_eps, qh);
         gdn_oracle_l2norm(ntok, 1, dk, p->l2_eps, kh);
         for (int64_t t = 0; t < ntok; ++t)

@@ -52,6 +52,13 @@ void gdn_oracle_conv_silu(int n_seq, const int64_t *seq_start, int nch, int widt
                           const float *x, int64_t x_stride, const float *w,
                           double *y);
 
+/* The same with the raw inputs of the width-1 tokens before each sequence
+ * start given: prefix rows [n_seq][width-1][prefix_stride] (oldest first)
+ * stand in for the zeros. prefix NULL: as gdn_oracle_conv_silu. */
+void gdn_oracle_conv_silu_prefix(int n_seq, const int64_t *seq_start, int nch, int width,
+                                 const float *x, int64_t x_stride, const float *w,
+                                 const float *prefix, int64_t prefix_stride, double *y);
+
 /* In place, per row and per head: x <- x / sqrt(sum x^2 + eps). x is
  * [nrows][nheads*d]. */
 void gdn_oracle_l2norm(int64_t nrows, int nheads, int d, double eps, double *x);
@@ -112,6 +119,10 @@ typedef struct {
     const float *A_log, *dt_bias, *norm_w, *initial_state;
     double *out, *final_state;
     int chunked;    /* 0: token loop; >0: chunked variant with this chunk length */
+    /* NULL, or the raw inputs of the width-1 tokens before each sequence start,
+     * [n_seq][width-1][2*Hk*dk+Hv*dv] (q|k|v channels, oldest first): the conv
+     * reads them instead of zeros (a sequence continued from an earlier part) */
+    const float *conv_prefix;
 } gdn_oracle_problem;
 
 int gdn_oracle_forward(const gdn_oracle_problem *p, int head_begin, int head_end);

@@ -47,6 +47,7 @@ class _Problem(ctypes.Structure):
         ("norm_w", _f32p), ("initial_state", _f32p),
         ("out", _f64p), ("final_state", _f64p),
         ("chunked", ctypes.c_int),
+        ("conv_prefix", _f32p),
     ]
 
 
@@ -214,17 +215,20 @@ def gated_rmsnorm(o, gate, norm_w, eps=1e-5, dtype="fp32"):
 def forward(*, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
             seq_start, Hk, Hv, dk, dv, dtype, initial_state=None,
             l2_eps=1e-6, norm_eps=1e-5, scale=1.0, conv_width=4,
-            heads: Optional[Sequence[int]] = None, threads: int = 1, chunked: int = 0):
+            heads: Optional[Sequence[int]] = None, threads: int = 1, chunked: int = 0,
+            conv_prefix=None):
     """Whole core forward on flattened token arrays (float32 values):
     q_raw/k_raw [ntok, Hk*dk], v_raw [ntok, Hv*dv], a/b [ntok, Hv],
     gate [ntok, Hv*dv], conv_w [ch, width], A_log/dt_bias [Hv], norm_w [dv],
-    initial_state [N, Hv, dk, dv] or None.
+    initial_state [N, Hv, dk, dv] or None, conv_prefix [N, width-1, ch] (the raw
+    inputs of the tokens before each sequence, oldest first) or None.
     Returns (out [ntok, Hv, dv] float64, final_state [N, Hv, dk, dv] float64);
     heads not in ``heads`` are left at zero."""
     arrs = dict(q_raw=_f32(q_raw), k_raw=_f32(k_raw), v_raw=_f32(v_raw), a=_f32(a), b=_f32(b),
                 gate=_f32(gate), conv_w=_f32(conv_w), A_log=_f32(A_log),
                 dt_bias=_f32(dt_bias), norm_w=_f32(norm_w))
     init = _f32(initial_state) if initial_state is not None else None
+    pre = _f32(conv_prefix) if conv_prefix is not None else None
     s = np.ascontiguousarray(np.asarray(seq_start, dtype=np.int64))
     n_seq = len(s) - 1
     ntok = int(s[-1])
@@ -234,7 +238,8 @@ def forward(*, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
         n_seq=n_seq, seq_start=s.ctypes.data_as(_i64p), Hk=Hk, Hv=Hv, dk=dk, dv=dv,
         conv_width=conv_width, act=ACT_CODES[dtype], l2_eps=l2_eps, norm_eps=norm_eps,
         scale=scale, **{k: _p32(v) for k, v in arrs.items()},
-        initial_state=_p32(init), out=_p64(out), final_state=_p64(fin), chunked=int(chunked))
+        initial_state=_p32(init), out=_p64(out), final_state=_p64(fin), chunked=int(chunked),
+        conv_prefix=_p32(pre))
     heads = list(range(Hv)) if heads is None else list(heads)
     L = lib()
 
