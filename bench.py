@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--decode-batch", type=int, default=256, help="sequences per decode step")
     ap.add_argument("--backward", action="store_true",
                     help="time forward + backward (gdn_forward then gdn_backward) per step")
+    ap.add_argument("--spans", type=int, default=0,
+                    help="time the sequence-sharded path with the sequence split into this many spans, "
+                         "all on this GPU (the method's cost, not a multi-GPU time)")
     return ap.parse_args()
 
 
@@ -486,6 +489,72 @@ def backward_main(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- split sequence
+def spans_main(args, w):
+    """One step = the sequence-sharded forward of one sequence split into
+    args.spans equal spans, every span's steps (conv prefix, maps A and B,
+    span scan, span forward) run one after another on this GPU."""
+    import torch
+    from linear_attention_sequence_qkv_gb300 import build, context_parallel as cp, gdn
+    from linear_attention_sequence_qkv_gb300.workloads import make_inputs_device, replace
+
+    build.build()
+    gdn.load()
+    dev = torch.device("cuda", 0)
+    wb = replace(w, B=1, n_packed=0, T=w.T if not w.n_packed else w.max_len)
+    inp = make_inputs_device(wb, dev)
+    T = inp.q_raw.shape[1]
+    K = args.spans
+    cuts = [round(i * T / K) for i in range(K + 1)]
+    ts = (inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.gate, inp.conv_w, inp.A_log, inp.dt_bias, inp.norm_w)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        return cp.emulate(*ts, cuts, Hk=wb.Hk, Hv=wb.Hv, dk=wb.dk, dv=wb.dv, initial_state=inp.initial_state)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = None if args.no_clocks else ClockSampler(None)
+    for e in evs:
+        flush.zero_()
+        e[0].record()
+        step()
+        e[1].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    # the same sequence unsplit, for the ratio
+    d = gdn.make_desc(inp)
+    bufs = gdn.alloc(d, dev)
+    for _ in range(3):
+        gdn.forward(inp, bufs)
+    torch.cuda.synchronize()
+    evu = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e in evu:
+        flush.zero_()
+        e[0].record()
+        gdn.forward(inp, bufs)
+        e[1].record()
+    torch.cuda.synchronize()
+    ms_unsplit = sum(a.elapsed_time(b) for a, b in evu) / len(evu)
+    line = {
+        "metric": "GDN core fwd tokens/s, one sequence split into spans, all spans on 1 GB300",
+        "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp32": "f32", "bf16": "bf16", "fp16": "f16"}[wb.dtype], "data": "synthetic",
+        "config": {"workload": f"spans{K}_{w.name}", "T": T, "spans": K, "Hk": wb.Hk, "Hv": wb.Hv, "dk": wb.dk,
+                   "dv": wb.dv, "l2": "flushed before every timed step (512 MiB write)",
+                   "unsplit_ms": ms_unsplit,
+                   "per_span": "2 map forwards (B from zeros; A with v = 0, dv = dk, identity state) + the "
+                               "span forward; one gdn_span_scan"},
+        "gpu_launches_per_step": None, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from linear_attention_sequence_qkv_gb300.workloads import WORKLOADS
@@ -498,6 +567,9 @@ def main():
         return
     if args.backward:
         backward_main(args, w)
+        return
+    if args.spans:
+        spans_main(args, w)
         return
 
     import torch

@@ -247,6 +247,51 @@ int gdn_decode_step(const gdn_desc *d,
                     void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /*
+ * gdn_forward for sequences that continue an earlier part (chunked prefill, or
+ * one span of a sequence split across ranks): the width-4 causal conv reads the
+ * raw inputs of the three tokens before each sequence from conv_prefix instead
+ * of zeros ("fused q/k/v short conv", flash-linear-attention PR #972, "Summary":
+ * a per-channel causal short conv over the projections; the earlier tokens are
+ * the conv's left context). Everything else is gdn_forward's, with the state
+ * carried in through initial_state.
+ *
+ * conv_prefix  act dtype [N][3][2*Hk*dk + Hv*dv] contiguous, 16-byte aligned:
+ *              per sequence the raw q|k|v inputs (conv_w's channel order) of
+ *              its three preceding tokens, oldest first; NULL = zeros (then
+ *              this is gdn_forward).
+ * Returns as gdn_forward (GDN_ERR_INVALID_ARG also for a misaligned prefix).
+ */
+int gdn_forward_with_prefix(const gdn_desc *d,
+                            const void *q_raw, const void *k_raw, const void *v_raw,
+                            const void *a, const void *b, const void *gate,
+                            const void *conv_w, const float *A_log, const float *dt_bias,
+                            const void *norm_w, const int32_t *cu_seqlens,
+                            const void *conv_prefix, const float *initial_state,
+                            void *out, float *final_state,
+                            void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * The exchange step of the sequence-sharded core. Over a span of one sequence
+ * the chunked gated delta rule (S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) +
+ * beta_t v_t k_t^T, state H = S^T) is affine in the span's initial state:
+ * H_end = A H_start + B, where B is the span's final state from zeros and A
+ * (dk x dk) the span's final state with v = 0, dv = dk and the identity as
+ * initial state (both by gdn_forward_with_prefix). Given every span's maps in
+ * sequence order, this writes each span's initial state:
+ *     H_in[0] = h0,  H_in[s] = A[s-1] H_in[s-1] + B[s-1].
+ *
+ * spans      number of spans (0: nothing to do).
+ * A          fp32 [spans][Hv][dk][dk]; B fp32 [spans][Hv][dk][dv] (the last
+ *            span's maps are not read); h0 fp32 [Hv][dk][dv] or NULL (zeros);
+ * H_in       fp32 [spans][Hv][dk][dv], written.
+ * All device pointers, 16-byte aligned. Returns GDN_OK, GDN_ERR_INVALID_ARG
+ * (bad size, null or misaligned pointer) or GDN_ERR_CUDA. Asynchronous on
+ * stream; H_in must not overlap A, B or h0.
+ */
+int gdn_span_scan(int spans, int Hv, int dk, int dv, const float *A, const float *B,
+                  const float *h0, float *H_in, gdn_stream_t stream);
+
+/*
  * Backward of the core: the gradients of
  *     L = sum(grad_out * out) + sum(grad_final * final_state)
  * with respect to every input of gdn_forward, first order. The pages define

@@ -216,7 +216,7 @@ int forward_impl(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
                  const float *A_log, const float *dt_bias, const void *norm_w,
                  const int32_t *cu_seqlens, const float *initial_state, void *out,
                  float *final_state, void *workspace, size_t workspace_bytes,
-                 gdn_stream_t stream, bool single_stream) {
+                 gdn_stream_t stream, bool single_stream, const void *conv_prefix = nullptr) {
     int rc = check_desc(d, cu_seqlens != nullptr);
     if (rc != GDN_OK) return rc;
     const bool tok = (int64_t)d->B * d->T > 0;   // token tensors may be empty (null)
@@ -226,7 +226,8 @@ int forward_impl(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
     if (!aligned(q_raw, 16) || !aligned(k_raw, 16) || !aligned(v_raw, 16) ||
         !aligned(conv_w, 16) || !aligned(out, 16) || !aligned(norm_w, 4))
         return GDN_ERR_INVALID_ARG;
-    if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)))
+    if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
+        (conv_prefix && !aligned(conv_prefix, 16)))
         return GDN_ERR_INVALID_ARG;
     if ((rc = check_ws(d, workspace, workspace_bytes)) != GDN_OK) return rc;
     Problem p = base_problem(d, cu_seqlens, workspace);
@@ -244,6 +245,7 @@ int forward_impl(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
     p.hT = final_state;
     p.out = out;
     p.single_stream = single_stream;
+    p.conv_prefix = conv_prefix;
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_prologue(p, s)) != GDN_OK) return rc;
     if ((rc = run_chunk(p, s)) != GDN_OK) return rc;
@@ -272,6 +274,26 @@ int gdn_forward(const gdn_desc *d, const void *q_raw, const void *k_raw, const v
                 gdn_stream_t stream) {
     return forward_impl(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w, cu_seqlens,
                         initial_state, out, final_state, workspace, workspace_bytes, stream, false);
+}
+
+int gdn_forward_with_prefix(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw,
+                            const void *a, const void *b, const void *gate, const void *conv_w,
+                            const float *A_log, const float *dt_bias, const void *norm_w,
+                            const int32_t *cu_seqlens, const void *conv_prefix, const float *initial_state,
+                            void *out, float *final_state, void *workspace, size_t workspace_bytes,
+                            gdn_stream_t stream) {
+    return forward_impl(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w, cu_seqlens,
+                        initial_state, out, final_state, workspace, workspace_bytes, stream, false, conv_prefix);
+}
+
+int gdn_span_scan(int spans, int Hv, int dk, int dv, const float *A, const float *B, const float *h0,
+                  float *H_in, gdn_stream_t stream) {
+    if (spans < 0 || Hv < 1 || !is_pow2_in(dk, 16, 512) || !is_pow2_in(dv, 16, 512)) return GDN_ERR_INVALID_ARG;
+    if (spans == 0) return GDN_OK;
+    if (!A || !B || !H_in) return GDN_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(H_in, 16) || (h0 && !aligned(h0, 16)))
+        return GDN_ERR_INVALID_ARG;
+    return cuda_status(gdn::launch_span_scan(spans, Hv, dk, dv, A, B, h0, H_in, (cudaStream_t)stream));
 }
 
 int gdn_decode_workspace_bytes(const gdn_desc *d, size_t *bytes) {

@@ -76,6 +76,9 @@ struct Problem {
     void *gamma;                  // float, or double for fp32 activations
     void *tpt;                    // [T; P T] tiles of the tensor-core kernels
     bool single_stream;           // no side stream (the no-allocation entry point)
+    // null, or act dtype [N][3][2*Hk*dk + Hv*dv]: the raw q|k|v inputs of the three
+    // tokens before each sequence (oldest first), read by the conv instead of zeros
+    const void *conv_prefix;
 };
 
 // Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one
@@ -100,6 +103,9 @@ int forward_single_stream(const gdn_desc *d, const void *q_raw, const void *k_ra
                           float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 bool chunk_tc_supports(const gdn_desc &d);
 cudaError_t launch_epilogue(const Problem &p, cudaStream_t s);
+// H_in[s] = A[s-1] H_in[s-1] + B[s-1], H_in[0] = h0 (or zeros), per v head
+cudaError_t launch_span_scan(int spans, int Hv, int dk, int dv, const float *A, const float *B, const float *h0,
+                             float *H_in, cudaStream_t s);
 
 // Backward: the forward's regions, then the backward's (all fp32), each on a
 // 256-byte boundary. Slots are chunk slots (chunk_slot_bound), tokens the

@@ -119,7 +119,7 @@ template <int U, int N, typename F> __device__ __forceinline__ void static_for(F
     }
 }
 
-template <typename T, int NVEC, bool NORM>
+template <typename T, int NVEC, bool NORM, bool PRE>
 __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc &c, int gy,
                                            uint4 *stage) {
     constexpr int VEC = Vec16<T>::N;
@@ -163,17 +163,27 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
     const int lanes_per_head = hd / CPT;      // <= 32 for q/k by construction
 
     // rows into shared memory, one copy group per row:
-    // stage[(r * NVEC + v) * kThreads + tid]
+    // stage[(r * NVEC + v) * kThreads + tid]. Rows before the sequence start are
+    // zeros, or the prefix rows (the raw inputs of the three earlier tokens).
     const int64_t first = c.tok0 + t_begin - (kConvW - 1);
     const int64_t brow = p.cu ? 0 : c.n;     // batch row of this sequence
     const T *rp = src + brow * sb + (first - brow * (int64_t)d.T) * st + (active ? c0 : 0);
+    const int64_t ch_all = 2 * (int64_t)ch_qk + (int64_t)d.Hv * d.dv;
+    const T *pre = PRE ? (const T *)p.conv_prefix + (int64_t)c.n * (kConvW - 1) * ch_all + w_base + (active ? c0 : 0)
+                       : nullptr;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
-        const bool ok = active && r < ntok + kConvW - 1 && first + r >= c.seq0;
+        const bool in_rows = active && r < ntok + kConvW - 1;
+        const bool ok = in_rows && first + r >= c.seq0;
+        // prefix row index: 0 = oldest of the three tokens before seq0
+        const int64_t pr = first + r - (c.seq0 - (kConvW - 1));
+        const bool okp = PRE && in_rows && !ok && pr >= 0;
 #pragma unroll
         for (int v = 0; v < NVEC; ++v)
-            cp_async16(&stage[(r * NVEC + v) * kThreads + tid], ok ? (const void *)(rp + r * st + v * VEC)
-                                                                   : (const void *)src, ok);
+            cp_async16(&stage[(r * NVEC + v) * kThreads + tid],
+                       ok ? (const void *)(rp + r * st + v * VEC)
+                          : (okp ? (const void *)(pre + pr * ch_all + v * VEC) : (const void *)src),
+                       ok || okp);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     // conv taps of my channels as pairs (overlaps the copies)
@@ -312,7 +322,7 @@ __device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c, 
     }
 }
 
-template <typename T, int NVEC>
+template <typename T, int NVEC, bool PRE>
 __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueArgs A) {
     extern __shared__ uint4 stage[];
     const Problem &p = A.p;
@@ -325,8 +335,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueArgs A
     if (!locate_chunk(blockIdx.x, p.cu, p.chunk_off, p.d.N, p.d.T, c)) return;
     const int gy = blockIdx.y;
     if (gy == (2 * A.groups_qk + A.groups_v) * ConvShape<NVEC>::SLICES) gate_group<T>(p, c, (float *)stage);
-    else if (gy < 2 * A.groups_qk * ConvShape<NVEC>::SLICES) conv_group<T, NVEC, true>(A, c, gy, stage);
-    else conv_group<T, NVEC, false>(A, c, gy, stage);
+    else if (gy < 2 * A.groups_qk * ConvShape<NVEC>::SLICES) conv_group<T, NVEC, true, PRE>(A, c, gy, stage);
+    else conv_group<T, NVEC, false, PRE>(A, c, gy, stage);
 }
 
 template <typename T, int NVEC>
@@ -340,12 +350,13 @@ cudaError_t launch_t(const Problem &p, cudaStream_t s) {
     using Shape = ConvShape<NVEC>;
     static_assert(Shape::SMEM >= 2 * kChunk * 33 * 4, "gate group scratch");
     dim3 grid((unsigned)chunk_slots(p), (2 * A.groups_qk + A.groups_v) * Shape::SLICES + 1);
+    // the prefix reads are compiled in only where a prefix is given
+    auto kernel = p.conv_prefix ? prologue_kernel<T, NVEC, true> : prologue_kernel<T, NVEC, false>;
     if (Shape::SMEM > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(prologue_kernel<T, NVEC>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Shape::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Shape::SMEM);
         if (e != cudaSuccess) return e;
     }
-    prologue_kernel<T, NVEC><<<grid, kThreads, Shape::SMEM, s>>>(A);
+    kernel<<<grid, kThreads, Shape::SMEM, s>>>(A);
     return cudaGetLastError();
 }
 

@@ -36,7 +36,7 @@ EXPORTS = ("gdn_desc_init", "gdn_workspace_bytes", "gdn_workspace_offsets", "gdn
            "gdn_prologue", "gdn_chunk_rule", "gdn_epilogue", "gdn_device_status",
            "gdn_status_string", "gdn_chunk_kernel_kind", "gdn_forward_static_ws",
            "gdn_decode_workspace_bytes", "gdn_decode_step", "gdn_backward_workspace_bytes",
-           "gdn_backward")
+           "gdn_backward", "gdn_forward_with_prefix", "gdn_span_scan")
 
 # bytes of the library's fixed device scratch used by gdn_forward_static_ws
 GDN_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
@@ -98,6 +98,8 @@ def load(path: str = LIB_PATH):
     L.gdn_forward_static_ws.argtypes = [dp] + [vp] * 14 + [vp]
     L.gdn_decode_workspace_bytes.argtypes = [dp, ctypes.POINTER(sz)]
     L.gdn_decode_step.argtypes = [dp] + [vp] * 13 + [vp, sz, vp]
+    L.gdn_forward_with_prefix.argtypes = [dp] + [vp] * 15 + [vp, sz, vp]
+    L.gdn_span_scan.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp]
     L.gdn_backward_workspace_bytes.argtypes = [dp, ctypes.POINTER(sz)]
     L.gdn_backward.argtypes = [dp] + [vp] * 25 + [vp, sz, vp]
     for name in EXPORTS:
@@ -236,6 +238,27 @@ def gdn_decode_step(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, 
                                 _ptr(workspace), int(workspace_bytes), _stream(stream))
     if check:
         _check(rc, "gdn_decode_step")
+    return rc
+
+
+def gdn_forward_with_prefix(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
+                            cu_seqlens, conv_prefix, initial_state, out, final_state, workspace,
+                            workspace_bytes, stream=None, check=True) -> int:
+    rc = load().gdn_forward_with_prefix(ctypes.byref(d), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(a),
+                                        _ptr(b), _ptr(gate), _ptr(conv_w), _ptr(A_log), _ptr(dt_bias),
+                                        _ptr(norm_w), _ptr(cu_seqlens), _ptr(conv_prefix),
+                                        _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(workspace),
+                                        int(workspace_bytes), _stream(stream))
+    if check:
+        _check(rc, "gdn_forward_with_prefix")
+    return rc
+
+
+def gdn_span_scan(spans, Hv, dk, dv, A, B, h0, H_in, stream=None, check=True) -> int:
+    rc = load().gdn_span_scan(int(spans), int(Hv), int(dk), int(dv), _ptr(A), _ptr(B), _ptr(h0), _ptr(H_in),
+                              _stream(stream))
+    if check:
+        _check(rc, "gdn_span_scan")
     return rc
 
 

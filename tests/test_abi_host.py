@@ -202,3 +202,19 @@ def test_backward_checks(lib):
     bad = gdn.gdn_desc_init(2, 100, 0, 2, 4, 64, 128, gdn.GDN_BF16)
     bad.dv = 96                             # not a power of two
     assert call(bad) == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_prefix_and_span_scan_checks(lib):
+    fake = 1 << 20
+    d = gdn.gdn_desc_init(2, 100, 0, 2, 4, 64, 128, gdn.GDN_BF16)
+    need = gdn.gdn_workspace_bytes(d)
+    args = [fake] * 15   # q_raw .. final_state
+    args[10] = None      # cu_seqlens
+    args[11] = fake + 8  # conv_prefix not 16-byte aligned
+    assert lib.gdn_forward_with_prefix(ctypes.byref(d), *args, fake, need, None) == gdn.GDN_ERR_INVALID_ARG
+    # span scan: sizes and pointers checked before any launch
+    assert lib.gdn_span_scan(0, 4, 64, 64, None, None, None, None, None) == gdn.GDN_OK
+    assert lib.gdn_span_scan(2, 4, 48, 64, fake, fake, None, fake, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_span_scan(2, 0, 64, 64, fake, fake, None, fake, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_span_scan(2, 4, 64, 64, None, fake, None, fake, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_span_scan(2, 4, 64, 64, fake + 4, fake, None, fake, None) == gdn.GDN_ERR_INVALID_ARG
