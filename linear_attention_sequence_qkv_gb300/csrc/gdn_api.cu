@@ -470,6 +470,8 @@ int gdn_backward(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
     bp.pa = (float *)(w + L.pa);
     bp.pnorm = (float *)(w + L.pnorm);
     bp.pconv = (float *)(w + L.pconv);
+    bp.xbuf = (float *)(w + L.xbuf);
+    bp.hdbuf = (float *)(w + L.hdbuf);
     return cuda_status(gdn::launch_backward(bp, s));
 }
 

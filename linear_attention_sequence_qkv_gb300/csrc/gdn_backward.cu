@@ -793,7 +793,7 @@ constexpr int kTileV = 16;
 
 size_t grad_smem_bytes() { return sizeof(float) * (4 * kChunk * LDK + 5 * kTileV * LDK); }
 
-template <typename T>
+template <typename T, bool XPRE>   // XPRE: X1, X2, X3 and <H0, dH1> come from chunk_x (tensor cores)
 __global__ void __launch_bounds__(kThreads, 2) chunk_grad_kernel(const BwdProblem bp) {
     using S = typename Inter<T>::S;
     using GT = typename Inter<T>::G;
@@ -936,12 +936,23 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_grad_kernel(const BwdProble
     float rg[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f}, kap = 0.f, hd = 0.f;
     float *dqo = bp.dq + ((size_t)j * p.ntok + tok0) * dk;
     float *dko = bp.dk + ((size_t)j * p.ntok + tok0) * dk;
+    const float *Xb = bp.xbuf + ((size_t)slot * Hv + j) * 3 * 64 * dk;
     for (int d0 = 0; d0 < dk; d0 += DK) {
         float X1[4][4], X2[4][4], X3[4][4];
         zero4x4(X1);
         zero4x4(X2);
         zero4x4(X3);
-        for (int c0 = 0; c0 < dv; c0 += kTileV) {
+        if (XPRE && d0 + 4 * ci < dk) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const size_t r = (size_t)(4 * ti + x) * dk + d0 + 4 * ci;
+                const float4 a = ld4(Xb + r), b = ld4(Xb + 64 * (size_t)dk + r), c = ld4(Xb + 128 * (size_t)dk + r);
+                X1[x][0] = a.x; X1[x][1] = a.y; X1[x][2] = a.z; X1[x][3] = a.w;
+                X2[x][0] = b.x; X2[x][1] = b.y; X2[x][2] = b.z; X2[x][3] = b.w;
+                X3[x][0] = c.x; X3[x][1] = c.y; X3[x][2] = c.z; X3[x][3] = c.w;
+            }
+        }
+        for (int c0 = 0; c0 < (XPRE ? 0 : dv); c0 += kTileV) {
             __syncthreads();
             load_rows_t(tO, dOg, c0);
             load_rows_t(tR, dRg, c0);
@@ -1043,6 +1054,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_grad_kernel(const BwdProble
             ks += red[w];
             hs_ += red[32 + w];
         }
+        if (XPRE) hs_ = bp.hdbuf[(size_t)slot * Hv + j];
         dgm[L - 1] += ks + expf((float)gam[kChunk - 1]) * hs_;
         float acc = 0.f;
         float *dbo = bp.dbeta + (size_t)j * p.ntok + tok0;
@@ -1312,8 +1324,15 @@ cudaError_t launch_t(const BwdProblem &bp, cudaStream_t s) {
     if (slots > 0 && (e = launch_per_chunk(dterms_kernel<T>, dterms_smem_bytes(), bp, slots, s)) != cudaSuccess)
         return e;
     if ((e = launch_serial_nv<T>(bp, true, s)) != cudaSuccess) return e;
-    if (slots > 0 && (e = launch_per_chunk(chunk_grad_kernel<T>, grad_smem_bytes(), bp, slots, s)) != cudaSuccess)
-        return e;
+    if (slots > 0) {
+        if (chunk_x_tc_supports(d)) {
+            if ((e = launch_chunk_x_tc(bp, slots, s)) != cudaSuccess) return e;
+            e = launch_per_chunk(chunk_grad_kernel<T, true>, grad_smem_bytes(), bp, slots, s);
+        } else {
+            e = launch_per_chunk(chunk_grad_kernel<T, false>, grad_smem_bytes(), bp, slots, s);
+        }
+        if (e != cudaSuccess) return e;
+    }
     const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
     if (p.ntok > 0) {
         const int pt = d.dk > 128 ? d.dk : 128;

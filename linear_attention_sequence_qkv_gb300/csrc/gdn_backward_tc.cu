@@ -1,0 +1,186 @@
+// gdn_backward_tc.cu -- the dv contractions of the backward's per-chunk
+// gradients on the tensor cores (tcgen05, bf16 operands, fp32 accumulators).
+//
+// Per (chunk slot, v head) the per-chunk gradient kernel needs three products
+// over dv (see gdn_backward.cu for the chunk form):
+//     X1 = dO' H0^T,  X2 = dR0 H0^T,  X3 = Vn dH1^T      (each 64 x dk)
+// Here they are two M = 128 products accumulated in tensor memory:
+//     [dO'; dR0] H0^T  -> TMEM columns [0, dk)      (rows 0..63 X1, 64..127 X2)
+//     [Vn;  0  ] dH1^T -> TMEM columns [256, 256+dk) (rows 0..63 X3)
+// over 64-column blocks of dv. The fp32 operands are rounded to bf16 (fp32's
+// exponent range: gradients of any scale) and written by the CTA's threads
+// into 128-byte-swizzled K-major tiles; one thread issues the MMAs. The
+// results go to the workspace ([slot][Hv][3][64][dk] fp32) together with
+// <H0, dH1>, which the same loads give for free. Shapes: dk <= 256, dv a
+// multiple of 64; 2-byte activations (fp32 activations keep the fp32 path).
+#include "gdn_common.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+constexpr int kXThreads = 128;      // one thread per TMEM lane / tile row
+
+// kind::f16 instruction descriptor with bf16 A and B, fp32 D, both K-major:
+// [4,6) D format 1 = f32, [7,10) A format 1 = bf16, [10,13) B format 1 = bf16,
+// [17,23) N >> 3, [24,29) M >> 4
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void st4f(float *p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+
+__device__ __forceinline__ uint32_t bf2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 64 fp32 from src (null: zeros) rounded to bf16 into row r of a swizzled tile
+__device__ __forceinline__ void put_row(unsigned char *tile, int r, const float *src) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (src) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(src + 8 * q));
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(src + 8 * q + 4));
+            u = make_uint4(bf2(a.x, a.y), bf2(a.z, a.w), bf2(b.x, b.y), bf2(b.z, b.w));
+        }
+        *reinterpret_cast<uint4 *>(tile + sw128_off(r, 8 * q)) = u;
+    }
+}
+
+// rows r of H0 and dH1 into their tiles, accumulating their dot product
+__device__ __forceinline__ void put_rows2(unsigned char *th, unsigned char *tg, int r, const float *h,
+                                          const float *g, float &hd) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(h + 8 * q));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(h + 8 * q + 4));
+        const float4 c = __ldg(reinterpret_cast<const float4 *>(g + 8 * q));
+        const float4 e = __ldg(reinterpret_cast<const float4 *>(g + 8 * q + 4));
+        hd = fmaf(a.x, c.x, fmaf(a.y, c.y, fmaf(a.z, c.z, fmaf(a.w, c.w, hd))));
+        hd = fmaf(b.x, e.x, fmaf(b.y, e.y, fmaf(b.z, e.z, fmaf(b.w, e.w, hd))));
+        *reinterpret_cast<uint4 *>(th + sw128_off(r, 8 * q)) = make_uint4(bf2(a.x, a.y), bf2(a.z, a.w), bf2(b.x, b.y),
+                                                                          bf2(b.z, b.w));
+        *reinterpret_cast<uint4 *>(tg + sw128_off(r, 8 * q)) = make_uint4(bf2(c.x, c.y), bf2(c.z, c.w), bf2(e.x, e.y),
+                                                                          bf2(e.z, e.w));
+    }
+}
+
+__global__ void __launch_bounds__(kXThreads, 1) chunk_x_kernel(const BwdProblem bp) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tslot;
+    __shared__ float red[kXThreads / 32];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    const int j = blockIdx.y;
+    const int64_t slot = blockIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    ChunkLoc loc;
+    if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, loc)) return;
+    const int64_t tok0 = loc.tok0;
+    const int L = loc.len;
+    unsigned char *A12 = sm, *A3 = sm + 16384, *BH = sm + 32768, *BD = BH + dk * 128;
+    const int t = threadIdx.x, warp = t >> 5;
+    if (t == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) tmem_alloc(&tslot, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = tslot;
+    const float *dOg = bp.dO + ((size_t)j * p.ntok + tok0) * dv;
+    const float *dRg = bp.dR + ((size_t)j * p.ntok + tok0) * dv;
+    const float *Vng = bp.vn + ((size_t)j * p.ntok + tok0) * dv;
+    const float *H0 = bp.h0 + ((size_t)slot * Hv + j) * dk * dv;
+    const float *dH1 = bp.dh1 + ((size_t)slot * Hv + j) * dk * dv;
+    const uint32_t idesc = idesc_bf16(128, dk);
+    const uint64_t da12 = sw128_desc(smem_u32(A12), 16, 1024), da3 = sw128_desc(smem_u32(A3), 16, 1024);
+    const uint64_t dbh = sw128_desc(smem_u32(BH), 16, 1024), dbd = sw128_desc(smem_u32(BD), 16, 1024);
+    float hd = 0.f;
+    if (t >= 64) put_row(A3, t, nullptr);     // rows 64..127 of [Vn; 0] stay zero
+    bool ok = true;
+    int step = 0;
+    for (int kb = 0; kb < dv; kb += 64, ++step) {
+        const int i = t & 63;
+        put_row(A12, t, i < L ? (t < 64 ? dOg : dRg) + (int64_t)i * dv + kb : nullptr);
+        if (t < 64) put_row(A3, t, t < L ? Vng + (int64_t)t * dv + kb : nullptr);
+        for (int r = t; r < dk; r += kXThreads)
+            put_rows2(BH, BD, r, H0 + (size_t)r * dv + kb, dH1 + (size_t)r * dv + kb, hd);
+        fence_async_smem();                   // the tiles are read by the tensor cores
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (t == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {   // K = 16 per MMA: the start advances 32 bytes
+                mma_f16(tbase, da12 + 2 * ks, dbh + 2 * ks, idesc, (kb | ks) != 0);
+                mma_f16(tbase + 256, da3 + 2 * ks, dbd + 2 * ks, idesc, (kb | ks) != 0);
+            }
+            mma_commit(&bar);
+        }
+        // every thread waits for the products before the tiles are rewritten
+        const bool done = mbar_wait(&bar, (uint32_t)step & 1);
+        fence_after_sync();
+        if (__syncthreads_or(!done)) {
+            ok = false;
+            break;
+        }
+    }
+    if (ok) {
+        float *X = bp.xbuf + ((size_t)slot * Hv + j) * 3 * 64 * dk;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        float *row12 = t < 64 ? X + (size_t)t * dk : X + 64 * (size_t)dk + (size_t)(t - 64) * dk;
+        for (int c = 0; c < dk; c += 32) {
+            float v[32];
+            tmem_ld32(tbase + lane_off + c, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) st4f(row12 + c + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            if (warp < 2) {                    // rows 0..63 of the second product
+                tmem_ld32(tbase + 256 + lane_off + c, v);
+                float *row3 = X + 128 * (size_t)dk + (size_t)t * dk + c;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) st4f(row3 + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, off);
+        if ((t & 31) == 0) red[warp] = hd;
+    } else {
+        // the products did not complete in time: report, wait (bounded) once more
+        // for what is in flight, then free the tensor memory
+        if (t == 0) *p.status = GDN_ERR_DEVICE_TIMEOUT;
+        mbar_wait(&bar, (uint32_t)step & 1);
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (ok && t == 0) bp.hdbuf[(size_t)slot * Hv + j] = red[0] + red[1] + red[2] + red[3];
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace
+
+bool chunk_x_tc_supports(const gdn_desc &d) {
+    return d.dtype != GDN_F32 && (d.dk == 64 || d.dk == 128 || d.dk == 256) && d.dv % 64 == 0;
+}
+
+cudaError_t launch_chunk_x_tc(const BwdProblem &bp, int64_t slots, cudaStream_t s) {
+    const gdn_desc &d = bp.f.d;
+    const size_t bytes = 1024 + 32768 + 2 * (size_t)d.dk * 128;
+    cudaError_t e = cudaFuncSetAttribute(chunk_x_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    chunk_x_kernel<<<dim3((unsigned)slots, d.Hv), kXThreads, bytes, s>>>(bp);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -126,6 +126,8 @@ struct BwdLayout {
     size_t pa;               // [2][Hv][ntok]       per-token terms of ddt_bias and dA_log
     size_t pnorm;            // [kBwdEpiWarps][dv]  per-warp partial sums of dnorm_w
     size_t pconv;            // [blocks][ch][4]     per-block partial sums of dconv_w
+    size_t xbuf;             // [slot][Hv][3][64][dk] dO' H0^T, dR0 H0^T, Vn dH1^T (tensor-core path)
+    size_t hdbuf;            // [slot][Hv]          <H0, dH1> (tensor-core path)
     size_t total;
 };
 inline int64_t bwd_epi_warps(const gdn_desc &d) {
@@ -159,6 +161,8 @@ inline BwdLayout make_bwd_layout(const gdn_desc &d) {
     L.pa = off;    off = align_up(off + 2 * (size_t)d.Hv * ntok * 4, 256);
     L.pnorm = off; off = align_up(off + (size_t)bwd_epi_warps(d) * d.dv * 4, 256);
     L.pconv = off; off = align_up(off + (size_t)bwd_conv_blocks(d) * ch * 4 * 4, 256);
+    L.xbuf = off;  off = align_up(off + slots * d.Hv * 3 * 64 * (size_t)d.dk * 4, 256);
+    L.hdbuf = off; off = align_up(off + slots * d.Hv * 4, 256);
     L.total = off;
     return L;
 }
@@ -171,8 +175,12 @@ struct BwdProblem {
     void *dgate;                        // gate dtype [B*T][Hv*dv]
     float *dconv_w, *dA_log, *ddt_bias, *dnorm_w, *dinit;
     float *h0, *dh1, *uq, *mats, *vn, *dO, *dR, *wv, *dq, *dk, *dbeta, *dgam, *dz, *pa, *pnorm, *pconv;
+    float *xbuf, *hdbuf;
 };
 cudaError_t launch_backward(const BwdProblem &p, cudaStream_t s);
+// the per-chunk gradients' dv contractions on the tensor cores (gdn_backward_tc.cu)
+bool chunk_x_tc_supports(const gdn_desc &d);
+cudaError_t launch_chunk_x_tc(const BwdProblem &p, int64_t slots, cudaStream_t s);
 
 // Decode (one token per sequence, d.T == 1): workspace regions, all fp32 but o.
 struct DecodeLayout {
