@@ -1318,7 +1318,10 @@ cudaError_t launch_t(const BwdProblem &bp, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
     if (slots > 0 && (e = launch_per_chunk(mats_kernel<T>, mats_smem_bytes(), bp, slots, s)) != cudaSuccess) return e;
     if ((e = launch_serial_nv<T>(bp, false, s)) != cudaSuccess) return e;
-    if (slots > 0 && (e = launch_per_chunk(out_kernel<T>, out_smem_bytes(), bp, slots, s)) != cudaSuccess) return e;
+    if (slots > 0) {
+        e = out_tc_supports(d) ? launch_out_tc(bp, slots, s) : launch_per_chunk(out_kernel<T>, out_smem_bytes(), bp, slots, s);
+        if (e != cudaSuccess) return e;
+    }
     e = d.gate_dtype == GDN_F32 ? launch_rms_w<T, float>(bp, s) : launch_rms_w<T, T>(bp, s);
     if (e != cudaSuccess) return e;
     if (slots > 0 && (e = launch_per_chunk(dterms_kernel<T>, dterms_smem_bytes(), bp, slots, s)) != cudaSuccess)

@@ -22,6 +22,7 @@ namespace {
 using namespace tc;
 
 constexpr int kXThreads = 128;      // one thread per TMEM lane / tile row
+constexpr int kC2 = kChunk * kChunk; // elements of a 64 x 64 chunk matrix
 
 // kind::f16 instruction descriptor with bf16 A and B, fp32 D, both K-major:
 // [4,6) D format 1 = f32, [7,10) A format 1 = bf16, [10,13) B format 1 = bf16,
@@ -168,7 +169,167 @@ __global__ void __launch_bounds__(kXThreads, 1) chunk_x_kernel(const BwdProblem 
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// ------------------------------------------------------------ outputs O
+// O = scale ((diag(e^gam) Q) H0 + Pm Vn) of a (chunk slot, v head) as one
+// tensor-memory accumulation (M = 128: rows 0..63 the chunk's tokens, 64..127
+// zero): A K-major (e^gam Q over 64-wide dk blocks, then Pm), B MN-major (rows
+// of H0, then Vn; dv in 64-column blocks 8 KB apart), N = dv in MMAs of at
+// most 256 columns. fp16 operands: these are forward quantities of bounded
+// size (unit-norm q, the state, the new values), where fp16's three extra
+// mantissa bits over bf16 keep O close to the forward's. Writes o (fp32,
+// [Hv][ntok][dv]) for the RMSNorm backward.
+constexpr int kOThreads = 256;
+
+__device__ __forceinline__ uint32_t h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 8 fp32 at src (16-byte aligned) -> fp16 into a 128-byte-swizzled tile
+__device__ __forceinline__ void put8(unsigned char *dst, const float *src, float scale) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(src));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(src + 4));
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(h2(scale * a.x, scale * a.y), h2(scale * a.z, scale * a.w),
+                                                 h2(scale * b.x, scale * b.y), h2(scale * b.z, scale * b.w));
+}
+
+__global__ void __launch_bounds__(kOThreads, 1) out_tc_kernel(const BwdProblem bp) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tslot;
+    __shared__ float egs[kChunk];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    const int j = blockIdx.y;
+    const int64_t slot = blockIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    ChunkLoc loc;
+    if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, loc)) return;
+    const int64_t tok0 = loc.tok0;
+    const int L = loc.len;
+    const int hk = j / (Hv / d.Hk);
+    unsigned char *At = sm, *Bt = sm + 16384;          // A: 128 x 64 K-major; B: 64 K-rows x dv MN-major
+    const int t = threadIdx.x, warp = t >> 5;
+    const int nblk = dv / 64;                          // 64-column blocks of B
+    if (t == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    if (t < kChunk) {
+        const int i = t < L ? t : L - 1;
+        egs[t] = expf(((const float *)p.gamma)[(int64_t)j * p.ntok + tok0 + i]);
+    }
+    if (warp == 0) tmem_alloc(&tslot, 512);
+    // rows 64..127 of A are zero for every product
+    for (int idx = t; idx < 64 * 8; idx += kOThreads)
+        *reinterpret_cast<uint4 *>(At + sw128_off(64 + idx / 8, 8 * (idx % 8))) = make_uint4(0u, 0u, 0u, 0u);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = tslot;
+    const __half *qh = (const __half *)p.q + ((int64_t)hk * p.ntok + tok0) * dk;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    const float *H0 = bp.h0 + ((size_t)slot * Hv + j) * dk * dv;
+    const float *Pm = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2 + kC2;
+    const float *Vng = bp.vn + ((size_t)j * p.ntok + tok0) * dv;
+    const int nmma = dv > 256 ? 2 : 1, nw = dv > 256 ? 256 : dv;
+    const uint32_t idesc = idesc_f16(128, nw, false, true);   // fp16 A K-major, B MN-major
+    const uint64_t da = sw128_desc(smem_u32(At), 16, 1024), db = sw128_desc(smem_u32(Bt), 8192, 1024);
+    // B tile: rows kr of src (row stride dv; null rows beyond nrows) into the MN-major layout
+    auto put_b = [&](const float *src, int nrows) {
+        for (int idx = t; idx < 64 * (dv / 8); idx += kOThreads) {
+            const int kr = idx / (dv / 8), n0 = 8 * (idx % (dv / 8));
+            unsigned char *dst = Bt + (n0 / 64) * 8192 + sw128_off(kr, n0 % 64);
+            if (kr < nrows) put8(dst, src + (int64_t)kr * dv + n0, 1.f);
+            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    bool ok = true;
+    const int steps = dk / 64 + 1;                     // dk blocks of (e^gam Q) H0, then Pm Vn
+    for (int st = 0; st < steps && ok; ++st) {
+        if (st < steps - 1) {
+            const int kb = 64 * st;
+            for (int idx = t; idx < 64 * 8; idx += kOThreads) {   // e^gam Q, rows 0..63
+                const int i = idx / 8, c = 8 * (idx % 8);
+                uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                if (i < L) {
+                    float h[8], l[8];
+                    unpack16<__half>(*reinterpret_cast<const uint4 *>(qh + (int64_t)i * dk + kb + c), h);
+                    unpack16<__half>(*reinterpret_cast<const uint4 *>(qh + (int64_t)i * dk + kb + c + plane), l);
+                    const float e = egs[i];
+                    u = make_uint4(h2(e * (h[0] + l[0]), e * (h[1] + l[1])), h2(e * (h[2] + l[2]), e * (h[3] + l[3])),
+                                   h2(e * (h[4] + l[4]), e * (h[5] + l[5])), h2(e * (h[6] + l[6]), e * (h[7] + l[7])));
+                }
+                *reinterpret_cast<uint4 *>(At + sw128_off(i, c)) = u;
+            }
+            put_b(H0 + (size_t)kb * dv, 64);
+        } else {
+            for (int idx = t; idx < 64 * 8; idx += kOThreads) {   // Pm
+                const int i = idx / 8, c = 8 * (idx % 8);
+                put8(At + sw128_off(i, c), Pm + i * kChunk + c, 1.f);
+            }
+            put_b(Vng, L);
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (t == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                for (int h = 0; h < nmma; ++h)
+                    mma_f16(tbase + 256 * h, da + 2 * ks, db + (uint64_t)((2048 * ks + 32768 * h) >> 4), idesc,
+                            (st | ks) != 0);
+            mma_commit(&bar);
+        }
+        const bool done = mbar_wait(&bar, (uint32_t)st & 1);
+        fence_after_sync();
+        if (__syncthreads_or(!done)) ok = false;
+    }
+    if (ok) {
+        // rows 0..63: warps 0, 1 (columns of the first half) and 4, 5 (second half)
+        const int q4 = warp & 3, half = warp >> 2;
+        if (q4 < 2) {
+            const int i = 32 * q4 + (t & 31);
+            const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+            for (int c = half * (dv / 2); c < (half + 1) * (dv / 2); c += 32) {
+                float v[32];
+                tmem_ld32(tbase + lane_off + c, v);
+                if (i < L) {
+                    float *dst = bp.dO + ((size_t)j * p.ntok + tok0 + i) * dv + c;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st4f(dst + 4 * q, d.scale * v[4 * q], d.scale * v[4 * q + 1], d.scale * v[4 * q + 2],
+                             d.scale * v[4 * q + 3]);
+                }
+            }
+        }
+    } else {
+        if (t == 0) *p.status = GDN_ERR_DEVICE_TIMEOUT;
+        mbar_wait(&bar, (uint32_t)(steps - 1) & 1);
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
 }  // namespace
+
+bool out_tc_supports(const gdn_desc &d) {
+    return d.dtype != GDN_F32 && d.dk % 64 == 0 && d.dv % 64 == 0 && d.dv <= 512 && d.dv >= 64;
+}
+
+cudaError_t launch_out_tc(const BwdProblem &bp, int64_t slots, cudaStream_t s) {
+    const gdn_desc &d = bp.f.d;
+    const size_t bytes = 1024 + 16384 + 64 * (size_t)d.dv * 2;
+    cudaError_t e = cudaFuncSetAttribute(out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    out_tc_kernel<<<dim3((unsigned)slots, d.Hv), kOThreads, bytes, s>>>(bp);
+    return cudaGetLastError();
+}
 
 bool chunk_x_tc_supports(const gdn_desc &d) {
     return d.dtype != GDN_F32 && (d.dk == 64 || d.dk == 128 || d.dk == 256) && d.dv % 64 == 0;
