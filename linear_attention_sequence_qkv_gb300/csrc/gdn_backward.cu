@@ -1324,8 +1324,11 @@ cudaError_t launch_t(const BwdProblem &bp, cudaStream_t s) {
     }
     e = d.gate_dtype == GDN_F32 ? launch_rms_w<T, float>(bp, s) : launch_rms_w<T, T>(bp, s);
     if (e != cudaSuccess) return e;
-    if (slots > 0 && (e = launch_per_chunk(dterms_kernel<T>, dterms_smem_bytes(), bp, slots, s)) != cudaSuccess)
-        return e;
+    if (slots > 0) {
+        e = dterms_tc_supports(d) ? launch_dterms_tc(bp, slots, s)
+                                  : launch_per_chunk(dterms_kernel<T>, dterms_smem_bytes(), bp, slots, s);
+        if (e != cudaSuccess) return e;
+    }
     if ((e = launch_serial_nv<T>(bp, true, s)) != cudaSuccess) return e;
     if (slots > 0) {
         if (chunk_x_tc_supports(d)) {

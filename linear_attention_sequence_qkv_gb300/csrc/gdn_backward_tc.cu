@@ -316,7 +316,190 @@ __global__ void __launch_bounds__(kOThreads, 1) out_tc_kernel(const BwdProblem b
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// ------------------------------------------------------------ dO' terms
+// U = (diag(e^gam) Q)^T dO' ([dk][dv] per chunk slot and v head) and
+// W = Pm^T dO' ([64][dv] rows of the chunk's tokens): both contract over the
+// chunk's 64 tokens, so B = dO' (64 token rows x dv, MN-major) is built once and
+// each 128-row block of U, then W, is one tensor-memory product. The A
+// operands are the transposes of token-major data, i.e. MN-major tiles whose
+// rows are tokens (64 M columns per 8 KB block). dO' is a gradient (any scale),
+// so the operands are bf16, each split into hi = bf16(x) and lo = bf16(x - hi):
+// hi.hi + hi.lo + lo.hi carries about 16 significant bits (W and U feed the
+// reverse chain directly).
+
+// x -> (hi, lo) bf16 pairs of two values
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+__device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
+    split2(v[0], v[1], hi.x, lo.x);
+    split2(v[2], v[3], hi.y, lo.y);
+    split2(v[4], v[5], hi.z, lo.z);
+    split2(v[6], v[7], hi.w, lo.w);
+}
+
+__global__ void __launch_bounds__(kOThreads, 1) dterms_tc_kernel(const BwdProblem bp) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tslot;
+    __shared__ float egs[kChunk];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int dk = d.dk, dv = d.dv, Hv = d.Hv;
+    const int j = blockIdx.y;
+    const int64_t slot = blockIdx.x;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    ChunkLoc loc;
+    if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, loc)) return;
+    const int64_t tok0 = loc.tok0;
+    const int L = loc.len;
+    const int hk = j / (Hv / d.Hk);
+    // A hi / lo: 64 token rows x 128 M (two 8 KB blocks each); B hi / lo: 64 x dv
+    unsigned char *Ah = sm, *Al = sm + 16384, *Bh = sm + 32768, *Bl = Bh + 64 * (size_t)dv * 2;
+    const int t = threadIdx.x, warp = t >> 5;
+    if (t == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    if (t < kChunk) {
+        const int i = t < L ? t : L - 1;
+        egs[t] = expf(((const float *)p.gamma)[(int64_t)j * p.ntok + tok0 + i]);
+    }
+    if (warp == 0) tmem_alloc(&tslot, 512);
+    // B = dO' rows (tokens i < L), MN-major
+    const float *dOg = bp.dO + ((size_t)j * p.ntok + tok0) * dv;
+    for (int idx = t; idx < 64 * (dv / 8); idx += kOThreads) {
+        const int kr = idx / (dv / 8), n0 = 8 * (idx % (dv / 8));
+        uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
+        if (kr < L) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(dOg + (int64_t)kr * dv + n0));
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(dOg + (int64_t)kr * dv + n0 + 4));
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            split8(v, hi, lo);
+        }
+        const uint32_t off = (n0 / 64) * 8192 + sw128_off(kr, n0 % 64);
+        *reinterpret_cast<uint4 *>(Bh + off) = hi;
+        *reinterpret_cast<uint4 *>(Bl + off) = lo;
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = tslot;
+    const __half *qh = (const __half *)p.q + ((int64_t)hk * p.ntok + tok0) * dk;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * dk;
+    const float *Pm = bp.mats + ((size_t)slot * Hv + j) * 3 * kC2 + kC2;
+    float *U = bp.uq + ((size_t)slot * Hv + j) * dk * dv;
+    const int nmma = dv > 256 ? 2 : 1, nw = dv > 256 ? 256 : dv;
+    const uint32_t idesc = idesc_bf16(128, nw) | (1u << 15) | (1u << 16);   // A and B MN-major
+    const uint64_t dah = sw128_desc(smem_u32(Ah), 8192, 1024), dal = sw128_desc(smem_u32(Al), 8192, 1024);
+    const uint64_t dbh = sw128_desc(smem_u32(Bh), 8192, 1024), dbl = sw128_desc(smem_u32(Bl), 8192, 1024);
+    const int ublocks = (dk + 127) / 128;
+    bool ok = true;
+    for (int blk = 0; blk <= ublocks && ok; ++blk) {
+        const bool isw = blk == ublocks;                // the last block is W
+        // A rows = tokens (K), 128 M columns: dk indices [128 blk, +128) of e^gam Q, or Pm^T rows
+        for (int idx = t; idx < 64 * 16; idx += kOThreads) {
+            const int kr = idx / 16, m0 = 8 * (idx % 16);
+            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (isw) {
+                if (m0 < kChunk) {                      // Pm^T: A[m][i] = Pm[m][i], row m of Pm
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(Pm + kr * kChunk + m0));
+                    const float4 b = __ldg(reinterpret_cast<const float4 *>(Pm + kr * kChunk + m0 + 4));
+                    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+                }
+            } else {
+                const int dd = 128 * blk + m0;
+                if (kr < L && dd < dk) {
+                    float h[8], l[8];
+                    unpack16<__half>(*reinterpret_cast<const uint4 *>(qh + (int64_t)kr * dk + dd), h);
+                    unpack16<__half>(*reinterpret_cast<const uint4 *>(qh + (int64_t)kr * dk + dd + plane), l);
+                    const float e = egs[kr];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = e * (h[u] + l[u]);
+                }
+            }
+            uint4 hi, lo;
+            split8(v, hi, lo);
+            const uint32_t off = (m0 / 64) * 8192 + sw128_off(kr, m0 % 64);
+            *reinterpret_cast<uint4 *>(Ah + off) = hi;
+            *reinterpret_cast<uint4 *>(Al + off) = lo;
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (t == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)             // K = 16 tokens per MMA: 2048 bytes per step
+                for (int h = 0; h < nmma; ++h) {
+                    const uint64_t ak = (uint64_t)((2048 * ks) >> 4), bk = (uint64_t)((2048 * ks + 32768 * h) >> 4);
+                    mma_f16(tbase + 256 * h, dah + ak, dbh + bk, idesc, ks != 0);
+                    mma_f16(tbase + 256 * h, dah + ak, dbl + bk, idesc, 1);
+                    mma_f16(tbase + 256 * h, dal + ak, dbh + bk, idesc, 1);
+                }
+            mma_commit(&bar);
+        }
+        const bool done = mbar_wait(&bar, (uint32_t)blk & 1);
+        fence_after_sync();
+        if (__syncthreads_or(!done)) {
+            ok = false;
+            break;
+        }
+        // read out: row = TMEM lane (warp % 4), columns split between warps < 4 and >= 4
+        const int q4 = warp & 3, half = warp >> 2;
+        const int row = 32 * q4 + (t & 31);
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const bool useful = isw ? q4 < 2 : 128 * blk + 32 * q4 < dk;   // warp-uniform
+        if (useful) {
+            for (int c = half * (dv / 2); c < (half + 1) * (dv / 2); c += 32) {
+                float v[32];
+                tmem_ld32(tbase + lane_off + c, v);
+                float *dst = nullptr;
+                if (isw) {
+                    if (row < L) dst = bp.wv + ((size_t)j * p.ntok + tok0 + row) * dv + c;
+                } else {
+                    dst = U + (size_t)(128 * blk + row) * dv + c;
+                }
+                if (dst) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) st4f(dst + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            }
+        }
+        // the tensor-memory reads are done before the next block's products
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
+    if (!ok) {
+        if (t == 0) *p.status = GDN_ERR_DEVICE_TIMEOUT;
+        mbar_wait(&bar, (uint32_t)ublocks & 1);
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
 }  // namespace
+
+bool dterms_tc_supports(const gdn_desc &d) {
+    return d.dtype != GDN_F32 && d.dk % 64 == 0 && d.dv % 64 == 0 && d.dv <= 512 && d.dv >= 64;
+}
+
+cudaError_t launch_dterms_tc(const BwdProblem &bp, int64_t slots, cudaStream_t s) {
+    const gdn_desc &d = bp.f.d;
+    const size_t bytes = 1024 + 32768 + 2 * 64 * (size_t)d.dv * 2;
+    cudaError_t e = cudaFuncSetAttribute(dterms_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    dterms_tc_kernel<<<dim3((unsigned)slots, d.Hv), kOThreads, bytes, s>>>(bp);
+    return cudaGetLastError();
+}
 
 bool out_tc_supports(const gdn_desc &d) {
     return d.dtype != GDN_F32 && d.dk % 64 == 0 && d.dv % 64 == 0 && d.dv <= 512 && d.dv >= 64;

@@ -184,6 +184,9 @@ cudaError_t launch_chunk_x_tc(const BwdProblem &p, int64_t slots, cudaStream_t s
 // the outputs O on the tensor cores (gdn_backward_tc.cu)
 bool out_tc_supports(const gdn_desc &d);
 cudaError_t launch_out_tc(const BwdProblem &p, int64_t slots, cudaStream_t s);
+// the dO' terms U, W on the tensor cores (gdn_backward_tc.cu)
+bool dterms_tc_supports(const gdn_desc &d);
+cudaError_t launch_dterms_tc(const BwdProblem &p, int64_t slots, cudaStream_t s);
 
 // Decode (one token per sequence, d.T == 1): workspace regions, all fp32 but o.
 struct DecodeLayout {
