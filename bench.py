@@ -415,11 +415,13 @@ def backward_main(args, w):
     fl = backward_flops(w, ntok)
     ach = fl / (ms_b / 1e3) / 1e12
     tc = gdn.gdn_chunk_kernel_kind(d) == 1
-    # forward: prologue (+ scan), chunk stage, epilogue; backward: prologue, scan,
-    # the fp32 chunk kernel with stores, rms, chain, per-chunk, prologue and conv
-    # backward, four sums
+    # forward: prologue (+ scan), chunk stage, epilogue; backward: prologue (+ scan),
+    # chunk matrices, state recompute, outputs, RMSNorm backward, dO' terms,
+    # reverse chain, (tensor-core dv contractions,) per-chunk gradients, prologue
+    # and conv backward, four sums
     scan = 1 if inp.cu_seqlens is not None else 0
-    launches = (2 + scan + (2 if tc else 1)) + (1 + scan + 1 + 3 + 2 + 4)
+    bwd_tc = w.dtype != "fp32" and w.dk in (64, 128, 256) and w.dv % 64 == 0
+    launches = (2 + scan + (2 if tc else 1)) + (1 + scan + 9 + (1 if bwd_tc else 0) + 4)
 
     e2e = None
     if not args.no_e2e:
@@ -478,7 +480,8 @@ def backward_main(args, w):
         "config": {"workload": f"fwd_bwd_{w.name}", "B": d.B, "T": d.T, "N": d.N, "Hk": w.Hk, "Hv": w.Hv,
                    "dk": w.dk, "dv": w.dv, "tokens_per_step": ntok, "chunk": CHUNK,
                    "l2": "flushed before every timed step (512 MiB write)",
-                   "fwd_ms": ms_f, "bwd_ms": ms_b, "bwd_arith": "fp32 CUDA cores"},
+                   "fwd_ms": ms_f, "bwd_ms": ms_b, "bwd_arith": ("fp32 CUDA cores; outputs, dO' terms and the per-chunk dv contractions on tcgen05"
+                                                 if bwd_tc else "fp32 CUDA cores")},
         "roofline": {"bound": "alu", "achieved": ach, "peak": pk_alu, "unit": "TFLOP/s", "frac": ach / pk_alu,
                      "algorithmic_flops": fl, "ms": ms_b, "traffic": None,
                      "kernel": "gdn_backward (recompute, rms, chain, per-chunk, prologue, conv, sums)",
