@@ -17,19 +17,20 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 
-// Rows (token, v head) of one thread: consecutive rows, so that one division
-// locates the first and the rest follow by carrying the head index.
-template <int NVEC> struct EpiRows { static constexpr int R = 2; };
+// Rows (token, v head) of one thread: R consecutive rows, so that one division
+// locates the first and the rest follow by carrying the head index. Small
+// problems take R = 2 (more, smaller CTAs: a shorter tail), large ones R = 4
+// (more loads in flight per thread).
+constexpr int64_t kManyRows = 1 << 20;
 
-template <typename T, typename G, typename W, int NVEC, bool GVEC>
+template <typename T, typename G, typename W, int NVEC, bool GVEC, int R>
 __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     constexpr int VEC = Vec16<T>::N;
     constexpr int CPT = NVEC * VEC;            // columns per thread
     constexpr int NP = CPT / 2;                // column pairs per thread
     constexpr int GN = GVEC ? CPT * (int)sizeof(G) / 16 : 1;   // 16-byte gate vectors
-    constexpr int R = EpiRows<NVEC>::R;
     using S = typename Inter<T>::S;            // storage of o
     // norm weights, one padding slot after every CPT of them: lane l reads
     // [l*(CPT+1), +CPT) without bank conflicts
@@ -142,19 +143,25 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
         *p.status = GDN_ERR_DEVICE_RANGE;
 }
 
-template <typename T, typename G, typename W, int NVEC>
-cudaError_t launch_g(const Problem &p, cudaStream_t s) {
+template <typename T, typename G, typename W, int NVEC, int R>
+cudaError_t launch_r(const Problem &p, cudaStream_t s) {
     constexpr int CPT = NVEC * Vec16<T>::N;
     const int lpr = p.d.dv / CPT;
-    const int rows_per_block = kThreads / lpr * EpiRows<NVEC>::R;
+    const int rows_per_block = kThreads / lpr * R;
     const int64_t nrows = p.ntok * p.d.Hv;
     const int64_t blocks = (nrows + rows_per_block - 1) / rows_per_block;
     const size_t gs = sizeof(G);
     const bool gvec = ((uintptr_t)p.gate % 16 == 0) && ((p.d.gate_stride_b * gs) % 16 == 0) &&
                       ((p.d.gate_stride_t * gs) % 16 == 0) && ((CPT * gs) % 16 == 0);
-    if (gvec) epilogue_kernel<T, G, W, NVEC, true><<<(unsigned)blocks, kThreads, 0, s>>>(p);
-    else epilogue_kernel<T, G, W, NVEC, false><<<(unsigned)blocks, kThreads, 0, s>>>(p);
+    if (gvec) epilogue_kernel<T, G, W, NVEC, true, R><<<(unsigned)blocks, kThreads, 0, s>>>(p);
+    else epilogue_kernel<T, G, W, NVEC, false, R><<<(unsigned)blocks, kThreads, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+template <typename T, typename G, typename W, int NVEC>
+cudaError_t launch_g(const Problem &p, cudaStream_t s) {
+    if (p.ntok * p.d.Hv >= kManyRows) return launch_r<T, G, W, NVEC, 4>(p, s);
+    return launch_r<T, G, W, NVEC, 2>(p, s);
 }
 
 template <typename T, typename G, typename W>
