@@ -246,6 +246,10 @@ int forward_impl(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
     p.out = out;
     p.single_stream = single_stream;
     p.conv_prefix = conv_prefix;
+    // prologue -> prep -> chain -> epilogue back to back on one stream (the
+    // plain tensor-core chunk stage): each later kernel is a programmatic
+    // dependent of the one before it
+    p.pdl = !single_stream && p.ntok > 0 && gdn::chunk_tc_supports(*d) && !gdn::chunk_tc_segmented(p);
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_prologue(p, s)) != GDN_OK) return rc;
     if ((rc = run_chunk(p, s)) != GDN_OK) return rc;

@@ -149,6 +149,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3) chunk_prep_kernel(const __gri
                                                                      const Problem p, int64_t nslots,
                                                                      unsigned char *tpt, int64_t slot_base) {
     extern __shared__ unsigned char smraw[];
+    pdl_wait();       // the prologue's q, k, beta, gamma (and status) are complete
+    pdl_trigger();
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const gdn_desc &d = p.d;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -478,6 +480,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles,
                    int64_t nslots, const unsigned char *prep_out, int cbase, int cmax) {
     extern __shared__ unsigned char smraw[];
+    pdl_wait();       // the prep tiles (and everything before them) are complete
+    pdl_trigger();
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const gdn_desc &d = p.d;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -961,9 +965,9 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
                                              (int)ps.total);
         if (e != cudaSuccess) return e;
         if (nslots > 0) {
-            chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt,
-                                                                                           (int64_t)0);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            e = launch_kernel(p.pdl, chunk_prep_kernel, dim3((unsigned)nslots, d.Hk), dim3(kPrepThreads), ps.total, s,
+                              pm, p, nslots_alloc, tpt, (int64_t)0);
+            if (e != cudaSuccess) return e;
         }
     }
     ChainMaps cm;
@@ -987,9 +991,8 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
     const int ntiles = d.dv / 64;
     const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
     if (blocks == 0) return cudaSuccess;
-    chain<<<(unsigned)blocks, kChainThreads, smem, s>>>(cm, p, ntiles, nslots_alloc, tpt, 0,
-                                                                   0x7fffffff);
-    return cudaGetLastError();
+    return launch_kernel(p.pdl && p.ntok > 0, chain, dim3((unsigned)blocks), dim3(kChainThreads), smem, s, cm, p, ntiles,
+                         nslots_alloc, (const unsigned char *)tpt, 0, 0x7fffffff);
 }
 
 // One long sequence whose chain occupies at most half of the SMs: the chunks are

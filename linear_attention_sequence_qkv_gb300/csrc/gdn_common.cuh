@@ -10,6 +10,35 @@
 
 namespace gdn {
 
+// Programmatic dependent launch. A kernel launched with the programmatic
+// stream-serialisation attribute may start while the kernel before it on the
+// stream is still running; pdl_wait() returns once that kernel has completed
+// and its writes are visible (at once when the kernel was launched plainly).
+// pdl_trigger() lets the next such kernel launch as soon as every CTA of this
+// one has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args &&...args) {
+    if (!pdl) {
+        kernel<<<grid, block, smem, s>>>(static_cast<Args &&>(args)...);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 constexpr int kChunk = 64;   // chunk length of the chunked gated delta rule
 constexpr int kConvW = 4;    // short-conv taps
 

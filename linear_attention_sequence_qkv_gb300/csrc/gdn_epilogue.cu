@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(const Problem p) {
     const gdn_desc &d = p.d;
     const int dv = d.dv;
     for (int i = threadIdx.x; i < dv; i += kThreads) nwp[(i / CPT) * (CPT + 1) + i % CPT] = to_f<W>(((const W *)p.norm_w)[i]);
+    pdl_wait();       // o (and the status word) of the chunk stage are complete
 
     const int lpr = dv / CPT;                  // lanes per row (power of two, <= 32)
     const int rows_per_pass = kThreads / lpr;
@@ -153,9 +154,8 @@ cudaError_t launch_r(const Problem &p, cudaStream_t s) {
     const size_t gs = sizeof(G);
     const bool gvec = ((uintptr_t)p.gate % 16 == 0) && ((p.d.gate_stride_b * gs) % 16 == 0) &&
                       ((p.d.gate_stride_t * gs) % 16 == 0) && ((CPT * gs) % 16 == 0);
-    if (gvec) epilogue_kernel<T, G, W, NVEC, true, R><<<(unsigned)blocks, kThreads, 0, s>>>(p);
-    else epilogue_kernel<T, G, W, NVEC, false, R><<<(unsigned)blocks, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    auto kernel = gvec ? epilogue_kernel<T, G, W, NVEC, true, R> : epilogue_kernel<T, G, W, NVEC, false, R>;
+    return launch_kernel(p.pdl, kernel, dim3((unsigned)blocks), dim3(kThreads), 0, s, p);
 }
 
 template <typename T, typename G, typename W, int NVEC>

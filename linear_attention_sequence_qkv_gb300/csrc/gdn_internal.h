@@ -76,6 +76,10 @@ struct Problem {
     void *gamma;                  // float, or double for fp32 activations
     void *tpt;                    // [T; P T] tiles of the tensor-core kernels
     bool single_stream;           // no side stream (the no-allocation entry point)
+    // launch the chunk kernels and the epilogue as programmatic dependents of the
+    // kernel before them on the stream (their CTAs become resident while that
+    // kernel drains and wait for its completion on the device)
+    bool pdl;
     // null, or act dtype [N][3][2*Hk*dk + Hv*dv]: the raw q|k|v inputs of the three
     // tokens before each sequence (oldest first), read by the conv instead of zeros
     const void *conv_prefix;

@@ -325,6 +325,7 @@ __device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c, 
 template <typename T, int NVEC, bool PRE>
 __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueArgs A) {
     extern __shared__ uint4 stage[];
+    pdl_trigger();    // the chunk stage's CTAs may become resident during the last wave
     const Problem &p = A.p;
     if (p.cu == nullptr) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = GDN_OK;
