@@ -43,8 +43,8 @@ CHUNK = 64
 # one launch each per step; the figure is the sum of the two launches.
 NCU_TRAFFIC: dict = {
     "chunk_rule": ("linear_attention_sequence_qkv_gb300/csrc/gdn_chunk_tc.cu",
-                   "3ae2f4b49bc143a3efc3edb71133333d767427d4ab5e306de2bad2040fc5841a",
-                   "layer_bf16", 117_354_752),
+                   "e71db4afea5b4bc63b933a21fb48af13222bd6255977ddd2561ade40b6736601",
+                   "layer_bf16", 115_235_072),
 }
 
 
@@ -419,7 +419,8 @@ def backward_main(args, w):
     ach = fl / (ms_b / 1e3) / 1e12
     tc = gdn.gdn_chunk_kernel_kind(d) == 1
     # forward: prologue (+ scan), chunk stage, epilogue; backward: prologue (+ scan),
-    # chunk matrices, state recompute, outputs, RMSNorm backward, dO' terms,
+    # chunk matrices, the state recompute and outputs (on the tensor-core path the
+    # forward's prep and chain with fp32 stores), RMSNorm backward, dO' terms,
     # reverse chain, (tensor-core dv contractions,) per-chunk gradients, prologue
     # and conv backward, four sums
     scan = 1 if inp.cu_seqlens is not None else 0

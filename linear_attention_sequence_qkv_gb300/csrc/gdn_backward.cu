@@ -1317,10 +1317,22 @@ cudaError_t launch_t(const BwdProblem &bp, cudaStream_t s) {
     const int64_t slots = chunk_slots(p);
     cudaError_t e = cudaSuccess;
     if (slots > 0 && (e = launch_per_chunk(mats_kernel<T>, mats_smem_bytes(), bp, slots, s)) != cudaSuccess) return e;
-    if ((e = launch_serial_nv<T>(bp, false, s)) != cudaSuccess) return e;
-    if (slots > 0) {
-        e = out_tc_supports(d) ? launch_out_tc(bp, slots, s) : launch_per_chunk(out_kernel<T>, out_smem_bytes(), bp, slots, s);
-        if (e != cudaSuccess) return e;
+    if (sizeof(T) == 2 && p.ntok > 0 && chunk_tc_supports(d)) {
+        // the forward's tensor-core chunk stage recomputes H0, Vn and O (fp32 stores)
+        Problem pr = p;
+        pr.rec_h0 = bp.h0;
+        pr.rec_vn = bp.vn;
+        pr.rec_o = bp.dO;
+        pr.hT = nullptr;
+        pr.pdl = false;
+        if ((e = launch_chunk_tc_rec(pr, s)) != cudaSuccess) return e;
+    } else {
+        if ((e = launch_serial_nv<T>(bp, false, s)) != cudaSuccess) return e;
+        if (slots > 0) {
+            e = out_tc_supports(d) ? launch_out_tc(bp, slots, s)
+                                   : launch_per_chunk(out_kernel<T>, out_smem_bytes(), bp, slots, s);
+            if (e != cudaSuccess) return e;
+        }
     }
     e = d.gate_dtype == GDN_F32 ? launch_rms_w<T, float>(bp, s) : launch_rms_w<T, T>(bp, s);
     if (e != cudaSuccess) return e;

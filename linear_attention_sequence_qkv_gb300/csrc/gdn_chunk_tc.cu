@@ -93,6 +93,12 @@ __device__ __forceinline__ void store_half_row_f16(unsigned char *tile, int row,
         *reinterpret_cast<uint4 *>(tile + sw128_off(row, c0 + 8 * c)) = u;
     }
 }
+// 32 fp32 to a 16-byte-aligned global row slice
+__device__ __forceinline__ void store_row_f32(float *dst, const float *v32) {
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v32[4 * q], v32[4 * q + 1], v32[4 * q + 2], v32[4 * q + 3]);
+}
 __device__ __forceinline__ void load_half_row_f16(const unsigned char *tile, int row, int c0, float *v32) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -475,7 +481,9 @@ constexpr int kMaxStages = 3;
 enum ChainBar { B_LOAD0 = 0, B_LQ0 = B_LOAD0 + kMaxStages, B_TPT = B_LQ0 + kMaxStages, B_QF0, B_KF0 = B_QF0 + kMaxStages,
                 B_C1 = B_KF0 + kMaxStages, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_COUNT };
 
-template <int NS>   // stages: 3 where they fit (dk <= 128), else 2
+// NS stages: 3 where they fit (dk <= 128), else 2. REC: the backward's
+// recompute, storing the state at each chunk's start, Vn and O in fp32.
+template <int NS, bool REC = false>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles,
                    int64_t nslots, const unsigned char *prep_out, int cbase, int cmax) {
@@ -518,6 +526,10 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     const __half *vw = (const __half *)p.v + (int64_t)j * p.ntok * dv;
     __half *o = (__half *)p.o;
     const bool state_warp = warp >= kRowWarps && warp < kMmaWarp;
+    // row hrow, columns c0..c0+31 of this tile in the recompute's state at chunk c's start
+    auto rec_h0_row = [&](int c, int hrow) {
+        return p.rec_h0 + ((size_t)(slot0 + c) * Hv + j) * dk * dv + (size_t)hrow * dv + v0 + c0;
+    };
 
     if (tid == 0) {
         s_err = 0;
@@ -585,6 +597,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             }
             tmem_st32(tH + 64 * h, t);
             if (hrow < dk) store_half_row_f16(h16, hrow, c0, t);
+            if (REC && hrow < dk && nchunks > 0) store_row_f32(rec_h0_row(0, hrow), t);
         }
     }
     fence_async_smem();
@@ -772,6 +785,12 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 for (int q = 0; q < 32; ++q) a[q] *= sc;
                 store_half_row_f16(vn16, r, c0, a);
                 warp_arrive(B_VN);
+                if (REC) {
+                    // D2 stays until this warp's next B_R arrival lets the next C2 in;
+                    // the load is warp-collective, only the store depends on the row
+                    tmem_ld32(tD2, a);
+                    if (r < len) store_row_f32(p.rec_vn + ((int64_t)j * p.ntok + t0 + r) * dv + v0 + c0, a);
+                }
                 // the next chunk's operands only now: the proxy fence of an arrival
                 // waits for this thread's loads in flight, so none may be pending
                 // at the two arrivals on the serial path
@@ -788,7 +807,12 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[B_O]);
-                if (r < len) {
+                if (REC && r < len) {
+                    const float eg = __expf(gr);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) a[q] = fmaf(eg, a[q], b2[q]) * d.scale;
+                    store_row_f32(p.rec_o + ((int64_t)j * p.ntok + t0 + r) * dv + v0 + c0, a);
+                } else if (!REC && r < len) {
                     const float eg = __expf(gr);
                     uint4 *dst = reinterpret_cast<uint4 *>(o + ((t0 + r) * Hv + j) * (int64_t)dv + v0 + c0);
 #pragma unroll
@@ -820,12 +844,14 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 for (int q = 0; q < 8; ++q) dst[q] = make_float4(t[4 * q], t[4 * q + 1], t[4 * q + 2], t[4 * q + 3]);
             }
         };
-        auto scale_state = [&](float e, bool copy) {
+        // rec_c >= 0: the state read is H0 of chunk rec_c (REC only)
+        auto scale_state = [&](float e, bool copy, int rec_c) {
             for (int h = 0; h < halves; ++h) {
                 const int hrow = 128 * h + row;
                 if (hrow >= dk) continue;
                 float t[32];
                 tmem_ld32(tH + 64 * h, t);
+                if (REC && rec_c >= 0) store_row_f32(rec_h0_row(rec_c, hrow), t);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) t[q] *= e;
                 tmem_st32(tH + 64 * h, t);
@@ -836,14 +862,14 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             // chunk 0's first product has read h16 = H_init: scale for chunk 0's
             // update and publish e^{gL_0} H_init for chunk 1
             if (wait(B_C1, 0)) {
-                scale_state(__expf(gamma_last(0)), nchunks > 1);
+                scale_state(__expf(gamma_last(0)), nchunks > 1, -1);
                 warp_arrive(B_H);
                 for (int c = 0; c < nchunks; ++c) {
                     const float gl_next = c + 1 < nchunks ? gamma_last(c + 1) : 0.f;
                     if (!wait(B_C4, c & 1)) break;
                     fence_after_sync();
                     if (c + 1 < nchunks) {
-                        scale_state(__expf(gl_next), c + 2 < nchunks);
+                        scale_state(__expf(gl_next), c + 2 < nchunks, c + 1);
                         warp_arrive(B_H);
                     }
                 }
@@ -993,6 +1019,49 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
     if (blocks == 0) return cudaSuccess;
     return launch_kernel(p.pdl && p.ntok > 0, chain, dim3((unsigned)blocks), dim3(kChainThreads), smem, s, cm, p, ntiles,
                          nslots_alloc, (const unsigned char *)tpt, 0, 0x7fffffff);
+}
+
+// The backward's recompute: the same prep and chain launches on one stream, the
+// chain instantiated with the stores of the state at every chunk's start, Vn and
+// O in fp32 (p.rec_h0 / rec_vn / rec_o) in place of the 16-bit o.
+cudaError_t launch_chunk_tc_rec(const Problem &p, cudaStream_t s) {
+    const gdn_desc &d = p.d;
+    if (!p.rec_h0 || !p.rec_vn || !p.rec_o) return cudaErrorInvalidValue;
+    const int64_t nslots_alloc = chunk_slot_bound(d);
+    const int64_t nslots = chunk_slots(p);
+    if (nslots > nslots_alloc || p.tpt == nullptr || p.ntok == 0) return cudaErrorInvalidValue;
+    unsigned char *tpt = (unsigned char *)p.tpt;
+    const int64_t plane = (int64_t)d.Hk * p.ntok * d.dk;
+    PrepMaps pm;
+    ChainMaps cm;
+    const __half *q = (const __half *)p.q, *k = (const __half *)p.k;
+    if (!encode_tile_map(&pm.q_hi, q, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&pm.q_lo, q + plane, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&pm.k_hi, k, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&pm.k_lo, k + plane, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&cm.q_hi, p.q, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&cm.k_hi, p.k, (uint64_t)d.Hk * p.ntok, d.dk) ||
+        !encode_tile_map(&cm.v, p.v, (uint64_t)d.Hv * p.ntok, d.dv))
+        return cudaErrorInvalidValue;
+    const PrepSmem ps(d.dk);
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)ps.total);
+    if (e != cudaSuccess) return e;
+    chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt,
+                                                                                   (int64_t)0);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int maxs = max_dyn_smem();
+    const ChainSmem cs(d.dk);
+    const size_t smem = cs.total > (size_t)(maxs / 2 + 1024) ? cs.total : (size_t)(maxs / 2 + 1024);
+    if ((int)smem > maxs) return cudaErrorInvalidValue;
+    auto chain = cs.stages == 3 ? chunk_chain_kernel<3, true> : chunk_chain_kernel<2, true>;
+    if ((e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+    const int ntiles = d.dv / 64;
+    const int64_t blocks = (int64_t)d.N * d.Hv * ntiles;
+    if (blocks == 0) return cudaSuccess;
+    chain<<<(unsigned)blocks, kChainThreads, smem, s>>>(cm, p, ntiles, nslots_alloc, tpt, 0, 0x7fffffff);
+    return cudaGetLastError();
 }
 
 // One long sequence whose chain occupies at most half of the SMs: the chunks are

@@ -80,6 +80,11 @@ struct Problem {
     // kernel before them on the stream (their CTAs become resident while that
     // kernel drains and wait for its completion on the device)
     bool pdl;
+    // null in the forward. The backward's recompute through the tensor-core chunk
+    // stage: the chain also stores the fp32 state at every chunk's start
+    // ([slot][Hv][dk][dv]), the new values Vn and the outputs O in fp32
+    // ([Hv][ntok][dv] each), and not the 16-bit o.
+    float *rec_h0, *rec_vn, *rec_o;
     // null, or act dtype [N][3][2*Hk*dk + Hv*dv]: the raw q|k|v inputs of the three
     // tokens before each sequence (oldest first), read by the conv instead of zeros
     const void *conv_prefix;
@@ -98,6 +103,8 @@ cudaError_t launch_chunk_simt(const Problem &p, cudaStream_t s);
 cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s);
 // a long single sequence: prep and chain in segments on two streams
 bool chunk_tc_segmented(const Problem &p);
+// the chunk stage with the recompute stores (p.rec_* set), one stream, no segments
+cudaError_t launch_chunk_tc_rec(const Problem &p, cudaStream_t s);
 cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s);
 // gdn_forward on one stream only (used by gdn_forward_static_ws)
 int forward_single_stream(const gdn_desc *d, const void *q_raw, const void *k_raw, const void *v_raw,
