@@ -484,7 +484,8 @@ def backward_main(args, w):
         "config": {"workload": f"fwd_bwd_{w.name}", "B": d.B, "T": d.T, "N": d.N, "Hk": w.Hk, "Hv": w.Hv,
                    "dk": w.dk, "dv": w.dv, "tokens_per_step": ntok, "chunk": CHUNK,
                    "l2": "flushed before every timed step (512 MiB write)",
-                   "fwd_ms": ms_f, "bwd_ms": ms_b, "bwd_arith": ("fp32 CUDA cores; outputs, dO' terms and the per-chunk dv contractions on tcgen05"
+                   "fwd_ms": ms_f, "bwd_ms": ms_b, "bwd_arith": ("state recompute and outputs through the forward's tcgen05 chunk stage; dO' terms "
+                                                  "and the per-chunk dv contractions on tcgen05; the rest fp32 CUDA cores"
                                                  if bwd_tc else "fp32 CUDA cores")},
         "roofline": {"bound": "alu", "achieved": ach, "peak": pk_alu, "unit": "TFLOP/s", "frac": ach / pk_alu,
                      "algorithmic_flops": fl, "ms": ms_b, "traffic": None,
