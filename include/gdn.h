@@ -314,6 +314,7 @@ int gdn_span_scan(int spans, int Hv, int dk, int dv, const float *A, const float
  * grad_out    act dtype [B*T][Hv][dv] contiguous (the gradient of out).
  * grad_final  fp32 [N][Hv][dk][dv] (S^T layout of final_state), or NULL = zeros.
  * dq_raw, dk_raw  act dtype, dense [B*T][Hk*dk]; dv_raw act dtype [B*T][Hv*dv];
+ *             these three 16-byte aligned;
  * da, db      act dtype [B*T][Hv]; dgate gate dtype [B*T][Hv*dv] (all dense,
  *             whatever the strides of the inputs);
  * dconv_w     fp32 [2*Hk*dk+Hv*dv][4]; dA_log, ddt_bias fp32 [Hv];

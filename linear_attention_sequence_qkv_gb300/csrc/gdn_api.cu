@@ -417,7 +417,7 @@ int gdn_backward(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
         !conv_w || !A_log || !dt_bias || !norm_w || !dconv_w || !dA_log || !ddt_bias || !dnorm_w)
         return GDN_ERR_INVALID_ARG;
     if (!aligned(q_raw, 16) || !aligned(k_raw, 16) || !aligned(v_raw, 16) || !aligned(conv_w, 16) ||
-        !aligned(norm_w, 4))
+        !aligned(norm_w, 4) || !aligned(dq_raw, 16) || !aligned(dk_raw, 16) || !aligned(dv_raw, 16))
         return GDN_ERR_INVALID_ARG;
     if ((initial_state && !aligned(initial_state, 16)) || (grad_final && !aligned(grad_final, 16)) ||
         (dinitial_state && !aligned(dinitial_state, 16)))

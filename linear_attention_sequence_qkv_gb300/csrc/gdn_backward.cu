@@ -1067,160 +1067,343 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_grad_kernel(const BwdProble
     }
 }
 
+// 4 adjacent act-dtype values as fp32 and back (8- or 16-byte accesses)
+template <typename T> __device__ __forceinline__ float4 ld4_act(const T *p) {
+    if constexpr (sizeof(T) == 4) {
+        return *reinterpret_cast<const float4 *>(p);
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        const T *h = reinterpret_cast<const T *>(&u);
+        return make_float4(to_f<T>(h[0]), to_f<T>(h[1]), to_f<T>(h[2]), to_f<T>(h[3]));
+    }
+}
+template <typename T> __device__ __forceinline__ void st4_act(T *p, float4 v) {
+    if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float4 *>(p) = v;
+    } else {
+        uint2 u;
+        T *h = reinterpret_cast<T *>(&u);
+        h[0] = from_f<T>(v.x); h[1] = from_f<T>(v.y); h[2] = from_f<T>(v.z); h[3] = from_f<T>(v.w);
+        *reinterpret_cast<uint2 *>(p) = u;
+    }
+}
+__device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {
+    return make_float4(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y), fmaf(a.z, b.z, c.z), fmaf(a.w, b.w, c.w));
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
 // ------------------------------------------------------------ prologue backward
-// Sum of v over the CTA, the same total in every thread (fixed order).
-__device__ __forceinline__ float block_sum(float v, float *red) {
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float t = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-    return t;
-}
+// One 1-D grid of 256-thread CTAs in three ranges. Each item recomputes the conv
+// pre-activation z of its channels and writes dz = dL/dz ([ntok][ch]):
+//   * q/k: a group of dk / CPL lanes per (token, q or k head), CPL adjacent
+//     channels per lane; the L2-norm backward's two sums over the head are
+//     shuffle reductions within the group;
+//   * v: one thread per 4 adjacent channels of a token;
+//   * beta / decay: one thread per (token, v head): db, da and the per-token
+//     terms of ddt_bias and dA_log.
+constexpr int kProThreads = 256;
 
-// grid (token, 2*Hk q/k heads + v channel groups + 1 beta/decay unit). Recomputes
-// the conv pre-activation z of the token and writes dz = dL/dz ([ntok][ch]);
-// the beta / decay unit writes db, da and the per-token terms of ddt_bias and dA_log.
-// one token of the prologue backward (all threads of the CTA take part)
-template <typename T>
-__device__ __forceinline__ void prologue_bwd_token(const BwdProblem &bp, int units_v, int64_t t, float *red) {
-    const Problem &p = bp.f;
-    const gdn_desc &d = p.d;
-    const int u = blockIdx.y, tid = threadIdx.x;
-    int64_t s0, s1, b, tau;
-    seq_of(d, p.cu, t, s0, s1);
-    tok_pos(d, t, b, tau);
-    const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
-    const T *w = (const T *)p.conv_w;
-    // z of channel c_in of input x (batch row b), conv weights of row cw
-    auto conv_z = [&](const T *x, int64_t sb, int64_t st, int c_in, int cw) {
-        float z = 0.f;
+template <typename T, int N> __device__ __forceinline__ void ld_act_n(const T *p, float *out) {
+    if constexpr (N % 4 == 0) {
 #pragma unroll
-        for (int m = 0; m < kConvW; ++m) {
-            const int64_t back = kConvW - 1 - m;
-            if (t - back >= s0) z = fmaf(to_f<T>(w[(int64_t)cw * kConvW + m]), to_f<T>(x[b * sb + (tau - back) * st + c_in]), z);
-        }
-        return z;
-    };
-    if (u < 2 * d.Hk) {
-        const bool isk = u >= d.Hk;
-        const int h = isk ? u - d.Hk : u;
-        const int i = tid;
-        const bool act = i < d.dk;
-        float z = 0.f, y = 0.f;
-        if (act) {
-            z = isk ? conv_z((const T *)p.k_raw, d.k_stride_b, d.k_stride_t, h * d.dk + i, ch_qk + h * d.dk + i)
-                    : conv_z((const T *)p.q_raw, d.q_stride_b, d.q_stride_t, h * d.dk + i, h * d.dk + i);
-            y = z * sigm(z);
-        }
-        const float rho = 1.0f / sqrtf(block_sum(y * y, red) + d.l2_eps);
-        const float xn = y * rho;
-        float dxn = 0.f;
-        if (act) {
-            const int G = d.Hv / d.Hk;
-            const float *src = isk ? bp.dk : bp.dq;
-            for (int jj = h * G; jj < (h + 1) * G; ++jj) dxn += src[((int64_t)jj * p.ntok + t) * d.dk + i];
-        }
-        const float dot = block_sum(xn * dxn, red);
-        if (act) bp.dz[t * ch + (isk ? ch_qk : 0) + h * d.dk + i] = rho * (dxn - xn * dot) * dsilu(z);
-    } else if (u < 2 * d.Hk + units_v) {
-        const int cv = (u - 2 * d.Hk) * (int)blockDim.x + tid;
-        if (cv < ch_v) {
-            const float z = conv_z((const T *)p.v_raw, d.v_stride_b, d.v_stride_t, cv, 2 * ch_qk + cv);
-            const int jh = cv / d.dv;
-            const int64_t r = (int64_t)jh * p.ntok + t;
-            bp.dz[t * ch + 2 * ch_qk + cv] = p.beta[r] * bp.dR[r * d.dv + (cv - jh * d.dv)] * dsilu(z);
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 f = ld4_act<T>(p + 4 * q);
+            out[4 * q] = f.x; out[4 * q + 1] = f.y; out[4 * q + 2] = f.z; out[4 * q + 3] = f.w;
         }
     } else {
-        for (int h = tid; h < d.Hv; h += blockDim.x) {
-            const float av = to_f<T>(((const T *)p.a)[b * d.a_stride_b + tau * d.a_stride_t + h]);
-            const float bv = to_f<T>(((const T *)p.b)[b * d.b_stride_b + tau * d.b_stride_t + h]);
-            const int64_t r = (int64_t)h * p.ntok + t;
-            const float be = sigm(bv);
-            ((T *)bp.db)[t * d.Hv + h] = from_f<T>(bp.dbeta[r] * be * (1.0f - be));
-            const float x = av + p.dt_bias[h], eA = expf(p.A_log[h]);
-            const float dg = bp.dgam[r];
-            const float dx = -dg * eA * sigm(x);
-            ((T *)bp.da)[t * d.Hv + h] = from_f<T>(dx);
-            bp.pa[r] = dx;
-            bp.pa[(int64_t)d.Hv * p.ntok + r] = dg * (-eA * softplus_f(x));
+#pragma unroll
+        for (int q = 0; q < N; ++q) out[q] = to_f<T>(p[q]);
+    }
+}
+template <int N> __device__ __forceinline__ void ld_f32_n(const float *p, float *out) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 f = ld4(p + 4 * q);
+            out[4 * q] = f.x; out[4 * q + 1] = f.y; out[4 * q + 2] = f.z; out[4 * q + 3] = f.w;
         }
+    } else {
+#pragma unroll
+        for (int q = 0; q < N; ++q) out[q] = p[q];
     }
 }
 
-constexpr int kProTokens = 8;   // tokens per CTA of the prologue backward
-
-template <typename T>
-__global__ void __launch_bounds__(512) prologue_bwd_kernel(const BwdProblem bp, int units_v) {
-    __shared__ float red[16];
-    const Problem &p = bp.f;
-    if (p.cu != nullptr && *p.status != GDN_OK) return;
-    const int64_t tb = (int64_t)blockIdx.x * kProTokens;
-    const int64_t te = tb + kProTokens < p.ntok ? tb + kProTokens : p.ntok;
-    for (int64_t t = tb; t < te; ++t)
-        prologue_bwd_token<T>(bp, units_v, t, red);
-}
-// ------------------------------------------------------------ conv backward
-// grid (blocks of kBwdConvTokens tokens, channel groups of 256): per channel,
-// dx_t = sum_m w_m dz_{t+3-m} within the sequence, and the block's partial
-// sums of dw_m = sum_t dz_t x_{t-3+m}.
-template <typename T>
-__global__ void __launch_bounds__(kThreads) conv_bwd_kernel(const BwdProblem bp) {
-    const Problem &p = bp.f;
-    const gdn_desc &d = p.d;
-    const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
-    const int c = blockIdx.y * kThreads + threadIdx.x;
-    if (c >= ch) return;
-    if (p.cu != nullptr && *p.status != GDN_OK) return;
-    const T *x;
-    T *dx;
-    int64_t sb, st, ostride;
-    int c_in;
-    if (c < ch_qk) {
-        x = (const T *)p.q_raw; sb = d.q_stride_b; st = d.q_stride_t; c_in = c;
-        dx = (T *)bp.dq_raw; ostride = ch_qk;
-    } else if (c < 2 * ch_qk) {
-        x = (const T *)p.k_raw; sb = d.k_stride_b; st = d.k_stride_t; c_in = c - ch_qk;
-        dx = (T *)bp.dk_raw; ostride = ch_qk;
-    } else {
-        x = (const T *)p.v_raw; sb = d.v_stride_b; st = d.v_stride_t; c_in = c - 2 * ch_qk;
-        dx = (T *)bp.dv_raw; ostride = ch_v;
-    }
-    float wm[kConvW], dw[kConvW];
+// z of N adjacent channels: x is the channel's column at flattened token t of
+// sequence [s0, s1) (batch row b, position tau), w the channels' rows of conv_w
+template <typename T, int N>
+__device__ __forceinline__ void conv_z_n(const T *x, int64_t sb, int64_t st, int64_t b, int64_t tau, int64_t t,
+                                         int64_t s0, const T *w, float *z) {
+    float wv[N * kConvW];
+    ld_act_n<T, N * kConvW>(w, wv);
+    float xs[kConvW][N];
 #pragma unroll
     for (int m = 0; m < kConvW; ++m) {
-        wm[m] = to_f<T>(((const T *)p.conv_w)[(int64_t)c * kConvW + m]);
-        dw[m] = 0.f;
+        const int64_t back = kConvW - 1 - m;
+        if (t - back >= s0) {
+            ld_act_n<T, N>(x + b * sb + (tau - back) * st, xs[m]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < N; ++q) xs[m][q] = 0.f;
+        }
     }
-    const int64_t t0 = (int64_t)blockIdx.x * kBwdConvTokens;
-    const int64_t t1 = t0 + kBwdConvTokens < p.ntok ? t0 + kBwdConvTokens : p.ntok;
-    int64_t s0 = 0, s1 = 0, b = 0, bT = 0;
-#pragma unroll 4
-    for (int64_t t = t0; t < t1; ++t) {
-        if (t >= s1) {                        // entering the next sequence
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < kConvW; ++m)
+            if (t - (kConvW - 1 - m) >= s0) acc = fmaf(wv[q * kConvW + m], xs[m][q], acc);
+        z[q] = acc;
+    }
+}
+
+template <typename T, int CPL>
+__global__ void __launch_bounds__(kProThreads) prologue_bwd_kernel(const BwdProblem bp, int64_t nA, int64_t nB) {
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
+    const int64_t blk = blockIdx.x;
+    if (blk < nA) {
+        // ---- q / k: groups of lph lanes, one (token, head) each
+        const int lph = d.dk / CPL;                    // lanes per head, a power of two <= 32
+        const int lane = threadIdx.x & 31;
+        const int64_t unit = (blk * kProThreads + threadIdx.x) / lph;
+        const int i = (lane % lph) * CPL;              // first channel of this lane in the head
+        const int64_t units = p.ntok * 2 * d.Hk;
+        const bool act = unit < units;                 // whole groups: uniform within a group
+        const int64_t t = act ? unit / (2 * d.Hk) : 0;
+        const int hh = act ? (int)(unit - t * 2 * d.Hk) : 0;
+        const bool isk = hh >= d.Hk;
+        const int h = isk ? hh - d.Hk : hh;
+        float z[CPL], y[CPL], dxn[CPL];
+        float ss = 0.f;
+        if (act) {
+            int64_t s0, s1, b, tau;
             seq_of(d, p.cu, t, s0, s1);
-            b = p.cu ? 0 : s0 / d.T;
-            bT = b * d.T;
-        }
-        const int64_t tau = t - bT;
-        float g = 0.f;
+            tok_pos(d, t, b, tau);
+            const T *x = isk ? (const T *)p.k_raw + h * d.dk + i : (const T *)p.q_raw + h * d.dk + i;
+            conv_z_n<T, CPL>(x, isk ? d.k_stride_b : d.q_stride_b, isk ? d.k_stride_t : d.q_stride_t, b, tau, t, s0,
+                             (const T *)p.conv_w + (int64_t)((isk ? ch_qk : 0) + h * d.dk + i) * kConvW, z);
+            const int G = d.Hv / d.Hk;
+            const float *src = (isk ? bp.dk : bp.dq) + ((int64_t)h * G * p.ntok + t) * d.dk + i;
 #pragma unroll
-        for (int m = 0; m < kConvW; ++m) {
-            const int64_t tt = t + (kConvW - 1 - m);
-            if (tt < s1) g = fmaf(wm[m], bp.dz[tt * ch + c], g);
-        }
-        dx[t * ostride + c_in] = from_f<T>(g);
-        const float dzt = bp.dz[t * ch + c];
+            for (int q = 0; q < CPL; ++q) dxn[q] = 0.f;
+            for (int jj = 0; jj < G; ++jj) {
+                float v[CPL];
+                ld_f32_n<CPL>(src + (int64_t)jj * p.ntok * d.dk, v);
 #pragma unroll
-        for (int m = 0; m < kConvW; ++m) {
-            const int64_t back = kConvW - 1 - m;
-            if (t - back >= s0) dw[m] = fmaf(dzt, to_f<T>(x[b * sb + (tau - back) * st + c_in]), dw[m]);
+                for (int q = 0; q < CPL; ++q) dxn[q] += v[q];
+            }
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) {
+                y[q] = z[q] * sigm(z[q]);
+                ss = fmaf(y[q], y[q], ss);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) z[q] = y[q] = dxn[q] = 0.f;
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            if (off < lph) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float rho = 1.0f / sqrtf(ss + d.l2_eps);
+        float dot = 0.f;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) dot = fmaf(y[q] * rho, dxn[q], dot);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            if (off < lph) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        if (act) {
+            float out[CPL];
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) out[q] = rho * (dxn[q] - y[q] * rho * dot) * dsilu(z[q]);
+            float *dst = bp.dz + t * ch + (isk ? ch_qk : 0) + h * d.dk + i;
+            if constexpr (CPL % 4 == 0) {
+#pragma unroll
+                for (int q = 0; q < CPL / 4; ++q)
+                    st4(dst + 4 * q, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < CPL; ++q) dst[q] = out[q];
+            }
+        }
+    } else if (blk < nA + nB) {
+        // ---- v: 4 adjacent channels of one token
+        const int64_t item = (blk - nA) * kProThreads + threadIdx.x;
+        const int quads = ch_v / 4;
+        if (item >= p.ntok * quads) return;
+        const int64_t t = item / quads;
+        const int cv = (int)(item - t * quads) * 4;
+        int64_t s0, s1, b, tau;
+        seq_of(d, p.cu, t, s0, s1);
+        tok_pos(d, t, b, tau);
+        float z[4];
+        conv_z_n<T, 4>((const T *)p.v_raw + cv, d.v_stride_b, d.v_stride_t, b, tau, t, s0,
+                       (const T *)p.conv_w + (int64_t)(2 * ch_qk + cv) * kConvW, z);
+        const int jh = cv / d.dv;
+        const int64_t r = (int64_t)jh * p.ntok + t;
+        const float be = p.beta[r];
+        const float4 g = ld4(bp.dR + r * d.dv + (cv - jh * d.dv));
+        st4(bp.dz + t * ch + 2 * ch_qk + cv, be * g.x * dsilu(z[0]), be * g.y * dsilu(z[1]), be * g.z * dsilu(z[2]),
+            be * g.w * dsilu(z[3]));
+    } else {
+        // ---- beta / decay of one (token, v head)
+        const int64_t item = (blk - nA - nB) * kProThreads + threadIdx.x;
+        if (item >= p.ntok * d.Hv) return;
+        const int64_t t = item / d.Hv;
+        const int h = (int)(item - t * d.Hv);
+        int64_t b, tau;
+        tok_pos(d, t, b, tau);
+        const float av = to_f<T>(((const T *)p.a)[b * d.a_stride_b + tau * d.a_stride_t + h]);
+        const float bv = to_f<T>(((const T *)p.b)[b * d.b_stride_b + tau * d.b_stride_t + h]);
+        const int64_t r = (int64_t)h * p.ntok + t;
+        const float be = sigm(bv);
+        ((T *)bp.db)[t * d.Hv + h] = from_f<T>(bp.dbeta[r] * be * (1.0f - be));
+        const float x = av + p.dt_bias[h], eA = expf(p.A_log[h]);
+        const float dg = bp.dgam[r];
+        const float dx = -dg * eA * sigm(x);
+        ((T *)bp.da)[t * d.Hv + h] = from_f<T>(dx);
+        bp.pa[r] = dx;
+        bp.pa[(int64_t)d.Hv * p.ntok + r] = dg * (-eA * softplus_f(x));
+    }
+}
+
+template <typename T, int CPL>
+cudaError_t launch_prologue_bwd_c(const BwdProblem &bp, cudaStream_t s) {
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    const int64_t lph = d.dk / CPL;
+    const int64_t nA = (p.ntok * 2 * d.Hk * lph + kProThreads - 1) / kProThreads;
+    const int64_t nB = (p.ntok * (d.Hv * d.dv / 4) + kProThreads - 1) / kProThreads;
+    const int64_t nC = (p.ntok * d.Hv + kProThreads - 1) / kProThreads;
+    if (nA + nB + nC == 0) return cudaSuccess;
+    prologue_bwd_kernel<T, CPL><<<(unsigned)(nA + nB + nC), kProThreads, 0, s>>>(bp, nA, nB);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_prologue_bwd(const BwdProblem &bp, cudaStream_t s) {
+    switch (bp.f.d.dk) {      // channels per lane: a head over at most one warp
+    case 512: return launch_prologue_bwd_c<T, 16>(bp, s);
+    case 256: return launch_prologue_bwd_c<T, 8>(bp, s);
+    case 128: return launch_prologue_bwd_c<T, 4>(bp, s);
+    case 64: return launch_prologue_bwd_c<T, 2>(bp, s);
+    default: return launch_prologue_bwd_c<T, 1>(bp, s);
+    }
+}
+
+// ------------------------------------------------------------ conv backward
+// grid (blocks of kBwdConvTokens tokens, groups of 4 * kConvQuads channels);
+// per channel, dx_t = sum_m w_m dz_{t+3-m} within the sequence, and the
+// block's partial sums of dw_m = sum_t dz_t x_{t-3+m}. A thread owns 4
+// adjacent channels (one tensor: the q|k|v boundaries are multiples of 16) and
+// walks runs of kConvRun tokens: the run's dz rows and raw-input rows, with
+// their 3-token halos, are all loaded before the run is computed. The CTA's
+// kConvRuns token rows then add their partial sums in a fixed order.
+constexpr int kConvQuads = 32;   // channel quads per CTA (x)
+constexpr int kConvRuns = 4;     // token runs side by side (y)
+constexpr int kConvRun = 8;      // tokens per run
+static_assert(kBwdConvTokens % (kConvRuns * kConvRun) == 0, "conv backward token tiling");
+
+template <typename T>
+__global__ void __launch_bounds__(kConvQuads * kConvRuns) conv_bwd_kernel(const BwdProblem bp) {
+    __shared__ float4 red[kConvRuns][kConvW][kConvQuads];
+    const Problem &p = bp.f;
+    const gdn_desc &d = p.d;
+    if (p.cu != nullptr && *p.status != GDN_OK) return;
+    const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int c = (blockIdx.y * kConvQuads + tx) * 4;
+    const bool active = c < ch;
+    const T *x = (const T *)p.q_raw;
+    T *dx = (T *)bp.dq_raw;
+    int64_t sb = d.q_stride_b, st = d.q_stride_t, ostride = ch_qk;
+    int c_in = c;
+    if (c >= 2 * ch_qk) {
+        x = (const T *)p.v_raw; sb = d.v_stride_b; st = d.v_stride_t; c_in = c - 2 * ch_qk;
+        dx = (T *)bp.dv_raw; ostride = ch_v;
+    } else if (c >= ch_qk) {
+        x = (const T *)p.k_raw; sb = d.k_stride_b; st = d.k_stride_t; c_in = c - ch_qk;
+        dx = (T *)bp.dk_raw;
+    }
+    // w[m] = tap m of the four channels
+    float4 w[kConvW];
+    {
+        float wv[4 * kConvW];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 f = active ? ld4_act<T>((const T *)p.conv_w + (int64_t)c * kConvW + 4 * q)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            wv[4 * q] = f.x; wv[4 * q + 1] = f.y; wv[4 * q + 2] = f.z; wv[4 * q + 3] = f.w;
+        }
+#pragma unroll
+        for (int m = 0; m < kConvW; ++m)
+            w[m] = make_float4(wv[m], wv[kConvW + m], wv[2 * kConvW + m], wv[3 * kConvW + m]);
+    }
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 dw[kConvW] = {z4, z4, z4, z4};
+    int64_t s0 = 0, s1 = -1;
+    const int64_t tb = (int64_t)blockIdx.x * kBwdConvTokens;
+    for (int run = ty; run * kConvRun < kBwdConvTokens; run += kConvRuns) {
+        const int64_t ta = tb + (int64_t)run * kConvRun;
+        if (ta >= p.ntok) break;
+        // dz rows ta .. ta + kConvRun + 2, raw-input rows ta - 3 .. ta + kConvRun - 1
+        float4 g[kConvRun + kConvW - 1], xr[kConvRun + kConvW - 1];
+#pragma unroll
+        for (int k = 0; k < kConvRun + kConvW - 1; ++k) {
+            const int64_t pz = ta + k, px = ta - (kConvW - 1) + k;
+            g[k] = (active && pz < p.ntok) ? ld4(bp.dz + pz * ch + c) : z4;
+            if (active && px >= 0 && px < p.ntok) {
+                const int64_t b = p.cu ? 0 : px / d.T;
+                xr[k] = ld4_act<T>(x + b * sb + (px - b * d.T) * st + c_in);
+            } else {
+                xr[k] = z4;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kConvRun; ++u) {
+            const int64_t t = ta + u;
+            if (t >= p.ntok) break;
+            if (t >= s1) seq_of(d, p.cu, t, s0, s1);
+            float4 gx = z4;
+#pragma unroll
+            for (int m = 0; m < kConvW; ++m)
+                if (t + (kConvW - 1 - m) < s1) gx = fma4(w[m], g[u + kConvW - 1 - m], gx);
+            if (active) st4_act<T>(dx + t * ostride + c_in, gx);
+#pragma unroll
+            for (int m = 0; m < kConvW; ++m)
+                if (t - (kConvW - 1 - m) >= s0) dw[m] = fma4(g[u], xr[u + m], dw[m]);
         }
     }
 #pragma unroll
-    for (int m = 0; m < kConvW; ++m) bp.pconv[((int64_t)blockIdx.x * ch + c) * kConvW + m] = dw[m];
+    for (int m = 0; m < kConvW; ++m) red[ty][m][tx] = dw[m];
+    __syncthreads();
+    if (ty == 0 && active) {
+        float out[4][kConvW];   // [channel][tap]
+#pragma unroll
+        for (int m = 0; m < kConvW; ++m) {
+            float4 a = red[0][m][tx];
+#pragma unroll
+            for (int r = 1; r < kConvRuns; ++r) a = add4(a, red[r][m][tx]);
+            out[0][m] = a.x; out[1][m] = a.y; out[2][m] = a.z; out[3][m] = a.w;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(bp.pconv + ((int64_t)blockIdx.x * ch + c) * kConvW);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_float4(out[q][0], out[q][1], out[q][2], out[q][3]);
+    }
+}
+
+// out[i] = sum_{r < R} part[r * rs + i] for i < n, one thread per i, r in order
+__global__ void __launch_bounds__(kThreads) sum_rows_kernel(const float *part, int64_t R, int64_t rs, int64_t n,
+                                                            float *out) {
+    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (i >= n) return;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int64_t r = 0; r < R; ++r) acc += part[r * rs + i];
+    out[i] = acc;
 }
 
 // out[i] = sum_{r < R} part[r * rs + i * cs], one CTA per i, fixed order
@@ -1353,19 +1536,16 @@ cudaError_t launch_t(const BwdProblem &bp, cudaStream_t s) {
     }
     const int ch_qk = d.Hk * d.dk, ch_v = d.Hv * d.dv, ch = 2 * ch_qk + ch_v;
     if (p.ntok > 0) {
-        const int pt = d.dk > 128 ? d.dk : 128;
-        const int units_v = (ch_v + pt - 1) / pt;
-        prologue_bwd_kernel<T><<<dim3((unsigned)((p.ntok + kProTokens - 1) / kProTokens), 2 * d.Hk + units_v + 1), pt,
-                                 0, s>>>(bp, units_v);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        conv_bwd_kernel<T><<<dim3((unsigned)bwd_conv_blocks(d), (ch + kThreads - 1) / kThreads), kThreads, 0, s>>>(bp);
+        if ((e = launch_prologue_bwd<T>(bp, s)) != cudaSuccess) return e;
+        conv_bwd_kernel<T><<<dim3((unsigned)bwd_conv_blocks(d), (ch + 4 * kConvQuads - 1) / (4 * kConvQuads)),
+                             dim3(kConvQuads, kConvRuns), 0, s>>>(bp);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // parameter gradients: fixed-order sums of the partials (zero without tokens)
     const int64_t rows = p.ntok * d.Hv;
     sum_kernel<<<d.dv, kThreads, 0, s>>>(bp.pnorm, rows > 0 ? bwd_epi_warps(d) : 0, d.dv, 1, bp.dnorm_w);
-    sum_kernel<<<ch * kConvW, kThreads, 0, s>>>(bp.pconv, p.ntok > 0 ? bwd_conv_blocks(d) : 0, (int64_t)ch * kConvW,
-                                                 1, bp.dconv_w);
+    sum_rows_kernel<<<(ch * kConvW + kThreads - 1) / kThreads, kThreads, 0, s>>>(
+        bp.pconv, p.ntok > 0 ? bwd_conv_blocks(d) : 0, (int64_t)ch * kConvW, (int64_t)ch * kConvW, bp.dconv_w);
     sum_kernel<<<d.Hv, kThreads, 0, s>>>(bp.pa, p.ntok, 1, p.ntok, bp.ddt_bias);
     sum_kernel<<<d.Hv, kThreads, 0, s>>>(bp.pa + (int64_t)d.Hv * p.ntok, p.ntok, 1, p.ntok, bp.dA_log);
     return cudaGetLastError();

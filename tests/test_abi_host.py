@@ -189,7 +189,8 @@ def test_backward_checks(lib):
         a = list(args)
         a[i] = None
         assert call(d, a) == gdn.GDN_ERR_INVALID_ARG, i
-    for i in (0, 1, 2, 6):                  # vector-loaded inputs must be 16-byte aligned
+    for i in (0, 1, 2, 6, 14, 15, 16):      # vector-loaded inputs and vector-stored input
+                                            # gradients must be 16-byte aligned
         a = list(args)
         a[i] = fake + 2
         assert call(d, a) == gdn.GDN_ERR_INVALID_ARG, i
