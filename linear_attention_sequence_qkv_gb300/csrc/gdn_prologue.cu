@@ -24,6 +24,8 @@
 namespace gdn {
 namespace {
 
+// CTA sizes: 128 threads, or 192 where that leaves no idle warp in the channel
+// groups and 128 does not (six 256-channel heads: 1536 q channels = 192 x 8)
 constexpr int kThreads = 128;
 
 // ------------------------------------------------------------------ K0
@@ -94,11 +96,11 @@ struct PrologueArgs {
 // channels (16-byte vectors, zero-filled before the sequence start) into shared
 // memory with cp.async, all in flight at once without holding registers, then
 // runs the 4-tap window over them.
-template <int NVEC> struct ConvShape {
+template <int NVEC, int TH> struct ConvShape {
     static constexpr int TOKS = 16 / NVEC;
     static constexpr int ROWS = TOKS + kConvW - 1;
     static constexpr int SLICES = kChunk / TOKS;
-    static constexpr size_t SMEM = (size_t)ROWS * NVEC * kThreads * 16;
+    static constexpr size_t SMEM = (size_t)ROWS * NVEC * TH * 16;
 };
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool ok) {
@@ -119,14 +121,14 @@ template <int U, int N, typename F> __device__ __forceinline__ void static_for(F
     }
 }
 
-template <typename T, int NVEC, bool NORM, bool PRE>
+template <typename T, int NVEC, bool NORM, bool PRE, int TH>
 __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc &c, int gy,
                                            uint4 *stage) {
     constexpr int VEC = Vec16<T>::N;
     constexpr int CPT = NVEC * VEC;           // channels per thread
     constexpr int NP = CPT / 2;               // channel pairs per thread
     constexpr int PV = VEC / 2;               // pairs per 16-byte vector
-    using Shape = ConvShape<NVEC>;
+    using Shape = ConvShape<NVEC, TH>;
     constexpr int TOKS = Shape::TOKS;
     constexpr int ROWS = Shape::ROWS;
     using S = typename Inter<T>::S;
@@ -156,14 +158,14 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
         src = (const T *)p.v_raw; dst = (S *)p.v; sb = d.v_stride_b; st = d.v_stride_t;
         nch = d.Hv * d.dv; hd = d.dv; w_base = 2 * ch_qk;
     }
-    const int c0 = g * (kThreads * CPT) + tid * CPT;
+    const int c0 = g * (TH * CPT) + tid * CPT;
     const bool active = c0 < nch;
     // a warp with no channel has nothing to do (no block barrier follows)
     if (!__any_sync(0xffffffffu, active)) return;
     const int lanes_per_head = hd / CPT;      // <= 32 for q/k by construction
 
     // rows into shared memory, one copy group per row:
-    // stage[(r * NVEC + v) * kThreads + tid]. Rows before the sequence start are
+    // stage[(r * NVEC + v) * TH + tid]. Rows before the sequence start are
     // zeros, or the prefix rows (the raw inputs of the three earlier tokens).
     const int64_t first = c.tok0 + t_begin - (kConvW - 1);
     const int64_t brow = p.cu ? 0 : c.n;     // batch row of this sequence
@@ -180,7 +182,7 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
         const bool okp = PRE && in_rows && !ok && pr >= 0;
 #pragma unroll
         for (int v = 0; v < NVEC; ++v)
-            cp_async16(&stage[(r * NVEC + v) * kThreads + tid],
+            cp_async16(&stage[(r * NVEC + v) * TH + tid],
                        ok ? (const void *)(rp + r * st + v * VEC)
                           : (okp ? (const void *)(pre + pr * ch_all + v * VEC) : (const void *)src),
                        ok || okp);
@@ -207,7 +209,7 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
 
     auto row = [&](int r, float2 *out) {   // each thread reads only its own rows
 #pragma unroll
-        for (int v = 0; v < NVEC; ++v) Pairs<T>::unpack(stage[(r * NVEC + v) * kThreads + tid], out + v * PV);
+        for (int v = 0; v < NVEC; ++v) Pairs<T>::unpack(stage[(r * NVEC + v) * TH + tid], out + v * PV);
     };
     const int head = c0 / hd;
     const int dd = c0 - head * hd;
@@ -274,7 +276,7 @@ __device__ __forceinline__ void conv_group(const PrologueArgs &A, const ChunkLoc
 }
 
 // ------------------------------------------------------- beta/decay group
-template <typename T>
+template <typename T, int TH>
 __device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c, float *smem) {
     float (*gs)[33] = reinterpret_cast<float (*)[33]>(smem);
     float (*bs)[33] = reinterpret_cast<float (*)[33]>(smem + kChunk * 33);
@@ -282,7 +284,7 @@ __device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c, 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int h0 = 0; h0 < d.Hv; h0 += 32) {
         const int nh = min(32, d.Hv - h0);
-        for (int idx = tid; idx < kChunk * 32; idx += kThreads) {
+        for (int idx = tid; idx < kChunk * 32; idx += TH) {
             const int i = idx >> 5, hh = idx & 31;
             float gv = 0.f, bv = 0.f;
             if (i < c.len && hh < nh) {
@@ -299,7 +301,7 @@ __device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c, 
         __syncthreads();
         using GT = typename Inter<T>::G;
         GT *gamma = (GT *)p.gamma;
-        for (int hh = warp; hh < nh; hh += kThreads / 32) {
+        for (int hh = warp; hh < nh; hh += TH / 32) {
             const GT g0 = gs[2 * lane][hh], g1 = gs[2 * lane + 1][hh];
             GT x = g0 + g1;
 #pragma unroll
@@ -322,8 +324,8 @@ __device__ __forceinline__ void gate_group(const Problem &p, const ChunkLoc &c, 
     }
 }
 
-template <typename T, int NVEC, bool PRE>
-__global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueArgs A) {
+template <typename T, int NVEC, bool PRE, int TH>
+__global__ void __launch_bounds__(TH) prologue_kernel(const PrologueArgs A) {
     extern __shared__ uint4 stage[];
     pdl_trigger();    // the chunk stage's CTAs may become resident during the last wave
     const Problem &p = A.p;
@@ -335,30 +337,39 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueArgs A
     ChunkLoc c;
     if (!locate_chunk(blockIdx.x, p.cu, p.chunk_off, p.d.N, p.d.T, c)) return;
     const int gy = blockIdx.y;
-    if (gy == (2 * A.groups_qk + A.groups_v) * ConvShape<NVEC>::SLICES) gate_group<T>(p, c, (float *)stage);
-    else if (gy < 2 * A.groups_qk * ConvShape<NVEC>::SLICES) conv_group<T, NVEC, true, PRE>(A, c, gy, stage);
-    else conv_group<T, NVEC, false, PRE>(A, c, gy, stage);
+    if (gy == (2 * A.groups_qk + A.groups_v) * ConvShape<NVEC, TH>::SLICES) gate_group<T, TH>(p, c, (float *)stage);
+    else if (gy < 2 * A.groups_qk * ConvShape<NVEC, TH>::SLICES) conv_group<T, NVEC, true, PRE, TH>(A, c, gy, stage);
+    else conv_group<T, NVEC, false, PRE, TH>(A, c, gy, stage);
+}
+
+template <typename T, int NVEC, int TH>
+cudaError_t launch_th(const Problem &p, cudaStream_t s) {
+    constexpr int CPT = NVEC * Vec16<T>::N;
+    PrologueArgs A;
+    A.p = p;
+    const int gc = TH * CPT;
+    A.groups_qk = (p.d.Hk * p.d.dk + gc - 1) / gc;
+    A.groups_v = (p.d.Hv * p.d.dv + gc - 1) / gc;
+    using Shape = ConvShape<NVEC, TH>;
+    static_assert(Shape::SMEM >= 2 * kChunk * 33 * 4, "gate group scratch");
+    dim3 grid((unsigned)chunk_slots(p), (2 * A.groups_qk + A.groups_v) * Shape::SLICES + 1);
+    // the prefix reads are compiled in only where a prefix is given
+    auto kernel = p.conv_prefix ? prologue_kernel<T, NVEC, true, TH> : prologue_kernel<T, NVEC, false, TH>;
+    if (Shape::SMEM > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Shape::SMEM);
+        if (e != cudaSuccess) return e;
+    }
+    kernel<<<grid, TH, Shape::SMEM, s>>>(A);
+    return cudaGetLastError();
 }
 
 template <typename T, int NVEC>
 cudaError_t launch_t(const Problem &p, cudaStream_t s) {
     constexpr int CPT = NVEC * Vec16<T>::N;
-    PrologueArgs A;
-    A.p = p;
-    const int gc = kThreads * CPT;
-    A.groups_qk = (p.d.Hk * p.d.dk + gc - 1) / gc;
-    A.groups_v = (p.d.Hv * p.d.dv + gc - 1) / gc;
-    using Shape = ConvShape<NVEC>;
-    static_assert(Shape::SMEM >= 2 * kChunk * 33 * 4, "gate group scratch");
-    dim3 grid((unsigned)chunk_slots(p), (2 * A.groups_qk + A.groups_v) * Shape::SLICES + 1);
-    // the prefix reads are compiled in only where a prefix is given
-    auto kernel = p.conv_prefix ? prologue_kernel<T, NVEC, true> : prologue_kernel<T, NVEC, false>;
-    if (Shape::SMEM > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Shape::SMEM);
-        if (e != cudaSuccess) return e;
-    }
-    kernel<<<grid, kThreads, Shape::SMEM, s>>>(A);
-    return cudaGetLastError();
+    const int th_qk = p.d.Hk * p.d.dk / CPT, th_v = p.d.Hv * p.d.dv / CPT;   // threads per tensor
+    if ((th_qk % 128 != 0 || th_v % 128 != 0) && th_qk % 192 == 0 && th_v % 192 == 0)
+        return launch_th<T, NVEC, 192>(p, s);
+    return launch_th<T, NVEC, kThreads>(p, s);
 }
 
 }  // namespace

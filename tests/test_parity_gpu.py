@@ -154,8 +154,18 @@ def test_run_to_run_bitwise_deterministic(dev):
     assert torch.equal(f1, b1.final_state)
 
 
-def test_stages_equal_forward_bitwise(dev):
-    inp = to_device(make_inputs(replace(WORKLOADS["ragged_fp16"])), dev)
+STAGED_CASES = {
+    "ragged_fp16": WORKLOADS["ragged_fp16"],
+    # gdn_forward chains its four kernels by programmatic dependent launch; the
+    # stage calls run them plainly: the results must not differ by a bit
+    "layer_bf16": WORKLOADS["layer_bf16"],
+    "packed_gqa_bf16": replace(WORKLOADS["varlen_bf16"], n_packed=6, max_len=700, seed=5),
+}
+
+
+@pytest.mark.parametrize("name", list(STAGED_CASES))
+def test_stages_equal_forward_bitwise(dev, name):
+    inp = to_device(make_inputs(STAGED_CASES[name]), dev)
     b1 = gdn.forward(inp)
     d = b1.desc
     b2 = gdn.alloc(d, dev)
