@@ -140,6 +140,13 @@ int gdn_workspace_offsets(const gdn_desc *d, gdn_workspace_layout *layout);
  *   workspace      device scratch of >= gdn_workspace_bytes(), 256-byte aligned;
  *                  calls that share a workspace must not overlap on the GPU
  * Inputs are only read; initial_state and final_state may alias.
+ * Ordering: the call's first kernel starts after everything queued on `stream`
+ * before it, and work queued after the call starts after its last kernel. On
+ * the tensor-core path without segments the later kernels of the call are
+ * programmatic dependents of the kernel before them (their CTAs may become
+ * resident early and wait on the device); a long single sequence runs part of
+ * the chunk stage on a high-priority stream the library creates once per
+ * device, joined back to `stream` by events.
  */
 int gdn_forward(const gdn_desc *d,
                 const void *q_raw, const void *k_raw, const void *v_raw,
