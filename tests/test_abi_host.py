@@ -32,6 +32,32 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(gdn.EXPORTS)
 
 
+def declared_arity():
+    """Parameter count of every prototype in include/gdn.h."""
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    out = {}
+    for m in re.finditer(r"(gdn_\w+)\s*\(", src):
+        name, i, depth = m.group(1), m.end(), 1
+        j = i
+        while depth:
+            depth += {"(": 1, ")": -1}.get(src[j], 0)
+            j += 1
+        params = src[i:j - 1].strip()
+        if src[j:].lstrip().startswith(";") or src[j:].lstrip().startswith("{"):
+            out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_header(lib):
+    # the ctypes declarations must take exactly the parameters the header declares
+    arity = declared_arity()
+    assert set(arity) == set(gdn.EXPORTS)
+    for name, n in arity.items():
+        assert len(getattr(lib, name).argtypes) == n, name
+
+
 def test_library_is_native_and_sm103a():
     # the built library exists and was compiled for sm_103a only
     assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
