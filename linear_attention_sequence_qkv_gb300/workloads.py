@@ -10,7 +10,12 @@ then rounded once to the activation dtype):
 
 * ``q_raw, k_raw, v_raw, a, b, gate`` ~ N(0, 1)
 * ``conv_w`` ~ N(0, 0.25)  (0.25 read as the standard deviation)
-* ``A_log`` = log U[1, 16]   (fp32, one per v head)
+* ``A_log`` = log U[1, 16]   (fp32, one per v head); a workload may set
+  ``decay_range = (lo, hi)`` to draw ``A_log = log U[lo, hi]`` instead (the
+  same uniform draw, mapped to another interval). ``MILD`` = (0.001, 0.05) is
+  the long-memory recipe of the tests: with it the per-chunk decay
+  ``exp(sum of g over 64 tokens)`` is about 0.05-0.95 instead of below 1e-90,
+  so the state carried from chunk to chunk reaches the outputs.
 * ``dt_bias`` ~ N(0, 0.1)    (fp32, one per v head; 0.1 read as std)
 * ``norm_w`` = 1 + N(0, 0.1) (activation dtype)
 * ``initial_state`` = 0, or N(0, 0.1) in fp32 where a workload asks for it
@@ -49,11 +54,15 @@ class Workload:
     init_state_std: float = 0.0
     seed: int = 0
     description: str = ""
+    decay_range: tuple = (1.0, 16.0)   # A = exp(A_log) ~ U[lo, hi]
 
     @property
     def G(self) -> int:
         return self.Hv // self.Hk
 
+
+# exp(A_log) range of the long-memory test recipe (see the module docstring)
+MILD = (0.001, 0.05)
 
 WORKLOADS = {
     "tiny_fp32": Workload(
@@ -151,7 +160,8 @@ def make_inputs(w: Workload, lengths: Optional[list] = None) -> Inputs:
     b = normal((B, T, w.Hv)).to(act)
     gate_buf = normal((B, T, ch_v + w.gate_extra)).to(act)
     conv_w = normal((2 * ch_qk + ch_v, 4), std=0.25).to(act)
-    A_log = torch.log(torch.rand((w.Hv,), generator=g, dtype=torch.float32) * 15.0 + 1.0)
+    lo, hi = (float(x) for x in w.decay_range)
+    A_log = torch.log(torch.rand((w.Hv,), generator=g, dtype=torch.float32) * (hi - lo) + lo)
     dt_bias = normal((w.Hv,), std=0.1)
     norm_w = normal((w.dv,), std=0.1, mean=1.0).to(act)
     n_seq = (cu.numel() - 1) if cu is not None else B
@@ -190,7 +200,8 @@ def make_inputs_device(w: Workload, device, lengths: Optional[list] = None) -> I
     b = normal((B, T, w.Hv)).to(act)
     gate_buf = normal((B, T, ch_v + w.gate_extra)).to(act)
     conv_w = normal((2 * ch_qk + ch_v, 4), std=0.25).to(act)
-    A_log = torch.log(torch.rand((w.Hv,), generator=g, dtype=torch.float32, device=device) * 15.0 + 1.0)
+    lo, hi = (float(x) for x in w.decay_range)
+    A_log = torch.log(torch.rand((w.Hv,), generator=g, dtype=torch.float32, device=device) * (hi - lo) + lo)
     dt_bias = normal((w.Hv,), std=0.1)
     norm_w = normal((w.dv,), std=0.1, mean=1.0).to(act)
     n_seq = (cu.numel() - 1) if cu is not None else B
