@@ -201,6 +201,12 @@ const char *gdn_status_string(int status);
  *    contents: calls that overlap on the GPU (different streams, or host
  *    threads racing on one device) race on it and must be serialised by the
  *    caller.
+ *  - Device-side status (GDN_ERR_DEVICE_SEQLENS, GDN_ERR_DEVICE_RANGE,
+ *    GDN_ERR_DEVICE_TIMEOUT) goes to the status word at the start of the
+ *    array, as gdn_forward's goes to its workspace; read it with
+ *    gdn_static_ws_device_status below.
+ *  - The address is looked up again when the device's context changes (e.g.
+ *    after cudaDeviceReset), so a reset between calls is safe.
  */
 #define GDN_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 int gdn_forward_static_ws(const gdn_desc *d,
@@ -210,6 +216,13 @@ int gdn_forward_static_ws(const gdn_desc *d,
                           const void *norm_w, const int32_t *cu_seqlens,
                           const float *initial_state, void *out, float *final_state,
                           gdn_stream_t stream);
+
+/* Wait for `stream`, then read the device status word of the last
+ * gdn_forward_static_ws call on the current device into *status (GDN_OK or a
+ * GDN_ERR_DEVICE_* code), like gdn_device_status for a caller's workspace. No
+ * counterpart on the pages either. Synchronises the stream; allocates nothing.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG (null status) or GDN_ERR_CUDA. */
+int gdn_static_ws_device_status(int *status, gdn_stream_t stream);
 
 /* Which gated-delta-rule kernel serves *d: 0 = fp32 CUDA-core kernel,
  * 1 = tcgen05 tensor-core kernel (bf16/fp16). */
@@ -311,10 +324,21 @@ int gdn_span_scan(int spans, int Hv, int dk, int dv, const float *A, const float
  * RMSNorm result to the activation dtype is taken as the identity (the
  * straight-through derivative of the rounded forward).
  *
- * The call recomputes the forward (prologue and the fp32 CUDA-core chunk
- * kernel, storing each chunk's start state) and then runs the reverse pass on
- * CUDA cores in fp32 for every dtype. Every sum has a fixed order: results are
- * run-to-run identical.
+ * The call recomputes the forward, storing each chunk's start state, and then
+ * runs the reverse pass. What runs depends on the activation dtype:
+ *  - fp32 activations: everything on CUDA cores in fp32 (the prologue, a
+ *    state recompute, the reverse pass);
+ *  - 2-byte activations with dk in {64, 128, 256} and dv a multiple of 64
+ *    (gdn_chunk_kernel_kind() == 1): the forward's tcgen05 chunk stage (prep
+ *    and chain) recomputes the states, the new values and the outputs in fp32;
+ *    the dO' terms and the per-chunk dv contractions are tcgen05 products
+ *    (split bf16 or fp16 operands, fp32 accumulators);
+ *  - other 2-byte shapes: an fp32 CUDA-core state recompute; where dk and dv
+ *    are multiples of 64 (dv <= 512) the outputs and the dO' terms are still
+ *    tcgen05 products;
+ *  - in every case the serial reverse chain, the per-chunk gradients' other
+ *    terms and the elementwise backward run on CUDA cores in fp32.
+ * Every sum has a fixed order: results are run-to-run identical.
  *
  * d, q_raw ... initial_state   exactly as for gdn_forward (same descriptor,
  *             strides, packing and alignment rules).

@@ -8,9 +8,12 @@
 // (GDN_STATIC_WORKSPACE_BYTES) until the process exits.
 //
 // Host code must not pass the array's name to a kernel: on the host it is only a
-// stand-in symbol, not a device address. The device address is looked up once
-// per device with cudaGetSymbolAddress, with that device current, on the first
-// call made on the device.
+// stand-in symbol, not a device address. The device address is looked up with
+// cudaGetSymbolAddress, with the device current, on the first call made on the
+// device, and again whenever the device's current context has changed since
+// (after a cudaDeviceReset the module is loaded anew, possibly elsewhere).
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -21,19 +24,44 @@ static __device__ __align__(256) unsigned char g_static_ws[GDN_STATIC_WORKSPACE_
 
 constexpr int kMaxDevices = 256;
 std::mutex g_mu;
-void *g_static_ws_ptr[kMaxDevices] = {};
+struct Cached {
+    void *ptr = nullptr;
+    CUcontext ctx = nullptr;
+};
+Cached g_static_ws_ptr[kMaxDevices];
 
-// Device address of g_static_ws on the current device (set-up on first use).
+PFN_cuCtxGetCurrent_v4000 ctx_fn() {
+    static PFN_cuCtxGetCurrent_v4000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (PFN_cuCtxGetCurrent_v4000) nullptr;
+        return (PFN_cuCtxGetCurrent_v4000)f;
+    }();
+    return fn;
+}
+
+// Device address of g_static_ws on the current device (set up on first use and
+// whenever the device's context is not the one the address was taken in).
 int static_ws_address(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+    // the same device again: initialises its primary context if needed and makes it
+    // current on this thread, so that the driver reports the context in use
+    if (cudaSetDevice(dev) != cudaSuccess) return GDN_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    auto get_ctx = ctx_fn();
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return GDN_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_static_ws_ptr[dev] == nullptr) {
+    Cached &c = g_static_ws_ptr[dev];
+    if (c.ptr == nullptr || c.ctx != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || p == nullptr) return GDN_ERR_CUDA;
-        g_static_ws_ptr[dev] = p;
+        c.ptr = p;
+        c.ctx = ctx;
     }
-    *out = g_static_ws_ptr[dev];
+    *out = c.ptr;
     return GDN_OK;
 }
 
@@ -60,4 +88,14 @@ extern "C" int gdn_forward_static_ws(const gdn_desc *d, const void *q_raw, const
     return gdn::forward_single_stream(d, q_raw, k_raw, v_raw, a, b, gate, conv_w, A_log, dt_bias, norm_w,
                                       cu_seqlens, initial_state, out, final_state, ws,
                                       (size_t)GDN_STATIC_WORKSPACE_BYTES, (cudaStream_t)stream);
+}
+
+// The status word at the start of the fixed scratch: what gdn_device_status
+// reads from a caller's workspace, for the calls above.
+extern "C" int gdn_static_ws_device_status(int *status, gdn_stream_t stream) {
+    if (!status) return GDN_ERR_INVALID_ARG;
+    void *ws = nullptr;
+    const int rc = static_ws_address(&ws);
+    if (rc != GDN_OK) return rc;
+    return gdn_device_status(ws, status, stream);
 }

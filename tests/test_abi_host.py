@@ -64,6 +64,16 @@ def test_library_is_native_and_sm103a():
     assert os.path.exists(gdn.LIB_PATH)
 
 
+def test_static_workspace_size_matches_header():
+    # the binding's copy of GDN_STATIC_WORKSPACE_BYTES is the header's #define
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    m = re.search(r"#define\s+GDN_STATIC_WORKSPACE_BYTES\s+\(([^)]*)\)", src)
+    assert m is not None
+    expr = re.sub(r"(\d+)u\b", r"\1", m.group(1))
+    assert re.fullmatch(r"[\d\s*+]+", expr)
+    assert eval(expr) == gdn.GDN_STATIC_WORKSPACE_BYTES
+
+
 def test_struct_layout_matches_header(lib):
     # gdn_desc: 12 int32 + 12 int64 + 3 float + 1 int32 = 160 bytes
     assert ctypes.sizeof(gdn.gdn_desc) == 160
