@@ -63,6 +63,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other four workloads (reported under 'workloads')")
+    ap.add_argument("--workload-steps", type=int, default=30,
+                    help="timed steps for each of the other workloads (at most --steps)")
     ap.add_argument("--decode", action="store_true",
                     help="time the decode step (one token per sequence) instead of the forward")
     ap.add_argument("--decode-batch", type=int, default=256, help="sequences per decode step")
@@ -563,6 +567,131 @@ def spans_main(args, w):
     print(json.dumps(line), flush=True)
 
 
+# the five workloads the bench line reports (the first is the headline)
+ALL_WORKLOADS = ("layer_bf16", "tiny_fp32", "ragged_fp16", "long_gqa_bf16", "varlen_bf16")
+
+
+def chunk_launch_count(gdn, d, w, inp, nsm):
+    """Launches of the chunk stage per step: prep + chain on the tensor-core path
+    (two per segment of a long single sequence), one kernel on the fp32 path."""
+    tc = gdn.gdn_chunk_kernel_kind(d) == 1
+    if not tc:
+        return 1
+    nch = (d.T + CHUNK - 1) // CHUNK
+    if inp.cu_seqlens is None and d.N == 1 and nch >= 256 and w.Hv * (w.dv // 64) * 2 <= nsm:
+        seg = max(-(-nch // 16), 64)
+        return 2 * (-(-nch // seg))
+    return 2
+
+
+def measure_workload(w, steps, warmup, dev, world, barrier, gpu_id, with_clocks, torch, gdn, make_inputs_device):
+    """Time one workload: ``steps`` gdn_forward calls (CUDA events around each,
+    L2 flushed before each), then the same count as the three stage calls with
+    events between them (the per-kernel breakdown). Returns the measurements and
+    the device buffers (the headline's end-to-end pass reuses them)."""
+    inp = make_inputs_device(w, dev)
+    d = gdn.make_desc(inp)
+    bufs = gdn.alloc(d, dev)
+    ntok = d.B * d.T
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MiB
+
+    def flush_l2():
+        # write more than L2 (129 MB), then read another 256 MiB so that L2 is
+        # left holding clean lines: the timed kernels then pay no write-back of
+        # the flush's dirty lines
+        flush.zero_()
+        flush_rd.sum()
+    stream = torch.cuda.current_stream()
+
+    def fwd_step(ev=None):
+        # one gdn_forward: the public call (its kernels back to back on the
+        # stream, each a programmatic dependent of the one before)
+        if ev:
+            ev[0].record()
+        gdn.gdn_forward(d, inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.gate, inp.conv_w, inp.A_log,
+                        inp.dt_bias, inp.norm_w, inp.cu_seqlens, inp.initial_state, bufs.out, bufs.final_state,
+                        bufs.workspace, bufs.ws_bytes, stream)
+        if ev:
+            ev[1].record()
+
+    def step(ev=None):
+        # the same work as three stage calls with events between them (the
+        # per-kernel breakdown; no overlap across the stage boundaries)
+        if ev:
+            ev[0].record()
+        gdn.gdn_prologue(d, inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.conv_w, inp.A_log,
+                         inp.dt_bias, inp.cu_seqlens, bufs.workspace, bufs.ws_bytes, stream)
+        if ev:
+            ev[1].record()
+        gdn.gdn_chunk_rule(d, inp.cu_seqlens, inp.initial_state, bufs.final_state, bufs.workspace,
+                           bufs.ws_bytes, stream)
+        if ev:
+            ev[2].record()
+        gdn.gdn_epilogue(d, inp.gate, inp.norm_w, bufs.out, bufs.workspace, bufs.ws_bytes, stream)
+        if ev:
+            ev[3].record()
+
+    for _ in range(warmup):
+        flush_l2()
+        fwd_step()
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status(bufs.workspace) == gdn.GDN_OK
+
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    sampler = ClockSampler(gpu_id) if with_clocks else None
+    torch.cuda.synchronize()
+    barrier()
+    for i in range(steps):          # the timed steps: gdn_forward
+        flush_l2()
+        fwd_step(evf[i])
+    torch.cuda.synchronize()
+    barrier()
+    for i in range(steps):          # the per-kernel breakdown: the three stages
+        flush_l2()
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    assert gdn.gdn_device_status(bufs.workspace) == gdn.GDN_OK
+
+    per = {"prologue": [], "chunk_rule": [], "epilogue": [], "staged": []}
+    for e in evs:
+        per["prologue"].append(e[0].elapsed_time(e[1]))
+        per["chunk_rule"].append(e[1].elapsed_time(e[2]))
+        per["epilogue"].append(e[2].elapsed_time(e[3]))
+        per["staged"].append(e[0].elapsed_time(e[3]))
+    times = [a.elapsed_time(b) for a, b in evf]
+    ms_mean = sum(times) / len(times)
+    ms_median = statistics.median(times)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_mean, ms_median], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_mean, ms_median = float(t[0].item()), float(t[1].item())
+
+    pk = peaks()
+    alg = algorithmic(w, ntok, d.N, inp.initial_state is not None)
+    kernels = {}
+    for name in ("prologue", "chunk_rule", "epilogue"):
+        ms = sum(per[name]) / len(per[name])
+        kernels[name] = roofline_entry(name, alg[name][0], alg[name][1], ms, pk, w.dtype)
+        kernels[name]["ms_median"] = statistics.median(per[name])
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    launches = 1 + (1 if inp.cu_seqlens is not None else 0) + chunk_launch_count(gdn, d, w, inp, nsm) + 1
+    res = {"ms_per_step": ms_mean, "ms_per_step_median": ms_median,
+           "value": ntok * world / (ms_mean / 1e3), "tokens_per_step": ntok,
+           "staged_ms_per_step": sum(per["staged"]) / len(per["staged"]), "kernels": kernels,
+           "gpu_launches_per_step": launches, "steps": steps, "warmup": warmup, "clocks": clocks,
+           "chunk_kernel": "tcgen05" if gdn.gdn_chunk_kernel_kind(d) == 1 else "cuda-core fp32",
+           "shape": {"B": d.B, "T": d.T, "N": d.N, "Hk": w.Hk, "Hv": w.Hv, "dk": w.dk, "dv": w.dv,
+                     "dtype": w.dtype}}
+    return res, inp, d, bufs, pk, flush_l2, stream
+
+
 def main():
     args = parse()
     from linear_attention_sequence_qkv_gb300.workloads import WORKLOADS
@@ -606,101 +735,17 @@ def main():
         if world > 1:
             dist.barrier()
 
-    inp = make_inputs_device(w, dev)
-    d = gdn.make_desc(inp)
-    bufs = gdn.alloc(d, dev)
-    ntok = d.B * d.T
-    n_seq = d.N
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    flush_rd = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MiB
-
-    def flush_l2():
-        # write more than L2 (129 MB), then read another 256 MiB so that L2 is
-        # left holding clean lines: the timed kernels then pay no write-back of
-        # the flush's dirty lines
-        flush.zero_()
-        flush_rd.sum()
-    stream = torch.cuda.current_stream()
-
-    def fwd_step(ev=None):
-        # one gdn_forward: the public call (its kernels back to back on the
-        # stream, each a programmatic dependent of the one before)
-        if ev:
-            ev[0].record()
-        gdn.gdn_forward(d, inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.gate, inp.conv_w, inp.A_log,
-                        inp.dt_bias, inp.norm_w, inp.cu_seqlens, inp.initial_state, bufs.out, bufs.final_state,
-                        bufs.workspace, bufs.ws_bytes, stream)
-        if ev:
-            ev[1].record()
-
-    def step(ev=None):
-        # the same work as three stage calls with events between them (the
-        # per-kernel breakdown; no overlap across the stage boundaries)
-        if ev:
-            ev[0].record()
-        gdn.gdn_prologue(d, inp.q_raw, inp.k_raw, inp.v_raw, inp.a, inp.b, inp.conv_w, inp.A_log,
-                         inp.dt_bias, inp.cu_seqlens, bufs.workspace, bufs.ws_bytes, stream)
-        if ev:
-            ev[1].record()
-        gdn.gdn_chunk_rule(d, inp.cu_seqlens, inp.initial_state, bufs.final_state, bufs.workspace,
-                           bufs.ws_bytes, stream)
-        if ev:
-            ev[2].record()
-        gdn.gdn_epilogue(d, inp.gate, inp.norm_w, bufs.out, bufs.workspace, bufs.ws_bytes, stream)
-        if ev:
-            ev[3].record()
-
-    for _ in range(args.warmup):
-        flush_l2()
-        fwd_step()
-        flush_l2()
-        step()
-    torch.cuda.synchronize()
-    assert gdn.gdn_device_status(bufs.workspace) == gdn.GDN_OK
-
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = None
-    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    sampler = None if args.no_clocks else ClockSampler(gpu_id)
-    torch.cuda.synchronize()
-    barrier()
-    for i in range(args.steps):          # the timed steps: gdn_forward
-        flush_l2()
-        fwd_step(evf[i])
-    torch.cuda.synchronize()
-    barrier()
-    for i in range(args.steps):          # the per-kernel breakdown: the three stages
-        flush_l2()
-        step(evs[i])
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop() if sampler else None
-
-    per = {"prologue": [], "chunk_rule": [], "epilogue": [], "staged": []}
-    for e in evs:
-        per["prologue"].append(e[0].elapsed_time(e[1]))
-        per["chunk_rule"].append(e[1].elapsed_time(e[2]))
-        per["epilogue"].append(e[2].elapsed_time(e[3]))
-        per["staged"].append(e[0].elapsed_time(e[3]))
-    ms_step = sum(a.elapsed_time(b) for a, b in evf) / len(evf)
-    ms_staged = sum(per["staged"]) / len(per["staged"])
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = ntok * world / (ms_step / 1e3)
-
-    pk = peaks()
-    alg = algorithmic(w, ntok, n_seq, inp.initial_state is not None)
-    kernels = {}
-    for name in ("prologue", "chunk_rule", "epilogue"):
-        ms = sum(per[name]) / len(per[name])
-        kernels[name] = roofline_entry(name, alg[name][0], alg[name][1], ms, pk, w.dtype)
-    tc = gdn.gdn_chunk_kernel_kind(d) == 1
+    res, inp, d, bufs, pk, flush_l2, stream = measure_workload(
+        w, args.steps, args.warmup, dev, world, barrier, gpu_id, not args.no_clocks, torch, gdn,
+        make_inputs_device)
+    ntok = d.B * d.T
+    kernels = res["kernels"]
+    tc = res["chunk_kernel"] == "tcgen05"
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     roof = dict(kernels[dom])
     roof["kernel"] = dom
@@ -715,7 +760,7 @@ def main():
     roof["peak_source"] = pk["source"]
 
     # end to end through the C ABI with host buffers: pinned H2D of every input,
-    # the forward, D2H of the output, all inside the events
+    # the forward, D2H of the output and the final state, all inside the events
     e2e = None
     if not args.no_e2e:
         host = {}
@@ -727,8 +772,9 @@ def main():
         for nm in names:
             host[nm] = getattr(inp, nm).cpu().pin_memory()
         out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+        fin_host = torch.empty(bufs.final_state.shape, dtype=bufs.final_state.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size()
+        d2h = out_host.numel() * out_host.element_size() + fin_host.numel() * fin_host.element_size()
         dv_ = {nm: torch.empty_like(getattr(inp, nm)) for nm in names}
         ksteps = min(args.steps, 100)
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -744,6 +790,7 @@ def main():
                             dv_.get("cu_seqlens"), dv_.get("initial_state"), bufs.out,
                             bufs.final_state, bufs.workspace, bufs.ws_bytes, stream)
             out_host.copy_(bufs.out, non_blocking=True)
+            fin_host.copy_(bufs.final_state, non_blocking=True)
             e[1].record()
 
         for _ in range(3):
@@ -766,14 +813,16 @@ def main():
         # Pipelined: the copies of step i+1 overlap the kernels of step i and the
         # read-back of step i-1 (a copy-in stream, the compute stream, a read-back
         # stream; inputs and outputs double-buffered on the device). Every step still
-        # copies its inputs from pinned host memory and reads its output back.
+        # copies its inputs from pinned host memory and reads its output and final
+        # state back.
         s_in = torch.cuda.Stream(device=dev)
         s_out = torch.cuda.Stream(device=dev)
         dvb = [dv_, {nm: torch.empty_like(getattr(inp, nm)) for nm in names}]
         outs = [bufs.out, torch.empty_like(bufs.out)]
+        fins = [bufs.final_state, torch.empty_like(bufs.final_state)]
         ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer k copied
         ev_used = [torch.cuda.Event() for _ in range(2)]   # kernels done with buffer k
-        ev_read = [torch.cuda.Event() for _ in range(2)]   # output k copied back
+        ev_read = [torch.cuda.Event() for _ in range(2)]   # outputs k copied back
 
         def pipe_step(i):
             k = i % 2
@@ -790,11 +839,12 @@ def main():
             gdn.gdn_forward(d, b_["q_raw"], b_["k_raw"], b_["v_raw"], b_["a"], b_["b"],
                             b_["gate_buf"][..., : w.Hv * w.dv], b_["conv_w"], b_["A_log"], b_["dt_bias"],
                             b_["norm_w"], b_.get("cu_seqlens"), b_.get("initial_state"), outs[k],
-                            bufs.final_state, bufs.workspace, bufs.ws_bytes, stream)
+                            fins[k], bufs.workspace, bufs.ws_bytes, stream)
             ev_used[k].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_used[k])
                 out_host.copy_(outs[k], non_blocking=True)
+                fin_host.copy_(fins[k], non_blocking=True)
                 ev_read[k].record(s_out)
 
         for i in range(4):
@@ -819,40 +869,51 @@ def main():
                "steps": ksteps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "mode": "pipelined: each step's host-to-device copies overlap the previous step's "
                        "kernels and read-back (a copy-in stream, the compute stream, a read-back "
-                       "stream; double-buffered device inputs and outputs); timed from the first copy "
-                       "to the last read-back",
+                       "stream; double-buffered device inputs, outputs and final states); timed from "
+                       "the first copy to the last read-back of out and final_state",
                "serial": serial}
+    del bufs, inp
 
-    # prologue (+ the cu_seqlens scan for packed input), the chunk stage (prep + chain on
-    # the tensor-core path, one kernel on the fp32 path), the epilogue
-    chunk_launches = 2 if tc else 1
-    nch = (d.T + CHUNK - 1) // CHUNK
-    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
-    if tc and inp.cu_seqlens is None and d.N == 1 and nch >= 256 and w.Hv * (w.dv // 64) * 2 <= nsm:
-        seg = max(-(-nch // 16), 64)            # the segmented schedule of one long sequence
-        chunk_launches = 2 * (-(-nch // seg))
-    launches_per_step = 1 + (1 if inp.cu_seqlens is not None else 0) + chunk_launches + 1
+    # the other workloads, each measured the same way in this run (one GPU only)
+    workloads = {}
+    if world == 1 and not args.no_workloads:
+        for name in ALL_WORKLOADS:
+            wk = WORKLOADS[name]
+            if name == w.name:
+                r = dict(res)
+            else:
+                r, _i, _d, _b, _p, _f, _s = measure_workload(
+                    wk, min(args.steps, args.workload_steps), min(args.warmup, 5), dev, world, barrier, gpu_id,
+                    not args.no_clocks, torch, gdn, make_inputs_device)
+                del _i, _b
+                torch.cuda.empty_cache()
+            r = {k: v for k, v in r.items() if k != "value"} | {"tokens_per_s": r["value"]}
+            workloads[name] = r
+
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+        "ms_per_step_median": res["ms_per_step_median"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"fp32": "f32", "bf16": "bf16", "fp16": "f16"}[w.dtype], "data": "synthetic",
         "config": {"workload": w.name, "B": d.B, "T": d.T, "N": d.N, "Hk": w.Hk, "Hv": w.Hv,
                    "dk": w.dk, "dv": w.dv, "tokens_per_step": ntok, "chunk": CHUNK,
                    "l2": "flushed before every timed step (512 MiB write, then 256 MiB read)",
                    "parallelism": f"replicas x{world}",
-                   "chunk_kernel": "tcgen05" if tc else "cuda-core fp32",
-                   "timing": "value: one gdn_forward per step, CUDA events around the call; kernels: "
-                             "the same work as gdn_prologue / gdn_chunk_rule / gdn_epilogue with events "
-                             "between them, a second pass of the same step count",
-                   "staged_ms_per_step": ms_staged},
+                   "chunk_kernel": res["chunk_kernel"],
+                   "timing": "value: one gdn_forward per step, CUDA events around the call, mean over the "
+                             "steps (ms_per_step_median beside it); kernels: the same work as gdn_prologue / "
+                             "gdn_chunk_rule / gdn_epilogue with events between them, a second pass of the "
+                             "same step count",
+                   "staged_ms_per_step": res["staged_ms_per_step"]},
         "roofline": roof,
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
-        "gpu_launches_per_step": launches_per_step,
-        "clocks": clocks,
+        "gpu_launches": res["gpu_launches_per_step"] * args.steps,
+        "gpu_launches_per_step": res["gpu_launches_per_step"],
+        "clocks": res["clocks"],
+        "workloads": workloads,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
