@@ -578,7 +578,9 @@ def chunk_launch_count(gdn, d, w, inp, nsm):
     if not tc:
         return 1
     nch = (d.T + CHUNK - 1) // CHUNK
-    if inp.cu_seqlens is None and d.N == 1 and nch >= 256 and w.Hv * (w.dv // 64) * 2 <= nsm:
+    tm = w.dtype != "fp32" and w.dk in (64, 128) and w.dv % 128 == 0     # the transposed chain: 128-row dv tiles
+    chain_ctas = w.Hv * (w.dv // 128 if tm else w.dv // 64)
+    if inp.cu_seqlens is None and d.N == 1 and nch >= 256 and chain_ctas * 2 <= nsm:
         seg = max(-(-nch // 16), 64)
         return 2 * (-(-nch // seg))
     return 2
@@ -750,7 +752,9 @@ def main():
     roof = dict(kernels[dom])
     roof["kernel"] = dom
     if dom == "chunk_rule":
-        roof["launches"] = ["chunk_prep_kernel", "chunk_chain_kernel"] if tc else ["chunk_simt_kernel"]
+        tm = w.dtype != "fp32" and w.dk in (64, 128) and w.dv % 128 == 0
+        roof["launches"] = (["chunk_prep_kernel", "chain_tm_kernel" if tm else "chunk_chain_kernel"] if tc
+                            else ["chunk_simt_kernel"])
     tr = NCU_TRAFFIC.get(dom)
     roof["traffic"] = None
     if tr is not None:

@@ -1,0 +1,558 @@
+// gdn_chain_tm.cu -- the serial state pass of the chunked gated delta rule for
+// dk <= 128 on the tcgen05 tensor cores, transposed so that 128 dv columns of
+// the state are the 128 rows (TMEM lanes) of every product, and the state and
+// the per-chunk operands stay in tensor memory.
+//
+// With H = S^T [dk][dv], and per chunk c of 64 tokens gam = in-chunk cumulative
+// decay, gL = its last value, and the prep kernel's tiles [T; P T] and
+// X_c = [K_c; Q_c] K_{c-1}^T (see gdn_chunk_tc.cu):
+//   D1^T  = H_{c-1}^T [K_c; Q_c]^T
+//         = (e^{gL_{c-1}} H_{c-2})^T [K_c; Q_c]^T + Vn'^T_{c-1} X_c^T
+//   R^T   = (V - diag(e^gam) K H_{c-1})^T diag(beta)      (K half of D1^T)
+//   D2^T  = R^T [T; P T]^T                                 (N = 128)
+//   Vn'^T = (T R)^T diag(e^{gL - gam})                     (top half of D2^T)
+//   O^T   = (Q H_{c-1})^T diag(e^gam) + (P T R)^T          (Q half of D1^T, bottom of D2^T)
+//   H_c^T = e^{gL_c} H_{c-1}^T + Vn'^T_c K_c
+// Each product has M = 128 dv rows and takes its A operand from tensor memory
+// (the fp16 copy of the state, R^T or Vn'^T, each written by the warps with
+// tcgen05.st); only its B operand ([K; Q], X, [T; P T]) comes from shared memory,
+// where a TMA warp stages it ahead of use. So the hand-offs on the serial path
+// (D1 -> R -> D2 -> Vn' -> next D1) are tensor-memory loads and stores with no
+// shared-memory round trip. The V tile also arrives by TMA; the outputs leave
+// through a shared staging tile and TMA tensor stores (a thread holds one dv
+// column across 64 tokens, so direct stores would be 2-byte scatters). Per-token
+// factors (beta, decays) reach the warps as broadcast reads of small per-warp
+// arrays rather than shuffles: the warps' shared-memory traffic shares the
+// issue path of the MMA-issuing thread.
+//
+// Every wait on an mbarrier gives up after about a second; the CTA then records
+// GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own copies and products in
+// flight, frees its tensor memory and returns.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "gdn_common.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+// warps 0..7: R and Vn' (the serial path); 8..15: state scaling and outputs;
+// 16: MMA issue; 17: TMA
+constexpr int kRowW = 8, kOutW = 8;
+constexpr int kMmaW = kRowW + kOutW, kTmaW = kMmaW + 1;
+constexpr int kTmThreads = (kTmaW + 1) * 32;
+
+// tensor-memory columns (lanes = the tile's 128 dv rows), each region aligned to its size
+constexpr uint32_t kTH = 0;      // H^T fp32, dk columns
+constexpr uint32_t kTD2 = 128;   // D2^T: [T R | P T R], 128 fp32 columns
+constexpr uint32_t kTD1 = 256;   // D1^T: [K H | Q H], 128 fp32 columns
+constexpr uint32_t kTH16 = 384;  // fp16 copy of (scaled) H^T, dk/2 columns
+constexpr uint32_t kTR = 448;    // R^T fp16, 32 columns
+constexpr uint32_t kTVN = 480;   // Vn'^T fp16, 32 columns
+
+struct TmMaps {
+    CUtensorMap q_hi, k_hi, v, o;
+};
+
+// T_FULL s / T_FREE s: operand stage s ([K; Q]) landed / free again (after the state
+// update that reads its K last); T_PFULL p / T_PFREE p: prep slot p (X and [T; P T])
+// landed / read by the chunk's second product; T_VFULL v / T_VFREE v: V tile slot v
+// landed / read by the row warps; T_OFREE / T_OSTAGE: the output staging tile may be
+// written / holds a chunk's outputs
+constexpr int kPSlots = 2, kVSlots = 2;
+enum TmBar { T_FULL0 = 0, T_FREE0 = 4, T_PFULL0 = 8, T_PFREE0 = T_PFULL0 + kPSlots, T_VFULL0 = T_PFREE0 + kPSlots,
+             T_VFREE0 = T_VFULL0 + kVSlots, T_C1 = T_VFREE0 + kVSlots, T_C2, T_C4, T_R, T_VN, T_O, T_H, T_OFREE,
+             T_OSTAGE, T_DRAIN, T_COUNT };
+static_assert(T_FREE0 >= T_FULL0 + 4 && T_PFULL0 >= T_FREE0 + 4, "barrier ranges overlap");
+
+template <int DK>
+struct TmSmem {
+    static constexpr int kStages = DK == 128 ? 3 : 4;
+    static constexpr uint32_t kBlocks = DK / 64;
+    static constexpr uint32_t kStage = kBlocks * 2 * kTileBytes;   // [K_b; Q_b] for each 64-column dk block
+    static constexpr uint32_t kP = kStages * kStage;                // kPSlots x (X, [T; P T])
+    static constexpr uint32_t kPSlot = kXBytes + kTPTBytes;
+    static constexpr uint32_t kV = kP + kPSlots * kPSlot;           // kVSlots V tiles (64 tokens x 128 dv)
+    static constexpr uint32_t kO = kV + kVSlots * 2 * kTileBytes;   // output staging tile (64 tokens x 128 dv)
+    static constexpr uint32_t kArr = kO + 2 * kTileBytes;           // per-warp token factors
+    static constexpr uint32_t kBars = kArr + 16 * 3 * 32 * 4;
+    static constexpr uint32_t kTotal = kBars + 256 + 1024;          // + barriers, + slack to align the base
+};
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kTmThreads, 1)
+chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles, int64_t nslots,
+                const unsigned char *prep_out, int cbase, int cmax) {
+    using L = TmSmem<DK>;
+    constexpr int NS = L::kStages;
+    constexpr int HC = DK / 2;            // state columns per state warp (two warps per lane group)
+    extern __shared__ unsigned char smraw[];
+    pdl_wait();        // the prep tiles (and everything before them) are complete
+    pdl_trigger();
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    const gdn_desc &d = p.d;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3;
+    const int vrow = quad * 32 + lane;           // this thread's dv row (TMEM lane)
+    const int half = (warp >> 2) & 1;            // row / out warps: tokens [32 half, 32 half + 32)
+    int bid = blockIdx.x;
+    const int tile = bid % ntiles;
+    bid /= ntiles;
+    const int j = bid % d.Hv;
+    const int n = bid / d.Hv;
+    const int dv = d.dv, Hv = d.Hv;
+    const int G = Hv / d.Hk;
+    const int hk = j / G;
+    const int v0 = tile * 128;
+    uint64_t *bar = (uint64_t *)(sm + L::kBars);
+    uint32_t *tslot = (uint32_t *)(bar + T_COUNT);
+    // this warp's token factors: 3 x 32 floats (row warps: beta, beta e^gam, e^{gL - gam};
+    // out warps: e^gam in the first 32)
+    float *arr = (float *)(sm + L::kArr) + (warp < 16 ? warp : 0) * 3 * 32;
+    __shared__ volatile int s_err;
+    __shared__ int s_skip;
+    if (tid == 0) s_skip = p.cu != nullptr && *p.status != GDN_OK;
+    __syncthreads();
+    if (s_skip) return;
+    // chunks [cbase, cbase + cmax) of the sequence (a segment of it, or all of it)
+    const int64_t sstart = p.cu ? (int64_t)p.cu[n] : (int64_t)n * d.T;
+    const int64_t seq1 = p.cu ? (int64_t)p.cu[n + 1] : sstart + d.T;
+    const int64_t seq0 = sstart + (int64_t)cbase * kChunk;
+    const int64_t left = seq1 > seq0 ? (seq1 - seq0 + kChunk - 1) / kChunk : 0;
+    const int nch = (int)(left < cmax ? left : cmax);
+    const int64_t slot0 = (p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk)) + cbase;
+    const size_t sbase = ((size_t)n * Hv + j) * DK * dv;
+    const float *gw = (const float *)p.gamma + (int64_t)j * p.ntok;
+    const float *bw = p.beta + (int64_t)j * p.ntok;
+    auto tok0 = [&](int c) { return seq0 + (int64_t)c * kChunk; };
+    auto clen = [&](int c) {
+        const int64_t r = seq1 - tok0(c);
+        return r < kChunk ? (int)r : kChunk;
+    };
+
+    if (tid == 0) {
+        s_err = 0;
+        for (int i = 0; i < T_COUNT; ++i) {
+            const bool warps8 = i == T_R || i == T_VN || i == T_O || i == T_H || i == T_VFREE0 || i == T_VFREE0 + 1 ||
+                                i == T_OSTAGE;
+            mbar_init(&bar[i], warps8 ? 8 : 1);
+        }
+        mbar_init_fence();
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *tslot;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    auto wait = [&](int b, uint32_t parity) -> bool {
+        if (s_err) return false;
+        if (!mbar_wait(&bar[b], parity)) { s_err = 1; return false; }
+        return true;
+    };
+    auto warp_arrive = [&](int b) {   // after this warp's tensor-memory accesses
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[b]);
+    };
+    const bool out_warp = warp >= kRowW && warp < kMmaW;
+    // state warps: H^T (row vrow, dk columns [half*HC, half*HC + HC)) and its fp16 copy
+    if (out_warp) {
+#pragma unroll
+        for (int q = 0; q < HC / 32; ++q) {
+            float t[32], h[16];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int dd = half * HC + 32 * q + k;
+                t[k] = p.h0 ? p.h0[sbase + (size_t)dd * dv + v0 + vrow] : 0.f;
+            }
+            tmem_st32(tbase + lane_off + kTH + half * HC + 32 * q, t);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) h[k] = __uint_as_float(pack_h2(t[2 * k], t[2 * k + 1]));
+            tmem_st16(tbase + lane_off + kTH16 + half * (HC / 2) + 16 * q, h);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    int tma_armed = 0, p_armed = 0, v_armed = 0;   // chunks whose loads the TMA thread has issued
+    if (warp == kTmaW) {
+        // ------------------------------------------------------------ TMA warp
+        if (lane == 0) {
+            auto load_kq = [&](int c) {
+                const int s = c % NS;
+                unsigned char *st = sm + s * L::kStage;
+                const int y = (int)((int64_t)hk * p.ntok + tok0(c));
+                mbar_expect_tx(&bar[T_FULL0 + s], L::kStage);
+                for (int b = 0; b < (int)L::kBlocks; ++b) {
+                    tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, y, &bar[T_FULL0 + s]);
+                    tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, y, &bar[T_FULL0 + s]);
+                }
+            };
+            auto load_prep = [&](int c) {   // X (not for a first chunk) and [T; P T]
+                const int ps = c % kPSlots;
+                unsigned char *dst = sm + L::kP + ps * L::kPSlot;
+                mbar_expect_tx(&bar[T_PFULL0 + ps], kTPTBytes + (c > 0 ? kXBytes : 0));
+                if (c > 0)
+                    bulk_load(dst, prep_out + ((int64_t)(hk * G) * nslots + slot0 + c) * kPrepOut + kTPTBytes,
+                              kXBytes, &bar[T_PFULL0 + ps]);
+                bulk_load(dst + kXBytes, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut, kTPTBytes,
+                          &bar[T_PFULL0 + ps]);
+            };
+            auto load_v = [&](int c) {
+                const int sv = c % kVSlots;
+                unsigned char *dst = sm + L::kV + sv * 2 * kTileBytes;
+                const int y = (int)((int64_t)j * p.ntok + tok0(c));
+                mbar_expect_tx(&bar[T_VFULL0 + sv], 2 * kTileBytes);
+                tma_load_2d(dst, &maps.v, v0, y, &bar[T_VFULL0 + sv]);
+                tma_load_2d(dst + kTileBytes, &maps.v, v0 + 64, y, &bar[T_VFULL0 + sv]);
+            };
+            for (int c = 0; c < nch; ++c) {
+                // stage c % NS is free once the state update of chunk c - NS is done
+                if (c >= NS && !wait(T_FREE0 + c % NS, (uint32_t)((c / NS) - 1) & 1)) break;
+                load_kq(c);
+                tma_armed = c + 1;
+                // prep slot c % 2 once the second product of chunk c - 2 has read it
+                if (c >= kPSlots && !wait(T_PFREE0 + c % kPSlots, (uint32_t)((c / kPSlots) - 1) & 1)) break;
+                load_prep(c);
+                p_armed = c + 1;
+                // V slot c % 2 once the row warps have read chunk c - 2's V
+                if (c >= kVSlots && !wait(T_VFREE0 + c % kVSlots, (uint32_t)((c / kVSlots) - 1) & 1)) break;
+                load_v(c);
+                v_armed = c + 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaW) {
+        // ------------------------------------------------------------ MMA warp
+        if (lane == 0) {
+            const uint32_t id128 = idesc_f16(128, 128, false, false);
+            const uint32_t idH = idesc_f16(128, DK, false, true);   // B = K, MN-major (dk contiguous)
+            // descriptors are built once; an offset adds (bytes >> 4) to the start field
+            // (shared addresses stay below 2^18, so the 14-bit field never carries)
+            const uint64_t dK0 = sw128_desc(smem_u32(sm), 16, 1024);              // K-major tiles
+            const uint64_t dKt0 = sw128_desc(smem_u32(sm), 2 * kTileBytes, 1024); // K as MN-major B
+            const uint64_t stg = L::kStage >> 4, pslot = L::kPSlot >> 4;
+            const uint64_t dP0 = dK0 + (L::kP >> 4);
+            // D1 = H16^T [K; Q]^T over dk ([K_b; Q_b] is a 128-row K-major tile per block)
+            auto c1a = [&](int s) {
+                const uint64_t b0 = dK0 + s * stg;
+#pragma unroll
+                for (int ks = 0; ks < DK / 16; ++ks)
+                    mma_f16_ta(tbase + kTD1, tbase + kTH16 + 8 * ks,
+                               b0 + (uint64_t)(((ks >> 2) * 2 * kTileBytes + 32 * (ks & 3)) >> 4), id128, ks != 0);
+            };
+            // D1 += Vn'^T_{c-1} X^T (X: 128 rows of [K_c; Q_c] tokens x 64 tokens of c-1)
+            auto c1b = [&](int ps) {
+                const uint64_t b0 = dP0 + ps * pslot;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16_ta(tbase + kTD1, tbase + kTVN + 8 * kk, b0 + (uint64_t)(2 * kk), id128, 1);
+            };
+            // H^T += Vn'^T K (K of stage s as an MN-major B: tokens are K, dk is N)
+            auto c4 = [&](int s) {
+                const uint64_t b0 = dKt0 + s * stg;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16_ta(tbase + kTH, tbase + kTVN + 8 * kk, b0 + (uint64_t)(128 * kk), idH, 1);
+                mma_commit(&bar[T_FREE0 + s]);
+            };
+            int c = 0;
+            for (; c < nch; ++c) {
+                const int s = c % NS, ps = c % kPSlots;
+                if (!wait(T_FULL0 + s, (uint32_t)(c / NS) & 1)) break;
+                // H16 = e^{gL_{c-1}} H_{c-2}; D1 of chunk c-1 read by the out warps
+                if (c >= 1 && (!wait(T_H, (uint32_t)(c - 1) & 1) || !wait(T_O, (uint32_t)(c - 1) & 1))) break;
+                fence_after_sync();
+                c1a(s);
+                if (!wait(T_PFULL0 + ps, (uint32_t)(c / kPSlots) & 1)) break;
+                if (c >= 1) {
+                    if (!wait(T_VN, (uint32_t)(c - 1) & 1)) break;     // Vn'_{c-1}
+                    fence_after_sync();
+                    c1b(ps);
+                }
+                mma_commit(&bar[T_C1]);
+                if (c >= 1) c4((c - 1) % NS);
+                // C4 of chunk c-1 (for c = 0: the first product, which read H16 = H_init)
+                mma_commit(&bar[T_C4]);
+                if (!wait(T_R, (uint32_t)c & 1)) break;
+                fence_after_sync();
+                const uint64_t bt = dP0 + ps * pslot + (kXBytes >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16_ta(tbase + kTD2, tbase + kTR + 8 * kk, bt + (uint64_t)(2 * kk), id128, kk != 0);
+                mma_commit(&bar[T_C2]);
+                mma_commit(&bar[T_PFREE0 + ps]);
+            }
+            if (c == nch && nch > 0) {   // the state update of the last chunk
+                if (wait(T_VN, (uint32_t)(nch - 1) & 1) && wait(T_H, (uint32_t)(nch - 1) & 1)) {
+                    fence_after_sync();
+                    c4((nch - 1) % NS);
+                    mma_commit(&bar[T_C4]);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < kRowW) {
+        // ------------------------------------------------------------ row warps
+        // lane l loads the decay and beta of token 32 half + l two chunks ahead (one chunk
+        // is shorter than a DRAM round trip); V comes through the TMA ring
+        struct RowIn {
+            float g, b, gl;
+        };
+        RowIn A, B;
+        auto prefetch = [&](int c, RowIn &x) {
+            const int64_t t0 = tok0(c);
+            const int len = clen(c);
+            const int i = 32 * half + lane;
+            x.g = gw[t0 + (i < len ? i : len - 1)];
+            x.b = i < len ? bw[t0 + i] : 0.f;
+            x.gl = gw[t0 + len - 1];
+        };
+        // element (token i, this thread's dv row) of a V slot: 64-column box vrow / 64
+        const uint32_t vcol = (uint32_t)(vrow & 63), vbox = (uint32_t)(vrow >> 6) * kTileBytes;
+        const float4 *a4 = reinterpret_cast<const float4 *>(arr);
+        if (nch > 0) prefetch(0, A);
+        if (nch > 1) prefetch(1, B);
+        for (int c = 0; c < nch; ++c) {
+            const int len = clen(c);
+            // this chunk's factors, one per lane, published to the warp's array
+            __syncwarp();                 // the previous chunk's reads of the array are done
+            arr[lane] = A.b;
+            arr[32 + lane] = A.b * __expf(A.g);
+            arr[64 + lane] = __expf(A.gl - A.g);
+            __syncwarp();
+            if (!wait(T_VFULL0 + c % kVSlots, (uint32_t)(c / kVSlots) & 1)) break;
+            const unsigned char *vs = sm + L::kV + (c % kVSlots) * 2 * kTileBytes + vbox;
+            float vv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int ti = 32 * half + i;
+                vv[i] = ti < len ? __half2float(*reinterpret_cast<const __half *>(vs + sw128_off(ti, vcol))) : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[T_VFREE0 + c % kVSlots]);
+            // R^T = beta V - beta e^gam (K H) for this half's 32 tokens
+            if (!wait(T_C1, (uint32_t)c & 1)) break;
+            fence_after_sync();
+            float a[32];
+            tmem_ld32(tbase + lane_off + kTD1 + 32 * half, a);
+            float r[16];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const float4 b4 = a4[m], e4 = a4[8 + m];
+                r[2 * m] = __uint_as_float(pack_h2(b4.x * vv[4 * m] - e4.x * a[4 * m],
+                                                   b4.y * vv[4 * m + 1] - e4.y * a[4 * m + 1]));
+                r[2 * m + 1] = __uint_as_float(pack_h2(b4.z * vv[4 * m + 2] - e4.z * a[4 * m + 2],
+                                                       b4.w * vv[4 * m + 3] - e4.w * a[4 * m + 3]));
+            }
+            tmem_st16(tbase + lane_off + kTR + 16 * half, r);
+            warp_arrive(T_R);
+            // Vn'^T = e^{gL - gam} (T R)^T
+            if (!wait(T_C2, (uint32_t)c & 1)) break;
+            fence_after_sync();
+            tmem_ld32(tbase + lane_off + kTD2 + 32 * half, a);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const float4 s4 = a4[16 + m];
+                r[2 * m] = __uint_as_float(pack_h2(s4.x * a[4 * m], s4.y * a[4 * m + 1]));
+                r[2 * m + 1] = __uint_as_float(pack_h2(s4.z * a[4 * m + 2], s4.w * a[4 * m + 3]));
+            }
+            tmem_st16(tbase + lane_off + kTVN + 16 * half, r);
+            warp_arrive(T_VN);
+            A = B;                                   // chunk c + 1 (loaded a chunk ago)
+            if (c + 2 < nch) prefetch(c + 2, B);
+        }
+    } else if (out_warp) {
+        // ------------------------------------------------ state and output warps
+        __half *o = (__half *)p.o;
+        auto store_final = [&]() {
+#pragma unroll
+            for (int q = 0; q < HC / 32; ++q) {
+                float t[32];
+                tmem_ld32(tbase + lane_off + kTH + half * HC + 32 * q, t);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) p.hT[sbase + (size_t)(half * HC + 32 * q + k) * dv + v0 + vrow] = t[k];
+            }
+        };
+        // the decay of this lane's token and the chunk's last decay
+        auto decays = [&](int c, float &g_tok, float &g_last) {
+            const int64_t t0 = tok0(c);
+            const int len = clen(c);
+            const int i = 32 * half + lane;
+            g_tok = gw[t0 + (i < len ? i : len - 1)];
+            g_last = gw[t0 + len - 1];
+        };
+        // one thread issues the output tile's tensor stores
+        const bool storer = warp == kRowW && lane == 0;
+        int nstored = 0;
+        const float4 *a4 = reinterpret_cast<const float4 *>(arr);
+        // two chunks ahead: chunk c's values move into place at the end of iteration c - 1,
+        // one iteration after their loads were issued, so no move waits on a load in flight
+        float g_tok = 0.f, g_last = 0.f, g_tok_n = 0.f, g_last_n = 0.f;
+        if (nch > 0) decays(0, g_tok, g_last);
+        if (nch > 1) decays(1, g_tok_n, g_last_n);
+        for (int c = 0; c < nch; ++c) {
+            // H_{c-1} is complete (or, for c = 0, the first product has read H16 = H_init):
+            // scale by e^{gL_c} for chunk c's update and publish its fp16 copy for chunk c+1
+            if (!wait(T_C4, (uint32_t)c & 1)) break;
+            fence_after_sync();
+            {
+                const float e = __expf(g_last);
+#pragma unroll
+                for (int q = 0; q < HC / 32; ++q) {
+                    float t[32];
+                    tmem_ld32(tbase + lane_off + kTH + half * HC + 32 * q, t);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) t[k] *= e;
+                    tmem_st32(tbase + lane_off + kTH + half * HC + 32 * q, t);
+                    if (c + 1 < nch) {
+                        float h[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) h[k] = __uint_as_float(pack_h2(t[2 * k], t[2 * k + 1]));
+                        tmem_st16(tbase + lane_off + kTH16 + half * (HC / 2) + 16 * q, h);
+                    }
+                }
+            }
+            warp_arrive(T_H);
+            __syncwarp();                 // the previous chunk's reads of the array are done
+            arr[lane] = __expf(g_tok);
+            __syncwarp();
+            // O^T = e^gam (Q H)^T + (P T R)^T for this half's 32 tokens
+            if (!wait(T_C2, (uint32_t)c & 1)) break;
+            fence_after_sync();
+            float a[32], b[32];
+            tmem_ld32x2(tbase + lane_off + kTD1 + 64 + 32 * half, tbase + lane_off + kTD2 + 64 + 32 * half, a, b);
+            warp_arrive(T_O);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const float4 e4 = a4[m];
+                a[4 * m] = fmaf(e4.x, a[4 * m], b[4 * m]) * d.scale;
+                a[4 * m + 1] = fmaf(e4.y, a[4 * m + 1], b[4 * m + 1]) * d.scale;
+                a[4 * m + 2] = fmaf(e4.z, a[4 * m + 2], b[4 * m + 2]) * d.scale;
+                a[4 * m + 3] = fmaf(e4.w, a[4 * m + 3], b[4 * m + 3]) * d.scale;
+            }
+            const int64_t t0 = tok0(c);
+            const int len = clen(c);
+            if (len == kChunk) {
+                // a full chunk: transpose through the staging tile, one tensor store per 64 columns
+                if (storer) {
+                    bulk_wait_read();                     // the previous store has read the tile
+                    mbar_arrive(&bar[T_OFREE]);
+                }
+                if (!wait(T_OFREE, (uint32_t)nstored & 1)) break;
+                unsigned char *ob = sm + L::kO + (uint32_t)(vrow >> 6) * kTileBytes;
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    *reinterpret_cast<__half *>(ob + sw128_off(32 * half + k, vrow & 63)) = __float2half_rn(a[k]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[T_OSTAGE]);
+                if (storer) {
+                    if (!wait(T_OSTAGE, (uint32_t)nstored & 1)) break;
+                    tma_store_2d(&maps.o, j * dv + v0, (int)t0, sm + L::kO);
+                    tma_store_2d(&maps.o, j * dv + v0 + 64, (int)t0, sm + L::kO + kTileBytes);
+                    bulk_commit();
+                }
+                ++nstored;
+            } else {
+                // the last, partial chunk of a sequence: the tile's other rows belong to the next
+                __half *dst = o + (t0 + 32 * half) * (int64_t)Hv * dv + (int64_t)j * dv + v0 + vrow;
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (32 * half + k < len) dst[(int64_t)k * Hv * dv] = __float2half_rn(a[k]);
+            }
+            g_tok = g_tok_n;
+            g_last = g_last_n;
+            if (c + 2 < nch) decays(c + 2, g_tok_n, g_last_n);
+        }
+        if (storer) bulk_wait();   // the output stores are complete before the CTA leaves
+        if (p.hT && !s_err) {
+            if (nch == 0) {
+                store_final();
+            } else if (wait(T_C4, (uint32_t)nch & 1)) {
+                fence_after_sync();
+                store_final();
+            }
+        }
+    }
+    __syncthreads();
+    if (s_err) {
+        // drain: this CTA's own copies and products, bounded, before the tensor memory is freed
+        if (tid == kMmaW * 32) {
+            atomicCAS(p.status, GDN_OK, GDN_ERR_DEVICE_TIMEOUT);
+            mma_commit(&bar[T_DRAIN]);
+            mbar_wait(&bar[T_DRAIN], 0);
+        }
+        if (tid == kTmaW * 32) {
+            for (int c = tma_armed - NS < 0 ? 0 : tma_armed - NS; c < tma_armed; ++c)
+                mbar_wait(&bar[T_FULL0 + c % NS], (uint32_t)(c / NS) & 1);
+            for (int c = p_armed - kPSlots < 0 ? 0 : p_armed - kPSlots; c < p_armed; ++c)
+                mbar_wait(&bar[T_PFULL0 + c % kPSlots], (uint32_t)(c / kPSlots) & 1);
+            for (int c = v_armed - kVSlots < 0 ? 0 : v_armed - kVSlots; c < v_armed; ++c)
+                mbar_wait(&bar[T_VFULL0 + c % kVSlots], (uint32_t)(c / kVSlots) & 1);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+int max_dyn_smem_tm() {
+    int dev = 0, v = 232448;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return v;
+}
+
+template <int DK>
+cudaError_t launch_tm(const Problem &p, cudaStream_t s, const unsigned char *prep_out, int64_t nslots_alloc,
+                      int cbase, int cmax, bool pdl, unsigned nblocks) {
+    const gdn_desc &d = p.d;
+    TmMaps m;
+    if (p.ntok > 0) {
+        if (!encode_tile_map(&m.q_hi, p.q, (uint64_t)d.Hk * p.ntok, DK) ||
+            !encode_tile_map(&m.k_hi, p.k, (uint64_t)d.Hk * p.ntok, DK) ||
+            !encode_tile_map(&m.v, p.v, (uint64_t)d.Hv * p.ntok, d.dv) ||
+            !encode_tile_map(&m.o, p.o, (uint64_t)p.ntok, (uint64_t)d.Hv * d.dv))
+            return cudaErrorInvalidValue;
+    } else {
+        memset(&m, 0, sizeof(m));   // no chunks: the kernel only copies the initial state
+    }
+    const int maxs = max_dyn_smem_tm();
+    // all 512 TMEM columns: enough shared memory that a second CTA never shares the SM
+    size_t smem = TmSmem<DK>::kTotal;
+    if (smem < (size_t)(maxs / 2 + 1024)) smem = (size_t)(maxs / 2 + 1024);
+    if ((int)smem > maxs) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(chain_tm_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (nblocks == 0) return cudaSuccess;
+    return launch_kernel(pdl, chain_tm_kernel<DK>, dim3(nblocks), dim3(kTmThreads), smem, s, m, p, d.dv / 128,
+                         nslots_alloc, prep_out, cbase, cmax);
+}
+
+}  // namespace
+
+bool chain_tm_supports(const gdn_desc &d) {
+    return (d.dtype == GDN_BF16 || d.dtype == GDN_F16) && (d.dk == 64 || d.dk == 128) && d.dv >= 128 &&
+           d.dv % 128 == 0;
+}
+
+int chain_tm_tiles(const gdn_desc &d) { return d.dv / 128; }
+
+cudaError_t launch_chain_tm(const Problem &p, cudaStream_t s, const unsigned char *prep_out, int64_t nslots_alloc,
+                            int cbase, int cmax, bool pdl, unsigned nblocks) {
+    return p.d.dk == 128 ? launch_tm<128>(p, s, prep_out, nslots_alloc, cbase, cmax, pdl, nblocks)
+                         : launch_tm<64>(p, s, prep_out, nslots_alloc, cbase, cmax, pdl, nblocks);
+}
+
+}  // namespace gdn

@@ -40,10 +40,6 @@ using namespace tc;
 
 constexpr int kThreads = 128;
 constexpr int LDA = kChunk + 1;
-constexpr uint32_t kTileBytes = 64 * 128;      // one 64x64 fp16 tile (8 KB)
-constexpr uint32_t kTPTBytes = 2 * kTileBytes; // [T; P T] 128x64 fp16
-constexpr uint32_t kXBytes = 2 * kTileBytes;   // X = [K_c; Q_c] K_{c-1}^T, 128x64 fp16
-constexpr uint32_t kPrepOut = kTPTBytes + kXBytes;   // per (v head, chunk) in the workspace
 
 struct PrepMaps {
     CUtensorMap q_hi, q_lo, k_hi, k_lo;
@@ -909,18 +905,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D fp16 map over [rows][cols] with 64x64 boxes and 128-byte swizzle
-bool encode_tile_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {64, 64};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 // Segmented schedule of a long single sequence: one high-priority stream per
 // device for the chain segments and the events that order them against the
@@ -957,6 +941,18 @@ int max_dyn_smem() {
 }
 
 }  // namespace
+
+bool encode_tile_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool chunk_tc_supports(const gdn_desc &d) {
     return (d.dtype == GDN_BF16 || d.dtype == GDN_F16) && (d.dk == 64 || d.dk == 128 || d.dk == 256) &&
@@ -996,6 +992,9 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
             if (e != cudaSuccess) return e;
         }
     }
+    if (chain_tm_supports(d))
+        return launch_chain_tm(p, s, tpt, nslots_alloc, 0, 0x7fffffff, p.pdl && p.ntok > 0,
+                               (unsigned)((int64_t)d.N * d.Hv * chain_tm_tiles(d)));
     ChainMaps cm;
     if (p.ntok > 0) {
         if (!encode_tile_map(&cm.q_hi, p.q, (uint64_t)d.Hk * p.ntok, d.dk) ||
@@ -1077,7 +1076,8 @@ bool chunk_tc_segmented(const Problem &p) {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
-    return nch >= 256 && (int64_t)d.Hv * (d.dv / 64) * 2 <= nsm;
+    const int64_t chain_ctas = (int64_t)d.Hv * (chain_tm_supports(d) ? chain_tm_tiles(d) : d.dv / 64);
+    return nch >= 256 && chain_ctas * 2 <= nsm;
 }
 
 cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
@@ -1134,9 +1134,14 @@ cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
         Problem pg = p;
         pg.h0 = g == 0 ? p.h0 : seg_state;
         pg.hT = g == nseg - 1 ? p.hT : seg_state;
-        chain<<<(unsigned)(d.Hv * ntiles), kChainThreads, smem, ss->hp>>>(cm, pg, ntiles,
-                                                                                      nslots_alloc, tpt, cb, cn);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (chain_tm_supports(d)) {
+            e = launch_chain_tm(pg, ss->hp, tpt, nslots_alloc, cb, cn, false, (unsigned)(d.Hv * chain_tm_tiles(d)));
+        } else {
+            chain<<<(unsigned)(d.Hv * ntiles), kChainThreads, smem, ss->hp>>>(cm, pg, ntiles, nslots_alloc, tpt,
+                                                                              cb, cn);
+            e = cudaGetLastError();
+        }
+        if (e != cudaSuccess) return e;
     }
     // the caller's stream continues once the last chain segment is done
     if ((e = cudaEventRecord(ss->ev[1 + nseg], ss->hp)) != cudaSuccess) return e;

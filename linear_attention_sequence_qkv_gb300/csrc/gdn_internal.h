@@ -113,6 +113,13 @@ int forward_single_stream(const gdn_desc *d, const void *q_raw, const void *k_ra
                           const int32_t *cu_seqlens, const float *initial_state, void *out,
                           float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 bool chunk_tc_supports(const gdn_desc &d);
+// the transposed chain (dk <= 128, 128-row dv tiles, operands in tensor memory;
+// gdn_chain_tm.cu): chunks [cbase, cbase + cmax) of every sequence, nblocks =
+// sequences x Hv x chain_tm_tiles CTAs
+bool chain_tm_supports(const gdn_desc &d);
+int chain_tm_tiles(const gdn_desc &d);
+cudaError_t launch_chain_tm(const Problem &p, cudaStream_t s, const unsigned char *prep_out, int64_t nslots_alloc,
+                            int cbase, int cmax, bool pdl, unsigned nblocks);
 cudaError_t launch_epilogue(const Problem &p, cudaStream_t s);
 // H_in[s] = A[s-1] H_in[s-1] + B[s-1], H_in[0] = h0 (or zeros), per v head
 cudaError_t launch_span_scan(int spans, int Hv, int dk, int dv, const float *A, const float *B, const float *h0,

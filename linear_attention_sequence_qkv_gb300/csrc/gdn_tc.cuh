@@ -182,6 +182,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], issued by one thread. A (M = 128 rows in the
+// 128 lanes, K-major) holds two 16-bit elements per 32-bit column, the lower
+// K index in the low half: a K step of 16 advances the A address by 8 columns.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -235,6 +246,17 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         :: "r"(smem_u32(smem_dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// 2-D tile store shared -> global through the tensor map's box; completes as a
+// bulk async group (commit with bulk_commit, wait with bulk_wait_read / bulk_wait).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, const void *smem_src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(smem_src)) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's committed bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and are complete
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Contiguous bulk copy global -> shared (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes,
                                           uint64_t *bar) {
@@ -243,5 +265,19 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint3
         :: "r"(smem_u32(smem_dst)), "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// ------------------------------------------------ prep-kernel output tiles
+// Per (v head, chunk slot) the prep kernel writes, already in the
+// 128-byte-swizzled shared-memory image, the [T; P T] tile (128 x 64 fp16) and
+// then X = [K_c; Q_c] K_{c-1}^T (128 x 64 fp16; written in the slot of the first
+// v head of each GQA group only). The chain kernels fetch each with one bulk copy.
+constexpr uint32_t kTileBytes = 64 * 128;      // one 64x64 fp16 tile (8 KB)
+constexpr uint32_t kTPTBytes = 2 * kTileBytes; // [T; P T] 128x64 fp16
+constexpr uint32_t kXBytes = 2 * kTileBytes;   // X, 128x64 fp16
+constexpr uint32_t kPrepOut = kTPTBytes + kXBytes;
+
 }  // namespace tc
+
+// 2-D fp16 tensor map over [rows][cols] with 64x64 boxes and 128-byte swizzle
+// (host; false when the driver entry point or the encoding fails).
+bool encode_tile_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols);
 }  // namespace gdn
