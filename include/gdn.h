@@ -181,6 +181,22 @@ int gdn_device_status(const void *workspace, int *status, gdn_stream_t stream);
 const char *gdn_status_string(int status);
 
 /*
+ * Test hook for the tensor-core kernels' bounded waits (GDN_ERR_DEVICE_TIMEOUT).
+ * Every wait of those kernels on one of their own mbarriers gives up after about
+ * a second; the CTA then records GDN_ERR_DEVICE_TIMEOUT, waits (again bounded) for
+ * its own copies and products in flight, frees its tensor memory and returns.
+ * With immediate = 1, calls made afterwards in this process launch these kernels
+ * so that a main-loop wait which is not already complete gives up at once (a
+ * non-blocking test instead of the timed wait), which drives that path on any
+ * input without stalling the GPU; the drains keep their ~1 s limit. immediate = 0
+ * restores the normal waits. The outputs of a call that timed out are
+ * unspecified; the next call in the normal mode is unaffected. Not meant for
+ * production use; there is no counterpart on the pages. Returns GDN_OK, or
+ * GDN_ERR_INVALID_ARG for another value.
+ */
+int gdn_set_wait_test_mode(int immediate);
+
+/*
  * gdn_forward without a caller-provided workspace, for callers that cannot
  * allocate device memory (code running inside another framework's memory
  * arena, plugins without an allocator, hosts that forbid allocation while

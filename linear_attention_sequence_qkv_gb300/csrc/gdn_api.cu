@@ -1,5 +1,6 @@
 // gdn_api.cu -- the C ABI (include/gdn.h): argument checks on metadata only,
 // workspace layout and the kernel launches of the GDN core forward.
+#include <atomic>
 #include <stdint.h>
 #include <string.h>
 
@@ -51,10 +52,13 @@ int check_ws(const gdn_desc *d, const void *ws, size_t bytes) {
     return GDN_OK;
 }
 
+std::atomic<int> g_wait_test_mode{0};
+
 Problem base_problem(const gdn_desc *d, const int32_t *cu, void *ws) {
     Problem p;
     memset(&p, 0, sizeof(p));
     p.d = *d;
+    p.wait_immediate = g_wait_test_mode.load();
     p.ntok = (int64_t)d->B * d->T;
     p.cu = cu;
     const Layout L = gdn::make_layout(*d);
@@ -370,6 +374,12 @@ int gdn_device_status(const void *workspace, int *status, gdn_stream_t stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     *status = v;
+    return GDN_OK;
+}
+
+int gdn_set_wait_test_mode(int immediate) {
+    if (immediate != 0 && immediate != 1) return GDN_ERR_INVALID_ARG;
+    g_wait_test_mode.store(immediate);
     return GDN_OK;
 }
 

@@ -156,7 +156,7 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     auto wait = [&](int b, uint32_t parity) -> bool {
         if (s_err) return false;
-        if (!mbar_wait(&bar[b], parity)) { s_err = 1; return false; }
+        if (!mbar_wait(&bar[b], parity, p.wait_immediate)) { s_err = 1; return false; }
         return true;
     };
     auto warp_arrive = [&](int b) {   // after this warp's tensor-memory accesses

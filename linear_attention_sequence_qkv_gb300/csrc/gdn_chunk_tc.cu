@@ -115,16 +115,17 @@ __device__ __forceinline__ void load_half_row_f16(const unsigned char *tile, int
 // and multiplied once; the decay masks, the solve and P T are per v head.
 constexpr int kPrepThreads = 256;   // 8 warps: warps w and w+4 share TMEM lanes, split columns
 constexpr int kLdc = kChunk + 4;    // column stride of A (column-major, 16-byte aligned columns)
-// v heads solved per pass (the solve scratch holds this many); one keeps the
-// shared memory of a CTA at ~58 KB and the TMEM at 128 columns, so that three
-// CTAs share an SM and hide each other's copy and barrier latency
-constexpr int kPassHeads = 1;
+// v heads solved per pass (the solve scratch holds this many), a template
+// parameter of the kernel. One keeps the CTA's shared memory at ~58 KB and its
+// TMEM at 128 columns, so that three CTAs share an SM and hide each other's copy
+// and barrier latency; two heads per pass under GQA (two CTAs per SM) measured
+// slower on the packed workload (6.55 against 5.83 ms for the chunk stage).
 
 struct PrepSmem {
     int blocks;            // dk / 64
     int bpp;               // dk blocks per load phase (operand buffers hold bpp blocks: one)
     size_t hi, lo, kp, Ac, Ts, Ws, tp, gam, bet, bars, total;
-    __host__ __device__ PrepSmem(int dk) {
+    __host__ __device__ PrepSmem(int dk, int ph) {
         blocks = dk / 64;
         bpp = 1;                                     // 40 KB of operands per phase
         size_t o = 0;
@@ -134,20 +135,21 @@ struct PrepSmem {
         // the solve's fp32 scratch reuses the operand buffers once S1 and X are done:
         // A (column-major), T (row-major), W = A21 T11 (row-major 32x33), per v head
         Ac = 0;
-        Ts = Ac + (size_t)kPassHeads * kChunk * kLdc * 4;
-        Ws = Ts + (size_t)kPassHeads * kChunk * LDA * 4;
-        const size_t solve_end = Ws + (size_t)kPassHeads * 32 * 33 * 4;
+        Ts = Ac + (size_t)ph * kChunk * kLdc * 4;
+        Ws = Ts + (size_t)ph * kChunk * LDA * 4;
+        const size_t solve_end = Ws + (size_t)ph * 32 * 33 * 4;
         if (solve_end > o) o = solve_end;
         o = (o + 1023) & ~(size_t)1023;
         tp = o; o += kTPTBytes;
-        gam = o; o += kPassHeads * kChunk * 4;
-        bet = o; o += kPassHeads * kChunk * 4;
+        gam = o; o += ph * kChunk * 4;
+        bet = o; o += ph * kChunk * 4;
         bars = o; o += 64;
         total = o + 1024;    // slack for aligning the base to 1024 B
     }
 };
 
-__global__ void __launch_bounds__(kPrepThreads, 3) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
+template <int PH>
+__global__ void __launch_bounds__(kPrepThreads, PH == 1 ? 3 : 2) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
                                                                      const Problem p, int64_t nslots,
                                                                      unsigned char *tpt, int64_t slot_base) {
     extern __shared__ unsigned char smraw[];
@@ -164,7 +166,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3) chunk_prep_kernel(const __gri
     if (p.cu != nullptr && *p.status != GDN_OK) return;
     ChunkLoc c;
     if (!locate_chunk(slot, p.cu, p.chunk_off, d.N, d.T, c)) return;
-    const PrepSmem L(d.dk);
+    constexpr int kPassHeads = PH;
+    const PrepSmem L(d.dk, PH);
     unsigned char *hi = sm + L.hi, *lo = sm + L.lo, *kp = sm + L.kp, *tp = sm + L.tp;
     float *Ac = (float *)(sm + L.Ac), *Ts = (float *)(sm + L.Ts), *Ws = (float *)(sm + L.Ws);
     float *gam = (float *)(sm + L.gam), *bet = (float *)(sm + L.bet);
@@ -221,30 +224,32 @@ __global__ void __launch_bounds__(kPrepThreads, 3) chunk_prep_kernel(const __gri
             }
         }
         load_out = true;
-        if (!mbar_wait(bar_load, load_phase & 1)) s_err = 1;
+        if (!mbar_wait(bar_load, load_phase & 1, p.wait_immediate)) s_err = 1;
         load_phase++;
         __syncthreads();
         if (s_err) goto cleanup;
         load_out = false;
         if (tid == 0) {
             const uint32_t id = idesc_f16(128, 64, false, false);
+            // descriptors built once; a K step adds 32 bytes (2 in the start field)
+            const uint64_t dh = sw128_desc(smem_u32(hi), 16, 1024), dl = sw128_desc(smem_u32(lo), 16, 1024);
+            const uint64_t dp = sw128_desc(smem_u32(kp), 16, 1024);
             for (int q = 0; q < L.bpp; ++q)
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t oh = smem_u32(hi + q * 2 * kTileBytes) + 32 * ks;
-                    const uint32_t ol = smem_u32(lo + q * 2 * kTileBytes) + 32 * ks;
-                    const uint64_t ah = sw128_desc(oh, 16, 1024), al = sw128_desc(ol, 16, 1024);
+                    const uint64_t off = (uint64_t)((q * 2 * kTileBytes) >> 4) + 2 * ks;
+                    const uint64_t ah = dh + off, al = dl + off;
                     mma_f16(tbase, ah, ah, id, (ph | q | ks) != 0);
                     mma_f16(tbase, ah, al, id, 1);
                     mma_f16(tbase, al, ah, id, 1);
                     if (has_prev)
-                        mma_f16(tbase + 64, ah, sw128_desc(smem_u32(kp + q * kTileBytes) + 32 * ks, 16, 1024),
-                                id, (ph | q | ks) != 0);
+                        mma_f16(tbase + 64, ah, dp + (uint64_t)((q * kTileBytes) >> 4) + 2 * ks, id, (ph | q | ks) != 0);
                 }
             mma_commit(bar_mma);
         }
         mma_out = true;
         // the buffers are reused by the next phase (and by the solve) once these MMAs are done
-        if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
+        if (!mbar_wait(bar_mma, mma_phase & 1, p.wait_immediate)) s_err = 1;
         mma_phase++;
         __syncthreads();
         if (s_err) goto cleanup;
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) chunk_prep_kernel(const __gri
                 mma_commit(bar_mma);
             }
             mma_out = true;
-            if (!mbar_wait(bar_mma, mma_phase & 1)) s_err = 1;
+            if (!mbar_wait(bar_mma, mma_phase & 1, p.wait_immediate)) s_err = 1;
             mma_phase++;
             __syncthreads();
             if (s_err) goto cleanup;
@@ -475,7 +480,7 @@ constexpr int kChainThreads = (kLoadWarp + 1) * 32;
 // the products reading stage s's Q + X part / K part are done (its refill may start).
 constexpr int kMaxStages = 3;
 enum ChainBar { B_LOAD0 = 0, B_LQ0 = B_LOAD0 + kMaxStages, B_TPT = B_LQ0 + kMaxStages, B_QF0, B_KF0 = B_QF0 + kMaxStages,
-                B_C1 = B_KF0 + kMaxStages, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_COUNT };
+                B_C1 = B_KF0 + kMaxStages, B_R, B_C2, B_VN, B_O, B_C4, B_H, B_DRAIN, B_COUNT };
 
 // NS stages: 3 where they fit (dk <= 128), else 2. REC: the backward's
 // recompute, storing the state at each chunk's start, Vn and O in fp32.
@@ -543,6 +548,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         mbar_init(&bar[B_VN], 4);
         mbar_init(&bar[B_O], 4);     // row warps of rows 64..127: 2, 3, 6, 7
         mbar_init(&bar[B_H], kStateWarps);
+        mbar_init(&bar[B_DRAIN], 1);
         mbar_init_fence();
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -564,7 +570,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     auto gamma_last = [&](int c) { return gw[chunk_tok0(c) + chunk_len(c) - 1]; };
     auto wait = [&](int b, uint32_t parity) -> bool {
         if (s_err) return false;
-        if (!mbar_wait(&bar[b], parity)) { s_err = 1; return false; }
+        if (!mbar_wait(&bar[b], parity, p.wait_immediate)) { s_err = 1; return false; }
         return true;
     };
     auto warp_arrive = [&](int b) {
@@ -601,6 +607,8 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     __syncthreads();
     fence_after_sync();
 
+    // loads the TMA thread has armed on each stage's K / Q+X barrier and on B_TPT
+    int armed_k[kMaxStages] = {}, armed_q[kMaxStages] = {}, armed_t = 0;
     if (warp == kLoadWarp) {
         // -------------------------------------------------------- TMA warp
         if (lane == 0) {
@@ -611,6 +619,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 unsigned char *st = sm + s * L.stage_bytes;
                 const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
                 mbar_expect_tx(&bar[B_LOAD0 + s], (uint32_t)L.blocks * kTileBytes);
+                ++armed_k[s];
                 for (int b = 0; b < L.blocks; ++b)
                     tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
             };
@@ -620,6 +629,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
                 const bool with_x = c > 0;
                 mbar_expect_tx(&bar[B_LQ0 + s], (uint32_t)L.blocks * kTileBytes + (with_x ? kXBytes : 0));
+                ++armed_q[s];
                 for (int b = 0; b < L.blocks; ++b)
                     tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar[B_LQ0 + s]);
                 if (with_x)
@@ -628,6 +638,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             };
             auto load_tpt = [&](int c) {
                 mbar_expect_tx(&bar[B_TPT], kTPTBytes);
+                ++armed_t;
                 bulk_load(tptb, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut, kTPTBytes, &bar[B_TPT]);
             };
             constexpr int ns = NS;
@@ -876,15 +887,22 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
         }
     }
     __syncthreads();
-    if (s_err && tid == kMmaWarp * 32) {
-        // drain: bounded waits for this CTA's own copies and MMAs before freeing TMEM
-        set_timeout(p);
-        for (int i = 0; i < NS; ++i)
-            for (int b : {B_LOAD0 + i, B_LQ0 + i}) { mbar_wait(&bar[b], 0); mbar_wait(&bar[b], 1); }
-        mbar_wait(&bar[B_TPT], 0);
-        mbar_wait(&bar[B_TPT], 1);
-        mbar_wait(&bar[B_C4], 0);
-        mbar_wait(&bar[B_C4], 1);
+    if (s_err) {
+        // drain, with bounded waits, before the tensor memory is freed: every MMA the
+        // MMA thread issued (one more commit covers them all) and every copy the TMA
+        // thread armed (each barrier's last armed phase)
+        if (tid == kMmaWarp * 32) {
+            set_timeout(p);
+            mma_commit(&bar[B_DRAIN]);
+            mbar_wait(&bar[B_DRAIN], 0);
+        }
+        if (tid == kLoadWarp * 32) {
+            for (int i = 0; i < NS; ++i) {
+                if (armed_k[i]) mbar_wait(&bar[B_LOAD0 + i], (uint32_t)(armed_k[i] - 1) & 1);
+                if (armed_q[i]) mbar_wait(&bar[B_LQ0 + i], (uint32_t)(armed_q[i] - 1) & 1);
+            }
+            if (armed_t) mbar_wait(&bar[B_TPT], (uint32_t)(armed_t - 1) & 1);
+        }
     }
     fence_before_sync();
     __syncthreads();
@@ -932,6 +950,11 @@ SideStream *side_stream(int dev) {   // caller holds g_side_mu
     ss.ready = true;
     return &ss;
 }
+
+// v heads per solve pass of the prep kernel, and its instance
+int prep_pass_heads(const gdn_desc &) { return 1; }
+using PrepFn = void (*)(const PrepMaps, const Problem, int64_t, unsigned char *, int64_t);
+PrepFn prep_kernel(int) { return chunk_prep_kernel<1>; }
 
 int max_dyn_smem() {
     int dev = 0, v = 232448;
@@ -982,12 +1005,13 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
             !encode_tile_map(&pm.k_hi, k, (uint64_t)d.Hk * p.ntok, d.dk) ||
             !encode_tile_map(&pm.k_lo, k + plane, (uint64_t)d.Hk * p.ntok, d.dk))
             return cudaErrorInvalidValue;
-        const PrepSmem ps(d.dk);
-        cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)ps.total);
+        const int ph = prep_pass_heads(d);
+        const PrepSmem ps(d.dk, ph);
+        auto prep = prep_kernel(ph);
+        cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
         if (e != cudaSuccess) return e;
         if (nslots > 0) {
-            e = launch_kernel(p.pdl, chunk_prep_kernel, dim3((unsigned)nslots, d.Hk), dim3(kPrepThreads), ps.total, s,
+            e = launch_kernel(p.pdl, prep, dim3((unsigned)nslots, d.Hk), dim3(kPrepThreads), ps.total, s,
                               pm, p, nslots_alloc, tpt, (int64_t)0);
             if (e != cudaSuccess) return e;
         }
@@ -1042,12 +1066,12 @@ cudaError_t launch_chunk_tc_rec(const Problem &p, cudaStream_t s) {
         !encode_tile_map(&cm.k_hi, p.k, (uint64_t)d.Hk * p.ntok, d.dk) ||
         !encode_tile_map(&cm.v, p.v, (uint64_t)d.Hv * p.ntok, d.dv))
         return cudaErrorInvalidValue;
-    const PrepSmem ps(d.dk);
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)ps.total);
+    const int ph = prep_pass_heads(d);
+    const PrepSmem ps(d.dk, ph);
+    auto prep = prep_kernel(ph);
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
     if (e != cudaSuccess) return e;
-    chunk_prep_kernel<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt,
-                                                                                   (int64_t)0);
+    prep<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt, (int64_t)0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int maxs = max_dyn_smem();
     const ChainSmem cs(d.dk);
@@ -1100,9 +1124,10 @@ cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
         !encode_tile_map(&cm.k_hi, p.k, (uint64_t)d.Hk * p.ntok, d.dk) ||
         !encode_tile_map(&cm.v, p.v, (uint64_t)d.Hv * p.ntok, d.dv))
         return cudaErrorInvalidValue;
-    const PrepSmem ps(d.dk);
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)ps.total);
+    const int ph = prep_pass_heads(d);
+    const PrepSmem ps(d.dk, ph);
+    auto prep = prep_kernel(ph);
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
     if (e != cudaSuccess) return e;
     const int maxs = max_dyn_smem();
     const ChainSmem cs(d.dk);
@@ -1123,8 +1148,7 @@ cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
     if ((e = cudaStreamWaitEvent(ss->hp, ss->ev[0], 0)) != cudaSuccess) return e;
     for (int g = 0; g < nseg; ++g) {
         const int cb = g * seg, cn = nch - cb < seg ? nch - cb : seg;
-        chunk_prep_kernel<<<dim3((unsigned)cn, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt,
-                                                                                   (int64_t)cb);
+        prep<<<dim3((unsigned)cn, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt, (int64_t)cb);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = cudaEventRecord(ss->ev[1 + g], s)) != cudaSuccess) return e;
     }

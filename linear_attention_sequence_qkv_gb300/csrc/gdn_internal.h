@@ -88,6 +88,10 @@ struct Problem {
     // null, or act dtype [N][3][2*Hk*dk + Hv*dv]: the raw q|k|v inputs of the three
     // tokens before each sequence (oldest first), read by the conv instead of zeros
     const void *conv_prefix;
+    // 0: the tensor-core kernels' main-loop waits give up after about a second;
+    // 1 (tests of the timeout path, gdn_set_wait_test_mode): a main-loop wait that is
+    // not already complete gives up at once. Drains always use the ~1 s limit.
+    int wait_immediate;
 };
 
 // Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one

@@ -226,8 +226,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Non-blocking test of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test_now(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
 // Wait for phase `parity` of `bar`, giving up after ~1 s. Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// immediate (tests of the timeout path only): give up at once unless the phase is
+// already complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, bool immediate = false) {
+    if (immediate) return mbar_test_now(bar, parity);
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_test(bar, parity)) {

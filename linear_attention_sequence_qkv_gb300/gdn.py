@@ -35,7 +35,7 @@ ACT_TORCH = {GDN_F32: torch.float32, GDN_BF16: torch.bfloat16, GDN_F16: torch.fl
 EXPORTS = ("gdn_desc_init", "gdn_workspace_bytes", "gdn_workspace_offsets", "gdn_forward",
            "gdn_prologue", "gdn_chunk_rule", "gdn_epilogue", "gdn_device_status",
            "gdn_status_string", "gdn_chunk_kernel_kind", "gdn_forward_static_ws",
-           "gdn_static_ws_device_status",
+           "gdn_static_ws_device_status", "gdn_set_wait_test_mode",
            "gdn_decode_workspace_bytes", "gdn_decode_step", "gdn_backward_workspace_bytes",
            "gdn_backward", "gdn_forward_with_prefix", "gdn_span_scan")
 
@@ -98,6 +98,7 @@ def load(path: str = LIB_PATH):
     L.gdn_chunk_kernel_kind.argtypes = [dp]
     L.gdn_forward_static_ws.argtypes = [dp] + [vp] * 14 + [vp]
     L.gdn_static_ws_device_status.argtypes = [ctypes.POINTER(i32), vp]
+    L.gdn_set_wait_test_mode.argtypes = [i32]
     L.gdn_decode_workspace_bytes.argtypes = [dp, ctypes.POINTER(sz)]
     L.gdn_decode_step.argtypes = [dp] + [vp] * 13 + [vp, sz, vp]
     L.gdn_forward_with_prefix.argtypes = [dp] + [vp] * 15 + [vp, sz, vp]
@@ -189,6 +190,12 @@ def gdn_static_ws_device_status(stream=None) -> int:
     st = ctypes.c_int(0)
     _check(load().gdn_static_ws_device_status(ctypes.byref(st), _stream(stream)), "gdn_static_ws_device_status")
     return st.value
+
+
+def gdn_set_wait_test_mode(immediate: int) -> None:
+    """Test hook: 1 makes the tensor-core kernels' main-loop waits give up at once
+    unless already complete (drives the GDN_ERR_DEVICE_TIMEOUT path); 0 restores them."""
+    _check(load().gdn_set_wait_test_mode(int(immediate)), "gdn_set_wait_test_mode")
 
 
 def gdn_prologue(d, q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, cu_seqlens,
