@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other four workloads (reported under 'workloads')")
+    ap.add_argument("--n-packed", type=int, default=0,
+                    help="packed workloads: this many sequences instead of the workload's (smaller cases for "
+                         "profiling)")
     ap.add_argument("--workload-steps", type=int, default=30,
                     help="timed steps for each of the other workloads (at most --steps)")
     ap.add_argument("--decode", action="store_true",
@@ -696,8 +699,10 @@ def measure_workload(w, steps, warmup, dev, world, barrier, gpu_id, with_clocks,
 
 def main():
     args = parse()
-    from linear_attention_sequence_qkv_gb300.workloads import WORKLOADS
+    from linear_attention_sequence_qkv_gb300.workloads import WORKLOADS, replace
     w = WORKLOADS[args.workload]
+    if args.n_packed and w.n_packed:
+        w = replace(w, name=f"{w.name}_n{args.n_packed}", n_packed=args.n_packed)
     if args.impl == "reference":
         reference_arm(args, w)
         return

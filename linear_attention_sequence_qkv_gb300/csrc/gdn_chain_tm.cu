@@ -88,7 +88,8 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int DK>
+// IMM: the test mode of the waits (gdn_set_wait_test_mode), a separate instance
+template <int DK, bool IMM>
 __global__ void __launch_bounds__(kTmThreads, 1)
 chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles, int64_t nslots,
                 const unsigned char *prep_out, int cbase, int cmax) {
@@ -156,7 +157,7 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     auto wait = [&](int b, uint32_t parity) -> bool {
         if (s_err) return false;
-        if (!mbar_wait(&bar[b], parity, p.wait_immediate)) { s_err = 1; return false; }
+        if (!mbar_wait(&bar[b], parity, IMM)) { s_err = 1; return false; }
         return true;
     };
     auto warp_arrive = [&](int b) {   // after this warp's tensor-memory accesses
@@ -319,8 +320,12 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             x.b = i < len ? bw[t0 + i] : 0.f;
             x.gl = gw[t0 + len - 1];
         };
-        // element (token i, this thread's dv row) of a V slot: 64-column box vrow / 64
-        const uint32_t vcol = (uint32_t)(vrow & 63), vbox = (uint32_t)(vrow >> 6) * kTileBytes;
+        // element (token 32 half + i, this thread's dv row) of a swizzled V slot sits at
+        // vbase + 128 i + (vchunk ^ 16 (i % 8)): the 16-byte chunk of column vrow % 64
+        // XORed with the row (32 half is a multiple of 8)
+        const uint32_t vcol = (uint32_t)(vrow & 63);
+        const uint32_t vbase = (uint32_t)(vrow >> 6) * kTileBytes + (uint32_t)(32 * half) * 128 + (vcol & 7) * 2;
+        const uint32_t vchunk = (vcol >> 3) << 4;
         const float4 *a4 = reinterpret_cast<const float4 *>(arr);
         if (nch > 0) prefetch(0, A);
         if (nch > 1) prefetch(1, B);
@@ -333,13 +338,13 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             arr[64 + lane] = __expf(A.gl - A.g);
             __syncwarp();
             if (!wait(T_VFULL0 + c % kVSlots, (uint32_t)(c / kVSlots) & 1)) break;
-            const unsigned char *vs = sm + L::kV + (c % kVSlots) * 2 * kTileBytes + vbox;
+            const unsigned char *vs = sm + L::kV + (c % kVSlots) * 2 * kTileBytes + vbase;
             float vv[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int ti = 32 * half + i;
-                vv[i] = ti < len ? __half2float(*reinterpret_cast<const __half *>(vs + sw128_off(ti, vcol))) : 0.f;
-            }
+            for (int i = 0; i < 32; ++i)
+                vv[i] = 32 * half + i < len
+                            ? __half2float(*reinterpret_cast<const __half *>(vs + 128 * i + (vchunk ^ (16u * (i & 7)))))
+                            : 0.f;
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[T_VFREE0 + c % kVSlots]);
             // R^T = beta V - beta e^gam (K H) for this half's 32 tokens
@@ -393,8 +398,11 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             g_tok = gw[t0 + (i < len ? i : len - 1)];
             g_last = gw[t0 + len - 1];
         };
-        // one thread issues the output tile's tensor stores
+        // one thread issues the output tile's tensor stores; staging-tile offsets as for V
         const bool storer = warp == kRowW && lane == 0;
+        const uint32_t ocol = (uint32_t)(vrow & 63);
+        const uint32_t obase = (uint32_t)(vrow >> 6) * kTileBytes + (uint32_t)(32 * half) * 128 + (ocol & 7) * 2;
+        const uint32_t ochunk = (ocol >> 3) << 4;
         int nstored = 0;
         const float4 *a4 = reinterpret_cast<const float4 *>(arr);
         // two chunks ahead: chunk c's values move into place at the end of iteration c - 1,
@@ -451,10 +459,10 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                     mbar_arrive(&bar[T_OFREE]);
                 }
                 if (!wait(T_OFREE, (uint32_t)nstored & 1)) break;
-                unsigned char *ob = sm + L::kO + (uint32_t)(vrow >> 6) * kTileBytes;
+                unsigned char *ob = sm + L::kO + obase;
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
-                    *reinterpret_cast<__half *>(ob + sw128_off(32 * half + k, vrow & 63)) = __float2half_rn(a[k]);
+                    *reinterpret_cast<__half *>(ob + 128 * k + (ochunk ^ (16u * (k & 7)))) = __float2half_rn(a[k]);
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[T_OSTAGE]);
@@ -533,11 +541,12 @@ cudaError_t launch_tm(const Problem &p, cudaStream_t s, const unsigned char *pre
     size_t smem = TmSmem<DK>::kTotal;
     if (smem < (size_t)(maxs / 2 + 1024)) smem = (size_t)(maxs / 2 + 1024);
     if ((int)smem > maxs) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chain_tm_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = p.wait_immediate ? chain_tm_kernel<DK, true> : chain_tm_kernel<DK, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (nblocks == 0) return cudaSuccess;
-    return launch_kernel(pdl, chain_tm_kernel<DK>, dim3(nblocks), dim3(kTmThreads), smem, s, m, p, d.dv / 128,
-                         nslots_alloc, prep_out, cbase, cmax);
+    return launch_kernel(pdl, kernel, dim3(nblocks), dim3(kTmThreads), smem, s, m, p, d.dv / 128, nslots_alloc,
+                         prep_out, cbase, cmax);
 }
 
 }  // namespace

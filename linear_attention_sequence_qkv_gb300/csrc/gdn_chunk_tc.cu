@@ -148,7 +148,9 @@ struct PrepSmem {
     }
 };
 
-template <int PH>
+// IMM: the test mode of the waits (gdn_set_wait_test_mode), a separate instance so
+// that the normal one carries nothing of it
+template <int PH, bool IMM>
 __global__ void __launch_bounds__(kPrepThreads, PH == 1 ? 3 : 2) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
                                                                      const Problem p, int64_t nslots,
                                                                      unsigned char *tpt, int64_t slot_base) {
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kPrepThreads, PH == 1 ? 3 : 2) chunk_prep_kern
             }
         }
         load_out = true;
-        if (!mbar_wait(bar_load, load_phase & 1, p.wait_immediate)) s_err = 1;
+        if (!mbar_wait(bar_load, load_phase & 1, IMM)) s_err = 1;
         load_phase++;
         __syncthreads();
         if (s_err) goto cleanup;
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kPrepThreads, PH == 1 ? 3 : 2) chunk_prep_kern
         }
         mma_out = true;
         // the buffers are reused by the next phase (and by the solve) once these MMAs are done
-        if (!mbar_wait(bar_mma, mma_phase & 1, p.wait_immediate)) s_err = 1;
+        if (!mbar_wait(bar_mma, mma_phase & 1, IMM)) s_err = 1;
         mma_phase++;
         __syncthreads();
         if (s_err) goto cleanup;
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(kPrepThreads, PH == 1 ? 3 : 2) chunk_prep_kern
                 mma_commit(bar_mma);
             }
             mma_out = true;
-            if (!mbar_wait(bar_mma, mma_phase & 1, p.wait_immediate)) s_err = 1;
+            if (!mbar_wait(bar_mma, mma_phase & 1, IMM)) s_err = 1;
             mma_phase++;
             __syncthreads();
             if (s_err) goto cleanup;
@@ -484,7 +486,8 @@ enum ChainBar { B_LOAD0 = 0, B_LQ0 = B_LOAD0 + kMaxStages, B_TPT = B_LQ0 + kMaxS
 
 // NS stages: 3 where they fit (dk <= 128), else 2. REC: the backward's
 // recompute, storing the state at each chunk's start, Vn and O in fp32.
-template <int NS, bool REC = false>
+// IMM: the test mode of the waits (gdn_set_wait_test_mode), a separate instance
+template <int NS, bool REC = false, bool IMM = false>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int ntiles,
                    int64_t nslots, const unsigned char *prep_out, int cbase, int cmax) {
@@ -570,7 +573,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     auto gamma_last = [&](int c) { return gw[chunk_tok0(c) + chunk_len(c) - 1]; };
     auto wait = [&](int b, uint32_t parity) -> bool {
         if (s_err) return false;
-        if (!mbar_wait(&bar[b], parity, p.wait_immediate)) { s_err = 1; return false; }
+        if (!mbar_wait(&bar[b], parity, IMM)) { s_err = 1; return false; }
         return true;
     };
     auto warp_arrive = [&](int b) {
@@ -607,8 +610,11 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     __syncthreads();
     fence_after_sync();
 
-    // loads the TMA thread has armed on each stage's K / Q+X barrier and on B_TPT
-    int armed_k[kMaxStages] = {}, armed_q[kMaxStages] = {}, armed_t = 0;
+    // per load barrier (B_LOAD s, B_LQ s, B_TPT): the parity of the last phase the TMA
+    // thread armed, or -1; kept in shared memory, read only by the drain
+    __shared__ int s_armed[B_TPT + 1];
+    if (tid <= B_TPT) s_armed[tid] = -1;
+    __syncthreads();
     if (warp == kLoadWarp) {
         // -------------------------------------------------------- TMA warp
         if (lane == 0) {
@@ -619,7 +625,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 unsigned char *st = sm + s * L.stage_bytes;
                 const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
                 mbar_expect_tx(&bar[B_LOAD0 + s], (uint32_t)L.blocks * kTileBytes);
-                ++armed_k[s];
+                s_armed[B_LOAD0 + s] = (c / NS) & 1;
                 for (int b = 0; b < L.blocks; ++b)
                     tma_load_2d(st + b * 2 * kTileBytes, &maps.k_hi, 64 * b, yk, &bar[B_LOAD0 + s]);
             };
@@ -629,7 +635,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
                 const int yk = (int)((int64_t)hk * p.ntok + chunk_tok0(c));
                 const bool with_x = c > 0;
                 mbar_expect_tx(&bar[B_LQ0 + s], (uint32_t)L.blocks * kTileBytes + (with_x ? kXBytes : 0));
-                ++armed_q[s];
+                s_armed[B_LQ0 + s] = (c / NS) & 1;
                 for (int b = 0; b < L.blocks; ++b)
                     tma_load_2d(st + b * 2 * kTileBytes + kTileBytes, &maps.q_hi, 64 * b, yk, &bar[B_LQ0 + s]);
                 if (with_x)
@@ -638,7 +644,7 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
             };
             auto load_tpt = [&](int c) {
                 mbar_expect_tx(&bar[B_TPT], kTPTBytes);
-                ++armed_t;
+                s_armed[B_TPT] = c & 1;
                 bulk_load(tptb, prep_out + ((int64_t)j * nslots + slot0 + c) * kPrepOut, kTPTBytes, &bar[B_TPT]);
             };
             constexpr int ns = NS;
@@ -889,20 +895,16 @@ chunk_chain_kernel(const __grid_constant__ ChainMaps maps, const Problem p, int 
     __syncthreads();
     if (s_err) {
         // drain, with bounded waits, before the tensor memory is freed: every MMA the
-        // MMA thread issued (one more commit covers them all) and every copy the TMA
-        // thread armed (each barrier's last armed phase)
+        // MMA thread issued (one more commit covers them all) and the last armed phase
+        // of every load barrier
         if (tid == kMmaWarp * 32) {
             set_timeout(p);
             mma_commit(&bar[B_DRAIN]);
             mbar_wait(&bar[B_DRAIN], 0);
         }
-        if (tid == kLoadWarp * 32) {
-            for (int i = 0; i < NS; ++i) {
-                if (armed_k[i]) mbar_wait(&bar[B_LOAD0 + i], (uint32_t)(armed_k[i] - 1) & 1);
-                if (armed_q[i]) mbar_wait(&bar[B_LQ0 + i], (uint32_t)(armed_q[i] - 1) & 1);
-            }
-            if (armed_t) mbar_wait(&bar[B_TPT], (uint32_t)(armed_t - 1) & 1);
-        }
+        if (tid == kLoadWarp * 32)
+            for (int b = 0; b <= B_TPT; ++b)
+                if (s_armed[b] >= 0) mbar_wait(&bar[b], (uint32_t)s_armed[b]);
     }
     fence_before_sync();
     __syncthreads();
@@ -954,7 +956,7 @@ SideStream *side_stream(int dev) {   // caller holds g_side_mu
 // v heads per solve pass of the prep kernel, and its instance
 int prep_pass_heads(const gdn_desc &) { return 1; }
 using PrepFn = void (*)(const PrepMaps, const Problem, int64_t, unsigned char *, int64_t);
-PrepFn prep_kernel(int) { return chunk_prep_kernel<1>; }
+PrepFn prep_kernel(int, bool imm) { return imm ? chunk_prep_kernel<1, true> : chunk_prep_kernel<1, false>; }
 
 int max_dyn_smem() {
     int dev = 0, v = 232448;
@@ -1007,7 +1009,7 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
             return cudaErrorInvalidValue;
         const int ph = prep_pass_heads(d);
         const PrepSmem ps(d.dk, ph);
-        auto prep = prep_kernel(ph);
+        auto prep = prep_kernel(ph, p.wait_immediate != 0);
         cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
         if (e != cudaSuccess) return e;
         if (nslots > 0) {
@@ -1034,7 +1036,8 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
     // second CTA never shares the SM (its allocation would wait for this one)
     const size_t smem = cs.total > (size_t)(maxs / 2 + 1024) ? cs.total : (size_t)(maxs / 2 + 1024);
     if ((int)smem > maxs) return cudaErrorInvalidValue;
-    auto chain = cs.stages == 3 ? chunk_chain_kernel<3> : chunk_chain_kernel<2>;
+    auto chain = p.wait_immediate ? (cs.stages == 3 ? chunk_chain_kernel<3, false, true> : chunk_chain_kernel<2, false, true>)
+                                  : (cs.stages == 3 ? chunk_chain_kernel<3> : chunk_chain_kernel<2>);
     cudaError_t e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int ntiles = d.dv / 64;
@@ -1068,7 +1071,7 @@ cudaError_t launch_chunk_tc_rec(const Problem &p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const int ph = prep_pass_heads(d);
     const PrepSmem ps(d.dk, ph);
-    auto prep = prep_kernel(ph);
+    auto prep = prep_kernel(ph, p.wait_immediate != 0);
     cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
     if (e != cudaSuccess) return e;
     prep<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt, (int64_t)0);
@@ -1126,14 +1129,15 @@ cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const int ph = prep_pass_heads(d);
     const PrepSmem ps(d.dk, ph);
-    auto prep = prep_kernel(ph);
+    auto prep = prep_kernel(ph, p.wait_immediate != 0);
     cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
     if (e != cudaSuccess) return e;
     const int maxs = max_dyn_smem();
     const ChainSmem cs(d.dk);
     const size_t smem = cs.total > (size_t)(maxs / 2 + 1024) ? cs.total : (size_t)(maxs / 2 + 1024);
     if ((int)smem > maxs) return cudaErrorInvalidValue;
-    auto chain = cs.stages == 3 ? chunk_chain_kernel<3> : chunk_chain_kernel<2>;
+    auto chain = p.wait_immediate ? (cs.stages == 3 ? chunk_chain_kernel<3, false, true> : chunk_chain_kernel<2, false, true>)
+                                  : (cs.stages == 3 ? chunk_chain_kernel<3> : chunk_chain_kernel<2>);
     if ((e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
         cudaSuccess)
         return e;

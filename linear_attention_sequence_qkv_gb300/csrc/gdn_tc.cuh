@@ -213,6 +213,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
+// Test of phase `parity` of `bar` (try_wait without a suspend-time hint: the
+// waiting thread returns promptly; a hint of ~1 ms made every tensor-core kernel
+// slower, the suspended waiters waking late after the phase completed).
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
