@@ -8,10 +8,16 @@
 // X_c = [K_c; Q_c] K_{c-1}^T (see gdn_chunk_tc.cu):
 //   D1^T  = H_{c-1}^T [K_c; Q_c]^T
 //         = (e^{gL_{c-1}} H_{c-2})^T [K_c; Q_c]^T + Vn'^T_{c-1} X_c^T
-//   R^T   = (V - diag(e^gam) K H_{c-1})^T diag(beta)      (K half of D1^T)
-//   D2^T  = R^T [T; P T]^T                                 (N = 128)
-//   Vn'^T = (T R)^T diag(e^{gL - gam})                     (top half of D2^T)
-//   O^T   = (Q H_{c-1})^T diag(e^gam) + (P T R)^T          (Q half of D1^T, bottom of D2^T)
+//   R~^T  = (V - diag(e^gam) K H_{c-1})^T                  (K half of D1^T)
+//   D2^T  = R~^T [T'; P']^T                                (N = 128)
+//   Vn'^T = top half of D2^T
+//   O^T   = (Q H_{c-1})^T diag(e^gam) + bottom half of D2^T  (Q half of D1^T)
+// where the prep kernel's tile already holds T' = diag(e^{gL - gam}) T diag(beta)
+// and P' = scale P T diag(beta), so the row warps apply no per-token factor but
+// e^gam. V^T reaches tensor memory through one more product, V^T I (the V tile
+// as an MN-major A operand, a 64 x 64 identity as B), into D2's top half, which is
+// free between the row warps' read of Vn'_{c-1} and the second product of chunk
+// c: the row warps read V^T and K H with one tensor-memory load.
 //   H_c^T = e^{gL_c} H_{c-1}^T + Vn'^T_c K_c
 // Each product has M = 128 dv rows and takes its A operand from tensor memory
 // (the fp16 copy of the state, R^T or Vn'^T, each written by the warps with
@@ -62,7 +68,10 @@ struct TmMaps {
 // update that reads its K last); T_PFULL p / T_PFREE p: prep slot p (X and [T; P T])
 // landed / read by the chunk's second product; T_VFULL v / T_VFREE v: V tile slot v
 // landed / read by the row warps; T_OFREE / T_OSTAGE: the output staging tile may be
-// written / holds a chunk's outputs
+// written / holds a chunk's outputs (T_VFREE is committed by the product V^T I). Products: T_C1 (D1 = [K H | Q H] done), T_C4 (the
+// state update done), T_C2 (D2 = [T R | P T R] done). Warps: T_R (R^T stored, D1's K half
+// read), T_VN (Vn'^T stored, D2's top read), T_H (the scaled state's fp16 copy stored and
+// D1's Q half read: the next chunk's first products may start), T_O (D2's bottom read).
 constexpr int kPSlots = 2, kVSlots = 2;
 enum TmBar { T_FULL0 = 0, T_FREE0 = 4, T_PFULL0 = 8, T_PFREE0 = T_PFULL0 + kPSlots, T_VFULL0 = T_PFREE0 + kPSlots,
              T_VFREE0 = T_VFULL0 + kVSlots, T_C1 = T_VFREE0 + kVSlots, T_C2, T_C4, T_R, T_VN, T_O, T_H, T_OFREE,
@@ -78,8 +87,9 @@ struct TmSmem {
     static constexpr uint32_t kPSlot = kXBytes + kTPTBytes;
     static constexpr uint32_t kV = kP + kPSlots * kPSlot;           // kVSlots V tiles (64 tokens x 128 dv)
     static constexpr uint32_t kO = kV + kVSlots * 2 * kTileBytes;   // output staging tile (64 tokens x 128 dv)
-    static constexpr uint32_t kArr = kO + 2 * kTileBytes;           // per-warp token factors
-    static constexpr uint32_t kBars = kArr + 16 * 3 * 32 * 4;
+    static constexpr uint32_t kI = kO + 2 * kTileBytes;             // 64 x 64 fp16 identity (K-major)
+    static constexpr uint32_t kArr = kI + kTileBytes;               // per-warp e^gam of the chunk's tokens
+    static constexpr uint32_t kBars = kArr + 16 * 32 * 4;
     static constexpr uint32_t kTotal = kBars + 256 + 1024;          // + barriers, + slack to align the base
 };
 
@@ -116,9 +126,8 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
     const int v0 = tile * 128;
     uint64_t *bar = (uint64_t *)(sm + L::kBars);
     uint32_t *tslot = (uint32_t *)(bar + T_COUNT);
-    // this warp's token factors: 3 x 32 floats (row warps: beta, beta e^gam, e^{gL - gam};
-    // out warps: e^gam in the first 32)
-    float *arr = (float *)(sm + L::kArr) + (warp < 16 ? warp : 0) * 3 * 32;
+    // this warp's e^gam of its half's 32 tokens of the current chunk
+    float *arr = (float *)(sm + L::kArr) + (warp < 16 ? warp : 0) * 32;
     __shared__ volatile int s_err;
     __shared__ int s_skip;
     if (tid == 0) s_skip = p.cu != nullptr && *p.status != GDN_OK;
@@ -133,7 +142,6 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
     const int64_t slot0 = (p.cu ? (int64_t)p.chunk_off[n] : (int64_t)n * ((d.T + kChunk - 1) / kChunk)) + cbase;
     const size_t sbase = ((size_t)n * Hv + j) * DK * dv;
     const float *gw = (const float *)p.gamma + (int64_t)j * p.ntok;
-    const float *bw = p.beta + (int64_t)j * p.ntok;
     auto tok0 = [&](int c) { return seq0 + (int64_t)c * kChunk; };
     auto clen = [&](int c) {
         const int64_t r = seq1 - tok0(c);
@@ -143,8 +151,7 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
     if (tid == 0) {
         s_err = 0;
         for (int i = 0; i < T_COUNT; ++i) {
-            const bool warps8 = i == T_R || i == T_VN || i == T_O || i == T_H || i == T_VFREE0 || i == T_VFREE0 + 1 ||
-                                i == T_OSTAGE;
+            const bool warps8 = i == T_R || i == T_VN || i == T_O || i == T_H || i == T_OSTAGE;
             mbar_init(&bar[i], warps8 ? 8 : 1);
         }
         mbar_init_fence();
@@ -155,7 +162,10 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
     fence_after_sync();
     const uint32_t tbase = *tslot;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    // a phase that has completed costs one barrier test; the error flag is read only
+    // when it has not
     auto wait = [&](int b, uint32_t parity) -> bool {
+        if (IMM ? mbar_test_now(&bar[b], parity) : mbar_test(&bar[b], parity)) return true;
         if (s_err) return false;
         if (!mbar_wait(&bar[b], parity, IMM)) { s_err = 1; return false; }
         return true;
@@ -181,6 +191,16 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             for (int k = 0; k < 16; ++k) h[k] = __uint_as_float(pack_h2(t[2 * k], t[2 * k + 1]));
             tmem_st16(tbase + lane_off + kTH16 + half * (HC / 2) + 16 * q, h);
         }
+    }
+    {   // the identity B operand of V^T I: element (n, k) = [n == k], 128-byte swizzled rows
+        unsigned char *idt = sm + L::kI;
+        for (int e = tid; e < kChunk * 8; e += kTmThreads) {
+            const int n = e >> 3, jc = e & 7;   // row n, 16-byte chunk jc (k = 8 jc .. 8 jc + 7)
+            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+            if ((n >> 3) == jc) (&u.x)[(n & 7) >> 1] = (n & 1) ? 0x3C000000u : 0x00003C00u;
+            *reinterpret_cast<uint4 *>(idt + n * 128 + ((jc ^ (n & 7)) << 4)) = u;
+        }
+        fence_async_smem();
     }
     fence_before_sync();
     __syncthreads();
@@ -223,14 +243,14 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                 if (c >= NS && !wait(T_FREE0 + c % NS, (uint32_t)((c / NS) - 1) & 1)) break;
                 load_kq(c);
                 tma_armed = c + 1;
-                // prep slot c % 2 once the second product of chunk c - 2 has read it
-                if (c >= kPSlots && !wait(T_PFREE0 + c % kPSlots, (uint32_t)((c / kPSlots) - 1) & 1)) break;
-                load_prep(c);
-                p_armed = c + 1;
                 // V slot c % 2 once the row warps have read chunk c - 2's V
                 if (c >= kVSlots && !wait(T_VFREE0 + c % kVSlots, (uint32_t)((c / kVSlots) - 1) & 1)) break;
                 load_v(c);
                 v_armed = c + 1;
+                // prep slot c % 2 once the second product of chunk c - 2 has read it
+                if (c >= kPSlots && !wait(T_PFREE0 + c % kPSlots, (uint32_t)((c / kPSlots) - 1) & 1)) break;
+                load_prep(c);
+                p_armed = c + 1;
             }
         }
         __syncwarp();
@@ -245,6 +265,18 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             const uint64_t dKt0 = sw128_desc(smem_u32(sm), 2 * kTileBytes, 1024); // K as MN-major B
             const uint64_t stg = L::kStage >> 4, pslot = L::kPSlot >> 4;
             const uint64_t dP0 = dK0 + (L::kP >> 4);
+            // V^T I into D2's top half: A = the V slot (dv contiguous: MN-major, two 64-wide
+            // dv blocks a tile apart), B = the identity; the V slot is free once it is done
+            const uint32_t idV = idesc_f16(128, 64, true, false);
+            const uint64_t dV0 = sw128_desc(smem_u32(sm + L::kV), kTileBytes, 1024);
+            const uint64_t dI = sw128_desc(smem_u32(sm + L::kI), 16, 1024);
+            auto cvv = [&](int sv) {
+                const uint64_t a0 = dV0 + (uint64_t)sv * ((2 * kTileBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(tbase + kTD2, a0 + (uint64_t)(128 * kk), dI + (uint64_t)(2 * kk), idV, kk != 0);
+                mma_commit(&bar[T_VFREE0 + sv]);
+            };
             // D1 = H16^T [K; Q]^T over dk ([K_b; Q_b] is a 128-row K-major tile per block)
             auto c1a = [&](int s) {
                 const uint64_t b0 = dK0 + s * stg;
@@ -268,25 +300,39 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                     mma_f16_ta(tbase + kTH, tbase + kTVN + 8 * kk, b0 + (uint64_t)(128 * kk), idH, 1);
                 mma_commit(&bar[T_FREE0 + s]);
             };
+            // the barriers each step needs are tested together (one round trip)
+            auto wait2 = [&](int b1, uint32_t p1, int b2, uint32_t p2) -> bool {
+                if (mbar_test2<IMM>(&bar[b1], p1, &bar[b2], p2)) return true;
+                return wait(b1, p1) && wait(b2, p2);
+            };
+            auto wait3 = [&](int b1, uint32_t p1, int b2, uint32_t p2, int b3, uint32_t p3) -> bool {
+                if (mbar_test3<IMM>(&bar[b1], p1, &bar[b2], p2, &bar[b3], p3)) return true;
+                return wait(b1, p1) && wait(b2, p2) && wait(b3, p3);
+            };
             int c = 0;
             for (; c < nch; ++c) {
-                const int s = c % NS, ps = c % kPSlots;
-                if (!wait(T_FULL0 + s, (uint32_t)(c / NS) & 1)) break;
-                // H16 = e^{gL_{c-1}} H_{c-2}; D1 of chunk c-1 read by the out warps
-                if (c >= 1 && (!wait(T_H, (uint32_t)(c - 1) & 1) || !wait(T_O, (uint32_t)(c - 1) & 1))) break;
+                const int s = c % NS, ps = c % kPSlots, sv = c % kVSlots;
+                const uint32_t fs = (uint32_t)(c / NS) & 1, fp = (uint32_t)(c / kPSlots) & 1,
+                               fv = (uint32_t)(c / kVSlots) & 1, f1 = (uint32_t)(c - 1) & 1;
+                // the stage, the prep slot and (c >= 1) H16 = e^{gL_{c-1}} H_{c-2} with D1's Q
+                // half of chunk c-1 read by the out warps (its K half was read before R_{c-1}):
+                // D1 may be overwritten while the second product of chunk c-1 still runs
+                if (c >= 1 ? !wait3(T_FULL0 + s, fs, T_PFULL0 + ps, fp, T_H, f1)
+                           : !wait2(T_FULL0 + s, fs, T_PFULL0 + ps, fp))
+                    break;
                 fence_after_sync();
                 c1a(s);
-                if (!wait(T_PFULL0 + ps, (uint32_t)(c / kPSlots) & 1)) break;
-                if (c >= 1) {
-                    if (!wait(T_VN, (uint32_t)(c - 1) & 1)) break;     // Vn'_{c-1}
-                    fence_after_sync();
-                    c1b(ps);
-                }
+                // Vn'_{c-1} (D2's top half read) and the V tile of chunk c
+                if (c >= 1 ? !wait2(T_VN, f1, T_VFULL0 + sv, fv) : !wait(T_VFULL0 + sv, fv)) break;
+                fence_after_sync();
+                if (c >= 1) c1b(ps);
+                cvv(sv);   // V^T of chunk c into D2's top half
                 mma_commit(&bar[T_C1]);
                 if (c >= 1) c4((c - 1) % NS);
                 // C4 of chunk c-1 (for c = 0: the first product, which read H16 = H_init)
                 mma_commit(&bar[T_C4]);
-                if (!wait(T_R, (uint32_t)c & 1)) break;
+                // R_c, and D2 of chunk c-1 read by the out warps
+                if (c >= 1 ? !wait2(T_R, (uint32_t)c & 1, T_O, f1) : !wait(T_R, (uint32_t)c & 1)) break;
                 fence_after_sync();
                 const uint64_t bt = dP0 + ps * pslot + (kXBytes >> 4);
 #pragma unroll
@@ -306,77 +352,58 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
         __syncwarp();
     } else if (warp < kRowW) {
         // ------------------------------------------------------------ row warps
-        // lane l loads the decay and beta of token 32 half + l two chunks ahead (one chunk
-        // is shorter than a DRAM round trip); V comes through the TMA ring
-        struct RowIn {
-            float g, b, gl;
-        };
-        RowIn A, B;
-        auto prefetch = [&](int c, RowIn &x) {
+        // lane l loads the decay of token 32 half + l two chunks ahead (one chunk is
+        // shorter than a DRAM round trip). beta and e^{gam_L - gam} are folded into
+        // the prep tile and V^T is in D2's top half, so R~ = V - e^gam (K H) and the
+        // tile's product is Vn' itself.
+        float A = 0.f, B = 0.f;
+        auto prefetch = [&](int c, float &x) {
             const int64_t t0 = tok0(c);
             const int len = clen(c);
             const int i = 32 * half + lane;
-            x.g = gw[t0 + (i < len ? i : len - 1)];
-            x.b = i < len ? bw[t0 + i] : 0.f;
-            x.gl = gw[t0 + len - 1];
+            x = gw[t0 + (i < len ? i : len - 1)];
         };
-        // element (token 32 half + i, this thread's dv row) of a swizzled V slot sits at
-        // vbase + 128 i + (vchunk ^ 16 (i % 8)): the 16-byte chunk of column vrow % 64
-        // XORed with the row (32 half is a multiple of 8)
-        const uint32_t vcol = (uint32_t)(vrow & 63);
-        const uint32_t vbase = (uint32_t)(vrow >> 6) * kTileBytes + (uint32_t)(32 * half) * 128 + (vcol & 7) * 2;
-        const uint32_t vchunk = (vcol >> 3) << 4;
         const float4 *a4 = reinterpret_cast<const float4 *>(arr);
+        // a chunk's e^gam, one per lane, published to the warp's array
+        auto publish = [&](float g) {
+            __syncwarp();                 // the previous chunk's reads of the array are done
+            arr[lane] = __expf(g);
+            __syncwarp();
+        };
         if (nch > 0) prefetch(0, A);
         if (nch > 1) prefetch(1, B);
+        if (nch > 0) publish(A);
         for (int c = 0; c < nch; ++c) {
-            const int len = clen(c);
-            // this chunk's factors, one per lane, published to the warp's array
-            __syncwarp();                 // the previous chunk's reads of the array are done
-            arr[lane] = A.b;
-            arr[32 + lane] = A.b * __expf(A.g);
-            arr[64 + lane] = __expf(A.gl - A.g);
-            __syncwarp();
-            if (!wait(T_VFULL0 + c % kVSlots, (uint32_t)(c / kVSlots) & 1)) break;
-            const unsigned char *vs = sm + L::kV + (c % kVSlots) * 2 * kTileBytes + vbase;
-            float vv[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                vv[i] = 32 * half + i < len
-                            ? __half2float(*reinterpret_cast<const __half *>(vs + 128 * i + (vchunk ^ (16u * (i & 7)))))
-                            : 0.f;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[T_VFREE0 + c % kVSlots]);
-            // R^T = beta V - beta e^gam (K H) for this half's 32 tokens
+            // R~^T = V - e^gam (K H) for this half's 32 tokens (tokens past the sequence's
+            // end hold other rows' values: beta = 0 in the tile removes them)
             if (!wait(T_C1, (uint32_t)c & 1)) break;
             fence_after_sync();
-            float a[32];
-            tmem_ld32(tbase + lane_off + kTD1 + 32 * half, a);
+            float a[32], v[32];
+            tmem_ld32x2(tbase + lane_off + kTD1 + 32 * half, tbase + lane_off + kTD2 + 32 * half, a, v);
             float r[16];
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-                const float4 b4 = a4[m], e4 = a4[8 + m];
-                r[2 * m] = __uint_as_float(pack_h2(b4.x * vv[4 * m] - e4.x * a[4 * m],
-                                                   b4.y * vv[4 * m + 1] - e4.y * a[4 * m + 1]));
-                r[2 * m + 1] = __uint_as_float(pack_h2(b4.z * vv[4 * m + 2] - e4.z * a[4 * m + 2],
-                                                       b4.w * vv[4 * m + 3] - e4.w * a[4 * m + 3]));
+                const float4 e4 = a4[m];
+                const float2 x0 = fma2(make_float2(-e4.x, -e4.y), make_float2(a[4 * m], a[4 * m + 1]),
+                                       make_float2(v[4 * m], v[4 * m + 1]));
+                const float2 x1 = fma2(make_float2(-e4.z, -e4.w), make_float2(a[4 * m + 2], a[4 * m + 3]),
+                                       make_float2(v[4 * m + 2], v[4 * m + 3]));
+                r[2 * m] = __uint_as_float(pack_h2(x0.x, x0.y));
+                r[2 * m + 1] = __uint_as_float(pack_h2(x1.x, x1.y));
             }
             tmem_st16(tbase + lane_off + kTR + 16 * half, r);
             warp_arrive(T_R);
-            // Vn'^T = e^{gL - gam} (T R)^T
+            // Vn'^T: the top half of D2, to fp16
             if (!wait(T_C2, (uint32_t)c & 1)) break;
             fence_after_sync();
             tmem_ld32(tbase + lane_off + kTD2 + 32 * half, a);
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const float4 s4 = a4[16 + m];
-                r[2 * m] = __uint_as_float(pack_h2(s4.x * a[4 * m], s4.y * a[4 * m + 1]));
-                r[2 * m + 1] = __uint_as_float(pack_h2(s4.z * a[4 * m + 2], s4.w * a[4 * m + 3]));
-            }
+            for (int m = 0; m < 16; ++m) r[m] = __uint_as_float(pack_h2(a[2 * m], a[2 * m + 1]));
             tmem_st16(tbase + lane_off + kTVN + 16 * half, r);
             warp_arrive(T_VN);
             A = B;                                   // chunk c + 1 (loaded a chunk ago)
             if (c + 2 < nch) prefetch(c + 2, B);
+            if (c + 1 < nch) publish(A);
         }
     } else if (out_warp) {
         // ------------------------------------------------ state and output warps
@@ -398,13 +425,9 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             g_tok = gw[t0 + (i < len ? i : len - 1)];
             g_last = gw[t0 + len - 1];
         };
-        // one thread issues the output tile's tensor stores; staging-tile offsets as for V
+        // one thread issues the output tile's tensor stores
         const bool storer = warp == kRowW && lane == 0;
-        const uint32_t ocol = (uint32_t)(vrow & 63);
-        const uint32_t obase = (uint32_t)(vrow >> 6) * kTileBytes + (uint32_t)(32 * half) * 128 + (ocol & 7) * 2;
-        const uint32_t ochunk = (ocol >> 3) << 4;
         int nstored = 0;
-        const float4 *a4 = reinterpret_cast<const float4 *>(arr);
         // two chunks ahead: chunk c's values move into place at the end of iteration c - 1,
         // one iteration after their loads were issued, so no move waits on a load in flight
         float g_tok = 0.f, g_last = 0.f, g_tok_n = 0.f, g_last_n = 0.f;
@@ -432,23 +455,38 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                     }
                 }
             }
+            // D1's Q half, Q H_{c-1} for this half's tokens (complete: C4 follows the first
+            // products of chunk c); once read, the next chunk's first products may overwrite D1.
+            // Read in the 16x256b layout (lanes g = lane / 4 and g + 8 of each 16-lane half,
+            // token pairs 8i + tq, 8i + tq + 1), whose pairs stmatrix stores transposed.
+            const uint32_t lq = tbase + ((uint32_t)(quad * 32) << 16);
+            const uint32_t cq = (uint32_t)(64 + 32 * half);
+            float qa[16], qb[16];   // lanes [0, 16) and [16, 32) of the warp's quarter
+            tmem_ld16x256_x4x2(lq + kTD1 + cq, lq + (16u << 16) + kTD1 + cq, qa, qb);
             warp_arrive(T_H);
             __syncwarp();                 // the previous chunk's reads of the array are done
-            arr[lane] = __expf(g_tok);
+            arr[lane] = d.scale * __expf(g_tok);   // P' carries the scale already
             __syncwarp();
-            // O^T = e^gam (Q H)^T + (P T R)^T for this half's 32 tokens
+            // O^T = scale e^gam (Q H)^T + bottom half of D2^T for this half's 32 tokens
             if (!wait(T_C2, (uint32_t)c & 1)) break;
             fence_after_sync();
-            float a[32], b[32];
-            tmem_ld32x2(tbase + lane_off + kTD1 + 64 + 32 * half, tbase + lane_off + kTD2 + 64 + 32 * half, a, b);
+            float pa[16], pb[16];
+            tmem_ld16x256_x4x2(lq + kTD2 + cq, lq + (16u << 16) + kTD2 + cq, pa, pb);
             warp_arrive(T_O);
+            const int tq = 2 * (lane & 3), g8 = lane >> 2;
+            // h[4i + m]: matrix m of token group i (m = 2 lane-half + (lane g or g + 8))
+            uint32_t h[16];
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const float4 e4 = a4[m];
-                a[4 * m] = fmaf(e4.x, a[4 * m], b[4 * m]) * d.scale;
-                a[4 * m + 1] = fmaf(e4.y, a[4 * m + 1], b[4 * m + 1]) * d.scale;
-                a[4 * m + 2] = fmaf(e4.z, a[4 * m + 2], b[4 * m + 2]) * d.scale;
-                a[4 * m + 3] = fmaf(e4.w, a[4 * m + 3], b[4 * m + 3]) * d.scale;
+            for (int i = 0; i < 4; ++i) {
+                const float2 e = *reinterpret_cast<const float2 *>(arr + 8 * i + tq);
+                const float2 x0 = fma2(e, make_float2(qa[4 * i], qa[4 * i + 1]), make_float2(pa[4 * i], pa[4 * i + 1]));
+                const float2 x1 = fma2(e, make_float2(qa[4 * i + 2], qa[4 * i + 3]), make_float2(pa[4 * i + 2], pa[4 * i + 3]));
+                const float2 y0 = fma2(e, make_float2(qb[4 * i], qb[4 * i + 1]), make_float2(pb[4 * i], pb[4 * i + 1]));
+                const float2 y1 = fma2(e, make_float2(qb[4 * i + 2], qb[4 * i + 3]), make_float2(pb[4 * i + 2], pb[4 * i + 3]));
+                h[4 * i] = pack_h2(x0.x, x0.y);
+                h[4 * i + 1] = pack_h2(x1.x, x1.y);
+                h[4 * i + 2] = pack_h2(y0.x, y0.y);
+                h[4 * i + 3] = pack_h2(y1.x, y1.y);
             }
             const int64_t t0 = tok0(c);
             const int len = clen(c);
@@ -459,10 +497,16 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                     mbar_arrive(&bar[T_OFREE]);
                 }
                 if (!wait(T_OFREE, (uint32_t)nstored & 1)) break;
-                unsigned char *ob = sm + L::kO + obase;
+                // this thread addresses row lane % 8 (a token) of stored matrix m = lane / 8:
+                // 8 dv columns from 32 quad + 16 (m / 2) + 8 (m % 2)
+                const int m = lane >> 3, rr = lane & 7;
+                const int dvl = 32 * quad + 16 * (m >> 1) + 8 * (m & 1);
+                const uint32_t obox = smem_u32(sm + L::kO) + (uint32_t)(dvl >> 6) * kTileBytes;
+                const uint32_t ochk = (uint32_t)(((dvl & 63) >> 3) ^ rr) << 4;
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    *reinterpret_cast<__half *>(ob + 128 * k + (ochunk ^ (16u * (k & 7)))) = __float2half_rn(a[k]);
+                for (int i = 0; i < 4; ++i)
+                    stmatrix_x4_trans(obox + (uint32_t)(32 * half + 8 * i + rr) * 128 + ochk, h[4 * i], h[4 * i + 1],
+                                      h[4 * i + 2], h[4 * i + 3]);
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[T_OSTAGE]);
@@ -475,10 +519,19 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                 ++nstored;
             } else {
                 // the last, partial chunk of a sequence: the tile's other rows belong to the next
-                __half *dst = o + (t0 + 32 * half) * (int64_t)Hv * dv + (int64_t)j * dv + v0 + vrow;
+                __half *dst = o + (int64_t)j * dv + v0 + 32 * quad + g8;
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (32 * half + k < len) dst[(int64_t)k * Hv * dv] = __float2half_rn(a[k]);
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int mm = 0; mm < 4; ++mm) {
+                        const __half2 hv = *reinterpret_cast<const __half2 *>(&h[4 * i + mm]);
+                        const int dvo = 16 * (mm >> 1) + 8 * (mm & 1);
+#pragma unroll
+                        for (int e2 = 0; e2 < 2; ++e2) {
+                            const int tok = 32 * half + 8 * i + tq + e2;
+                            if (tok < len) dst[(t0 + tok) * (int64_t)Hv * dv + dvo] = e2 ? __high2half(hv) : __low2half(hv);
+                        }
+                    }
             }
             g_tok = g_tok_n;
             g_last = g_last_n;

@@ -15,7 +15,11 @@
 //    needs for nearly orthogonal q, k), decay masks, the 64x64 unit-triangular
 //    solve on CUDA cores in fp32, then P T on the tensor cores. Writes the
 //    [T; P T] tile (128 x 64 fp16, 16 KB) already in the 128-byte-swizzled
-//    layout, so the chain kernel fetches it with one bulk copy.
+//    layout, so the chain kernel fetches it with one bulk copy. For the
+//    transposed chain (gdn_chain_tm.cu) the per-token factors of the row
+//    updates and the output scale are folded into the tile instead:
+//    [diag(e^{gam_L - gam}) T diag(beta); scale P T diag(beta)], whose product
+//    with V - diag(e^gam) K H is [Vn'; scale P Vn].
 //  * chain (one CTA of 8 warps per sequence, v head and 64-column dv tile): the
 //    state slice H [dk][64] stays in registers in fp32 across chunks (warps w
 //    and w+4 read the same tensor-memory lanes and split the columns; an fp16
@@ -149,8 +153,9 @@ struct PrepSmem {
 };
 
 // IMM: the test mode of the waits (gdn_set_wait_test_mode), a separate instance so
-// that the normal one carries nothing of it
-template <int PH, bool IMM>
+// that the normal one carries nothing of it. FOLD: the tile with beta and
+// e^{gam_L - gam} folded in, for the transposed chain.
+template <int PH, bool IMM, bool FOLD>
 __global__ void __launch_bounds__(kPrepThreads, PH == 1 ? 3 : 2) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
                                                                      const Problem p, int64_t nslots,
                                                                      unsigned char *tpt, int64_t slot_base) {
@@ -413,6 +418,18 @@ __global__ void __launch_bounds__(kPrepThreads, PH == 1 ? 3 : 2) chunk_prep_kern
             if (row >= kChunk) {   // P T replaces P in rows 64..127
                 float v[32];
                 tmem_ld32(lane_addr + 64, v);
+                if (FOLD) {        // P' = scale P T diag(beta)
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] *= d.scale * bet[h * kChunk + c0 + q];
+                }
+                store_half_row_f16(tp, row, c0, v);
+            } else if (FOLD) {     // diag(e^{gam_L - gam}) T diag(beta) in rows 0..63 (P T has read T)
+                // gam is clamped to the chunk's last token, so gam[63] is gam_L
+                const float er = __expf(gam[h * kChunk + kChunk - 1] - gam[h * kChunk + row]);
+                const float *Th = Ts + h * kChunk * LDA + row * LDA + c0;
+                float v[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = er * Th[q] * bet[h * kChunk + c0 + q];
                 store_half_row_f16(tp, row, c0, v);
             }
             fence_before_sync();
@@ -956,7 +973,10 @@ SideStream *side_stream(int dev) {   // caller holds g_side_mu
 // v heads per solve pass of the prep kernel, and its instance
 int prep_pass_heads(const gdn_desc &) { return 1; }
 using PrepFn = void (*)(const PrepMaps, const Problem, int64_t, unsigned char *, int64_t);
-PrepFn prep_kernel(int, bool imm) { return imm ? chunk_prep_kernel<1, true> : chunk_prep_kernel<1, false>; }
+PrepFn prep_kernel(int, bool imm, bool fold) {
+    return fold ? (imm ? chunk_prep_kernel<1, true, true> : chunk_prep_kernel<1, false, true>)
+                : (imm ? chunk_prep_kernel<1, true, false> : chunk_prep_kernel<1, false, false>);
+}
 
 int max_dyn_smem() {
     int dev = 0, v = 232448;
@@ -1009,7 +1029,7 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
             return cudaErrorInvalidValue;
         const int ph = prep_pass_heads(d);
         const PrepSmem ps(d.dk, ph);
-        auto prep = prep_kernel(ph, p.wait_immediate != 0);
+        auto prep = prep_kernel(ph, p.wait_immediate != 0, chain_tm_supports(d));
         cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
         if (e != cudaSuccess) return e;
         if (nslots > 0) {
@@ -1071,7 +1091,7 @@ cudaError_t launch_chunk_tc_rec(const Problem &p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const int ph = prep_pass_heads(d);
     const PrepSmem ps(d.dk, ph);
-    auto prep = prep_kernel(ph, p.wait_immediate != 0);
+    auto prep = prep_kernel(ph, p.wait_immediate != 0, false);   // the 64-column chain's tile
     cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
     if (e != cudaSuccess) return e;
     prep<<<dim3((unsigned)nslots, d.Hk), kPrepThreads, ps.total, s>>>(pm, p, nslots_alloc, tpt, (int64_t)0);
@@ -1129,7 +1149,7 @@ cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const int ph = prep_pass_heads(d);
     const PrepSmem ps(d.dk, ph);
-    auto prep = prep_kernel(ph, p.wait_immediate != 0);
+    auto prep = prep_kernel(ph, p.wait_immediate != 0, chain_tm_supports(d));
     cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
     if (e != cudaSuccess) return e;
     const int maxs = max_dyn_smem();

@@ -173,6 +173,35 @@ __device__ __forceinline__ void tmem_st32x2(uint32_t ta, uint32_t tb, const floa
         :: "r"(ta), "r"(tb), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63]) : "memory");
 }
 
+// Two loads of shape 16x256b with 4 repetitions (32 columns) and one wait: thread
+// t receives, per repetition i (columns 8i .. 8i + 7 from the address), the
+// columns 8i + 2 (t % 4) and 8i + 2 (t % 4) + 1 of lanes t / 4 and t / 4 + 8
+// (relative to the address's lane): v[4i + 0, 1] from lane t / 4, v[4i + 2, 3]
+// from lane t / 4 + 8.
+__device__ __forceinline__ void tmem_ld16x256_x4x2(uint32_t ta, uint32_t tb, float *va, float *vb) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb) : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[16 + i]);
+    }
+}
+
+// Four 8x8 matrices of 16-bit elements to shared memory, transposed: thread t
+// holds in r[m] the elements (t / 4, 2 (t % 4)) and (t / 4, 2 (t % 4) + 1) of
+// matrix m (low half first) and gives the address of row t % 8 of the stored
+// matrix t / 8, i.e. of column t % 8 of matrix t / 8 (16 bytes, 16-byte aligned).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
+                 :: "r"(saddr), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem], issued by one thread.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                         uint32_t idesc, uint32_t accumulate) {
@@ -241,6 +270,50 @@ __device__ __forceinline__ bool mbar_test_now(uint64_t *bar, uint32_t parity) {
 // Wait for phase `parity` of `bar`, giving up after ~1 s. Returns false on timeout.
 // immediate (tests of the timeout path only): give up at once unless the phase is
 // already complete.
+// Tests of two or three barriers at once (the tests are independent, so their
+// round trips overlap): true when every phase has completed. IMM uses the
+// non-blocking test.
+template <bool IMM>
+__device__ __forceinline__ bool mbar_test2(uint64_t *b1, uint32_t p1, uint64_t *b2, uint32_t p2) {
+    uint32_t ok;
+    if (IMM)
+        asm volatile(
+            "{\n\t.reg .pred q1, q2;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
+            "and.pred q1, q1, q2;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
+            : "=r"(ok) : "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2) : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred q1, q2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
+            "and.pred q1, q1, q2;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
+            : "=r"(ok) : "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2) : "memory");
+    return ok != 0;
+}
+template <bool IMM>
+__device__ __forceinline__ bool mbar_test3(uint64_t *b1, uint32_t p1, uint64_t *b2, uint32_t p2, uint64_t *b3,
+                                           uint32_t p3) {
+    uint32_t ok;
+    if (IMM)
+        asm volatile(
+            "{\n\t.reg .pred q1, q2, q3;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 q3, [%5], %6;\n\t"
+            "and.pred q1, q1, q2;\n\tand.pred q1, q1, q3;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
+            : "=r"(ok) : "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2), "r"(smem_u32(b3)), "r"(p3) : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred q1, q2, q3;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 q3, [%5], %6;\n\t"
+            "and.pred q1, q1, q2;\n\tand.pred q1, q1, q3;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
+            : "=r"(ok) : "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2), "r"(smem_u32(b3)), "r"(p3) : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, bool immediate = false) {
     if (immediate) return mbar_test_now(bar, parity);
     if (mbar_test(bar, parity)) return true;
