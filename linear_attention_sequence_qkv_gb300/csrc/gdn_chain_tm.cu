@@ -438,22 +438,29 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             // scale by e^{gL_c} for chunk c's update and publish its fp16 copy for chunk c+1
             if (!wait(T_C4, (uint32_t)c & 1)) break;
             fence_after_sync();
-            {
-                const float e = __expf(g_last);
+            {   // on the path to the next chunk's first products: the stores go out without
+                // waiting one by one, one wait at the end
+                const float el = __expf(g_last);
+                const float2 e2 = make_float2(el, el);
 #pragma unroll
                 for (int q = 0; q < HC / 32; ++q) {
                     float t[32];
                     tmem_ld32(tbase + lane_off + kTH + half * HC + 32 * q, t);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) t[k] *= e;
-                    tmem_st32(tbase + lane_off + kTH + half * HC + 32 * q, t);
+                    for (int k = 0; k < 16; ++k) {
+                        const float2 x = mul2(make_float2(t[2 * k], t[2 * k + 1]), e2);
+                        t[2 * k] = x.x;
+                        t[2 * k + 1] = x.y;
+                    }
+                    tmem_st32_nw(tbase + lane_off + kTH + half * HC + 32 * q, t);
                     if (c + 1 < nch) {
                         float h[16];
 #pragma unroll
                         for (int k = 0; k < 16; ++k) h[k] = __uint_as_float(pack_h2(t[2 * k], t[2 * k + 1]));
-                        tmem_st16(tbase + lane_off + kTH16 + half * (HC / 2) + 16 * q, h);
+                        tmem_st16_nw(tbase + lane_off + kTH16 + half * (HC / 2) + 16 * q, h);
                     }
                 }
+                tmem_wait_st();
             }
             // D1's Q half, Q H_{c-1} for this half's tokens (complete: C4 follows the first
             // products of chunk c); once read, the next chunk's first products may overwrite D1.
