@@ -144,7 +144,8 @@ struct PrepSmem {
         const size_t solve_end = Ws + (size_t)ph * 32 * 33 * 4;
         if (solve_end > o) o = solve_end;
         o = (o + 1023) & ~(size_t)1023;
-        tp = o; o += kTPTBytes;
+        // the [T; P] tile over A's scratch (A is dead once T21 is formed; T stays)
+        tp = 0;
         gam = o; o += ph * kChunk * 4;
         bet = o; o += ph * kChunk * 4;
         bars = o; o += 64;
@@ -154,9 +155,12 @@ struct PrepSmem {
 
 // IMM: the test mode of the waits (gdn_set_wait_test_mode), a separate instance so
 // that the normal one carries nothing of it. FOLD: the tile with beta and
-// e^{gam_L - gam} folded in, for the transposed chain.
-template <int PH, bool IMM, bool FOLD>
-__global__ void __launch_bounds__(kPrepThreads, PH == 1 ? 3 : 2) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
+// e^{gam_L - gam} folded in, for the transposed chain. MINB: CTAs per SM the
+// registers allow: four (64 registers) when the prep has the GPU to itself, three
+// (80 registers, fewer spills) beside a chain segment, where four CTAs slowed the
+// chain through the memory system more than they sped the prep.
+template <int PH, bool IMM, bool FOLD, int MINB>
+__global__ void __launch_bounds__(kPrepThreads, MINB) chunk_prep_kernel(const __grid_constant__ PrepMaps maps,
                                                                      const Problem p, int64_t nslots,
                                                                      unsigned char *tpt, int64_t slot_base) {
     extern __shared__ unsigned char smraw[];
@@ -973,9 +977,14 @@ SideStream *side_stream(int dev) {   // caller holds g_side_mu
 // v heads per solve pass of the prep kernel, and its instance
 int prep_pass_heads(const gdn_desc &) { return 1; }
 using PrepFn = void (*)(const PrepMaps, const Problem, int64_t, unsigned char *, int64_t);
-PrepFn prep_kernel(int, bool imm, bool fold) {
-    return fold ? (imm ? chunk_prep_kernel<1, true, true> : chunk_prep_kernel<1, false, true>)
-                : (imm ? chunk_prep_kernel<1, true, false> : chunk_prep_kernel<1, false, false>);
+template <int MINB>
+PrepFn prep_instance(bool imm, bool fold) {
+    return fold ? (imm ? chunk_prep_kernel<1, true, true, MINB> : chunk_prep_kernel<1, false, true, MINB>)
+                : (imm ? chunk_prep_kernel<1, true, false, MINB> : chunk_prep_kernel<1, false, false, MINB>);
+}
+// three_per_sm: beside a chain segment, or a grid that fits one round of three
+PrepFn prep_kernel(int, bool imm, bool fold, bool three_per_sm = false) {
+    return three_per_sm ? prep_instance<3>(imm, fold) : prep_instance<4>(imm, fold);
 }
 
 int max_dyn_smem() {
@@ -1029,7 +1038,13 @@ cudaError_t launch_chunk_tc(const Problem &p, cudaStream_t s) {
             return cudaErrorInvalidValue;
         const int ph = prep_pass_heads(d);
         const PrepSmem ps(d.dk, ph);
-        auto prep = prep_kernel(ph, p.wait_immediate != 0, chain_tm_supports(d));
+        // a grid that fits in one round of three CTAs per SM takes the 80-register instance
+        int dev = 0, nsm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            nsm = 0;
+        const bool one_round = nslots * d.Hk <= 3 * (int64_t)nsm;
+        auto prep = prep_kernel(ph, p.wait_immediate != 0, chain_tm_supports(d), one_round);
         cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
         if (e != cudaSuccess) return e;
         if (nslots > 0) {
@@ -1149,7 +1164,7 @@ cudaError_t launch_chunk_tc_segmented(const Problem &p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const int ph = prep_pass_heads(d);
     const PrepSmem ps(d.dk, ph);
-    auto prep = prep_kernel(ph, p.wait_immediate != 0, chain_tm_supports(d));
+    auto prep = prep_kernel(ph, p.wait_immediate != 0, chain_tm_supports(d), true);
     cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps.total);
     if (e != cudaSuccess) return e;
     const int maxs = max_dyn_smem();
