@@ -589,6 +589,18 @@ def chunk_launch_count(gdn, d, w, inp, nsm):
     return 2
 
 
+def fused_output_step(gdn, d, w, inp, nsm):
+    """Whether gdn_forward applies the output step inside the transposed chain (dv = 128,
+    a 16-byte-aligned gate view, not the segmented schedule): then it launches no
+    separate output kernel."""
+    if gdn.gdn_chunk_kernel_kind(d) != 1 or w.dtype == "fp32" or w.dk not in (64, 128) or w.dv != 128:
+        return False
+    if chunk_launch_count(gdn, d, w, inp, nsm) != 2:
+        return False
+    g = inp.gate
+    return g.data_ptr() % 16 == 0 and (g.stride(1) * g.element_size()) % 16 == 0
+
+
 def measure_workload(w, steps, warmup, dev, world, barrier, gpu_id, with_clocks, torch, gdn, make_inputs_device):
     """Time one workload: ``steps`` gdn_forward calls (CUDA events around each,
     L2 flushed before each), then the same count as the three stage calls with
@@ -686,8 +698,10 @@ def measure_workload(w, steps, warmup, dev, world, barrier, gpu_id, with_clocks,
         kernels[name] = roofline_entry(name, alg[name][0], alg[name][1], ms, pk, w.dtype)
         kernels[name]["ms_median"] = statistics.median(per[name])
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
-    launches = 1 + (1 if inp.cu_seqlens is not None else 0) + chunk_launch_count(gdn, d, w, inp, nsm) + 1
-    res = {"ms_per_step": ms_mean, "ms_per_step_median": ms_median,
+    fused = fused_output_step(gdn, d, w, inp, nsm)
+    launches = (1 + (1 if inp.cu_seqlens is not None else 0) + chunk_launch_count(gdn, d, w, inp, nsm) +
+                (0 if fused else 1))
+    res = {"ms_per_step": ms_mean, "ms_per_step_median": ms_median, "fused_output_step": fused,
            "value": ntok * world / (ms_mean / 1e3), "tokens_per_step": ntok,
            "staged_ms_per_step": sum(per["staged"]) / len(per["staged"]), "kernels": kernels,
            "gpu_launches_per_step": launches, "steps": steps, "warmup": warmup, "clocks": clocks,
@@ -913,7 +927,9 @@ def main():
                    "timing": "value: one gdn_forward per step, CUDA events around the call, mean over the "
                              "steps (ms_per_step_median beside it); kernels: the same work as gdn_prologue / "
                              "gdn_chunk_rule / gdn_epilogue with events between them, a second pass of the "
-                             "same step count",
+                             "same step count (where a workload's fused_output_step is true, gdn_forward runs the "
+                             "output step inside the chunk kernel instead of the separate output kernel the "
+                             "stage calls time)",
                    "staged_ms_per_step": res["staged_ms_per_step"]},
         "roofline": roof,
         "kernels": kernels,

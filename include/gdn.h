@@ -157,7 +157,13 @@ int gdn_forward(const gdn_desc *d,
                 void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /* The three stages of gdn_forward, callable one by one on the same workspace
- * (gdn_forward is exactly prologue, chunk_rule, epilogue in this order).
+ * (gdn_forward gives bit for bit the results of prologue, chunk_rule, epilogue in
+ * this order). Where the transposed tensor-core chunk kernel holds a whole v-head
+ * row (16-bit activations, dk 64 or 128, dv = 128), the gate and norm_w match the
+ * activation dtype (norm_w may be fp32), the gate view has a 16-byte aligned base
+ * and row pitch with its batch rows back to back, and the chunk stage is not cut
+ * into segments (one long sequence), gdn_forward applies step 5 inside that kernel,
+ * with the same arithmetic, and leaves o in the workspace unwritten.
  * gdn_prologue: steps 1-3 plus the in-chunk cumulative decay -> workspace q, k,
  *   v, beta, gamma (and the chunk table / status word when cu_seqlens is set).
  * gdn_chunk_rule: step 4 -> workspace o, final_state.

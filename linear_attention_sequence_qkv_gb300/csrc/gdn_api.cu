@@ -98,7 +98,7 @@ int run_chunk(const Problem &p, cudaStream_t s) {
 }
 
 int run_epilogue(const Problem &p, cudaStream_t s) {
-    if (p.ntok == 0) return GDN_OK;
+    if (p.ntok == 0 || p.fuse_epilogue) return GDN_OK;
     return cuda_status(gdn::launch_epilogue(p, s));
 }
 
@@ -254,6 +254,7 @@ int forward_impl(const gdn_desc *d, const void *q_raw, const void *k_raw, const 
     // plain tensor-core chunk stage): each later kernel is a programmatic
     // dependent of the one before it
     p.pdl = !single_stream && p.ntok > 0 && gdn::chunk_tc_supports(*d) && !gdn::chunk_tc_segmented(p);
+    p.fuse_epilogue = gdn::chain_tm_fuses_epilogue(p);
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_prologue(p, s)) != GDN_OK) return rc;
     if ((rc = run_chunk(p, s)) != GDN_OK) return rc;

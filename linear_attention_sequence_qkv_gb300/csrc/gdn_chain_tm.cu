@@ -62,6 +62,7 @@ constexpr uint32_t kTVN = 480;   // Vn'^T fp16, 32 columns
 
 struct TmMaps {
     CUtensorMap q_hi, k_hi, v, o;
+    CUtensorMap gate, out;   // the fused output step only
 };
 
 // T_FULL s / T_FREE s: operand stage s ([K; Q]) landed / free again (after the state
@@ -75,19 +76,22 @@ struct TmMaps {
 constexpr int kPSlots = 2, kVSlots = 2;
 enum TmBar { T_FULL0 = 0, T_FREE0 = 4, T_PFULL0 = 8, T_PFREE0 = T_PFULL0 + kPSlots, T_VFULL0 = T_PFREE0 + kPSlots,
              T_VFREE0 = T_VFULL0 + kVSlots, T_C1 = T_VFREE0 + kVSlots, T_C2, T_C4, T_R, T_VN, T_O, T_H, T_OFREE,
-             T_OSTAGE, T_DRAIN, T_COUNT };
+             T_OSTAGE, T_GFULL, T_GFREE, T_OFULL, T_DRAIN, T_COUNT };
 static_assert(T_FREE0 >= T_FULL0 + 4 && T_PFULL0 >= T_FREE0 + 4, "barrier ranges overlap");
 
-template <int DK>
+// EPI (the output step fused): one V slot, and a gate tile in the second one's place
+template <int DK, bool EPI>
 struct TmSmem {
     static constexpr int kStages = DK == 128 ? 3 : 4;
+    static constexpr int kVS = EPI ? 1 : kVSlots;
     static constexpr uint32_t kBlocks = DK / 64;
     static constexpr uint32_t kStage = kBlocks * 2 * kTileBytes;   // [K_b; Q_b] for each 64-column dk block
     static constexpr uint32_t kP = kStages * kStage;                // kPSlots x (X, [T; P T])
     static constexpr uint32_t kPSlot = kXBytes + kTPTBytes;
-    static constexpr uint32_t kV = kP + kPSlots * kPSlot;           // kVSlots V tiles (64 tokens x 128 dv)
-    static constexpr uint32_t kO = kV + kVSlots * 2 * kTileBytes;   // output staging tile (64 tokens x 128 dv)
-    static constexpr uint32_t kI = kO + 2 * kTileBytes;             // 64 x 64 fp16 identity (K-major)
+    static constexpr uint32_t kV = kP + kPSlots * kPSlot;           // kVS V tiles (64 tokens x 128 dv)
+    static constexpr uint32_t kO = kV + kVS * 2 * kTileBytes;       // output staging tile (64 tokens x 128 dv)
+    static constexpr uint32_t kG = kO + 2 * kTileBytes;             // gate tile (64 tokens x 128 dv), EPI only
+    static constexpr uint32_t kI = kG + (EPI ? 2 * kTileBytes : 0); // 64 x 64 fp16 identity (K-major)
     static constexpr uint32_t kArr = kI + kTileBytes;               // per-warp e^gam of the chunk's tokens
     static constexpr uint32_t kBars = kArr + 16 * 32 * 4;
     static constexpr uint32_t kTotal = kBars + 256 + 1024;          // + barriers, + slack to align the base
@@ -99,12 +103,13 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 }
 
 // IMM: the test mode of the waits (gdn_set_wait_test_mode), a separate instance
-template <int DK, bool IMM>
+template <int DK, bool IMM, bool EPI>
 __global__ void __launch_bounds__(kTmThreads, 1)
 chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles, int64_t nslots,
                 const unsigned char *prep_out, int cbase, int cmax) {
-    using L = TmSmem<DK>;
+    using L = TmSmem<DK, EPI>;
     constexpr int NS = L::kStages;
+    constexpr int VS = L::kVS;
     constexpr int HC = DK / 2;            // state columns per state warp (two warps per lane group)
     extern __shared__ unsigned char smraw[];
     pdl_wait();        // the prep tiles (and everything before them) are complete
@@ -151,7 +156,8 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
     if (tid == 0) {
         s_err = 0;
         for (int i = 0; i < T_COUNT; ++i) {
-            const bool warps8 = i == T_R || i == T_VN || i == T_O || i == T_H || i == T_OSTAGE;
+            const bool warps8 = i == T_R || i == T_VN || i == T_O || i == T_H || i == T_OSTAGE || i == T_GFREE ||
+                                i == T_OFULL;
             mbar_init(&bar[i], warps8 ? 8 : 1);
         }
         mbar_init_fence();
@@ -206,7 +212,7 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
     __syncthreads();
     fence_after_sync();
 
-    int tma_armed = 0, p_armed = 0, v_armed = 0;   // chunks whose loads the TMA thread has issued
+    int tma_armed = 0, p_armed = 0, v_armed = 0, g_armed = 0;   // chunks whose loads the TMA thread issued
     if (warp == kTmaW) {
         // ------------------------------------------------------------ TMA warp
         if (lane == 0) {
@@ -231,12 +237,19 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                           &bar[T_PFULL0 + ps]);
             };
             auto load_v = [&](int c) {
-                const int sv = c % kVSlots;
+                const int sv = c % VS;
                 unsigned char *dst = sm + L::kV + sv * 2 * kTileBytes;
                 const int y = (int)((int64_t)j * p.ntok + tok0(c));
                 mbar_expect_tx(&bar[T_VFULL0 + sv], 2 * kTileBytes);
                 tma_load_2d(dst, &maps.v, v0, y, &bar[T_VFULL0 + sv]);
                 tma_load_2d(dst + kTileBytes, &maps.v, v0 + 64, y, &bar[T_VFULL0 + sv]);
+            };
+            // the fused output step's gate rows of chunk c (rows past the tensor read zeros)
+            auto load_gate = [&](int c) {
+                const int y = (int)tok0(c);
+                mbar_expect_tx(&bar[T_GFULL], 2 * kTileBytes);
+                tma_load_2d(sm + L::kG, &maps.gate, j * dv + v0, y, &bar[T_GFULL]);
+                tma_load_2d(sm + L::kG + kTileBytes, &maps.gate, j * dv + v0 + 64, y, &bar[T_GFULL]);
             };
             for (int c = 0; c < nch; ++c) {
                 // stage c % NS is free once the state update of chunk c - NS is done
@@ -244,13 +257,19 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                 load_kq(c);
                 tma_armed = c + 1;
                 // V slot c % 2 once the row warps have read chunk c - 2's V
-                if (c >= kVSlots && !wait(T_VFREE0 + c % kVSlots, (uint32_t)((c / kVSlots) - 1) & 1)) break;
+                if (c >= VS && !wait(T_VFREE0 + c % VS, (uint32_t)((c / VS) - 1) & 1)) break;
                 load_v(c);
                 v_armed = c + 1;
                 // prep slot c % 2 once the second product of chunk c - 2 has read it
                 if (c >= kPSlots && !wait(T_PFREE0 + c % kPSlots, (uint32_t)((c / kPSlots) - 1) & 1)) break;
                 load_prep(c);
                 p_armed = c + 1;
+                if (EPI) {
+                    // the gate tile once the out warps have read chunk c - 1's
+                    if (c >= 1 && !wait(T_GFREE, (uint32_t)(c - 1) & 1)) break;
+                    load_gate(c);
+                    g_armed = c + 1;
+                }
             }
         }
         __syncwarp();
@@ -311,9 +330,9 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             };
             int c = 0;
             for (; c < nch; ++c) {
-                const int s = c % NS, ps = c % kPSlots, sv = c % kVSlots;
+                const int s = c % NS, ps = c % kPSlots, sv = c % VS;
                 const uint32_t fs = (uint32_t)(c / NS) & 1, fp = (uint32_t)(c / kPSlots) & 1,
-                               fv = (uint32_t)(c / kVSlots) & 1, f1 = (uint32_t)(c - 1) & 1;
+                               fv = (uint32_t)(c / VS) & 1, f1 = (uint32_t)(c - 1) & 1;
                 // the stage, the prep slot and (c >= 1) H16 = e^{gL_{c-1}} H_{c-2} with D1's Q
                 // half of chunk c-1 read by the out warps (its K half was read before R_{c-1}):
                 // D1 may be overwritten while the second product of chunk c-1 still runs
@@ -425,9 +444,32 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             g_tok = gw[t0 + (i < len ? i : len - 1)];
             g_last = gw[t0 + len - 1];
         };
-        // one thread issues the output tile's tensor stores
+        // one thread issues the output tile's tensor stores; nfree / nstage count the
+        // phases of T_OFREE / T_OSTAGE
         const bool storer = warp == kRowW && lane == 0;
-        int nstored = 0;
+        int nfree = 0, nstage = 0;
+        // the fused output step: this thread's 8 norm weights (dv 8 (lane % 16) ..) as pairs
+        const bool bf16_act = d.dtype == GDN_BF16;
+        bool out_finite = true;
+        float2 nw[4] = {};
+        if (EPI) {
+            const int cw = v0 + 8 * (lane & 15);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float w0, w1;
+                if (d.norm_w_dtype == GDN_F32) {
+                    w0 = ((const float *)p.norm_w)[cw + 2 * i];
+                    w1 = ((const float *)p.norm_w)[cw + 2 * i + 1];
+                } else if (bf16_act) {
+                    w0 = __bfloat162float(((const __nv_bfloat16 *)p.norm_w)[cw + 2 * i]);
+                    w1 = __bfloat162float(((const __nv_bfloat16 *)p.norm_w)[cw + 2 * i + 1]);
+                } else {
+                    w0 = __half2float(((const __half *)p.norm_w)[cw + 2 * i]);
+                    w1 = __half2float(((const __half *)p.norm_w)[cw + 2 * i + 1]);
+                }
+                nw[i] = make_float2(w0, w1);
+            }
+        }
         // two chunks ahead: chunk c's values move into place at the end of iteration c - 1,
         // one iteration after their loads were issued, so no move waits on a load in flight
         float g_tok = 0.f, g_last = 0.f, g_tok_n = 0.f, g_last_n = 0.f;
@@ -497,13 +539,15 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             }
             const int64_t t0 = tok0(c);
             const int len = clen(c);
-            if (len == kChunk) {
-                // a full chunk: transpose through the staging tile, one tensor store per 64 columns
+            if (EPI || len == kChunk) {
+                // through the staging tile: a full chunk leaves with one tensor store per 64
+                // columns; with the fused output step every chunk is staged
                 if (storer) {
                     bulk_wait_read();                     // the previous store has read the tile
                     mbar_arrive(&bar[T_OFREE]);
                 }
-                if (!wait(T_OFREE, (uint32_t)nstored & 1)) break;
+                if (!wait(T_OFREE, (uint32_t)nfree & 1)) break;
+                ++nfree;
                 // this thread addresses row lane % 8 (a token) of stored matrix m = lane / 8:
                 // 8 dv columns from 32 quad + 16 (m / 2) + 8 (m % 2)
                 const int m = lane >> 3, rr = lane & 7;
@@ -514,16 +558,67 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                 for (int i = 0; i < 4; ++i)
                     stmatrix_x4_trans(obox + (uint32_t)(32 * half + 8 * i + rr) * 128 + ochk, h[4 * i], h[4 * i + 1],
                                       h[4 * i + 2], h[4 * i + 3]);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[T_OSTAGE]);
-                if (storer) {
-                    if (!wait(T_OSTAGE, (uint32_t)nstored & 1)) break;
-                    tma_store_2d(&maps.o, j * dv + v0, (int)t0, sm + L::kO);
-                    tma_store_2d(&maps.o, j * dv + v0 + 64, (int)t0, sm + L::kO + kTileBytes);
-                    bulk_commit();
+                if (EPI) {
+                    // the gated RMSNorm over whole rows once every out warp's o is in the tile:
+                    // 16 lanes per token, 8 consecutive dv each, the same arithmetic (and order
+                    // of the sums) as the separate output step, in place in the tile
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[T_OFULL]);
+                    if (!wait(T_OFULL, (uint32_t)c & 1) || !wait(T_GFULL, (uint32_t)c & 1)) break;
+                    const int ot = (warp - kRowW) * 32 + lane;
+                    const uint32_t cb = (uint32_t)(ot & 15);
+#pragma unroll
+                    for (int sg = 0; sg < 4; ++sg) {
+                        const int r = (ot >> 4) + 16 * sg;
+                        const uint32_t off = (cb >> 3) * kTileBytes + (uint32_t)r * 128 + (((cb & 7) ^ (uint32_t)(r & 7)) << 4);
+                        float2 x[4];
+                        Pairs<__half>::unpack(*reinterpret_cast<const uint4 *>(sm + L::kO + off), x);
+                        float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) ss2 = fma2(x[i], x[i], ss2);
+                        float ss = ss2.x + ss2.y;
+#pragma unroll
+                        for (int sh = 8; sh >= 1; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
+                        if (r < len) out_finite = out_finite && isfinite(ss);
+                        const float2 inv = splat2(rsqrtf(ss * (1.0f / (float)dv) + d.norm_eps));
+                        const uint4 gu = *reinterpret_cast<const uint4 *>(sm + L::kG + off);
+                        float2 gp[4], y[4];
+                        uint4 pk;
+                        if (bf16_act) {
+                            Pairs<__nv_bfloat16>::unpack(gu, gp);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                y[i] = mul2(Pairs<__nv_bfloat16>::round(mul2(nw[i], mul2(x[i], inv))), silu2_fast(gp[i]));
+                            pk = Pairs<__nv_bfloat16>::pack(y);
+                        } else {
+                            Pairs<__half>::unpack(gu, gp);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                y[i] = mul2(Pairs<__half>::round(mul2(nw[i], mul2(x[i], inv))), silu2_fast(gp[i]));
+                            pk = Pairs<__half>::pack(y);
+                        }
+                        if (len == kChunk)
+                            *reinterpret_cast<uint4 *>(sm + L::kO + off) = pk;
+                        else if (r < len)
+                            *reinterpret_cast<uint4 *>((unsigned char *)p.out +
+                                                       ((t0 + r) * (int64_t)Hv * dv + (int64_t)j * dv + v0 + 8 * cb) * 2) = pk;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[T_GFREE]);   // this warp's gate reads are done
                 }
-                ++nstored;
+                if (len == kChunk) {
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[T_OSTAGE]);
+                    if (storer) {
+                        if (!wait(T_OSTAGE, (uint32_t)nstage & 1)) break;
+                        const CUtensorMap *om = EPI ? &maps.out : &maps.o;
+                        tma_store_2d(om, j * dv + v0, (int)t0, sm + L::kO);
+                        tma_store_2d(om, j * dv + v0 + 64, (int)t0, sm + L::kO + kTileBytes);
+                        bulk_commit();
+                    }
+                    ++nstage;
+                }
             } else {
                 // the last, partial chunk of a sequence: the tile's other rows belong to the next
                 __half *dst = o + (int64_t)j * dv + v0 + 32 * quad + g8;
@@ -545,6 +640,8 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
             if (c + 2 < nch) decays(c + 2, g_tok_n, g_last_n);
         }
         if (storer) bulk_wait();   // the output stores are complete before the CTA leaves
+        // a non-finite gated-delta-rule output (unless an earlier error was recorded)
+        if (EPI && !out_finite) atomicCAS(p.status, GDN_OK, GDN_ERR_DEVICE_RANGE);
         if (p.hT && !s_err) {
             if (nch == 0) {
                 store_final();
@@ -567,8 +664,9 @@ chain_tm_kernel(const __grid_constant__ TmMaps maps, const Problem p, int ntiles
                 mbar_wait(&bar[T_FULL0 + c % NS], (uint32_t)(c / NS) & 1);
             for (int c = p_armed - kPSlots < 0 ? 0 : p_armed - kPSlots; c < p_armed; ++c)
                 mbar_wait(&bar[T_PFULL0 + c % kPSlots], (uint32_t)(c / kPSlots) & 1);
-            for (int c = v_armed - kVSlots < 0 ? 0 : v_armed - kVSlots; c < v_armed; ++c)
-                mbar_wait(&bar[T_VFULL0 + c % kVSlots], (uint32_t)(c / kVSlots) & 1);
+            for (int c = v_armed - VS < 0 ? 0 : v_armed - VS; c < v_armed; ++c)
+                mbar_wait(&bar[T_VFULL0 + c % VS], (uint32_t)(c / VS) & 1);
+            if (EPI && g_armed > 0) mbar_wait(&bar[T_GFULL], (uint32_t)(g_armed - 1) & 1);
         }
     }
     fence_before_sync();
@@ -593,15 +691,26 @@ cudaError_t launch_tm(const Problem &p, cudaStream_t s, const unsigned char *pre
             !encode_tile_map(&m.v, p.v, (uint64_t)d.Hv * p.ntok, d.dv) ||
             !encode_tile_map(&m.o, p.o, (uint64_t)p.ntok, (uint64_t)d.Hv * d.dv))
             return cudaErrorInvalidValue;
+        if (p.fuse_epilogue) {
+            // the gate view's rows are tokens (one sequence row, or batches back to back)
+            const uint64_t grows = p.cu ? (uint64_t)p.ntok : (uint64_t)d.B * d.T;
+            if (!encode_tile_map_pitch(&m.gate, p.gate, grows, (uint64_t)d.Hv * d.dv, (uint64_t)d.gate_stride_t * 2) ||
+                !encode_tile_map(&m.out, p.out, (uint64_t)p.ntok, (uint64_t)d.Hv * d.dv))
+                return cudaErrorInvalidValue;
+        } else {
+            memset(&m.gate, 0, sizeof(m.gate));
+            memset(&m.out, 0, sizeof(m.out));
+        }
     } else {
         memset(&m, 0, sizeof(m));   // no chunks: the kernel only copies the initial state
     }
     const int maxs = max_dyn_smem_tm();
     // all 512 TMEM columns: enough shared memory that a second CTA never shares the SM
-    size_t smem = TmSmem<DK>::kTotal;
+    size_t smem = p.fuse_epilogue ? TmSmem<DK, true>::kTotal : TmSmem<DK, false>::kTotal;
     if (smem < (size_t)(maxs / 2 + 1024)) smem = (size_t)(maxs / 2 + 1024);
     if ((int)smem > maxs) return cudaErrorInvalidValue;
-    auto kernel = p.wait_immediate ? chain_tm_kernel<DK, true> : chain_tm_kernel<DK, false>;
+    auto kernel = p.fuse_epilogue ? (p.wait_immediate ? chain_tm_kernel<DK, true, true> : chain_tm_kernel<DK, false, true>)
+                                  : (p.wait_immediate ? chain_tm_kernel<DK, true, false> : chain_tm_kernel<DK, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (nblocks == 0) return cudaSuccess;
@@ -617,6 +726,23 @@ bool chain_tm_supports(const gdn_desc &d) {
 }
 
 int chain_tm_tiles(const gdn_desc &d) { return d.dv / 128; }
+
+// The output step (gated RMSNorm over dv) fused into the transposed chain: one CTA
+// holds a token's whole row when dv = 128; the gate must be a 16-bit view whose rows
+// a tensor map can address (16-byte aligned base and row pitch, batches back to back).
+// Not for the segmented schedule: the fused instance keeps one V slot (the gate tile
+// takes the other), too shallow beside the prep segments (one 131072-token sequence:
+// 5.1 -> 6.8 ms per step).
+bool chain_tm_fuses_epilogue(const Problem &p) {
+    const gdn_desc &d = p.d;
+    if (!chain_tm_supports(d) || d.dv != 128 || p.ntok == 0 || !p.gate || !p.out || p.rec_o) return false;
+    if (chunk_tc_segmented(p)) return false;
+    if (d.gate_dtype != d.dtype || (d.norm_w_dtype != d.dtype && d.norm_w_dtype != GDN_F32)) return false;
+    if ((uintptr_t)p.gate % 16 != 0 || (uintptr_t)p.out % 16 != 0 || (d.gate_stride_t * 2) % 16 != 0 ||
+        d.gate_stride_t < (int64_t)d.Hv * d.dv)
+        return false;
+    return p.cu != nullptr || d.B == 1 || d.gate_stride_b == (int64_t)d.T * d.gate_stride_t;
+}
 
 cudaError_t launch_chain_tm(const Problem &p, cudaStream_t s, const unsigned char *prep_out, int64_t nslots_alloc,
                             int cbase, int cmax, bool pdl, unsigned nblocks) {

@@ -997,10 +997,14 @@ int max_dyn_smem() {
 }  // namespace
 
 bool encode_tile_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+    return encode_tile_map_pitch(m, base, rows, cols, cols * 2);
+}
+
+bool encode_tile_map_pitch(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint64_t pitch) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {pitch};
     cuuint32_t box[2] = {64, 64};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,

@@ -92,6 +92,9 @@ struct Problem {
     // 1 (tests of the timeout path, gdn_set_wait_test_mode): a main-loop wait that is
     // not already complete gives up at once. Drains always use the ~1 s limit.
     int wait_immediate;
+    // gdn_forward on the transposed chain with dv = 128: the chain applies the output
+    // step (gated RMSNorm) itself and writes out; o in the workspace is not written
+    bool fuse_epilogue;
 };
 
 // Upper bound on chunk slots: ceil(ntok/64) + N (each sequence adds at most one
@@ -121,6 +124,7 @@ bool chunk_tc_supports(const gdn_desc &d);
 // gdn_chain_tm.cu): chunks [cbase, cbase + cmax) of every sequence, nblocks =
 // sequences x Hv x chain_tm_tiles CTAs
 bool chain_tm_supports(const gdn_desc &d);
+bool chain_tm_fuses_epilogue(const Problem &p);
 int chain_tm_tiles(const gdn_desc &d);
 cudaError_t launch_chain_tm(const Problem &p, cudaStream_t s, const unsigned char *prep_out, int64_t nslots_alloc,
                             int cbase, int cmax, bool pdl, unsigned nblocks);

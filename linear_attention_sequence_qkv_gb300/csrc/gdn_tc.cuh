@@ -391,4 +391,6 @@ constexpr uint32_t kPrepOut = kTPTBytes + kXBytes;
 // 2-D fp16 tensor map over [rows][cols] with 64x64 boxes and 128-byte swizzle
 // (host; false when the driver entry point or the encoding fails).
 bool encode_tile_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols);
+// the same with a row pitch in bytes (a multiple of 16) other than cols * 2
+bool encode_tile_map_pitch(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint64_t pitch);
 }  // namespace gdn
