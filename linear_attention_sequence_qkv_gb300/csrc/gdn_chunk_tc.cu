@@ -117,7 +117,8 @@ __device__ __forceinline__ void load_half_row_f16(const unsigned char *tile, int
 // One CTA per (q/k head, chunk slot): the products of the chunk's keys and
 // queries are shared by the v heads of the q/k head (GQA), so they are loaded
 // and multiplied once; the decay masks, the solve and P T are per v head.
-constexpr int kPrepThreads = 256;   // 8 warps: warps w and w+4 share TMEM lanes, split columns
+constexpr int kPrepThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;   // 8 warps: warps w and w+4 share TMEM lanes, split columns
 constexpr int kLdc = kChunk + 4;    // column stride of A (column-major, 16-byte aligned columns)
 // v heads solved per pass (the solve scratch holds this many), a template
 // parameter of the kernel. One keeps the CTA's shared memory at ~58 KB and its
@@ -211,7 +212,8 @@ __global__ void __launch_bounds__(kPrepThreads, MINB) chunk_prep_kernel(const __
             const int h = tid >> 6, i = tid & (kChunk - 1);
             if (g0 + h < G) {
                 const int64_t base = (int64_t)(hk * G + g0 + h) * p.ntok + c.tok0;
-                gam[tid] = ((const float *)p.gamma)[base + (i < c.len ? i : c.len - 1)];
+                // kept as gam * log2(e): every mask entry is then one ex2 of a difference
+                gam[tid] = ((const float *)p.gamma)[base + (i < c.len ? i : c.len - 1)] * kLog2e;
                 bet[tid] = i < c.len ? p.beta[base + i] : 0.f;
             }
         }
@@ -294,10 +296,16 @@ __global__ void __launch_bounds__(kPrepThreads, MINB) chunk_prep_kernel(const __
             for (int h = 0; h < nh; ++h) {
                 const float gi = gam[h * kChunk + row], bi = bet[h * kChunk + row];
                 float *Ah = Ac + h * kChunk * kLdc;
+                const float4 *g4 = reinterpret_cast<const float4 *>(gam + h * kChunk + c0);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int jj = c0 + q;
-                    Ah[jj * kLdc + row] = jj < row ? bi * __expf(gi - gam[h * kChunk + jj]) * s1[q] : 0.f;
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 gj = g4[q4];
+                    const float gv[4] = {gj.x, gj.y, gj.z, gj.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int q = 4 * q4 + e, jj = c0 + q;
+                        Ah[jj * kLdc + row] = jj < row ? bi * ex2_approx(gi - gv[e]) * s1[q] : 0.f;
+                    }
                 }
             }
         }
@@ -394,10 +402,16 @@ __global__ void __launch_bounds__(kPrepThreads, MINB) chunk_prep_kernel(const __
                     const float gi = gam[h * kChunk + i];
                     float s1[32];
                     tmem_ld32(lane_addr, s1);
+                    const float4 *g4 = reinterpret_cast<const float4 *>(gam + h * kChunk + c0);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int jj = c0 + q;
-                        v[q] = jj <= i ? __expf(gi - gam[h * kChunk + jj]) * s1[q] : 0.f;
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 gj = g4[q4];
+                        const float gv[4] = {gj.x, gj.y, gj.z, gj.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int q = 4 * q4 + e, jj = c0 + q;
+                            v[q] = jj <= i ? ex2_approx(gi - gv[e]) * s1[q] : 0.f;
+                        }
                     }
                 }
                 store_half_row_f16(tp, row, c0, v);
@@ -429,7 +443,7 @@ __global__ void __launch_bounds__(kPrepThreads, MINB) chunk_prep_kernel(const __
                 store_half_row_f16(tp, row, c0, v);
             } else if (FOLD) {     // diag(e^{gam_L - gam}) T diag(beta) in rows 0..63 (P T has read T)
                 // gam is clamped to the chunk's last token, so gam[63] is gam_L
-                const float er = __expf(gam[h * kChunk + kChunk - 1] - gam[h * kChunk + row]);
+                const float er = ex2_approx(gam[h * kChunk + kChunk - 1] - gam[h * kChunk + row]);
                 const float *Th = Ts + h * kChunk * LDA + row * LDA + c0;
                 float v[32];
 #pragma unroll
