@@ -43,8 +43,8 @@ CHUNK = 64
 # one launch each per step; the figure is the sum of the two launches.
 NCU_TRAFFIC: dict = {
     "chunk_rule": ("linear_attention_sequence_qkv_gb300/csrc/gdn_chunk_tc.cu",
-                   "46c81d02d4a9e56c297f603d2cefdd379b7650169026e5c33b136b97dbb6346b",
-                   "layer_bf16", 117_440_768),
+                   "8d495cf4f0617f1807d0c4dcfea7be63c61ffedcd46eb1ad91580abaeed0bad0",
+                   "layer_bf16", 117_008_896),
 }
 
 
