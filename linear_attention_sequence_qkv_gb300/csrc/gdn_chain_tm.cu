@@ -25,11 +25,16 @@
 // where a TMA warp stages it ahead of use. So the hand-offs on the serial path
 // (D1 -> R -> D2 -> Vn' -> next D1) are tensor-memory loads and stores with no
 // shared-memory round trip. The V tile also arrives by TMA; the outputs leave
-// through a shared staging tile and TMA tensor stores (a thread holds one dv
-// column across 64 tokens, so direct stores would be 2-byte scatters). Per-token
-// factors (beta, decays) reach the warps as broadcast reads of small per-warp
-// arrays rather than shuffles: the warps' shared-memory traffic shares the
-// issue path of the MMA-issuing thread.
+// through a swizzled staging tile (16x256b tensor-memory loads give each thread
+// token pairs of two dv rows, which stmatrix stores transposed) and TMA tensor
+// stores. The per-token factor e^gam reaches the warps as broadcast reads of small
+// per-warp arrays rather than shuffles.
+//
+// EPI instance (gdn_forward with dv = 128, chain_tm_fuses_epilogue): one CTA holds
+// every dv of a token, so the output step (gated RMSNorm) runs here: the out warps
+// read the staged o rows back in the separate output kernel's layout, repeat its
+// arithmetic and order of sums (bit for bit the same out), and the tile leaves as
+// out; the gate tile arrives by TMA in place of the second V slot.
 //
 // Every wait on an mbarrier gives up after about a second; the CTA then records
 // GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own copies and products in
