@@ -11,7 +11,11 @@ its arithmetic and order of sums, so gdn_forward must equal the three stage call
 the oracle. Cases: ragged packed sequences with an empty and a one-token sequence
 and a strided gate; two batch rows; fp16 with fp32 norm weights; and a gate view
 at an odd element offset, which the fused step does not take (the separate kernel
-runs), to show that the fallback gives the same bits.
+runs), to show that the fallback gives the same bits. Which path ran is observed,
+not assumed: the fused step never writes the intermediate o of the workspace, so
+a NaN pattern put there beforehand survives it and is overwritten by the separate
+path. A non-finite output reports GDN_ERR_DEVICE_RANGE from the fused step as it
+does from the separate kernel.
 """
 from types import SimpleNamespace
 
@@ -55,9 +59,25 @@ def view(di, **kw):
     return SimpleNamespace(**fields)
 
 
-def run_both(di):
-    a = gdn.forward(di)
+SENTINEL = 0x7E7E   # an fp16 NaN pattern: no finite o has these bits
+
+
+def forward_marked(di):
+    """gdn.forward with the workspace's intermediate o filled with SENTINEL first;
+    returns the buffers and whether o was left untouched (the fused step ran)."""
+    a = gdn.alloc(gdn.make_desc(di), "cuda")
+    o = a.ws_view("o").view(torch.int16)
+    o.fill_(SENTINEL)
+    gdn.forward(di, a)
     torch.cuda.synchronize()
+    hits = int((o == SENTINEL).sum())
+    assert hits in (0, o.numel()), "o partly written"
+    return a, hits == o.numel()
+
+
+def run_both(di, fused=True):
+    a, untouched = forward_marked(di)
+    assert untouched == fused
     assert gdn.gdn_device_status(a.workspace) == gdn.GDN_OK
     b = staged(di, a.desc)
     assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
@@ -85,4 +105,21 @@ def test_unaligned_gate_takes_the_separate_output_step():
     ch = w.Hv * w.dv
     odd = di.gate_buf[..., 1:1 + ch]            # 2-byte offset: no tensor map, no fusion
     assert odd.data_ptr() % 16 != 0
-    run_both(view(di, gate=odd))
+    run_both(view(di, gate=odd), fused=False)
+
+
+def test_fused_step_reports_non_finite_output():
+    # bf16 activations keep their intermediates in fp16: a conv output beyond the fp16
+    # range becomes inf, and the fused step's row sums see it
+    w = replace(BASE, name="fo_range", B=1, T=70, Hk=1, Hv=1, dk=64, n_packed=0)
+    inp = make_inputs(w)
+    inp.v_raw[0, 5, :] = 1e30
+    di = to_device(inp, "cuda")
+    a, untouched = forward_marked(di)
+    assert untouched
+    assert gdn.gdn_device_status(a.workspace) == gdn.GDN_ERR_DEVICE_RANGE
+    # the next well-formed call on the same buffers clears it
+    di.v_raw[0, 5, :] = 0.5
+    gdn.forward(di, a)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status(a.workspace) == gdn.GDN_OK
