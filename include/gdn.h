@@ -111,8 +111,10 @@ int gdn_workspace_bytes(const gdn_desc *d, size_t *bytes);
  *   bf16/fp16 activations, fp32 for fp32 activations; beta [Hv][Ntok] fp32;
  *   gamma [Hv][Ntok] = in-chunk inclusive cumulative sum of g, fp64 for fp32
  *   activations and fp32 otherwise; status: int32 device status word;
- *   chunk_off: int32 [N+1]; tpt: per (v head, chunk) the 128x64 fp16 tile
- *   [T; P T] of the tensor-core kernels (empty where they do not run). */
+ *   chunk_off: int32 [N+1]; tpt: the tensor-core kernels' region (empty where
+ *   they do not run): per (v head, chunk slot) 32 KB of prep tiles (the 128x64
+ *   fp16 tile [T; P T], then X), and for one sequence (N = 1) after them the fp32
+ *   state handed between the segments of its chain, [Hv][dk][dv]. */
 typedef struct {
     size_t status, chunk_off, q, k, v, beta, gamma, o, tpt, total;
 } gdn_workspace_layout;
