@@ -212,7 +212,6 @@ __global__ void __launch_bounds__(kOThreads, 1) out_tc_kernel(const BwdProblem b
     const int hk = j / (Hv / d.Hk);
     unsigned char *At = sm, *Bt = sm + 16384;          // A: 128 x 64 K-major; B: 64 K-rows x dv MN-major
     const int t = threadIdx.x, warp = t >> 5;
-    const int nblk = dv / 64;                          // 64-column blocks of B
     if (t == 0) {
         mbar_init(&bar, 1);
         mbar_init_fence();
