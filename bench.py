@@ -43,8 +43,8 @@ CHUNK = 64
 # one launch each per step; the figure is the sum of the two launches.
 NCU_TRAFFIC: dict = {
     "chunk_rule": ("linear_attention_sequence_qkv_gb300/csrc/gdn_chunk_tc.cu",
-                   "8d495cf4f0617f1807d0c4dcfea7be63c61ffedcd46eb1ad91580abaeed0bad0",
-                   "layer_bf16", 117_008_896),
+                   "7e27d03e8366d5c7351d3b271ab0772303bf47da73b0f4f5293d30bab827f58c",
+                   "layer_bf16", 115_082_240),
 }
 
 

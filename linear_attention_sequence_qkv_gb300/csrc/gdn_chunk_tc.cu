@@ -42,7 +42,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 128;
 constexpr int LDA = kChunk + 1;
 
 struct PrepMaps {
@@ -56,33 +55,7 @@ __device__ __forceinline__ void set_timeout(const Problem &p) {
     atomicCAS(p.status, GDN_OK, GDN_ERR_DEVICE_TIMEOUT);
 }
 
-// row of 64 fp32 -> fp16, written into a 128-byte-swizzled tile row
-__device__ __forceinline__ void store_row_f16(unsigned char *tile, int row, const float *v64) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4 u;
-        __half2 *h = reinterpret_cast<__half2 *>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v64[8 * c + 2 * e], v64[8 * c + 2 * e + 1]);
-        *reinterpret_cast<uint4 *>(tile + sw128_off(row, 8 * c)) = u;
-    }
-}
-
-__device__ __forceinline__ void load_row_f16(const unsigned char *tile, int row, float *v64) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_off(row, 8 * c));
-        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(h[e]);
-            v64[8 * c + 2 * e] = f.x;
-            v64[8 * c + 2 * e + 1] = f.y;
-        }
-    }
-}
-
-// 32 columns [c0, c0 + 32) of a swizzled tile row, fp32 <-> fp16
+// 32 columns [c0, c0 + 32) of a swizzled tile row, fp32 -> fp16
 __device__ __forceinline__ void store_half_row_f16(unsigned char *tile, int row, int c0, const float *v32) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -98,19 +71,6 @@ __device__ __forceinline__ void store_row_f32(float *dst, const float *v32) {
     float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v32[4 * q], v32[4 * q + 1], v32[4 * q + 2], v32[4 * q + 3]);
-}
-__device__ __forceinline__ void load_half_row_f16(const unsigned char *tile, int row, int c0, float *v32) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_off(row, c0 + 8 * c));
-        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(h[e]);
-            v32[8 * c + 2 * e] = f.x;
-            v32[8 * c + 2 * e + 1] = f.y;
-        }
-    }
 }
 
 // ================================================================ prep kernel

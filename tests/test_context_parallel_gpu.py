@@ -15,7 +15,7 @@ from linear_attention_sequence_qkv_gb300 import context_parallel as cp
 from linear_attention_sequence_qkv_gb300 import gdn
 from linear_attention_sequence_qkv_gb300.workloads import WORKLOADS, make_inputs, replace, to_device
 from oracle import oracle as O
-from tests._harness import check, flat, oracle_forward
+from tests._harness import check, oracle_forward
 
 pytestmark = pytest.mark.gpu
 

@@ -30,7 +30,7 @@ from linear_attention_sequence_qkv_gb300 import gdn
 from linear_attention_sequence_qkv_gb300.workloads import (MILD, WORKLOADS, head_subproblem, make_cotangents,
                                                            make_inputs, replace, to_device)
 from oracle import oracle as O
-from tests._harness import check, check_grad, chunk_survival, flat, oracle_backward, oracle_forward
+from tests._harness import check, check_grad, chunk_survival, oracle_backward, oracle_forward
 
 pytestmark = pytest.mark.gpu
 
