@@ -594,19 +594,24 @@ def arena(tensors, device, pin=False):
     return buf, views
 
 
-def chunk_launch_count(gdn, d, w, inp, nsm):
-    """Launches of the chunk stage per step: prep + chain on the tensor-core path
-    (two per segment of a long single sequence), one kernel on the fp32 path."""
-    tc = gdn.gdn_chunk_kernel_kind(d) == 1
-    if not tc:
-        return 1
+def chunk_segments(w, d, inp, nsm):
+    """Segments of the tensor-core chunk stage's schedule (1: not segmented): one
+    long sequence whose chain CTAs fill at most half of the SMs is cut into up to 16."""
     nch = (d.T + CHUNK - 1) // CHUNK
     tm = w.dtype != "fp32" and w.dk in (64, 128) and w.dv % 128 == 0     # the transposed chain: 128-row dv tiles
     chain_ctas = w.Hv * (w.dv // 128 if tm else w.dv // 64)
     if inp.cu_seqlens is None and d.N == 1 and nch >= 256 and chain_ctas * 2 <= nsm:
         seg = max(-(-nch // 16), 64)
-        return 2 * (-(-nch // seg))
-    return 2
+        return -(-nch // seg)
+    return 1
+
+
+def chunk_launch_count(gdn, d, w, inp, nsm):
+    """Launches of the chunk stage per step: prep + chain on the tensor-core path
+    (two per segment of a long single sequence), one kernel on the fp32 path."""
+    if gdn.gdn_chunk_kernel_kind(d) != 1:
+        return 1
+    return 2 * chunk_segments(w, d, inp, nsm)
 
 
 def fused_output_step(gdn, d, w, inp, nsm):
