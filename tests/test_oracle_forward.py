@@ -114,6 +114,28 @@ def test_packed_sequences_equal_separate_runs():
         np.testing.assert_array_equal(f1[0], fin[n])
 
 
+def test_empty_sequences_keep_their_initial_state():
+    # a sequence without tokens applies no step of the recurrence: its final state is
+    # its initial state, and the sequences around it are as if it were not there
+    lengths = [0, 9, 0, 0, 70, 0]
+    w = replace(SMALL, B=1, T=0, n_packed=len(lengths), init_state_std=0.1)
+    inp = make_inputs(w, lengths=lengths)
+    out, fin = run(inp)
+    assert out.shape[0] == sum(lengths)
+    h0 = inp.initial_state.numpy()
+    for n, L in enumerate(lengths):
+        if L == 0:
+            np.testing.assert_array_equal(fin[n], h0[n])
+    keep = [n for n, L in enumerate(lengths) if L > 0]
+    dense = make_inputs(replace(w, n_packed=len(keep)), lengths=[lengths[n] for n in keep])
+    for name in ("q_raw", "k_raw", "v_raw", "a", "b", "gate_buf", "conv_w", "A_log", "dt_bias", "norm_w"):
+        setattr(dense, name, getattr(inp, name))
+    dense.initial_state = inp.initial_state[keep]
+    out2, fin2 = run(dense)
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(fin[keep], fin2)
+
+
 def test_gqa_equals_explicit_head_replication():
     import torch
     w = replace(SMALL, Hk=2, Hv=4)
