@@ -56,8 +56,10 @@ typedef enum {
     GDN_ERR_DEVICE_SEQLENS = -5, /* (device status) cu_seqlens not 0-based, not
                                     non-decreasing or not ending at T */
     GDN_ERR_DEVICE_RANGE = -6,  /* (device status) a non-finite gated-delta-rule output
-                                   reached the epilogue: a non-finite input, or a value
-                                   beyond the fp16 range of the intermediates */
+                                   reached step 5 (the separate output kernel, or the
+                                   output step inside the chunk kernel): a non-finite
+                                   input, or a value beyond the fp16 range of the
+                                   intermediates */
     GDN_ERR_DEVICE_TIMEOUT = -7 /* (device status) a tensor-core kernel gave up waiting
                                    (about 1 s) for a copy or an MMA; results are invalid */
 } gdn_status;
